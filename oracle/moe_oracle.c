@@ -1,0 +1,505 @@
+/*
+ * moe_oracle.c -- plain, slow, obviously-correct CPU oracle for the
+ * single-GPU MoE layer with router replay and block-scaled FP8.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the bench's CPU
+ * baseline do.  It shares no code, header or table with the CUDA library.
+ *
+ * Sources (prime-rl 0.6.0 performance deep dive, "RL at 1T Scale"):
+ *   - section "Router replay" (R3): routing decisions made at inference are
+ *     captured and replayed on the trainer; the routed-experts payload is a
+ *     tensor of shape [num_layers, top_k, seq_len].
+ *   - section "FP8 training": block-scaled FP8 as proposed by DeepSeek-V3
+ *     (1x128 activation tiles, 128x128 weight blocks, fp32 scales, e4m3).
+ *   - section "Parallelism", "Expert parallelism (EP)": tokens are dispatched
+ *     to experts and combined back.
+ * What the pages leave open (score function, tie-break, SwiGLU, layouts,
+ * accumulation order) is fixed by the plainest reading, listed in the design doc.
+ *
+ * Every routine below computes the definition directly: no tiling, no
+ * fusion, no reordering beyond what the definition states.  Floating point
+ * follows C99 IEEE semantics; build with -ffp-contract=off -fno-fast-math so
+ * that only the explicit fmaf() calls fuse.
+ *
+ * Parity status: every function here is pinned by tests/test_oracle_*.py
+ * (brute force, closed forms, invariants, library routines).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_OK 0
+#define OR_ERR_BAD_IDS 5
+
+/* ------------------------------------------------------------------ */
+/* scalar formats                                                       */
+/* ------------------------------------------------------------------ */
+
+/* bf16 is the upper 16 bits of an IEEE binary32: widening is exact. */
+float or_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Round a binary32 to bf16, round-to-nearest-even.  Works on the bit pattern:
+ * adding 0x7FFF plus the lowest kept bit rounds the discarded 16 bits to
+ * nearest with ties to the even kept value (a carry into the exponent is the
+ * correct next binade, and past the largest finite value it gives inf). */
+uint16_t or_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays a quiet NaN */
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + keep_lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* OCP FP8 E4M3 ("e4m3fn"): sign, 4 exponent bits (bias 7), 3 mantissa bits;
+ * exponent field 0 is subnormal (m * 2^-9); 0x7F / 0xFF are NaN; no inf;
+ * largest finite 0x7E = 1.75 * 2^8 = 448. */
+double or_e4m3_decode(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Encode a finite binary32 as E4M3, round-to-nearest-even, saturating to
+ * +-448 (the "satfinite" rule: a value whose rounding would leave the finite
+ * range becomes the largest finite code).  The sign is kept, so -0 -> 0x80.
+ *
+ * Rounding: the E4M3 grid spacing in the binade [2^e, 2^(e+1)) is 2^(e-3)
+ * for e >= -6 and 2^-9 below 2^-6 (subnormals).  Dividing by that power of
+ * two is exact in double, rint() rounds to the nearest integer with ties to
+ * even, and multiplying back is exact. */
+uint8_t or_e4m3_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (isnan(v))
+        return 0x7F;
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);          /* a = f * 2^ex, f in [0.5, 1) -> binade 2^(ex-1) */
+    int e = ex - 1;
+    int qexp = (e < -6) ? -9 : e - 3;
+    double n = rint(ldexp(a, -qexp));
+    double r = ldexp(n, qexp);
+    if (r > 448.0)
+        r = 448.0;
+    if (r == 0.0)
+        return sign;
+    /* r is now an exact E4M3 value; write its bit fields. */
+    frexp(r, &ex);
+    e = ex - 1;
+    uint8_t code;
+    if (e < -6) {
+        code = (uint8_t)ldexp(r, 9);                  /* subnormal: m = r / 2^-9 */
+    } else {
+        int m = (int)(ldexp(r, -e) * 8.0) - 8;        /* r = 2^e * (1 + m/8) */
+        code = (uint8_t)(((e + 7) << 3) | m);
+    }
+    return (uint8_t)(sign | code);
+}
+
+/* ------------------------------------------------------------------ */
+/* block-scaled quantisation (DeepSeek-V3 recipe, "FP8 training")       */
+/* ------------------------------------------------------------------ */
+
+/* One block: amax over its elements, s = amax / 448 (IEEE binary32
+ * division), code = e4m3(v / s) with IEEE division.  An all-zero block (or a
+ * block so small that amax / 448 underflows to zero) takes s = 1. */
+static float block_scale(float amax)
+{
+    float s = amax / 448.0f;
+    if (s == 0.0f)
+        s = 1.0f;
+    return s;
+}
+
+/* Activations: 1 x 128 blocks along each row.  src [rows, cols] bf16 with row
+ * stride ld_src elements; q [rows, cols] e4m3; s [rows, cols/128] fp32. */
+void or_quant_1x128(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
+                    uint8_t *q, float *s)
+{
+    int64_t nb = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < nb; b++) {
+            const uint16_t *v = src + r * ld_src + b * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; i++) {
+                float a = fabsf(or_bf16_to_f32(v[i]));
+                if (a > amax)
+                    amax = a;
+            }
+            float sc = block_scale(amax);
+            s[r * nb + b] = sc;
+            for (int i = 0; i < 128; i++)
+                q[r * cols + b * 128 + i] = or_e4m3_encode(or_bf16_to_f32(v[i]) / sc);
+        }
+    }
+}
+
+/* Weights: 128 x 128 blocks.  src [rows, cols] bf16; q [rows, cols];
+ * s [rows/128, cols/128]. */
+void or_quant_128x128(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
+                      uint8_t *q, float *s)
+{
+    int64_t nbr = rows / 128, nbc = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t br = 0; br < nbr; br++) {
+        for (int64_t bc = 0; bc < nbc; bc++) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 128; i++)
+                for (int64_t j = 0; j < 128; j++) {
+                    float a = fabsf(or_bf16_to_f32(src[(br * 128 + i) * ld_src + bc * 128 + j]));
+                    if (a > amax)
+                        amax = a;
+                }
+            float sc = block_scale(amax);
+            s[br * nbc + bc] = sc;
+            for (int64_t i = 0; i < 128; i++)
+                for (int64_t j = 0; j < 128; j++) {
+                    int64_t r = br * 128 + i, c = bc * 128 + j;
+                    q[r * cols + c] = or_e4m3_encode(or_bf16_to_f32(src[r * ld_src + c]) / sc);
+                }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* routing ("Router replay": the decision that is captured)             */
+/* ------------------------------------------------------------------ */
+
+/* l[t,e] = sum_i x[t,i] * Wr[e,i] as one binary32 fused-multiply-add chain in
+ * ascending i, starting from +0. */
+void or_router_logits(const uint16_t *x, const uint16_t *wr, int64_t T, int d, int E,
+                      float *logits)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++)
+        for (int e = 0; e < E; e++) {
+            float acc = 0.0f;
+            for (int i = 0; i < d; i++)
+                acc = fmaf(or_bf16_to_f32(x[t * d + i]), or_bf16_to_f32(wr[(int64_t)e * d + i]), acc);
+            logits[t * E + e] = acc;
+        }
+}
+
+/* Selection order: larger logit first; equal logits (including -0 == +0)
+ * go to the lower expert index; NaN ranks below every number. */
+static int ranks_before(float a, int ia, float b, int ib)
+{
+    int na = isnan(a), nb = isnan(b);
+    if (na != nb)
+        return nb;              /* a number beats NaN */
+    if (!na && a != b)
+        return a > b;
+    return ia < ib;
+}
+
+/* Top-k by repeated selection of the best unselected expert; slot j holds the
+ * j-th pick. */
+void or_topk(const float *logits, int64_t T, int E, int k, int32_t *ids)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++) {
+        const float *l = logits + t * E;
+        unsigned char *taken = calloc((size_t)E, 1);
+        for (int j = 0; j < k; j++) {
+            int best = -1;
+            for (int e = 0; e < E; e++) {
+                if (taken[e])
+                    continue;
+                if (best < 0 || ranks_before(l[e], e, l[best], best))
+                    best = e;
+            }
+            taken[best] = 1;
+            ids[t * k + j] = best;
+        }
+        free(taken);
+    }
+}
+
+/* Gate weights over the chosen experts, in double, rounded once to binary32.
+ *   softmax: p_e = exp(l_e) / sum over all experts; renorm divides by the sum
+ *            over the chosen ones (the full denominator cancels).
+ *   sigmoid: p_e = 1 / (1 + exp(-l_e)); renorm divides by the chosen sum.
+ * The result is multiplied by route_scale.  Tokens flagged invalid (valid !=
+ * NULL and valid[t] == 0) get zero gates. */
+void or_gates(const float *logits, const int32_t *ids, const uint8_t *valid, int64_t T, int E, int k,
+              int score_fn, int renorm, float route_scale, float *gates)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++) {
+        const float *l = logits + t * E;
+        if (valid && !valid[t]) {
+            for (int j = 0; j < k; j++)
+                gates[t * k + j] = 0.0f;
+            continue;
+        }
+        double p[64];
+        double denom = 0.0;
+        if (score_fn == 0) {
+            double m = -INFINITY;
+            if (renorm) {
+                for (int j = 0; j < k; j++)
+                    if (l[ids[t * k + j]] > m)
+                        m = l[ids[t * k + j]];
+                for (int j = 0; j < k; j++)
+                    denom += exp((double)l[ids[t * k + j]] - m);
+            } else {
+                for (int e = 0; e < E; e++)
+                    if (l[e] > m)
+                        m = l[e];
+                for (int e = 0; e < E; e++)
+                    denom += exp((double)l[e] - m);
+            }
+            for (int j = 0; j < k; j++)
+                p[j] = exp((double)l[ids[t * k + j]] - m) / denom;
+        } else {
+            for (int j = 0; j < k; j++) {
+                p[j] = 1.0 / (1.0 + exp(-(double)l[ids[t * k + j]]));
+                denom += p[j];
+            }
+            for (int j = 0; j < k; j++)
+                if (renorm)
+                    p[j] = p[j] / denom;
+        }
+        for (int j = 0; j < k; j++)
+            gates[t * k + j] = (float)(p[j] * (double)route_scale);
+    }
+}
+
+/* Replay one layer slice of the routed-experts payload: payload_kT is
+ * [top_k, seq_len] row-major (the layer's slab of [num_layers, top_k,
+ * seq_len]); ids[t, j] = payload_kT[j, t], an exact copy in slot order.
+ * A token is valid when its k ids are in [0, E) and pairwise distinct.
+ * valid[t] (nullable) receives 1/0; returns the number of invalid tokens. */
+int64_t or_replay(const int32_t *payload_kT, int64_t T, int E, int k, int32_t *ids, uint8_t *valid)
+{
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; t++) {
+        int ok = 1;
+        for (int j = 0; j < k; j++) {
+            int32_t v = payload_kT[(int64_t)j * T + t];
+            ids[t * k + j] = v;
+            if (v < 0 || v >= E)
+                ok = 0;
+            for (int i = 0; i < j; i++)
+                if (ids[t * k + i] == v)
+                    ok = 0;
+        }
+        if (valid)
+            valid[t] = (uint8_t)ok;
+        if (!ok)
+            bad++;
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* dispatch ("Expert parallelism": tokens to experts and back)          */
+/* ------------------------------------------------------------------ */
+
+/* Counting sort of the slots s = t*k + j by expert id, visiting slots in
+ * ascending order (stable).  counts[e] = slots routed to e; offsets is the
+ * exclusive prefix sum (offsets[E] = routed slots); sorted_to_slot[r] is the
+ * slot at sorted position r; slot_to_sorted is its inverse.  Slots whose id is
+ * out of [0, E) are not routed: slot_to_sorted = -1, and sorted_to_slot has
+ * only offsets[E] entries (the rest are set to -1).  Returns the number of
+ * such slots. */
+int64_t or_dispatch(const int32_t *ids, int64_t T, int k, int E, int32_t *counts, int32_t *offsets,
+                    int32_t *sorted_to_slot, int32_t *slot_to_sorted)
+{
+    int64_t A = T * (int64_t)k, dropped = 0;
+    for (int e = 0; e < E; e++)
+        counts[e] = 0;
+    for (int64_t s = 0; s < A; s++) {
+        if (ids[s] >= 0 && ids[s] < E)
+            counts[ids[s]]++;
+        else
+            dropped++;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; e++)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *next = malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; e++)
+        next[e] = offsets[e];
+    for (int64_t r = 0; r < A; r++)
+        sorted_to_slot[r] = -1;
+    for (int64_t s = 0; s < A; s++) {
+        int32_t e = ids[s];
+        if (e < 0 || e >= E) {
+            slot_to_sorted[s] = -1;
+            continue;
+        }
+        int32_t r = next[e]++;
+        sorted_to_slot[r] = (int32_t)s;
+        slot_to_sorted[s] = r;
+    }
+    free(next);
+    return dropped;
+}
+
+/* rows_sorted[r] = rows[sorted_to_slot[r] / k] for the first n_sorted rows
+ * (byte rows of row_bytes each). */
+void or_gather_rows(const uint8_t *rows, int64_t row_bytes, const int32_t *sorted_to_slot,
+                    int64_t n_sorted, int k, uint8_t *rows_sorted)
+{
+    for (int64_t r = 0; r < n_sorted; r++) {
+        int64_t t = sorted_to_slot[r] / k;
+        memcpy(rows_sorted + r * row_bytes, rows + t * row_bytes, (size_t)row_bytes);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* expert FFN: SwiGLU with block-scaled FP8 GEMMs ("FP8 training")      */
+/* ------------------------------------------------------------------ */
+
+/* One 128-long block of a dot product of E4M3 codes.  Each product of two
+ * E4M3 values has at most 8 significant bits and lies in [2^-18, 2^17.6], so
+ * every partial sum of 128 of them is an exact double; the order of the
+ * additions therefore cannot matter and the result is the exact block sum. */
+static double e4m3_block_dot(const uint8_t *a, const uint8_t *b, const double *dec)
+{
+    double s = 0.0;
+    for (int i = 0; i < 128; i++)
+        s += dec[a[i]] * dec[b[i]];
+    return s;
+}
+
+/* out[n] = sum over K blocks kb of (sa[kb] * sb[n/128, kb]) * P_kb(n), where
+ * P_kb is the exact block dot product rounded to binary32 (what an ideal FP8
+ * MMA with an fp32 accumulator yields for one 128-deep block) and the sum
+ * over kb is a binary32 fma chain in ascending kb -- the per-128 "promotion"
+ * of the DeepSeek-V3 recipe.  a: one row [K] of codes, sa: its [K/128]
+ * scales; w: [N, K] codes, sw: [N/128, K/128]. */
+static void fp8_row_gemm(const uint8_t *a, const float *sa, const uint8_t *w, const float *sw,
+                         int64_t N, int64_t K, const double *dec, float *out)
+{
+    int64_t nkb = K / 128;
+    for (int64_t n = 0; n < N; n++) {
+        float acc = 0.0f;
+        for (int64_t kb = 0; kb < nkb; kb++) {
+            float p = (float)e4m3_block_dot(a + kb * 128, w + n * K + kb * 128, dec);
+            float sc = sa[kb] * sw[(n / 128) * nkb + kb];
+            acc = fmaf(sc, p, acc);
+        }
+        out[n] = acc;
+    }
+}
+
+/* The block-scaled GEMM alone: out [M, N] fp32 = A [M, K] (scales [M, K/128])
+ * times W [N, K] (scales [N/128, K/128]) transposed, by fp8_row_gemm. */
+void or_fp8_gemm(const uint8_t *a, const float *sa, int64_t M, const uint8_t *w, const float *sw,
+                 int64_t N, int64_t K, float *out)
+{
+    double dec[256];
+    for (int c = 0; c < 256; c++)
+        dec[c] = or_e4m3_decode((uint8_t)c);
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        fp8_row_gemm(a + m * K, sa + m * (K / 128), w, sw, N, K, dec, out + m * N);
+}
+
+/* SwiGLU expert FFN on n sorted rows.  Row r belongs to expert
+ * row_expert[r], an index into the weight arrays:
+ *   w13_q [*, 2F, d] (rows 0..F-1 gate, F..2F-1 up), w13_s [*, 2F/128, d/128]
+ *   w2_q  [*, d, F],                                 w2_s  [*, d/128, F/128]
+ * h = X W13^T (block-scaled), act = silu(h_gate) * h_up in double rounded to
+ * binary32, act re-quantised 1x128 along F, out = bf16(act_q W2^T).
+ * act_f (nullable) [n, F], act_q [n, F], act_s [n, F/128], out [n, d]. */
+void or_expert_ffn(const uint8_t *xq, const float *xs, int64_t n, const int32_t *row_expert, int d, int F,
+                   const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q, const float *w2_s,
+                   float *act_f, uint8_t *act_q, float *act_s, uint16_t *out)
+{
+    double dec[256];
+    for (int c = 0; c < 256; c++)
+        dec[c] = or_e4m3_decode((uint8_t)c);
+    int64_t nkd = d / 128, nkf = F / 128;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; r++) {
+        int64_t e = row_expert[r];
+        float *h = malloc(sizeof(float) * 2 * (size_t)F);
+        float *o = malloc(sizeof(float) * (size_t)d);
+        float *act = malloc(sizeof(float) * (size_t)F);
+        fp8_row_gemm(xq + r * d, xs + r * nkd, w13_q + e * 2 * F * (int64_t)d,
+                     w13_s + e * (2 * F / 128) * nkd, 2 * F, d, dec, h);
+        for (int64_t c = 0; c < F; c++) {
+            double g = h[c], u = h[F + c];
+            act[c] = (float)((g / (1.0 + exp(-g))) * u);
+        }
+        for (int64_t b = 0; b < nkf; b++) {
+            float amax = 0.0f;
+            for (int i = 0; i < 128; i++)
+                if (fabsf(act[b * 128 + i]) > amax)
+                    amax = fabsf(act[b * 128 + i]);
+            float sc = block_scale(amax);
+            act_s[r * nkf + b] = sc;
+            for (int i = 0; i < 128; i++)
+                act_q[r * F + b * 128 + i] = or_e4m3_encode(act[b * 128 + i] / sc);
+        }
+        if (act_f)
+            memcpy(act_f + r * F, act, sizeof(float) * (size_t)F);
+        fp8_row_gemm(act_q + r * F, act_s + r * nkf, w2_q + e * (int64_t)d * F,
+                     w2_s + e * (d / 128) * nkf, d, F, dec, o);
+        for (int64_t c = 0; c < d; c++)
+            out[r * d + c] = or_f32_to_bf16(o[c]);
+        free(h);
+        free(o);
+        free(act);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* combine                                                              */
+/* ------------------------------------------------------------------ */
+
+/* y[t] = bf16( sum_j g[t,j] * out_sorted[slot_to_sorted[t*k+j]] ), a binary32
+ * fma chain over j in slot order starting at +0; unrouted slots (-1) are
+ * skipped.  out_sorted rows are bf16 [*, d]. */
+void or_combine(const uint16_t *out_sorted, const int32_t *slot_to_sorted, const float *gates,
+                int64_t T, int k, int d, uint16_t *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++)
+        for (int c = 0; c < d; c++) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; j++) {
+                int32_t r = slot_to_sorted[t * k + j];
+                if (r < 0)
+                    continue;
+                acc = fmaf(gates[t * k + j], or_bf16_to_f32(out_sorted[(int64_t)r * d + c]), acc);
+            }
+            y[t * d + c] = or_f32_to_bf16(acc);
+        }
+}
+
+/* Number of OpenMP threads the parallel loops above use (1 without OpenMP). */
+#ifdef _OPENMP
+#include <omp.h>
+int or_num_threads(void) { return omp_get_max_threads(); }
+void or_set_num_threads(int n) { omp_set_num_threads(n); }
+#else
+int or_num_threads(void) { return 1; }
+void or_set_num_threads(int n) { (void)n; }
+#endif

@@ -1,0 +1,258 @@
+"""Python face of the CPU oracle (moe_oracle.c): ctypes marshalling only.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only callers allowed.  The product
+library never imports this module, and this module never imports the
+product.  All arithmetic lives in ``moe_oracle.c``; here arrays are only
+checked for dtype/shape, made contiguous and passed by pointer.
+
+Semantics and citations are in the C file's comments.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_BASE_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into liboracle.so next to it (gcc; OpenMP when the
+    compiler has it).  Returns the library path."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    for extra in (["-fopenmp"], []):
+        cmd = ["gcc", *_BASE_FLAGS, *extra, "-o", tmp, _SRC, "-lm"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode == 0:
+            os.replace(tmp, _LIB)
+            return _LIB
+    raise RuntimeError("oracle build failed:\n" + r.stderr)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            F = ctypes.c_float
+            sig = {
+                "or_bf16_to_f32": (F, [ctypes.c_uint16]),
+                "or_f32_to_bf16": (ctypes.c_uint16, [F]),
+                "or_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
+                "or_e4m3_encode": (ctypes.c_uint8, [F]),
+                "or_quant_1x128": (None, [P, I64, I64, I64, P, P]),
+                "or_quant_128x128": (None, [P, I64, I64, I64, P, P]),
+                "or_router_logits": (None, [P, P, I64, I, I, P]),
+                "or_topk": (None, [P, I64, I, I, P]),
+                "or_gates": (None, [P, P, P, I64, I, I, I, I, F, P]),
+                "or_replay": (I64, [P, I64, I, I, P, P]),
+                "or_dispatch": (I64, [P, I64, I, I, P, P, P, P]),
+                "or_gather_rows": (None, [P, I64, P, I64, I, P]),
+                "or_fp8_gemm": (None, [P, P, I64, P, P, I64, I64, P]),
+                "or_expert_ffn": (None, [P, P, I64, P, I, I, P, P, P, P, P, P, P, P]),
+                "or_combine": (None, [P, P, P, I64, I, I, P]),
+                "or_num_threads": (I, []),
+                "or_set_num_threads": (None, [I]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.dtype(dtype):
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _p(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ---------------------------------------------------------------- scalars
+
+def bf16_to_f32(h: int) -> float:
+    return _load().or_bf16_to_f32(h)
+
+
+def f32_to_bf16(f: float) -> int:
+    return _load().or_f32_to_bf16(f)
+
+
+def e4m3_decode(c: int) -> float:
+    return _load().or_e4m3_decode(c)
+
+
+def e4m3_encode(v: float) -> int:
+    return _load().or_e4m3_encode(v)
+
+
+def num_threads() -> int:
+    return _load().or_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().or_set_num_threads(n)
+
+
+# ---------------------------------------------------------------- tensors
+# bf16 tensors travel as np.uint16 bit patterns, e4m3 as np.uint8 codes.
+
+def quant_1x128(x_bf16: np.ndarray):
+    """[rows, cols] bf16 bits -> (codes uint8 [rows, cols], scales f32 [rows, cols/128])."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    assert cols % 128 == 0
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows, cols // 128), np.float32)
+    _load().or_quant_1x128(_p(x), rows, cols, cols, _p(q), _p(s))
+    return q, s
+
+
+def quant_128x128(w_bf16: np.ndarray):
+    """[rows, cols] bf16 bits -> (codes [rows, cols], scales [rows/128, cols/128])."""
+    w = _c(w_bf16, np.uint16)
+    rows, cols = w.shape
+    assert rows % 128 == 0 and cols % 128 == 0
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows // 128, cols // 128), np.float32)
+    _load().or_quant_128x128(_p(w), rows, cols, cols, _p(q), _p(s))
+    return q, s
+
+
+def router_logits(x_bf16: np.ndarray, wr_bf16: np.ndarray) -> np.ndarray:
+    x = _c(x_bf16, np.uint16)
+    wr = _c(wr_bf16, np.uint16)
+    T, d = x.shape
+    E, d2 = wr.shape
+    assert d == d2
+    out = np.empty((T, E), np.float32)
+    _load().or_router_logits(_p(x), _p(wr), T, d, E, _p(out))
+    return out
+
+
+def topk(logits: np.ndarray, k: int) -> np.ndarray:
+    l = _c(logits, np.float32)
+    T, E = l.shape
+    assert 1 <= k <= E
+    ids = np.empty((T, k), np.int32)
+    _load().or_topk(_p(l), T, E, k, _p(ids))
+    return ids
+
+
+def gates(logits: np.ndarray, ids: np.ndarray, score_fn: int, renorm: int = 1,
+          route_scale: float = 1.0, valid: np.ndarray | None = None) -> np.ndarray:
+    l = _c(logits, np.float32)
+    ids = _c(ids, np.int32)
+    T, E = l.shape
+    k = ids.shape[1]
+    assert k <= 64
+    v = None if valid is None else _c(valid, np.uint8)
+    g = np.empty((T, k), np.float32)
+    _load().or_gates(_p(l), _p(ids), _p(v), T, E, k, score_fn, renorm, route_scale, _p(g))
+    return g
+
+
+def replay(payload_kT: np.ndarray, E: int):
+    """[k, T] int32 layer slice -> (ids [T, k], valid uint8 [T], n_invalid)."""
+    p = _c(payload_kT, np.int32)
+    k, T = p.shape
+    ids = np.empty((T, k), np.int32)
+    valid = np.empty((T,), np.uint8)
+    bad = _load().or_replay(_p(p), T, E, k, _p(ids), _p(valid))
+    return ids, valid, int(bad)
+
+
+def dispatch(ids: np.ndarray, E: int):
+    """[T, k] ids -> (counts [E], offsets [E+1], sorted_to_slot [A], slot_to_sorted [A], dropped)."""
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    A = T * k
+    counts = np.empty((E,), np.int32)
+    offsets = np.empty((E + 1,), np.int32)
+    s2s = np.empty((A,), np.int32)
+    sl2 = np.empty((A,), np.int32)
+    dropped = _load().or_dispatch(_p(ids), T, k, E, _p(counts), _p(offsets), _p(s2s), _p(sl2))
+    return counts, offsets, s2s, sl2, int(dropped)
+
+
+def gather_rows(rows: np.ndarray, sorted_to_slot: np.ndarray, n_sorted: int, k: int) -> np.ndarray:
+    """Rows of any dtype [T, ...] -> rows_sorted [n_sorted, ...]."""
+    r = np.ascontiguousarray(rows)
+    s2s = _c(sorted_to_slot, np.int32)
+    row_bytes = r.strides[0] if r.ndim > 1 else r.itemsize
+    out = np.empty((n_sorted,) + r.shape[1:], r.dtype)
+    _load().or_gather_rows(_p(r), row_bytes, _p(s2s), n_sorted, k, _p(out))
+    return out
+
+
+def fp8_gemm(a_q: np.ndarray, a_s: np.ndarray, w_q: np.ndarray, w_s: np.ndarray) -> np.ndarray:
+    """Block-scaled GEMM: A [M,K] codes + [M,K/128] scales, W [N,K] codes +
+    [N/128,K/128] scales -> fp32 [M,N]."""
+    a_q = _c(a_q, np.uint8)
+    a_s = _c(a_s, np.float32)
+    w_q = _c(w_q, np.uint8)
+    w_s = _c(w_s, np.float32)
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    assert w_q.shape == (N, K) and a_s.shape == (M, K // 128) and w_s.shape == (N // 128, K // 128)
+    out = np.empty((M, N), np.float32)
+    _load().or_fp8_gemm(_p(a_q), _p(a_s), M, _p(w_q), _p(w_s), N, K, _p(out))
+    return out
+
+
+def expert_ffn(xq: np.ndarray, xs: np.ndarray, row_expert: np.ndarray,
+               w13_q: np.ndarray, w13_s: np.ndarray, w2_q: np.ndarray, w2_s: np.ndarray):
+    """SwiGLU FFN on sorted rows.  Returns (act_f [n,F] f32, act_q [n,F], act_s [n,F/128], out bf16 [n,d])."""
+    xq = _c(xq, np.uint8)
+    xs = _c(xs, np.float32)
+    re = _c(row_expert, np.int32)
+    w13_q = _c(w13_q, np.uint8)
+    w13_s = _c(w13_s, np.float32)
+    w2_q = _c(w2_q, np.uint8)
+    w2_s = _c(w2_s, np.float32)
+    n, d = xq.shape
+    Ew, twoF, d2 = w13_q.shape
+    F = twoF // 2
+    assert d2 == d and w2_q.shape == (Ew, d, F)
+    assert w13_s.shape == (Ew, twoF // 128, d // 128) and w2_s.shape == (Ew, d // 128, F // 128)
+    assert xs.shape == (n, d // 128) and re.shape == (n,)
+    if n:
+        assert re.min() >= 0 and re.max() < Ew
+    act_f = np.empty((n, F), np.float32)
+    act_q = np.empty((n, F), np.uint8)
+    act_s = np.empty((n, F // 128), np.float32)
+    out = np.empty((n, d), np.uint16)
+    _load().or_expert_ffn(_p(xq), _p(xs), n, _p(re), d, F, _p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s),
+                          _p(act_f), _p(act_q), _p(act_s), _p(out))
+    return act_f, act_q, act_s, out
+
+
+def combine(out_sorted: np.ndarray, slot_to_sorted: np.ndarray, gates_: np.ndarray) -> np.ndarray:
+    o = _c(out_sorted, np.uint16)
+    sl2 = _c(slot_to_sorted, np.int32)
+    g = _c(gates_, np.float32)
+    T, k = g.shape
+    d = o.shape[1]
+    y = np.empty((T, d), np.uint16)
+    _load().or_combine(_p(o), _p(sl2), _p(g), T, k, d, _p(y))
+    return y
