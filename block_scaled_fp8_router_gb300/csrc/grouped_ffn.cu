@@ -1,0 +1,566 @@
+// grouped_ffn.cu -- per-expert SwiGLU FFN as two grouped block-scaled FP8
+// GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Block-scaled FP8 of the DeepSeek-V3 recipe, which the prime-rl post ("RL at
+// 1T Scale: prime-rl Performance Deep Dive", section "FP8 training") trains
+// with: E4M3 operands, one fp32 scale per 1x128 activation tile and per
+// 128x128 weight block.  The scales are arbitrary fp32 (not powers of two),
+// so the hardware block-scaled MMA kinds do not apply; instead every
+// 128-deep K block is one MMA group whose fp32 partial is read back from
+// tensor memory and promoted into an fp32 register accumulator with the
+// product of the two scales:
+//     acc[r, n] = fma(sa[r, kb] * sb[n/128, kb], P_kb[r, n], acc[r, n]).
+//
+// Kernel shape (one persistent CTA per SM, 576 threads):
+//   warps 0-15  epilogue: warp w reads TMEM lane quadrant w % 4 (32 rows),
+//               column group w / 4 (64 of the 256 accumulator columns);
+//               promotion per K block, then the tile epilogue
+//   warp 16     TMA producer: A tile 128 x 128 B and B tile 256 x 128 B per
+//               K block into a 4-stage shared-memory ring (128-byte swizzle)
+//   warp 17     MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=32, E4M3 x E4M3
+//               -> fp32) per K block into one of two 256-column TMEM
+//               buffers, so the epilogue reads block kb while block kb+1
+//               accumulates.
+// Tiles are (expert, N block, M block) with M fastest, read from the device
+// expert offsets (no host sync), so the CTAs working on the same weight tile
+// at the same time share it through L2.
+//   GEMM1: A = x_sorted [rows, d], B = W13[e] (gate rows n, up rows F + n);
+//          one tile = 128 rows x (128 gate + 128 up) columns; the epilogue
+//          forms silu(gate) * up for 128 act columns = one 1x128 block and
+//          requantises it to E4M3 with its fp32 scale.
+//   GEMM2: A = act_q [rows, F], B = W2[e] [d, F]; one tile = 128 x 256
+//          output columns, stored as bf16.
+// Every mbarrier wait is bounded; on expiry the CTA flags MOE_DEV_TIMEOUT,
+// drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace ffn {
+
+constexpr int BM = 128;                 // rows per tile (MMA M)
+constexpr int BN = 256;                 // accumulator columns per tile (MMA N)
+constexpr int BK = 128;                 // K block = one scale block (bytes of E4M3)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;        // 16 KB
+constexpr int B_BYTES = BN * BK;        // 32 KB
+constexpr int EPI_WARPS = 16;
+constexpr int PRODUCER_WARP = 16;
+constexpr int MMA_WARP = 17;
+constexpr int THREADS = 18 * 32;
+constexpr int TMEM_COLS = 512;          // two 256-column fp32 buffers
+constexpr int MAX_E = 1024;
+constexpr uint64_t TIMEOUT_NS = 1000ull * 1000ull * 1000ull;
+
+struct Smem {
+    uint8_t a[STAGES][A_BYTES];
+    uint8_t b[STAGES][B_BYTES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    float red[4][BM];                   // GEMM1: per-column-group partial amax
+    int32_t tile_prefix[MAX_E + 1];     // tiles before expert e
+    int32_t row_lo[MAX_E + 1];          // clipped expert row ranges
+};
+constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + alignment slack
+
+struct Params {
+    const float *a_scales;      // [max_rows, K/128]
+    const float *b_scales;      // GEMM1 [E, 2F/128, d/128]; GEMM2 [E, d/128, F/128]
+    const int32_t *offsets;     // [E+1]
+    uint8_t *act_q;             // GEMM1 out [max_rows, F]
+    float *act_s;               // GEMM1 out [max_rows, F/128]
+    uint16_t *out;              // GEMM2 out [max_rows, d] bf16
+    int32_t *dev_status;
+    int64_t max_rows;
+    int E, d, F;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 x E4M3 -> fp32, shapes in idesc
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// arrive once on `bar` when every tcgen05 operation this thread issued so far completes
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 TMEM lanes x 16 consecutive 32-bit columns; thread i gets lane base+i
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// barrier over the 16 epilogue warps that also ORs a predicate across them
+__device__ __forceinline__ bool epi_bar_or(bool pred)
+{
+    uint32_t out;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "barrier.cta.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(out)
+                 : "r"((uint32_t)pred), "n"(EPI_WARPS * 32)
+                 : "memory");
+    return out != 0;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("barrier.cta.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory"); }
+
+// K-major operand tile in shared memory written by TMA with 128-byte
+// swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked along
+// M/N.  Descriptor: start address >> 4, leading offset (unused for this
+// layout) 16 B, stride offset 1024 B between 8-row groups, fixed version
+// bits 0b001 at 46, swizzle mode 2 (128 B) at 61.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t desc = 0;
+    desc |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    desc |= (uint64_t)(16u >> 4) << 16;
+    desc |= (uint64_t)(1024u >> 4) << 32;
+    desc |= (uint64_t)1 << 46;
+    desc |= (uint64_t)2 << 61;
+    return desc;
+}
+
+// instruction descriptor: fp32 accumulate, A = B = E4M3, both K-major, N, M
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N)
+{
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *dev_status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 32; i++)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > TIMEOUT_NS) {
+            *abort_flag = 1;
+            dev_flag(dev_status, MOE_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ tiles
+
+struct Tile {
+    int e, m_blk, n_blk;
+    int row0;       // first sorted row
+    int rows;       // valid rows in this tile (1..128)
+};
+
+__device__ __forceinline__ Tile decode_tile(const Smem &s, int E, int n_tiles, int t)
+{
+    int lo = 0, hi = E;  // largest e with tile_prefix[e] <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s.tile_prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    Tile tl;
+    tl.e = lo;
+    const int rows_e = s.row_lo[lo + 1] - s.row_lo[lo];
+    const int m_tiles = (rows_e + BM - 1) / BM;
+    const int local = t - s.tile_prefix[lo];
+    tl.n_blk = local / m_tiles;
+    tl.m_blk = local - tl.n_blk * m_tiles;
+    tl.row0 = s.row_lo[lo] + tl.m_blk * BM;
+    tl.rows = min(BM, rows_e - tl.m_blk * BM);
+    return tl;
+}
+
+// per-CTA tile table from the device offsets, by warp 0
+__device__ void build_schedule(Smem &s, const Params &p, int n_tiles)
+{
+    const int lane = threadIdx.x & 31;
+    int32_t carry = 0;
+    bool clipped = false;
+    for (int base = 0; base <= p.E; base += 32) {
+        const int e = base + lane;
+        int32_t lo = 0, hi = 0;
+        if (e <= p.E) {
+            lo = __ldg(p.offsets + e);
+            if ((int64_t)lo > p.max_rows) { lo = (int32_t)p.max_rows; clipped = true; }
+            s.row_lo[e] = lo;
+        }
+        if (e < p.E) {
+            hi = __ldg(p.offsets + e + 1);
+            if ((int64_t)hi > p.max_rows) hi = (int32_t)p.max_rows;
+        }
+        const int32_t tiles = (e < p.E && hi > lo) ? ((hi - lo + BM - 1) / BM) * n_tiles : 0;
+        int32_t incl = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (e <= p.E) s.tile_prefix[e] = carry + incl - tiles;
+        carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (__any_sync(0xFFFFFFFFu, clipped) && lane == 0 && blockIdx.x == 0) dev_flag(p.dev_status, MOE_DEV_ROWS);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                        const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // K extent and N tiling of this GEMM
+    const int K = MODE == 1 ? p.d : p.F;
+    const int nkb = K / BK;
+    const int n_tiles = MODE == 1 ? p.F / 128 : (p.d + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; i++) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&s.tfull[i], 1);
+            mbar_init(&s.tempty[i], EPI_WARPS);
+        }
+        mbar_init(&s.mma_done, 1);
+        s.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) build_schedule(s, p, n_tiles);
+    if (warp == MMA_WARP) tmem_alloc(&s.tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+    const int total = s.tile_prefix[p.E];
+    volatile int *abort_flag = &s.abort_flag;
+
+    if (warp == PRODUCER_WARP) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint32_t j = 0;
+            uint32_t issued = 0;  // per-stage "has an outstanding load" bits
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const Tile tl = decode_tile(s, p.E, n_tiles, t);
+                for (int kb = 0; kb < nkb; kb++, j++) {
+                    const int st = j % STAGES;
+                    if (!wait_or_abort(&s.empty[st], ((j / STAGES) & 1) ^ 1, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+                    tma_load_2d(s.a[st], &tm_a, kb * BK, tl.row0, &s.full[st]);
+                    if (MODE == 1) {
+                        const int wrow = tl.e * 2 * p.F + tl.n_blk * 128;
+                        tma_load_2d(s.b[st], &tm_b, kb * BK, wrow, &s.full[st]);
+                        tma_load_2d(s.b[st] + B_BYTES / 2, &tm_b, kb * BK, wrow + p.F, &s.full[st]);
+                    } else {
+                        tma_load_2d(s.b[st], &tm_b, kb * BK, tl.e * p.d + tl.n_blk * BN, &s.full[st]);
+                    }
+                    issued |= 1u << st;
+                }
+            }
+            // drain: wait for the last load issued into every stage
+            for (int i = 0; i < STAGES; i++) {
+                if (!(issued & (1u << i)) || j == 0) continue;
+                // last use of stage i was at the largest j' < j with j' % STAGES == i
+                const uint32_t last = j - 1 - ((j - 1 - i) % STAGES);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&s.full[i], (last / STAGES) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_f8(BM, BN);
+            uint32_t j = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; kb++, j++) {
+                    const int st = j % STAGES;
+                    const int buf = j & 1;
+                    if (!wait_or_abort(&s.tempty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.dev_status) ||
+                        !wait_or_abort(&s.full[st], (j / STAGES) & 1, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(smem_u32(s.a[st]));
+                    const uint64_t bdesc = sw128_desc(smem_u32(s.b[st]));
+#pragma unroll
+                    for (int ks = 0; ks < BK / 32; ks++)  // K = 32 bytes per MMA: +2 in the >>4 address field
+                        mma_f8(tmem + buf * BN, adesc + 2 * ks, bdesc + 2 * ks, IDESC, ks > 0);
+                    mma_commit(&s.empty[st]);
+                    mma_commit(&s.tfull[buf]);
+                }
+            }
+            mma_commit(&s.mma_done);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&s.mma_done, 0) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 0..15) ----------------
+        const int q = warp & 3;        // TMEM lane quadrant = rows 32q .. 32q+31
+        const int cg = warp >> 2;      // column group 0..3
+        const int r_in = q * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        const int nkb_a = K / 128;     // A scale row length
+        uint32_t j = 0;
+        bool aborted = false;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile tl = decode_tile(s, p.E, n_tiles, t);
+            const bool row_ok = r_in < tl.rows;
+            const int64_t row = (int64_t)tl.row0 + r_in;
+            // accumulator columns of this thread: two 32-wide halves (GEMM1:
+            // gate 32cg.., up 128+32cg..) or one 64-wide run (GEMM2: 64cg..)
+            const int col0 = MODE == 1 ? 32 * cg : 64 * cg;
+            const int col1 = MODE == 1 ? 128 + 32 * cg : 64 * cg + 32;
+            // weight-scale rows (128-column blocks) of the two halves
+            const int64_t nb0 = MODE == 1 ? (int64_t)tl.e * (2 * p.F / 128) + tl.n_blk
+                                          : (int64_t)tl.e * (p.d / 128) + tl.n_blk * 2 + (cg >> 1);
+            const int64_t nb1 = MODE == 1 ? nb0 + p.F / 128 : nb0;
+            const bool nb_ok = MODE == 1 || (tl.n_blk * 2 + (cg >> 1)) < p.d / 128;
+            float acc0[32], acc1[32];
+#pragma unroll
+            for (int i = 0; i < 32; i++) acc0[i] = acc1[i] = 0.0f;
+            float sa_next = row_ok ? __ldg(p.a_scales + row * nkb_a) : 0.0f;
+            for (int kb = 0; kb < nkb; kb++, j++) {
+                const int buf = j & 1;
+                const float sa = sa_next;
+                if (kb + 1 < nkb) sa_next = row_ok ? __ldg(p.a_scales + row * nkb_a + kb + 1) : 0.0f;
+                const float sb0 = nb_ok ? __ldg(p.b_scales + nb0 * nkb + kb) : 0.0f;
+                const float sb1 = nb_ok ? __ldg(p.b_scales + nb1 * nkb + kb) : 0.0f;
+                const float c0 = sa * sb0, c1 = sa * sb1;
+                if (!aborted && !wait_or_abort(&s.tfull[buf], (j >> 1) & 1, abort_flag, p.dev_status))
+                    aborted = true;
+                if (!aborted) {
+                    tc_fence_after();
+                    const uint32_t base = tmem + lane_addr + buf * BN;
+                    float v[16];
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        tmem_ld16(base + col0 + 16 * h, v);
+#pragma unroll
+                        for (int i = 0; i < 16; i++) acc0[16 * h + i] = fmaf(c0, v[i], acc0[16 * h + i]);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        tmem_ld16(base + col1 + 16 * h, v);
+#pragma unroll
+                        for (int i = 0; i < 16; i++) acc1[16 * h + i] = fmaf(c1, v[i], acc1[16 * h + i]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.tempty[buf]);
+                }
+            }
+            if (MODE == 1) {
+                // act = silu(gate) * up for 32 of the tile's 128 act columns
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    const float g = acc0[i];
+                    acc0[i] = __fdiv_rn(g, 1.0f + expf(-g)) * acc1[i];
+                    amax = fmaxf(amax, fabsf(acc0[i]));
+                }
+                s.red[cg][r_in] = amax;
+                epi_bar();
+                amax = fmaxf(fmaxf(s.red[0][r_in], s.red[1][r_in]), fmaxf(s.red[2][r_in], s.red[3][r_in]));
+                const float sc = block_scale(amax);
+                if (row_ok && !aborted) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++)
+                        w[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i], sc), __fdiv_rn(acc0[4 * i + 1], sc)) |
+                               ((uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sc),
+                                                      __fdiv_rn(acc0[4 * i + 3], sc))
+                                << 16);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.act_q + row * p.F + tl.n_blk * 128 + 32 * cg);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    if (cg == 0) p.act_s[row * (p.F / 128) + tl.n_blk] = sc;
+                }
+            } else {
+                const int c_glob = tl.n_blk * BN + 64 * cg;
+                if (row_ok && !aborted && c_glob < p.d) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * p.d + c_glob);
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        dst[i] = make_uint4(pack_bf16x2(acc0[8 * i], acc0[8 * i + 1]),
+                                            pack_bf16x2(acc0[8 * i + 2], acc0[8 * i + 3]),
+                                            pack_bf16x2(acc0[8 * i + 4], acc0[8 * i + 5]),
+                                            pack_bf16x2(acc0[8 * i + 6], acc0[8 * i + 7]));
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        dst[4 + i] = make_uint4(pack_bf16x2(acc1[8 * i], acc1[8 * i + 1]),
+                                                pack_bf16x2(acc1[8 * i + 2], acc1[8 * i + 3]),
+                                                pack_bf16x2(acc1[8 * i + 4], acc1[8 * i + 5]),
+                                                pack_bf16x2(acc1[8 * i + 6], acc1[8 * i + 7]));
+                }
+            }
+            // uniform decision across the epilogue warps (also separates the
+            // red[] reads of this tile from the writes of the next)
+            if (epi_bar_or(aborted || *abort_flag)) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+// 2-D uint8 tensor [rows, cols] (row stride = cols bytes), box box_rows x 128 B, 128-byte swizzle
+static bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *base, uint64_t cols,
+                     uint64_t rows, uint32_t box_rows)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+} // namespace ffn
+} // namespace moe
+
+using namespace moe;
+using namespace moe::ffn;
+
+MOE_API size_t moe_grouped_ffn_workspace_size(int64_t max_rows, int d, int F)
+{
+    (void)d;
+    if (max_rows < 0 || F <= 0) return 0;
+    return align256((size_t)max_rows * F) + align256((size_t)max_rows * (F / 128) * sizeof(float));
+}
+
+MOE_API moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs_sorted,
+                                       const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                                       const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q,
+                                       const float *w2_s, uint16_t *out_sorted, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    if (max_rows < 0 || max_rows >= (1LL << 31) || E < 1 || E > MAX_E || d <= 0 || F <= 0 || d % 128 != 0 ||
+        F % 128 != 0)
+        return MOE_ERR_SHAPE;
+    if ((int64_t)E * 2 * F >= (1LL << 31) || (int64_t)E * d >= (1LL << 31)) return MOE_ERR_SHAPE;
+    const size_t need = moe_grouped_ffn_workspace_size(max_rows, d, F);
+    if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    if (max_rows == 0) return MOE_OK;
+    if (!xq_sorted || !xs_sorted || !expert_offsets || !w13_q || !w13_s || !w2_q || !w2_s || !out_sorted)
+        return MOE_ERR_NULL;
+    if (!aligned16(xq_sorted) || !aligned16(w13_q) || !aligned16(w2_q) || !aligned16(out_sorted) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return MOE_ERR_ALIGN;
+    auto enc = encode_fn();
+    if (!enc) return MOE_ERR_CUDA;
+    uint8_t *act_q = reinterpret_cast<uint8_t *>(workspace);
+    float *act_s = reinterpret_cast<float *>(reinterpret_cast<char *>(workspace) + align256((size_t)max_rows * F));
+    CUtensorMap ma1, mb1, ma2, mb2;
+    if (!make_map(enc, &ma1, xq_sorted, d, max_rows, 128) || !make_map(enc, &mb1, w13_q, d, (uint64_t)E * 2 * F, 128) ||
+        !make_map(enc, &ma2, act_q, F, max_rows, 128) || !make_map(enc, &mb2, w2_q, F, (uint64_t)E * d, 256))
+        return MOE_ERR_CUDA;
+    Params prm;
+    prm.b_scales = nullptr;
+    prm.offsets = expert_offsets;
+    prm.act_q = act_q;
+    prm.act_s = act_s;
+    prm.out = out_sorted;
+    prm.dev_status = dev_status;
+    prm.max_rows = max_rows;
+    prm.E = E;
+    prm.d = d;
+    prm.F = F;
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int grid = sm_count();
+    cudaStream_t st = as_stream(stream);
+    Params p1 = prm;
+    p1.a_scales = xs_sorted;
+    p1.b_scales = w13_s;
+    grouped_gemm_kernel<1><<<grid, THREADS, SMEM_BYTES, st>>>(ma1, mb1, p1);
+    Params p2 = prm;
+    p2.a_scales = act_s;
+    p2.b_scales = w2_s;
+    grouped_gemm_kernel<2><<<grid, THREADS, SMEM_BYTES, st>>>(ma2, mb2, p2);
+    return launch_status();
+}

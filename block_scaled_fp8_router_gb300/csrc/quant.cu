@@ -1,0 +1,121 @@
+// quant.cu -- fused amax / scale / E4M3 block quantiser.
+//
+// Block-scaled FP8 as in the DeepSeek-V3 recipe that the prime-rl post
+// ("RL at 1T Scale", section "FP8 training") trains with: one fp32 scale per
+// 1x128 activation tile or 128x128 weight block, s = amax / 448, codes =
+// E4M3(v / s) rounded to nearest even and saturated.
+//
+// HBM-bound: 2 bytes read and 1 + 4/128 (1x128) or 1 + 4/16384 (128x128)
+// bytes written per element.  Each 16-byte load carries 8 bf16; a 1x128 block
+// is 16 lanes of one half-warp (amax by 4 shuffles), a 128x128 block is one
+// 256-thread CTA holding its 64 values per thread in registers between the
+// amax pass and the encode pass (the block is read from HBM once).
+#include "common.cuh"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t *__restrict__ src, int64_t rows,
+                                                          int64_t cols, int64_t ld, uint8_t *__restrict__ q,
+                                                          float *__restrict__ scales)
+{
+    const int64_t nbc = cols >> 7;
+    const int64_t nblocks = rows * nbc;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & 15;
+    const unsigned half_mask = 0xFFFFu << (lane & 16);
+    int64_t b = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 4;
+    const int64_t step = ((int64_t)gridDim.x * blockDim.x) >> 4;
+    for (; b < nblocks; b += step) {
+        const int64_t r = b / nbc, cb = b - r * nbc;
+        const uint4 raw = __ldcs(reinterpret_cast<const uint4 *>(src + r * ld + cb * 128 + sub * 8));
+        float v[8];
+        unpack_bf16x8(raw, v);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o, 16));
+        const float s = block_scale(amax);
+        uint2 out;
+        out.x = (uint32_t)pack_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
+                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
+        out.y = (uint32_t)pack_e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) |
+                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
+        *reinterpret_cast<uint2 *>(q + r * cols + cb * 128 + sub * 8) = out;
+        if (sub == 0) scales[b] = s;
+    }
+}
+
+__global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t *__restrict__ src, int64_t cols,
+                                                            int64_t ld, uint8_t *__restrict__ q,
+                                                            float *__restrict__ scales)
+{
+    __shared__ float warp_amax[8];
+    const int64_t nbc = cols >> 7;
+    const int64_t b = blockIdx.x;
+    const int64_t br = b / nbc, bc = b - br * nbc;
+    const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+    uint4 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int64_t r = br * 128 + tr + 16 * i;
+        raw[i] = __ldcs(reinterpret_cast<const uint4 *>(src + r * ld + bc * 128 + tc * 8));
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        float v[8];
+        unpack_bf16x8(raw[i], v);
+#pragma unroll
+        for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(v[j]));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((tid & 31) == 0) warp_amax[tid >> 5] = amax;
+    __syncthreads();
+    amax = warp_amax[0];
+#pragma unroll
+    for (int w = 1; w < 8; w++) amax = fmaxf(amax, warp_amax[w]);
+    const float s = block_scale(amax);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        float v[8];
+        unpack_bf16x8(raw[i], v);
+        uint2 out;
+        out.x = (uint32_t)pack_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
+                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
+        out.y = (uint32_t)pack_e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) |
+                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
+        const int64_t r = br * 128 + tr + 16 * i;
+        *reinterpret_cast<uint2 *>(q + r * cols + bc * 128 + tc * 8) = out;
+    }
+    if (tid == 0) scales[b] = s;
+}
+
+} // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status fp8_block_quant(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
+                                   int block_rows, uint8_t *q, float *scales, void *stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 128 != 0 || ld_src < cols) return MOE_ERR_SHAPE;
+    if (block_rows != 1 && block_rows != 128) return MOE_ERR_SHAPE;
+    if (block_rows == 128 && rows % 128 != 0) return MOE_ERR_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!src || !q || !scales) return MOE_ERR_NULL;
+    if (!aligned16(src) || !aligned16(q) || (ld_src * 2) % 16 != 0) return MOE_ERR_ALIGN;
+    cudaStream_t st = as_stream(stream);
+    if (block_rows == 1) {
+        const int64_t nblocks = rows * (cols / 128);
+        int64_t grid = (nblocks + 15) / 16;
+        const int64_t cap = (int64_t)sm_count() * 16;
+        if (grid > cap) grid = cap;
+        quant_1x128_kernel<<<(unsigned)grid, 256, 0, st>>>(src, rows, cols, ld_src, q, scales);
+    } else {
+        const int64_t nblocks = (rows / 128) * (cols / 128);
+        if (nblocks > 0x7FFFFFFFLL) return MOE_ERR_SHAPE;
+        quant_128x128_kernel<<<(unsigned)nblocks, 256, 0, st>>>(src, cols, ld_src, q, scales);
+    }
+    return launch_status();
+}

@@ -1,0 +1,113 @@
+"""The MoE layer with router replay as one sequence of libmoe_r3 calls.
+
+Sequencing and buffer ownership only: every step is a library kernel.
+Buffers are allocated once for a maximum token count and reused, so a
+forward pass launches kernels and nothing else (no host sync, no
+allocation).  The step order follows the layer of the prime-rl post
+("Router replay", "FP8 training"): route or replay -> quantise x (1x128) ->
+dispatch -> grouped FP8 SwiGLU FFN -> combine.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import moe_r3 as L
+
+
+@dataclass
+class MoEWeightsFP8:
+    w_router: torch.Tensor   # [E, d] bf16
+    w13_q: torch.Tensor      # [E, 2F, d] e4m3 codes (rows 0..F-1 gate, F..2F-1 up)
+    w13_s: torch.Tensor      # [E, 2F/128, d/128] fp32
+    w2_q: torch.Tensor       # [E, d, F] e4m3 codes
+    w2_s: torch.Tensor       # [E, d/128, F/128] fp32
+
+    @property
+    def E(self) -> int:
+        return self.w13_q.shape[0]
+
+    @property
+    def d(self) -> int:
+        return self.w13_q.shape[2]
+
+    @property
+    def F(self) -> int:
+        return self.w13_q.shape[1] // 2
+
+
+def quantize_weights(w13: torch.Tensor, w2: torch.Tensor, out: MoEWeightsFP8 | None = None, e0: int = 0):
+    """128x128 block quantisation of bf16 expert weights (once per weight
+    update).  w13 [n, 2F, d], w2 [n, d, F] -> codes and scales; with `out`,
+    writes experts e0 .. e0+n-1 of it in place."""
+    n, twoF, d = w13.shape
+    F = twoF // 2
+    if out is None:
+        w13_q, w13_s = L.fp8_block_quant(w13.reshape(n * twoF, d), 128)
+        w2_q, w2_s = L.fp8_block_quant(w2.reshape(n * d, F), 128)
+        return (w13_q.view(n, twoF, d), w13_s.view(n, twoF // 128, d // 128),
+                w2_q.view(n, d, F), w2_s.view(n, d // 128, F // 128))
+    L.fp8_block_quant(w13.reshape(n * twoF, d), 128, q=out.w13_q[e0:e0 + n].view(n * twoF, d),
+                      scales=out.w13_s[e0:e0 + n].view(n * twoF // 128, d // 128))
+    L.fp8_block_quant(w2.reshape(n * d, F), 128, q=out.w2_q[e0:e0 + n].view(n * d, F),
+                      scales=out.w2_s[e0:e0 + n].view(n * d // 128, F // 128))
+    return out
+
+
+class MoELayerFP8:
+    """Forward of one MoE layer on one GPU with preallocated buffers."""
+
+    def __init__(self, weights: MoEWeightsFP8, T_max: int, k: int, score_fn: int, renorm: int = 1,
+                 route_scale: float = 1.0, device=None):
+        self.w = weights
+        self.k, self.score_fn, self.renorm, self.route_scale = k, score_fn, renorm, route_scale
+        dev = weights.w13_q.device if device is None else device
+        E, d, F = weights.E, weights.d, weights.F
+        A = T_max * k
+        self.T_max = T_max
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+        self.ids = e((T_max, k), torch.int32)
+        self.gates = e((T_max, k), torch.float32)
+        self.xq = e((T_max, d), torch.uint8)
+        self.xs = e((T_max, d // 128), torch.float32)
+        self.counts = e((E,), torch.int32)
+        self.offsets = e((E + 1,), torch.int32)
+        self.s2s = e((A,), torch.int32)
+        self.sl2 = e((A,), torch.int32)
+        self.xq_sorted = e((A, d), torch.uint8)
+        self.xs_sorted = e((A, d // 128), torch.float32)
+        self.out_sorted = e((A, d), torch.bfloat16)
+        self.y = e((T_max, d), torch.bfloat16)
+        self.dsp_ws = e((L.moe_dispatch_workspace_size(T_max, k, E),), torch.uint8)
+        self.ffn_ws = e((L.moe_grouped_ffn_workspace_size(A, d, F),), torch.uint8)
+        self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def route(self, x: torch.Tensor, replay_kT: torch.Tensor | None = None, capture_kT: torch.Tensor | None = None):
+        T = x.shape[0]
+        ids, gates = self.ids[:T], self.gates[:T]
+        if replay_kT is None:
+            L.moe_route_topk(x, self.w.w_router, self.k, self.score_fn, self.renorm, self.route_scale,
+                             topk_ids=ids, topk_gates=gates, capture_kT=capture_kT)
+        else:
+            L.moe_route_replay(replay_kT, self.w.E, x, self.w.w_router, self.score_fn, self.renorm,
+                               self.route_scale, topk_ids=ids, topk_gates=gates, dev_status=self.dev_status)
+        return ids, gates
+
+    def forward(self, x: torch.Tensor, replay_kT: torch.Tensor | None = None,
+                capture_kT: torch.Tensor | None = None, y: torch.Tensor | None = None) -> torch.Tensor:
+        T = x.shape[0]
+        if T > self.T_max:
+            raise ValueError(f"T={T} exceeds T_max={self.T_max}")
+        A = T * self.k
+        ids, gates = self.route(x, replay_kT, capture_kT)
+        xq, xs = L.fp8_block_quant(x, 1, q=self.xq[:T], scales=self.xs[:T])
+        L.moe_dispatch(ids, self.w.E, rows=xq, row_scales=xs, expert_counts=self.counts,
+                       expert_offsets=self.offsets, sorted_to_slot=self.s2s[:A], slot_to_sorted=self.sl2[:A],
+                       rows_sorted=self.xq_sorted[:A], scales_sorted=self.xs_sorted[:A], workspace=self.dsp_ws,
+                       dev_status=self.dev_status)
+        L.moe_grouped_ffn_fp8(self.xq_sorted[:A], self.xs_sorted[:A], self.offsets, self.w.w13_q, self.w.w13_s,
+                              self.w.w2_q, self.w.w2_s, out_sorted=self.out_sorted[:A], workspace=self.ffn_ws,
+                              dev_status=self.dev_status)
+        y = self.y[:T] if y is None else y
+        return L.moe_combine(self.out_sorted[:A], self.sl2[:A], gates, y=y)

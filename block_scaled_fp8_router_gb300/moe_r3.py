@@ -1,0 +1,258 @@
+"""Python binding of libmoe_r3 (argument marshalling only).
+
+Every function has the name of the C entry point it calls (include/moe_r3.h)
+and takes torch CUDA tensors: it checks dtypes and shapes, allocates outputs
+the caller did not pass, and hands raw device pointers plus the current CUDA
+stream to the library.  All arithmetic runs in the library's kernels; there is
+no fallback: if libmoe_r3.so is missing or fails to load, this module raises
+on import.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libmoe_r3.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libmoe_r3.so is not built ({_LIB_PATH}); run __graft_entry__.build() first")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+P = ctypes.c_void_p
+I = ctypes.c_int
+I64 = ctypes.c_int64
+F = ctypes.c_float
+SZ = ctypes.c_size_t
+
+_SIGS = {
+    "moe_status_str": (ctypes.c_char_p, [I]),
+    "moe_route_topk": (I, [P, P, I, I, I, I, I, I, F, P, P, P, P, P]),
+    "moe_route_replay": (I, [P, P, P, I, I, I, I, I, I, F, P, P, P, P]),
+    "fp8_block_quant": (I, [P, I64, I64, I64, I, P, P, P]),
+    "moe_dispatch_workspace_size": (SZ, [I, I, I]),
+    "moe_dispatch": (I, [P, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, SZ, P, P]),
+    "moe_grouped_ffn_workspace_size": (SZ, [I64, I, I]),
+    "moe_grouped_ffn_fp8": (I, [P, P, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
+    "moe_combine": (I, [P, P, P, I, I, I, P, P]),
+    "moe_debug_bounded_wait": (I, [I64, P, P]),
+    "moe_device_sm_count": (I, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+LIB_PATH = _LIB_PATH
+
+MOE_SCORE_SOFTMAX = 0
+MOE_SCORE_SIGMOID = 1
+MOE_DEV_BAD_IDS = 0x1
+MOE_DEV_TIMEOUT = 0x2
+MOE_DEV_ROWS = 0x4
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {_lib.moe_status_str(status).decode()} (status {status})")
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MoEError(fn, status)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _want(t: torch.Tensor, dtype, shape, name: str) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _empty(shape, dtype, like: torch.Tensor) -> torch.Tensor:
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def moe_status_str(status: int) -> str:
+    return _lib.moe_status_str(status).decode()
+
+
+def moe_device_sm_count() -> int:
+    return _lib.moe_device_sm_count()
+
+
+def moe_route_topk(x, w_router, k, score_fn, renorm=1, route_scale=1.0, topk_ids=None, topk_gates=None,
+                   capture_kT=None, logits_out=None, stream=None):
+    """Router logits (fp32 fma chain) -> top-k ids [T,k] int32, gates [T,k] fp32."""
+    T, d = x.shape
+    E = w_router.shape[0]
+    _want(x, torch.bfloat16, (T, d), "x")
+    _want(w_router, torch.bfloat16, (E, d), "w_router")
+    topk_ids = _empty((T, k), torch.int32, x) if topk_ids is None else topk_ids
+    topk_gates = _empty((T, k), torch.float32, x) if topk_gates is None else topk_gates
+    _want(topk_ids, torch.int32, (T, k), "topk_ids")
+    _want(topk_gates, torch.float32, (T, k), "topk_gates")
+    if capture_kT is not None:
+        _want(capture_kT, torch.int32, (k, T), "capture_kT")
+    if logits_out is not None:
+        _want(logits_out, torch.float32, (T, E), "logits_out")
+    _check("moe_route_topk", _lib.moe_route_topk(
+        _ptr(x), _ptr(w_router), T, d, E, k, score_fn, renorm, route_scale, _ptr(topk_ids),
+        _ptr(topk_gates), _ptr(capture_kT), _ptr(logits_out), _stream(stream)))
+    return topk_ids, topk_gates
+
+
+def moe_route_replay(replay_kT, E, x=None, w_router=None, score_fn=MOE_SCORE_SOFTMAX, renorm=1,
+                     route_scale=1.0, topk_ids=None, topk_gates=None, dev_status=None, stream=None):
+    """Replay one [k, T] layer slab of the routed-experts payload -> ids [T,k]
+    (exact copy) and, when x is given, gates [T,k] from the router logits."""
+    k, T = replay_kT.shape
+    _want(replay_kT, torch.int32, (k, T), "replay_kT")
+    topk_ids = _empty((T, k), torch.int32, replay_kT) if topk_ids is None else topk_ids
+    _want(topk_ids, torch.int32, (T, k), "topk_ids")
+    d = 128
+    if x is not None:
+        d = x.shape[1]
+        _want(x, torch.bfloat16, (T, d), "x")
+        _want(w_router, torch.bfloat16, (E, d), "w_router")
+        topk_gates = _empty((T, k), torch.float32, x) if topk_gates is None else topk_gates
+        _want(topk_gates, torch.float32, (T, k), "topk_gates")
+    if dev_status is not None:
+        _want(dev_status, torch.int32, (1,), "dev_status")
+    _check("moe_route_replay", _lib.moe_route_replay(
+        _ptr(replay_kT), _ptr(x), _ptr(w_router), T, d, E, k, score_fn, renorm, route_scale, _ptr(topk_ids),
+        _ptr(topk_gates), _ptr(dev_status), _stream(stream)))
+    return topk_ids, topk_gates
+
+
+def fp8_block_quant(src, block_rows, q=None, scales=None, stream=None):
+    """bf16 [rows, cols] -> (E4M3 codes uint8 [rows, cols], fp32 scales
+    [rows/block_rows, cols/128]); block_rows 1 (activations) or 128 (weights)."""
+    if src.dim() != 2:
+        raise ValueError("src must be 2-D")
+    rows, cols = src.shape
+    if src.dtype != torch.bfloat16 or not src.is_cuda or src.stride(1) != 1:
+        raise ValueError("src: bf16 CUDA tensor with unit column stride")
+    ld = src.stride(0)
+    q = _empty((rows, cols), torch.uint8, src) if q is None else q
+    scales = _empty((rows // block_rows, cols // 128), torch.float32, src) if scales is None else scales
+    _want(q, torch.uint8, (rows, cols), "q")
+    _want(scales, torch.float32, (rows // block_rows, cols // 128), "scales")
+    _check("fp8_block_quant", _lib.fp8_block_quant(
+        _ptr(src), rows, cols, ld, block_rows, _ptr(q), _ptr(scales), _stream(stream)))
+    return q, scales
+
+
+def moe_dispatch_workspace_size(T, k, E) -> int:
+    return int(_lib.moe_dispatch_workspace_size(T, k, E))
+
+
+def moe_dispatch(topk_ids, E, rows=None, row_scales=None, expert_counts=None, expert_offsets=None,
+                 sorted_to_slot=None, slot_to_sorted=None, rows_sorted=None, scales_sorted=None,
+                 workspace=None, dev_status=None, stream=None):
+    """Stable counting sort of the T*k slots by expert and the row gather.
+    rows: [T, ...] uint8 (e4m3 codes) or bf16; row_scales: [T, spr] fp32.
+    Returns (counts, offsets, sorted_to_slot, slot_to_sorted, rows_sorted, scales_sorted)."""
+    T, k = topk_ids.shape
+    A = T * k
+    _want(topk_ids, torch.int32, (T, k), "topk_ids")
+    dev = topk_ids
+    expert_counts = _empty((E,), torch.int32, dev) if expert_counts is None else expert_counts
+    expert_offsets = _empty((E + 1,), torch.int32, dev) if expert_offsets is None else expert_offsets
+    sorted_to_slot = _empty((A,), torch.int32, dev) if sorted_to_slot is None else sorted_to_slot
+    slot_to_sorted = _empty((A,), torch.int32, dev) if slot_to_sorted is None else slot_to_sorted
+    _want(expert_counts, torch.int32, (E,), "expert_counts")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(sorted_to_slot, torch.int32, (A,), "sorted_to_slot")
+    _want(slot_to_sorted, torch.int32, (A,), "slot_to_sorted")
+    row_bytes, spr = 0, 0
+    if rows is not None:
+        if rows.shape[0] != T or not rows.is_contiguous() or not rows.is_cuda:
+            raise ValueError("rows: contiguous CUDA tensor with T rows")
+        row_bytes = rows[0].numel() * rows.element_size() if T > 0 else rows.stride(0) * rows.element_size()
+        rows_sorted = _empty((A,) + tuple(rows.shape[1:]), rows.dtype, dev) if rows_sorted is None else rows_sorted
+        if row_scales is not None:
+            spr = row_scales.shape[1]
+            _want(row_scales, torch.float32, (T, spr), "row_scales")
+            scales_sorted = _empty((A, spr), torch.float32, dev) if scales_sorted is None else scales_sorted
+            _want(scales_sorted, torch.float32, (A, spr), "scales_sorted")
+    need = moe_dispatch_workspace_size(T, k, E)
+    if workspace is None:
+        workspace = _empty((need,), torch.uint8, dev)
+    _check("moe_dispatch", _lib.moe_dispatch(
+        _ptr(topk_ids), T, k, E, _ptr(rows), row_bytes, _ptr(row_scales), spr, _ptr(expert_counts),
+        _ptr(expert_offsets), _ptr(sorted_to_slot), _ptr(slot_to_sorted), _ptr(rows_sorted),
+        _ptr(scales_sorted), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _stream(stream)))
+    return expert_counts, expert_offsets, sorted_to_slot, slot_to_sorted, rows_sorted, scales_sorted
+
+
+def moe_grouped_ffn_workspace_size(max_rows, d, F) -> int:
+    return int(_lib.moe_grouped_ffn_workspace_size(max_rows, d, F))
+
+
+def moe_grouped_ffn_fp8(xq_sorted, xs_sorted, expert_offsets, w13_q, w13_s, w2_q, w2_s, out_sorted=None,
+                        workspace=None, dev_status=None, stream=None):
+    """Per-expert SwiGLU FFN as two grouped block-scaled FP8 GEMMs ->
+    out_sorted [max_rows, d] bf16."""
+    max_rows, d = xq_sorted.shape
+    E, twoF, d2 = w13_q.shape
+    F = twoF // 2
+    _want(xq_sorted, torch.uint8, (max_rows, d), "xq_sorted")
+    _want(xs_sorted, torch.float32, (max_rows, d // 128), "xs_sorted")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(w13_q, torch.uint8, (E, 2 * F, d), "w13_q")
+    _want(w13_s, torch.float32, (E, 2 * F // 128, d // 128), "w13_s")
+    _want(w2_q, torch.uint8, (E, d, F), "w2_q")
+    _want(w2_s, torch.float32, (E, d // 128, F // 128), "w2_s")
+    out_sorted = _empty((max_rows, d), torch.bfloat16, xq_sorted) if out_sorted is None else out_sorted
+    _want(out_sorted, torch.bfloat16, (max_rows, d), "out_sorted")
+    need = moe_grouped_ffn_workspace_size(max_rows, d, F)
+    if workspace is None:
+        workspace = _empty((need,), torch.uint8, xq_sorted)
+    _check("moe_grouped_ffn_fp8", _lib.moe_grouped_ffn_fp8(
+        _ptr(xq_sorted), _ptr(xs_sorted), _ptr(expert_offsets), max_rows, E, d, F, _ptr(w13_q), _ptr(w13_s),
+        _ptr(w2_q), _ptr(w2_s), _ptr(out_sorted), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))
+    return out_sorted
+
+
+def moe_combine(out_sorted, slot_to_sorted, gates, y=None, stream=None):
+    """y [T, d] bf16 = gate-weighted sum of each token's k expert rows."""
+    T, k = gates.shape
+    d = out_sorted.shape[1]
+    if out_sorted.dtype != torch.bfloat16 or not out_sorted.is_contiguous():
+        raise ValueError("out_sorted: contiguous bf16")
+    _want(slot_to_sorted, torch.int32, (T * k,), "slot_to_sorted")
+    _want(gates, torch.float32, (T, k), "gates")
+    y = _empty((T, d), torch.bfloat16, out_sorted) if y is None else y
+    _want(y, torch.bfloat16, (T, d), "y")
+    _check("moe_combine", _lib.moe_combine(
+        _ptr(out_sorted), _ptr(slot_to_sorted), _ptr(gates), T, k, d, _ptr(y), _stream(stream)))
+    return y
+
+
+def moe_debug_bounded_wait(timeout_ns, dev_status, stream=None):
+    _want(dev_status, torch.int32, (1,), "dev_status")
+    _check("moe_debug_bounded_wait", _lib.moe_debug_bounded_wait(timeout_ns, _ptr(dev_status), _stream(stream)))
+
+
+def check_status(dev_status: torch.Tensor) -> int:
+    """Read the device status word (synchronises with the current stream)."""
+    return int(dev_status.item())

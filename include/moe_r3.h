@@ -1,0 +1,213 @@
+/*
+ * moe_r3.h -- C ABI of libmoe_r3: one GPU's Mixture-of-Experts layer with
+ * router replay (R3) and block-scaled FP8 expert GEMMs, for sm_103a (GB300).
+ *
+ * The method is the one described in "RL at 1T Scale: prime-rl Performance
+ * Deep Dive" (prime-rl 0.6.0):
+ *   - section "Router replay": the routing decisions made during inference are
+ *     captured and replayed on the trainer; the routed-experts payload has
+ *     shape [num_layers, top_k, seq_len] and is handled as an opaque tensor;
+ *   - section "FP8 training": block-scaled FP8 as proposed by DeepSeek-V3
+ *     (E4M3 values, one fp32 scale per 1x128 activation tile and per 128x128
+ *     weight block);
+ *   - section "Parallelism", "Expert parallelism (EP)": tokens are dispatched
+ *     to their experts and combined back.
+ * The page leaves the kernel-level contract open; this header states it.
+ *
+ * Conventions for every entry point
+ *   - Tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *     dense unless a leading dimension is given.  bf16 travels as uint16_t,
+ *     E4M3 as uint8_t (OCP "e4m3fn": bias 7, max 448, no inf).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued on it; no call synchronises the host or
+ *     copies device data to the host, and no call allocates or frees memory.
+ *     Scratch memory is caller-provided workspace whose size is queried.
+ *   - Errors the host can see (NULL pointers, unsupported shapes, misaligned
+ *     pointers, short workspace) are returned before anything is launched and
+ *     nothing is written.  A failed launch returns MOE_ERR_CUDA.
+ *   - Errors only the device can see are OR-ed, as MOE_DEV_* bits, into the
+ *     caller-zeroed int32 word `dev_status` (nullable: then not reported).
+ *     Kernels never write out of bounds because of them.  Every device wait
+ *     is bounded; on expiry the kernel sets MOE_DEV_TIMEOUT and returns.
+ *   - Calls are thread-safe (no global mutable state) and stream-ordered.
+ */
+#ifndef MOE_R3_H
+#define MOE_R3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status;
+
+/* host return codes */
+#define MOE_OK 0
+#define MOE_ERR_NULL 1        /* a required pointer is NULL */
+#define MOE_ERR_SHAPE 2       /* unsupported sizes (see each call) */
+#define MOE_ERR_ALIGN 3       /* a pointer or leading dimension breaks 16-byte alignment */
+#define MOE_ERR_WORKSPACE 4   /* workspace NULL or smaller than the queried size */
+#define MOE_ERR_CUDA 5        /* a CUDA launch or driver call failed */
+#define MOE_ERR_UNSUPPORTED 6 /* valid request this build does not implement */
+
+/* device status bits (OR-ed into *dev_status) */
+#define MOE_DEV_BAD_IDS 0x1   /* a replayed / dispatched id is out of [0,E) or repeated in a token */
+#define MOE_DEV_TIMEOUT 0x2   /* a bounded device wait expired */
+#define MOE_DEV_ROWS 0x4      /* routed rows exceed the max_rows the GEMM was sized for */
+
+/* score functions */
+#define MOE_SCORE_SOFTMAX 0
+#define MOE_SCORE_SIGMOID 1
+
+/* Limits of this build: 1 <= k <= min(E, 32); 1 <= E <= 1024; d and F
+ * multiples of 128; T * k < 2^31. */
+
+const char *moe_status_str(moe_status s);
+
+/* ------------------------------------------------------------------------
+ * moe_route_topk -- router logits, top-k selection, gates, optional capture.
+ * ("Router replay": this is the decision that inference captures.)
+ *
+ *   logits[t,e] = sum_{i=0}^{d-1} x[t,i] * w_router[e,i], evaluated as one
+ *                 binary32 fused multiply-add chain in ascending i from +0
+ *                 (bit-reproducible; denormals honoured);
+ *   topk_ids[t,j] = the j-th largest logit's expert; equal logits (-0 == +0)
+ *                 go to the lower index; NaN ranks below every number;
+ *   topk_gates[t,j] = score(l_j) / sum_{i<k} score(l_i) if renorm (softmax
+ *                 over the chosen k; sigmoid normalised over the chosen k),
+ *                 else the full softmax over E / the plain sigmoid; then
+ *                 times route_scale;
+ *   capture_kT[j*T + t] = topk_ids[t,j] (nullable): one layer's [k, T] slab
+ *                 of the routed-experts payload [num_layers, top_k, seq_len];
+ *   logits_out[t,e] (nullable) = logits.
+ * x [T,d] bf16; w_router [E,d] bf16; topk_ids [T,k] int32; topk_gates [T,k]
+ * fp32.  T may be 0 (nothing launched).  Errors: NULL, SHAPE.
+ * ---------------------------------------------------------------------- */
+moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, int T, int d, int E, int k,
+                          int score_fn, int renorm, float route_scale, int32_t *topk_ids,
+                          float *topk_gates, int32_t *capture_kT, float *logits_out, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_route_replay -- replay one layer of a captured routing payload
+ * ("Router replay": decisions captured at inference replace the trainer's
+ * own routing).
+ *
+ *   topk_ids[t,j] = replay_kT[j*T + t], an exact copy in slot order, where
+ *   replay_kT = payload + layer*k*T is the layer's [k, T] slab.
+ *   A token whose k ids are not all in [0,E) and pairwise distinct sets
+ *   MOE_DEV_BAD_IDS; its ids are still copied and its gates are 0.
+ *   If x != NULL: topk_gates from the router logits of the replayed experts
+ *   (same logits, score function, renormalisation and scale as
+ *   moe_route_topk, so replaying a capture reproduces its gates bit for
+ *   bit).  If x == NULL, topk_gates may be NULL and is not written.
+ * Errors: NULL, SHAPE.
+ * ---------------------------------------------------------------------- */
+moe_status moe_route_replay(const int32_t *replay_kT, const uint16_t *x, const uint16_t *w_router,
+                            int T, int d, int E, int k, int score_fn, int renorm, float route_scale,
+                            int32_t *topk_ids, float *topk_gates, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * fp8_block_quant -- block-scaled E4M3 quantisation ("FP8 training",
+ * DeepSeek-V3 recipe).
+ *
+ * Blocks are 1 x 128 (block_rows = 1, activations) or 128 x 128
+ * (block_rows = 128, weights).  Per block: amax = max |v|, s = amax / 448
+ * (IEEE binary32 division; s = 1 if that is 0), q = E4M3(v / s) with IEEE
+ * division, round to nearest even, saturating to +-448, sign of zero kept.
+ * src [rows, cols] bf16 with row stride ld_src elements; q [rows, cols]
+ * (row stride cols); scales [rows/block_rows, cols/128] fp32.
+ * rows may be 0.  Errors: NULL, SHAPE (cols % 128, rows % block_rows),
+ * ALIGN (src, q, ld_src not 16-byte aligned).
+ * ---------------------------------------------------------------------- */
+moe_status fp8_block_quant(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
+                           int block_rows, uint8_t *q, float *scales, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_dispatch -- permute token rows into expert-contiguous order
+ * ("Expert parallelism": dispatch).
+ *
+ * Slots s = t*k + j are counting-sorted by expert id in ascending slot order
+ * (stable):
+ *   expert_counts[e]  = #slots routed to e;
+ *   expert_offsets[e] = sum_{e'<e} expert_counts[e'], expert_offsets[E] =
+ *                       routed slots;
+ *   sorted_to_slot[r] = the slot at sorted position r (r < expert_offsets[E]);
+ *   slot_to_sorted[s] = its inverse (-1 for a slot whose id is outside
+ *                       [0,E): such slots are not routed and set
+ *                       MOE_DEV_BAD_IDS);
+ *   rows_sorted[r]    = rows[sorted_to_slot[r] / k]  (row_bytes each),
+ *   scales_sorted[r]  = row_scales[sorted_to_slot[r] / k] (scales_per_row
+ *                       fp32 each; 0 = no scales, both pointers ignored).
+ * rows may be e4m3 codes (row_bytes = d) or bf16 (row_bytes = 2d);
+ * row_bytes must be a multiple of 16; rows, rows_sorted 16-byte aligned.
+ * rows / rows_sorted may be NULL to build the maps only.
+ * Sorted positions >= expert_offsets[E] are left unwritten.
+ * workspace: moe_dispatch_workspace_size(T, k, E) bytes, 256-byte aligned.
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE.
+ * ---------------------------------------------------------------------- */
+size_t moe_dispatch_workspace_size(int T, int k, int E);
+moe_status moe_dispatch(const int32_t *topk_ids, int T, int k, int E, const void *rows,
+                        int64_t row_bytes, const float *row_scales, int scales_per_row,
+                        int32_t *expert_counts, int32_t *expert_offsets, int32_t *sorted_to_slot,
+                        int32_t *slot_to_sorted, void *rows_sorted, float *scales_sorted,
+                        void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_ffn_fp8 -- per-expert SwiGLU FFN as two grouped block-scaled
+ * FP8 GEMMs on the tensor cores ("FP8 training", DeepSeek-V3 recipe).
+ *
+ * For every expert e and sorted row r in [expert_offsets[e],
+ * expert_offsets[e+1]) (offsets read on the device; no host sync):
+ *   h[r,n]   = sum_kb (xs_sorted[r,kb] * w13_s[e,n/128,kb]) * P_kb(r,n),
+ *              P_kb = the 128-deep block product of E4M3 codes accumulated
+ *              in fp32, promoted into an fp32 accumulator block by block;
+ *   act[r,c] = silu(h[r,c]) * h[r,F+c]   (c < F; w13 rows 0..F-1 gate,
+ *              F..2F-1 up), requantised 1x128 along F as fp8_block_quant;
+ *   out_sorted[r,:] = bf16 (round to nearest even) of act_q[r,:] W2[e]^T by
+ *              the same block promotion.
+ * xq_sorted [max_rows, d] e4m3, xs_sorted [max_rows, d/128] fp32;
+ * w13_q [E, 2F, d], w13_s [E, 2F/128, d/128]; w2_q [E, d, F],
+ * w2_s [E, d/128, F/128]; out_sorted [max_rows, d] bf16.  max_rows bounds
+ * expert_offsets[E] (rows beyond it set MOE_DEV_ROWS and are skipped).
+ * workspace: moe_grouped_ffn_workspace_size(max_rows, d, F) bytes (holds
+ * act_q and its scales), 256-byte aligned.
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
+ * ---------------------------------------------------------------------- */
+size_t moe_grouped_ffn_workspace_size(int64_t max_rows, int d, int F);
+moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs_sorted,
+                               const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                               const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q,
+                               const float *w2_s, uint16_t *out_sorted, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_combine -- gate-weighted sum back to token order ("Expert
+ * parallelism": combine).
+ *
+ *   y[t,c] = bf16( sum_{j=0}^{k-1} gates[t,j] * out_sorted[slot_to_sorted[t*k+j], c] ),
+ *   one binary32 fused multiply-add chain over j in slot order from +0,
+ *   rounded to nearest even; slots with slot_to_sorted = -1 are skipped.
+ * out_sorted [*, d] bf16, y [T, d] bf16; d a multiple of 8; out_sorted and y
+ * 16-byte aligned.  Errors: NULL, SHAPE, ALIGN.
+ * ---------------------------------------------------------------------- */
+moe_status moe_combine(const uint16_t *out_sorted, const int32_t *slot_to_sorted, const float *gates,
+                       int T, int k, int d, uint16_t *y, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_debug_bounded_wait -- exercises the bounded device wait that every
+ * pipelined kernel uses: one CTA waits on an mbarrier that nothing arrives
+ * at, for at most timeout_ns, then sets MOE_DEV_TIMEOUT in *dev_status and
+ * returns.  For fault-handling tests; no counterpart in the method.
+ * ---------------------------------------------------------------------- */
+moe_status moe_debug_bounded_wait(int64_t timeout_ns, int32_t *dev_status, void *stream);
+
+/* Number of SMs and the device ordinal the library sees (for sizing). */
+int moe_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_R3_H */

@@ -1,0 +1,67 @@
+"""The C-ABI library loads, exports every entry point include/moe_r3.h
+declares, and rejects bad arguments on the host before launching anything
+(these calls return before any CUDA API is touched, so they run without a
+GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_scaled_fp8_router_gb300 import moe_r3
+    return moe_r3
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe_r3.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+|fp8_block_quant)\s*\(", src)))
+
+
+def test_header_symbols_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(so, n), n
+    assert set(names) == set(lib.EXPORTED)
+
+
+def test_host_side_errors(lib):
+    L = lib._lib
+    null = None
+    # shapes
+    assert L.moe_route_topk(null, null, 10, 100, 8, 2, 0, 1, 1.0, null, null, null, null, null) == 2   # d % 128
+    assert L.moe_route_topk(null, null, 10, 128, 8, 9, 0, 1, 1.0, null, null, null, null, null) == 2   # k > E
+    assert L.moe_route_topk(null, null, 10, 128, 2000, 2, 0, 1, 1.0, null, null, null, null, null) == 2  # E > 1024
+    assert L.moe_route_topk(null, null, 10, 128, 8, 2, 5, 1, 1.0, null, null, null, null, null) == 2   # score fn
+    assert L.moe_route_topk(null, null, 10, 128, 8, 2, 0, 1, 1.0, null, null, null, null, null) == 1   # NULL
+    assert L.moe_route_topk(null, null, 0, 128, 8, 2, 0, 1, 1.0, null, null, null, null, null) == 0    # empty
+    x = ctypes.c_void_p(0x1000)
+    assert L.moe_route_replay(x, x, x, 10, 128, 8, 2, 0, 0, 1.0, x, x, null, null) == 6   # softmax w/o renorm
+    assert L.fp8_block_quant(null, 4, 100, 100, 1, null, null, null) == 2
+    assert L.fp8_block_quant(null, 4, 128, 128, 128, null, null, null) == 2                 # rows % 128
+    assert L.fp8_block_quant(null, 0, 128, 128, 1, null, null, null) == 0
+    assert L.fp8_block_quant(ctypes.c_void_p(0x1008), 4, 128, 128, 1, x, x, null) == 3     # misaligned
+    ws = L.moe_dispatch_workspace_size(100, 4, 16)
+    assert ws > 0
+    assert L.moe_dispatch(x, 100, 4, 16, null, 0, null, 0, x, x, x, x, null, null, x, ws - 1, null, null) == 4
+    assert L.moe_dispatch(x, 100, 4, 16, null, 0, null, 0, x, x, x, x, null, null, null, ws, null, null) == 4
+    assert L.moe_dispatch(x, 100, 4, 16, x, 24, null, 0, x, x, x, x, x, null, x, ws, null, null) == 2  # row_bytes % 16
+    assert L.moe_dispatch(x, 100, 33, 64, null, 0, null, 0, x, x, x, x, null, null, x, ws, null, null) == 2
+    assert L.moe_combine(null, null, null, 10, 2, 100, null, null) == 2
+    assert L.moe_combine(null, null, null, 10, 2, 128, null, null) == 1
+    fws = L.moe_grouped_ffn_workspace_size(1000, 256, 512)
+    assert fws > 0
+    assert L.moe_grouped_ffn_fp8(x, x, x, 1000, 8, 200, 512, x, x, x, x, x, x, fws, null, null) in (2, 6)
+    assert L.moe_grouped_ffn_fp8(x, x, x, 1000, 8, 256, 512, x, x, x, x, x, x, fws - 1, null, null) in (4, 6)
+    assert L.moe_debug_bounded_wait(1000, null, null) == 1
+    for s in range(7):
+        assert lib.moe_status_str(s)

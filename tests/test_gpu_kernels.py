@@ -1,0 +1,292 @@
+"""GPU parity of the SIMT kernels against the CPU oracle, through the C ABI:
+quantiser codes/scales, router ids/logits/capture, replay, dispatch maps and
+rows, combine -- all bit-exact; gates within 1e-5 relative."""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_router_gb300 import synthetic as S
+from tests.helpers import bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_scaled_fp8_router_gb300 import moe_r3
+    return moe_r3
+
+
+# ------------------------------------------------------------------ quantiser
+
+def _edge_rows(rows, cols, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g, device=DEV)
+    scale = torch.exp2(torch.randint(-30, 30, (rows, 1), generator=g, device=DEV).float())
+    x = (x * scale).to(torch.bfloat16)
+    if rows >= 6 and cols >= 256:
+        x[0, :128] = 0.0
+        x[1, 128:256] = -0.0
+        x[2, :128] = 1e-40                       # bf16 subnormals
+        x[3, :] = torch.linspace(-448 * 2.0 ** -9, 448 * 2.0 ** -9, cols, device=DEV).to(torch.bfloat16)
+        x[4, :128] = 3.0e38
+        x[5, :128] = 2.0 ** -130
+    return x
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 128), (37, 256), (300, 2048), (1031, 7168)])
+def test_quant_1x128_bit_exact(L, oracle, rows, cols):
+    x = _edge_rows(rows, cols, rows)
+    q, s = L.fp8_block_quant(x, 1)
+    rq, rs = oracle.quant_1x128(bf16_bits(x))
+    np.testing.assert_array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_1x128_strided_source(L, oracle):
+    big = _edge_rows(64, 512, 3)
+    x = big[:, 128:384]                          # leading dimension 512
+    q, s = L.fp8_block_quant(x, 1)
+    rq, rs = oracle.quant_1x128(bf16_bits(x))
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("rows,cols", [(128, 128), (384, 256), (1408 * 2, 2048)])
+def test_quant_128x128_bit_exact(L, oracle, rows, cols):
+    w = _edge_rows(rows, cols, rows + cols)
+    q, s = L.fp8_block_quant(w, 128)
+    rq, rs = oracle.quant_128x128(bf16_bits(w))
+    np.testing.assert_array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_large_weight_sampled(L, oracle):
+    cfg = S.CONFIGS["large"]
+    for e in (0, 255):
+        w = S.make_w13_expert(cfg, e, DEV)
+        q, s = L.fp8_block_quant(w, 128)
+        rows = slice(128 * 7, 128 * 9)             # two block rows checked fully
+        rq, rs = oracle.quant_128x128(bf16_bits(w[rows]))
+        np.testing.assert_array_equal(q[rows].cpu().numpy(), rq)
+        np.testing.assert_array_equal(s[7:9].cpu().numpy(), rs)
+
+
+# ------------------------------------------------------------------ router
+
+def _route_case(cfg, T=None, seed=0):
+    x = S.make_x(cfg, DEV, seed, T=T)
+    wr = S.make_router_w(cfg, DEV, seed)
+    return x, wr
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("replay", 1000), ("large", 200)])
+def test_route_topk_bit_exact(L, oracle, name, T):
+    cfg = S.CONFIGS[name]
+    x, wr = _route_case(cfg, T)
+    T = x.shape[0]
+    cap = torch.full((cfg.k, T), -7, dtype=torch.int32, device=DEV)
+    lg = torch.empty((T, cfg.E), dtype=torch.float32, device=DEV)
+    ids, gates = L.moe_route_topk(x, wr, cfg.k, cfg.score_fn, cfg.renorm, cfg.route_scale,
+                                  capture_kT=cap, logits_out=lg)
+    rl = oracle.router_logits(bf16_bits(x), bf16_bits(wr))
+    np.testing.assert_array_equal(lg.cpu().numpy().view(np.uint32), rl.view(np.uint32))
+    rid = oracle.topk(rl, cfg.k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_array_equal(cap.cpu().numpy(), rid.T)
+    rg = oracle.gates(rl, rid, cfg.score_fn, cfg.renorm, cfg.route_scale)
+    np.testing.assert_allclose(gates.cpu().numpy(), rg, rtol=1e-5, atol=0)
+
+
+@pytest.mark.parametrize("score_fn,renorm,scale", [(0, 0, 1.0), (1, 0, 2.5), (0, 1, 0.5), (1, 1, 1.0)])
+def test_route_topk_score_modes_and_ragged(L, oracle, score_fn, renorm, scale):
+    cfg = S.CONFIGS["replay"].with_(E=300, d=384)    # two expert passes, ragged last pass
+    x, wr = _route_case(cfg, 77, seed=5)
+    ids, gates = L.moe_route_topk(x, wr, 7, score_fn, renorm, scale)
+    rl = oracle.router_logits(bf16_bits(x), bf16_bits(wr))
+    rid = oracle.topk(rl, 7)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(gates.cpu().numpy(), oracle.gates(rl, rid, score_fn, renorm, scale), rtol=1e-5)
+
+
+def test_route_topk_ties(L, oracle):
+    """Duplicate router rows give exactly equal logits: lower index first."""
+    cfg = S.CONFIGS["tiny"].with_(E=64)
+    x, wr = _route_case(cfg, 100, seed=9)
+    wr[10] = wr[3]
+    wr[40] = wr[3]
+    wr[33] = wr[7]
+    x[5] = 0.0                                   # all logits +0: ids 0..k-1
+    ids, _ = L.moe_route_topk(x, wr, 6, 0, 1, 1.0)
+    rid = oracle.topk(oracle.router_logits(bf16_bits(x), bf16_bits(wr)), 6)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    assert list(rid[5]) == [0, 1, 2, 3, 4, 5]
+
+
+def test_route_topk_k_equals_E_and_k32(L, oracle):
+    for E, k in [(8, 8), (64, 32), (1024, 32)]:
+        cfg = S.CONFIGS["tiny"].with_(E=E)
+        x, wr = _route_case(cfg, 40, seed=E)
+        ids, gates = L.moe_route_topk(x, wr, k, 1, 1, 1.0)
+        rl = oracle.router_logits(bf16_bits(x), bf16_bits(wr))
+        rid = oracle.topk(rl, k)
+        np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+        np.testing.assert_allclose(gates.cpu().numpy(), oracle.gates(rl, rid, 1, 1, 1.0), rtol=1e-5)
+
+
+def test_route_empty(L):
+    cfg = S.CONFIGS["tiny"]
+    x = torch.empty((0, cfg.d), dtype=torch.bfloat16, device=DEV)
+    ids, gates = L.moe_route_topk(x, S.make_router_w(cfg, DEV), 2, 0)
+    assert ids.shape == (0, 2)
+
+
+# ------------------------------------------------------------------ replay
+
+def test_replay_copies_and_round_trips(L, oracle):
+    cfg = S.CONFIGS["large"]
+    x, wr = _route_case(cfg, 300)
+    cap = torch.empty((cfg.k, 300), dtype=torch.int32, device=DEV)
+    ids, gates = L.moe_route_topk(x, wr, cfg.k, cfg.score_fn, 1, 1.0, capture_kT=cap)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rids, rgates = L.moe_route_replay(cap, cfg.E, x, wr, cfg.score_fn, 1, 1.0, dev_status=st)
+    assert torch.equal(rids, ids)
+    assert torch.equal(rgates.view(torch.int32), gates.view(torch.int32))   # bit for bit
+    assert L.check_status(st) == 0
+
+
+@pytest.mark.parametrize("name", ["replay", "multilayer_replay"])
+def test_replay_payload_against_oracle(L, oracle, name):
+    cfg = S.CONFIGS[name].with_(T=2000, layers=2)
+    payload = S.make_replay_payload(cfg, DEV)
+    x, wr = _route_case(cfg, 2000)
+    for l in range(2):
+        slab = payload[l]
+        ids, gates = L.moe_route_replay(slab, cfg.E, x, wr, cfg.score_fn, 1, 1.0)
+        rid, valid, bad = oracle.replay(slab.cpu().numpy(), cfg.E)
+        assert bad == 0
+        np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+        rl = oracle.router_logits(bf16_bits(x), bf16_bits(wr))
+        np.testing.assert_allclose(gates.cpu().numpy(), oracle.gates(rl, rid, cfg.score_fn, 1, 1.0), rtol=1e-5)
+
+
+def test_replay_bad_ids_flagged(L, oracle):
+    cfg = S.CONFIGS["tiny"]
+    x, wr = _route_case(cfg, 64)
+    p = torch.stack([torch.arange(64, device=DEV) % 8, (torch.arange(64, device=DEV) + 1) % 8]).to(torch.int32)
+    p[0, 3] = 8          # out of range
+    p[1, 9] = p[0, 9]    # duplicate
+    p[0, 20] = -1
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ids, gates = L.moe_route_replay(p, cfg.E, x, wr, 0, 1, 1.0, dev_status=st)
+    assert L.check_status(st) & L.MOE_DEV_BAD_IDS
+    rid, valid, bad = oracle.replay(p.cpu().numpy(), cfg.E)
+    assert bad == 3
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    g = gates.cpu().numpy()
+    assert np.all(g[valid == 0] == 0) and np.all(g[valid == 1].sum(1) > 0.99)
+    # ids only (no x): no gates, still flags
+    st.zero_()
+    ids2, g2 = L.moe_route_replay(p, cfg.E, dev_status=st)
+    assert g2 is None and torch.equal(ids2, ids) and L.check_status(st) & L.MOE_DEV_BAD_IDS
+
+
+# ------------------------------------------------------------------ dispatch
+
+def _check_dispatch(L, oracle, ids, E, rows=None, scales=None):
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    counts, offsets, s2s, sl2, rs, ss = L.moe_dispatch(ids, E, rows=rows, row_scales=scales, dev_status=st)
+    rc, ro, rs2s, rsl2, dropped = oracle.dispatch(ids.cpu().numpy(), E)
+    n = int(ro[-1])
+    np.testing.assert_array_equal(counts.cpu().numpy(), rc)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
+    np.testing.assert_array_equal(s2s[:n].cpu().numpy(), rs2s[:n])
+    np.testing.assert_array_equal(sl2.cpu().numpy(), rsl2)
+    k = ids.shape[1]
+    if rows is not None:
+        ref = oracle.gather_rows(rows.cpu().contiguous().view(torch.uint8).numpy().reshape(rows.shape[0], -1),
+                                 rs2s, n, k)
+        got = rs[:n].cpu().contiguous().view(torch.uint8).numpy().reshape(n, -1)
+        np.testing.assert_array_equal(got, ref)
+    if scales is not None:
+        np.testing.assert_array_equal(ss[:n].cpu().numpy(), oracle.gather_rows(scales.cpu().numpy(), rs2s, n, k))
+    return L.check_status(st), dropped
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (129, 2, 8), (4096, 6, 64), (1500, 8, 256), (777, 32, 1024)])
+def test_dispatch_maps_and_rows(L, oracle, T, k, E):
+    g = torch.Generator(device=DEV).manual_seed(T)
+    ids = torch.argsort(torch.rand((T, E), generator=g, device=DEV), dim=1)[:, :k].to(torch.int32)
+    d = 256
+    xq = torch.randint(0, 256, (T, d), generator=g, device=DEV, dtype=torch.uint8)
+    xs = torch.rand((T, d // 128), generator=g, device=DEV)
+    st, dropped = _check_dispatch(L, oracle, ids, E, xq, xs)
+    assert st == 0 and dropped == 0
+
+
+def test_dispatch_bf16_rows_skewed_with_empty_experts(L, oracle):
+    cfg = S.CONFIGS["multilayer_replay"].with_(T=3000, d=384, layers=1)
+    ids = S.make_replay_payload(cfg, DEV)[0].t().contiguous()
+    x = S.make_x(cfg, DEV)
+    st, _ = _check_dispatch(L, oracle, ids, cfg.E, x, None)
+    assert st == 0
+
+
+def test_dispatch_bad_ids_dropped(L, oracle):
+    ids = torch.tensor([[2, 9], [-1, 1], [0, 2], [3, 3]], dtype=torch.int32, device=DEV)
+    x = torch.randn(4, 128, device=DEV).to(torch.bfloat16)
+    st, dropped = _check_dispatch(L, oracle, ids, 4, x, None)
+    assert dropped == 2 and st & 1
+
+
+def test_dispatch_empty(L):
+    ids = torch.empty((0, 4), dtype=torch.int32, device=DEV)
+    counts, offsets, *_ = L.moe_dispatch(ids, 16)
+    assert counts.sum().item() == 0 and offsets.cpu().tolist() == [0] * 17
+
+
+# ------------------------------------------------------------------ combine
+
+@pytest.mark.parametrize("T,k,d", [(1, 1, 128), (300, 6, 2048), (129, 32, 128), (64, 8, 7168)])
+def test_combine_bit_exact(L, oracle, T, k, d):
+    g = torch.Generator(device=DEV).manual_seed(T * k)
+    out = torch.randn((T * k + 5, d), generator=g, device=DEV).to(torch.bfloat16)
+    sl2 = torch.randperm(T * k, generator=g, device=DEV).to(torch.int32)
+    sl2[::7] = -1
+    gates = torch.rand((T, k), generator=g, device=DEV)
+    y = L.moe_combine(out, sl2, gates)
+    ref = oracle.combine(bf16_bits(out), sl2.cpu().numpy(), gates.cpu().numpy())
+    np.testing.assert_array_equal(bf16_bits(y), ref)
+
+
+def test_identity_experts_round_trip(L, oracle):
+    """combine(dispatch(x)) == x for identity experts and Dirichlet gates."""
+    cfg = S.CONFIGS["long_dispatch"].with_(T=5000)
+    ids = S.make_replay_payload(cfg, DEV)[0].t().contiguous()
+    gates = S.make_dirichlet_gates(cfg, DEV)
+    x = S.make_x(cfg, DEV)
+    counts, offsets, s2s, sl2, rows, _ = L.moe_dispatch(ids, cfg.E, rows=x)
+    y = L.moe_combine(rows, sl2, gates)
+    assert torch.equal(y.view(torch.int16), x.view(torch.int16))
+
+
+# ------------------------------------------------------------------ faults
+
+def test_bounded_wait_times_out(L):
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_debug_bounded_wait(2_000_000, st)     # 2 ms, nothing ever arrives
+    torch.cuda.synchronize()
+    assert L.check_status(st) == L.MOE_DEV_TIMEOUT
+    # the context is still usable
+    y = torch.ones(4, device=DEV) * 2
+    assert y.sum().item() == 8.0
+
+
+def test_host_errors_raise(L):
+    x = torch.zeros((4, 100), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(L.MoEError):
+        L.fp8_block_quant(x, 1)
