@@ -245,9 +245,10 @@ def rooflines(cfg, avg, peaks):
            else "FP8 dense = 2 x fallback bf16", "traffic": None}
     ffn["frac"] = ffn["achieved"] / ffn["peak"]
     hbm = peaks["hbm_gbs"]
-    bytes_quant = T * d * (2 + 1 + 4 / 128)
-    bytes_disp = A * (d + 4 * d / 128) * 2 + T * (d + 4 * d / 128) + 3 * A * 4 + T * k * 4
-    bytes_comb = A * d * 2 + T * d * 2 + T * k * 8
+    row = d + 4 * d / 128                       # one FP8 row with its 1x128 scales
+    bytes_quant = T * d * 2 + T * row
+    bytes_disp = A * 4 + 2 * A * 4 + T * row + A * row      # ids, two maps, rows in once, A rows out
+    bytes_comb = A * d * 2 + A * 4 + T * k * 4 + T * d * 2  # A bf16 rows + map + gates in, y out
     route_flops = 2.0 * T * d * E if cfg.mode == "route" else 2.0 * T * d * k
     extra = {
         "quant_1x128": {"ms": avg["quant"], "GB/s": bytes_quant / (avg["quant"] * 1e-3) / 1e9},
@@ -260,6 +261,63 @@ def rooflines(cfg, avg, peaks):
     for key in ("quant_1x128", "dispatch", "combine"):
         extra[key]["frac_hbm"] = extra[key]["GB/s"] / hbm
     return ffn, extra
+
+
+def run_dispatch_combine(dev, seed, steps, warmup, peaks):
+    """Dispatch + combine alone on the long-context shape (T=131072, d=7168
+    bf16 rows, 256 experts, top-8, replayed uniform ids, Dirichlet gates,
+    identity experts): replay copy -> dispatch (maps + bf16 row gather) ->
+    combine.  Inputs (1.9 GB of x, 15 GB of dispatched rows) dwarf L2."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    cfg = S.CONFIGS["long_dispatch"]
+    T, k, d, E = cfg.T, cfg.k, cfg.d, cfg.E
+    A = T * k
+    payload = S.make_replay_payload(cfg, dev, seed)[0]
+    gates = S.make_dirichlet_gates(cfg, dev, seed)
+    x = S.make_x(cfg, dev, seed)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    rows = torch.empty((A, d), dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    s2s = torch.empty(A, dtype=torch.int32, device=dev)
+    sl2 = torch.empty(A, dtype=torch.int32, device=dev)
+    ws = torch.empty(Lb.moe_dispatch_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = torch.empty_like(x)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(e=None):
+        if e: e[0].record()
+        Lb.moe_route_replay(payload, E, topk_ids=ids, dev_status=st)
+        Lb.moe_dispatch(ids, E, rows=x, expert_counts=counts, expert_offsets=offs, sorted_to_slot=s2s,
+                        slot_to_sorted=sl2, rows_sorted=rows, workspace=ws, dev_status=st)
+        if e: e[1].record()
+        Lb.moe_combine(rows, sl2, gates, y=y)
+        if e: e[2].record()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[ev(), ev(), ev()] for _ in range(steps)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize()
+    t_disp = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    t_comb = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    exact = bool(torch.equal(y.view(torch.int16), x.view(torch.int16)))
+    b_disp = 2 * A * 4 + A * 4 + 2 * A * 4 + T * d * 2 + A * d * 2   # replay in/out, ids, maps, rows
+    b_comb = A * d * 2 + A * 4 + T * k * 4 + T * d * 2
+    gbs = (b_disp + b_comb) / ((t_disp + t_comb) * 1e-3) / 1e9
+    out = {"workload": f"long_dispatch: T={T} d={d} bf16 rows E={E} top_k={k}, identity experts",
+           "ms": t_disp + t_comb, "dispatch_ms": t_disp, "combine_ms": t_comb, "GB/s": gbs,
+           "frac": gbs / peaks["hbm_gbs"], "peak_GB/s": peaks["hbm_gbs"],
+           "bytes": b_disp + b_comb, "bytes_rows_only": 2 * T * d * (2 + 2 * k),
+           "combine_of_dispatch_exact": exact, "status": Lb.check_status(st)}
+    del rows, x, y
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -342,8 +400,10 @@ def main():
     ap.add_argument("--workload", default="large")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=16)
+    ap.add_argument("--cpu-tokens", type=int, default=256, help="token sample of the CPU baseline")
+    ap.add_argument("--ref-tokens", type=int, default=32, help="token sample per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dispatch-combine", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -363,10 +423,10 @@ def main():
         import torch
         from oracle import oracle as O
         gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
-        smp = OracleSample(cfg, args.cpu_tokens, args.seed, gen_dev)
+        smp = OracleSample(cfg, args.ref_tokens, args.seed, gen_dev)
         times = [smp.run() for _ in range(args.warmup + args.steps)][args.warmup:]
         total = sum(times)
-        value = args.cpu_tokens * args.steps / total
+        value = args.ref_tokens * args.steps / total
         print(json.dumps({"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s",
                           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -400,6 +460,12 @@ def main():
                    "d2h_bytes_per_step": r["d2h"]},
            "roofline": ffn, "extra": extra, "gpu_launches": launches * args.steps, "clocks": r["clocks"],
            "dev_status": r["status"], "peaks_source": peaks["source"]}
+    if cfg.name == "large" and not args.no_dispatch_combine:
+        import torch
+        del r
+        torch.cuda.empty_cache()
+        out["dispatch_combine"] = run_dispatch_combine(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
+                                                       args.seed + rank, max(3, args.steps // 2), 3, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, args.seed, args.cpu_tokens, "cuda")
     if rank == 0:

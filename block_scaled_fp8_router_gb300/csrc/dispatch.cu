@@ -16,8 +16,9 @@
 //                   stable sorted position.  Writes both maps.
 //   gather_kernel   one warp per token: the row is read from HBM once
 //                   (16-byte vectors) and written to its k sorted positions.
-// Combine is one warp per token: for each 16-byte column segment the k
-// source rows are loaded before the fma chain runs over j in slot order.
+// Combine is one warp per token: for each pair of 16-byte column vectors per
+// lane the k source rows are loaded before the fma chain runs over j in slot
+// order.
 #include "common.cuh"
 
 namespace moe {
@@ -211,7 +212,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint8_t *__restrict__
 }
 
 // y[t] = bf16( sum_j g[t,j] * out_sorted[slot_to_sorted[t*k+j]] ), fma chain
-// over j in slot order from +0.
+// over j in slot order from +0.  One warp per token; each lane owns two
+// 16-byte column vectors (v, v + 32) per pass and has all 2 x 8 source loads
+// in flight before the first fma (16 x 16 B per lane keeps enough bytes in
+// flight to saturate HBM).  k > 8 runs the slots in groups of 8, in order.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ out_sorted,
                                                       const int32_t *__restrict__ slot_to_sorted,
                                                       const float *__restrict__ gates, int T, int k, int d,
@@ -224,40 +228,53 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     for (int64_t t = gw; t < T; t += nw) {
         const int32_t my_src = lane < k ? __ldg(slot_to_sorted + t * k + lane) : -1;
         const float my_g = lane < k ? __ldg(gates + t * k + lane) : 0.0f;
-        for (int v0 = 0; v0 < nvec; v0 += 32) {
-            const int v = v0 + lane;
-            const bool act = v < nvec;
-            float acc[8];
+        for (int v0 = 0; v0 < nvec; v0 += 64) {
+            float acc[2][8];
 #pragma unroll
-            for (int i = 0; i < 8; i++) acc[i] = 0.0f;
+            for (int h = 0; h < 2; h++)
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[h][i] = 0.0f;
             for (int j0 = 0; j0 < k; j0 += 8) {
-                uint4 buf[8];
-                float g[8];
                 int32_t src[8];
+                float g[8];
 #pragma unroll
                 for (int u = 0; u < 8; u++) {
-                    const int j = j0 + u;
-                    src[u] = __shfl_sync(0xFFFFFFFFu, my_src, j & 31);
-                    g[u] = __shfl_sync(0xFFFFFFFFu, my_g, j & 31);
-                    if (j >= k || !act) src[u] = -1;
-                    if (src[u] >= 0)
-                        buf[u] = __ldcs(reinterpret_cast<const uint4 *>(out_sorted + (int64_t)src[u] * d) + v);
+                    src[u] = __shfl_sync(0xFFFFFFFFu, my_src, (j0 + u) & 31);
+                    g[u] = __shfl_sync(0xFFFFFFFFu, my_g, (j0 + u) & 31);
+                    if (j0 + u >= k) src[u] = -1;
+                }
+                uint4 buf[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int v = v0 + h * 32 + lane;
+#pragma unroll
+                    for (int u = 0; u < 8; u++)
+                        if (src[u] >= 0 && v < nvec)
+                            buf[h][u] = __ldcs(reinterpret_cast<const uint4 *>(out_sorted + (int64_t)src[u] * d) + v);
                 }
 #pragma unroll
-                for (int u = 0; u < 8; u++) {
-                    if (src[u] < 0) continue;
-                    float f[8];
-                    unpack_bf16x8(buf[u], f);
+                for (int h = 0; h < 2; h++) {
 #pragma unroll
-                    for (int i = 0; i < 8; i++) acc[i] = fmaf(g[u], f[i], acc[i]);
+                    for (int u = 0; u < 8; u++) {
+                        if (src[u] < 0) continue;
+                        float f[8];
+                        unpack_bf16x8(buf[h][u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; i++) acc[h][i] = fmaf(g[u], f[i], acc[h][i]);
+                    }
                 }
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            if (act) __stcs(reinterpret_cast<uint4 *>(y + t * d) + v, o);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int v = v0 + h * 32 + lane;
+                if (v >= nvec) continue;
+                uint4 o;
+                o.x = pack_bf16x2(acc[h][0], acc[h][1]);
+                o.y = pack_bf16x2(acc[h][2], acc[h][3]);
+                o.z = pack_bf16x2(acc[h][4], acc[h][5]);
+                o.w = pack_bf16x2(acc[h][6], acc[h][7]);
+                __stcs(reinterpret_cast<uint4 *>(y + t * d) + v, o);
+            }
         }
     }
 }

@@ -9,12 +9,13 @@
 // index, computed by one thread (a SIMT register-tiled GEMM, not the tensor
 // cores, whose accumulation order is not specified).
 //
-// route_topk_kernel: CTA = 32 tokens x all experts (passes of 256); each
-// thread owns 4 tokens x 8 experts of fp32 accumulators; bf16 tiles of x and
-// W_r (32 deep) are widened to fp32 in shared memory, the next tile is loaded
-// into registers while the current one is consumed.  Logits never leave the
-// SM: they go to shared memory, and each warp then selects top-k for 4 tokens
-// with k rounds of a (value, index) arg-max over the warp.
+// route_topk_kernel: CTA = 128 threads, 32 tokens x all experts (passes of
+// 256); each thread owns 8 tokens x 8 experts of fp32 accumulators (6
+// shared-memory wavefronts per 64 FMAs per warp); bf16 tiles of x and W_r (32
+// deep) are widened to fp32 in shared memory with conflict-free stores, the
+// next tile is loaded into registers while the current one is consumed.
+// Logits never leave the SM: they go to shared memory, and each warp then
+// selects top-k for 8 tokens with k rounds of a (value, index) arg-max.
 #include "common.cuh"
 
 namespace moe {
@@ -72,12 +73,12 @@ __device__ __forceinline__ float warp_gate(int lane, int k, float my_l, int scor
     return g * route_scale;
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restrict__ x,
-                                                         const uint16_t *__restrict__ wr, int T, int d, int E,
-                                                         int k, int score_fn, int renorm, float route_scale,
-                                                         int32_t *__restrict__ ids, float *__restrict__ gates,
-                                                         int32_t *__restrict__ capture,
-                                                         float *__restrict__ logits_out)
+__global__ void __launch_bounds__(128, 3) route_topk_kernel(const uint16_t *__restrict__ x,
+                                                            const uint16_t *__restrict__ wr, int T, int d, int E,
+                                                            int k, int score_fn, int renorm, float route_scale,
+                                                            int32_t *__restrict__ ids, float *__restrict__ gates,
+                                                            int32_t *__restrict__ capture,
+                                                            float *__restrict__ logits_out)
 {
     extern __shared__ float4 smem4[];
     float *xs = reinterpret_cast<float *>(smem4);   // [RT_BK][RT_BT]
@@ -87,28 +88,28 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * RT_BT;
-    const int tt = (warp >> 2) * 16 + (lane >> 3) * 4;  // my 4 tokens in the tile
-    const int ee = (warp & 3) * 64 + (lane & 7) * 8;    // my 8 experts in the pass
+    const int tt = (lane >> 3) * 8;                // my 8 tokens in the tile
+    const int ee = warp * 64 + (lane & 7) * 8;     // my 8 experts in the pass
 
-    // global -> register tile loader: x chunk (tid < 128) and 4 W_r chunks
-    const int xt = tid >> 2, xp = tid & 3;
+    // tile loaders: x chunk (token = tid & 31, 8-wide part = tid >> 5) and
+    // 8 W_r chunks (expert = tid + 128 (r & 1), part = r >> 1); consecutive
+    // lanes write consecutive shared-memory words (no bank conflicts)
+    const int xt = tid & 31, xp = tid >> 5;
     for (int e0 = 0; e0 < E; e0 += RT_EP) {
-        float acc[4][8];
+        float acc[8][8];
 #pragma unroll
-        for (int a = 0; a < 4; a++)
+        for (int a = 0; a < 8; a++)
 #pragma unroll
             for (int b = 0; b < 8; b++) acc[a][b] = 0.0f;
 
-        uint4 rx = make_uint4(0, 0, 0, 0), rw[4];
+        uint4 rx, rw[8];
         auto load_tile = [&](int k0) {
-            if (tid < 128) {
-                const int t = t0 + xt;
-                rx = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 8))
-                           : make_uint4(0, 0, 0, 0);
-            }
+            const int t = t0 + xt;
+            rx = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 8))
+                       : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int r = 0; r < 4; r++) {
-                const int c = tid + 256 * r, e = e0 + (c >> 2), p = c & 3;
+            for (int r = 0; r < 8; r++) {
+                const int e = e0 + tid + 128 * (r & 1), p = r >> 1;
                 rw[r] = e < E ? __ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + k0 + p * 8))
                               : make_uint4(0, 0, 0, 0);
             }
@@ -118,14 +119,12 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
             __syncthreads();
             {
                 float f[8];
-                if (tid < 128) {
-                    unpack_bf16x8(rx, f);
+                unpack_bf16x8(rx, f);
 #pragma unroll
-                    for (int j = 0; j < 8; j++) xs[(xp * 8 + j) * RT_BT + xt] = f[j];
-                }
+                for (int j = 0; j < 8; j++) xs[(xp * 8 + j) * RT_BT + xt] = f[j];
 #pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    const int c = tid + 256 * r, e = c >> 2, p = c & 3;
+                for (int r = 0; r < 8; r++) {
+                    const int e = tid + 128 * (r & 1), p = r >> 1;
                     unpack_bf16x8(rw[r], f);
 #pragma unroll
                     for (int j = 0; j < 8; j++) ws[(p * 8 + j) * RT_EP + e] = f[j];
@@ -135,19 +134,20 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
             if (k0 + RT_BK < d) load_tile(k0 + RT_BK);
 #pragma unroll
             for (int i = 0; i < RT_BK; i++) {
-                const float4 xv = *reinterpret_cast<const float4 *>(&xs[i * RT_BT + tt]);
+                const float4 x0 = *reinterpret_cast<const float4 *>(&xs[i * RT_BT + tt]);
+                const float4 x1 = *reinterpret_cast<const float4 *>(&xs[i * RT_BT + tt + 4]);
                 const float4 w0 = *reinterpret_cast<const float4 *>(&ws[i * RT_EP + ee]);
                 const float4 w1 = *reinterpret_cast<const float4 *>(&ws[i * RT_EP + ee + 4]);
-                const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+                const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                 const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                for (int a = 0; a < 4; a++)
+                for (int a = 0; a < 8; a++)
 #pragma unroll
                     for (int b = 0; b < 8; b++) acc[a][b] = fmaf(xa[a], wb[b], acc[a][b]);
             }
         }
 #pragma unroll
-        for (int a = 0; a < 4; a++)
+        for (int a = 0; a < 8; a++)
 #pragma unroll
             for (int b = 0; b < 8; b++) {
                 const int e = e0 + ee + b;
@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
     }
     __syncthreads();
 
-    // ---- top-k + gates: warp w handles tokens 4w .. 4w+3 of the tile ----
-    for (int tl = warp * 4; tl < warp * 4 + 4; tl++) {
+    // ---- top-k + gates: warp w handles tokens 8w .. 8w+7 of the tile ----
+    for (int tl = warp * 8; tl < warp * 8 + 8; tl++) {
         const int t = t0 + tl;
         if (t >= T) break;
         const float *row = lg + tl * Epad;
@@ -335,7 +335,7 @@ MOE_API moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, i
         cudaSuccess)
         return MOE_ERR_CUDA;
     const int grid = (T + RT_BT - 1) / RT_BT;
-    route_topk_kernel<<<grid, 256, smem, as_stream(stream)>>>(x, w_router, T, d, E, k, score_fn, renorm,
+    route_topk_kernel<<<grid, 128, smem, as_stream(stream)>>>(x, w_router, T, d, E, k, score_fn, renorm,
                                                                route_scale, topk_ids, topk_gates, capture_kT,
                                                                logits_out);
     return launch_status();

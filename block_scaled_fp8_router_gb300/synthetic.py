@@ -17,6 +17,7 @@ FP8; the post prints no data, so all inputs are synthetic):
   large              T=8192, d=7168, E=256, k=8, F=2048, sigmoid top-k routing
   long_dispatch      T=131072, d=7168, E=256, k=8, identity experts (bf16 rows)
   multilayer_replay  8 layers x T=16384 at the large shape, skewed replayed ids
+  large_e64          T=2048, d=7168, E=64, k=8, F=2048 (profiling size of "large")
 """
 from __future__ import annotations
 
@@ -68,6 +69,10 @@ CONFIGS = {
                                "uniform", w_std=0.006),
     "multilayer_replay": MoEConfig("multilayer_replay", 16384, 7168, 256, 8, 2048, SIGMOID, "replay",
                                    "hot_cold", w_std=0.006, layers=8),
+    # profiling shape: the large layer's per-expert GEMM shape (about 256 rows
+    # per expert, d=7168, F=2048) with a quarter of the experts and tokens, so
+    # that a profiler capture holds ~3.5 GB instead of ~14 GB
+    "large_e64": MoEConfig("large_e64", 2048, 7168, 64, 8, 2048, SIGMOID, "route", "router", w_std=0.006),
 }
 
 
