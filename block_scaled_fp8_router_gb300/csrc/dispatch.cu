@@ -19,6 +19,8 @@
 // Combine is one warp per token: for each pair of 16-byte column vectors per
 // lane the k source rows are loaded before the fma chain runs over j in slot
 // order.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace moe {
@@ -357,4 +359,59 @@ MOE_API moe_status moe_combine(const uint16_t *out_sorted, const int32_t *slot_t
     if (grid > cap) grid = cap;
     combine_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(out_sorted, slot_to_sorted, gates, T, k, d, y);
     return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// moe_dispatch_noalloc: moe_dispatch with its scratch in a static device array
+// of this library, for callers that cannot lend a workspace (see moe_r3.h).
+// The array is a fixed MOE_DISPATCH_NOALLOC_MAX_SCRATCH bytes on every device
+// that loads the library and stays allocated until the process exits.  All
+// calls share it, so two calls whose work overlaps on the GPU (different
+// streams, or different host threads) race on it.  No word of it needs to
+// start at zero: every word the dispatch kernels read was written earlier in
+// the same call, so the contents left by the previous call do not matter.
+
+namespace moe {
+
+static __device__ __align__(256) uint8_t g_dispatch_scratch[MOE_DISPATCH_NOALLOC_MAX_SCRATCH];
+
+// Device address of g_dispatch_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in; the device address comes
+// from cudaGetSymbolAddress, queried once per device (with that device
+// current) and kept in a per-device slot.  Concurrent first calls store the
+// same value.
+static void *dispatch_scratch_address()
+{
+    static std::atomic<void *> slot[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (dev >= 0 && dev < 64) {
+        void *p = slot[dev].load(std::memory_order_acquire);
+        if (p) return p;
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (dev >= 0 && dev < 64) slot[dev].store(p, std::memory_order_release);
+    return p;
+}
+
+} // namespace moe
+
+MOE_API moe_status moe_dispatch_noalloc(const int32_t *topk_ids, int T, int k, int E, const void *rows,
+                                        int64_t row_bytes, const float *row_scales, int scales_per_row,
+                                        int32_t *expert_counts, int32_t *expert_offsets, int32_t *sorted_to_slot,
+                                        int32_t *slot_to_sorted, void *rows_sorted, float *scales_sorted,
+                                        int32_t *dev_status, void *stream)
+{
+    if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024) return MOE_ERR_SHAPE;
+    if ((int64_t)T * k >= (1LL << 31)) return MOE_ERR_SHAPE;
+    if (moe_dispatch_workspace_size(T, k, E) > (size_t)MOE_DISPATCH_NOALLOC_MAX_SCRATCH) return MOE_ERR_WORKSPACE;
+    void *scratch = dispatch_scratch_address();
+    if (!scratch) return MOE_ERR_CUDA;
+    return moe_dispatch(topk_ids, T, k, E, rows, row_bytes, row_scales, scales_per_row, expert_counts,
+                        expert_offsets, sorted_to_slot, slot_to_sorted, rows_sorted, scales_sorted, scratch,
+                        (size_t)MOE_DISPATCH_NOALLOC_MAX_SCRATCH, dev_status, stream);
 }

@@ -33,6 +33,7 @@ _SIGS = {
     "fp8_block_quant": (I, [P, I64, I64, I64, I, P, P, P]),
     "moe_dispatch_workspace_size": (SZ, [I, I, I]),
     "moe_dispatch": (I, [P, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, SZ, P, P]),
+    "moe_dispatch_noalloc": (I, [P, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, P]),
     "moe_grouped_ffn_workspace_size": (SZ, [I64, I, I]),
     "moe_grouped_ffn_fp8": (I, [P, P, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_combine": (I, [P, P, P, I, I, I, P, P]),
@@ -200,6 +201,47 @@ def moe_dispatch(topk_ids, E, rows=None, row_scales=None, expert_counts=None, ex
         _ptr(expert_offsets), _ptr(sorted_to_slot), _ptr(slot_to_sorted), _ptr(rows_sorted),
         _ptr(scales_sorted), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream)))
+    return expert_counts, expert_offsets, sorted_to_slot, slot_to_sorted, rows_sorted, scales_sorted
+
+
+MOE_DISPATCH_NOALLOC_MAX_SCRATCH = 4 << 20
+
+
+def moe_dispatch_noalloc(topk_ids, E, rows=None, row_scales=None, expert_counts=None, expert_offsets=None,
+                         sorted_to_slot=None, slot_to_sorted=None, rows_sorted=None, scales_sorted=None,
+                         dev_status=None, stream=None):
+    """moe_dispatch without a workspace: the library's static device scratch
+    is used instead (for callers that cannot allocate device memory at call
+    time).  Outputs not passed in are still allocated here by torch; pass
+    them all to keep the call allocation-free.  Calls that overlap on the GPU
+    share the scratch and race."""
+    T, k = topk_ids.shape
+    A = T * k
+    _want(topk_ids, torch.int32, (T, k), "topk_ids")
+    dev = topk_ids
+    expert_counts = _empty((E,), torch.int32, dev) if expert_counts is None else expert_counts
+    expert_offsets = _empty((E + 1,), torch.int32, dev) if expert_offsets is None else expert_offsets
+    sorted_to_slot = _empty((A,), torch.int32, dev) if sorted_to_slot is None else sorted_to_slot
+    slot_to_sorted = _empty((A,), torch.int32, dev) if slot_to_sorted is None else slot_to_sorted
+    _want(expert_counts, torch.int32, (E,), "expert_counts")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(sorted_to_slot, torch.int32, (A,), "sorted_to_slot")
+    _want(slot_to_sorted, torch.int32, (A,), "slot_to_sorted")
+    row_bytes, spr = 0, 0
+    if rows is not None:
+        if rows.shape[0] != T or not rows.is_contiguous() or not rows.is_cuda:
+            raise ValueError("rows: contiguous CUDA tensor with T rows")
+        row_bytes = rows[0].numel() * rows.element_size() if T > 0 else rows.stride(0) * rows.element_size()
+        rows_sorted = _empty((A,) + tuple(rows.shape[1:]), rows.dtype, dev) if rows_sorted is None else rows_sorted
+        if row_scales is not None:
+            spr = row_scales.shape[1]
+            _want(row_scales, torch.float32, (T, spr), "row_scales")
+            scales_sorted = _empty((A, spr), torch.float32, dev) if scales_sorted is None else scales_sorted
+            _want(scales_sorted, torch.float32, (A, spr), "scales_sorted")
+    _check("moe_dispatch_noalloc", _lib.moe_dispatch_noalloc(
+        _ptr(topk_ids), T, k, E, _ptr(rows), row_bytes, _ptr(row_scales), spr, _ptr(expert_counts),
+        _ptr(expert_offsets), _ptr(sorted_to_slot), _ptr(slot_to_sorted), _ptr(rows_sorted),
+        _ptr(scales_sorted), _ptr(dev_status), _stream(stream)))
     return expert_counts, expert_offsets, sorted_to_slot, slot_to_sorted, rows_sorted, scales_sorted
 
 

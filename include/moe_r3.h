@@ -155,6 +155,35 @@ moe_status moe_dispatch(const int32_t *topk_ids, int T, int k, int E, const void
                         void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * moe_dispatch_noalloc -- moe_dispatch without a caller workspace.
+ *
+ * The page describes no such call; it exists for callers of this library
+ * that cannot allocate device memory when they dispatch: a process that
+ * plans its whole device-memory budget up front and has no spare buffer to
+ * lend, or a latency-critical path that must not call cudaMalloc (which may
+ * synchronise the device).  Arguments, results and errors are those of
+ * moe_dispatch, without `workspace` / `workspace_bytes`: the scratch lives
+ * in a static device array of MOE_DISPATCH_NOALLOC_MAX_SCRATCH bytes inside
+ * the library, held on every GPU that loads the library until the process
+ * exits.  A request whose moe_dispatch_workspace_size(T, k, E) exceeds that
+ * limit returns MOE_ERR_WORKSPACE before anything is launched (4 MiB covers,
+ * e.g., E = 256 with T*k up to 4M slots, or E = 1024 with T*k up to 1M).
+ * Nothing is allocated or freed: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and keeps it, so
+ * make that first call before any stream capture.  Every call shares the one
+ * array: calls whose work overlaps on the GPU (other streams or threads)
+ * race on it and must be ordered by the caller.  No part of the array needs
+ * to start zeroed; the contents a previous call left are never read.
+ * ---------------------------------------------------------------------- */
+#define MOE_DISPATCH_NOALLOC_MAX_SCRATCH (4u << 20)
+moe_status moe_dispatch_noalloc(const int32_t *topk_ids, int T, int k, int E, const void *rows,
+                                int64_t row_bytes, const float *row_scales, int scales_per_row,
+                                int32_t *expert_counts, int32_t *expert_offsets, int32_t *sorted_to_slot,
+                                int32_t *slot_to_sorted, void *rows_sorted, float *scales_sorted,
+                                int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * moe_grouped_ffn_fp8 -- per-expert SwiGLU FFN as two grouped block-scaled
  * FP8 GEMMs on the tensor cores ("FP8 training", DeepSeek-V3 recipe).
  *
