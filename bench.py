@@ -140,7 +140,7 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     cfg = S.CONFIGS[args.workload]
-    layer, x, replay = build_workload(cfg, dev, args.seed + rank)
+    layer, x, replay = build_workload(cfg, dev, rank_seed(args.seed, rank))
     T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
     A = T * k
     stream = torch.cuda.current_stream()
@@ -224,14 +224,35 @@ def run_gpu(args, rank, world):
     e2e_ms = a.elapsed_time(b)
     h2d = T * d * 2 + (rh.numel() * 4 if rh is not None else 0)
 
-    vals = torch.tensor([total_ms, e2e_ms], dtype=torch.float64)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = vals.tolist()
+    total_ms, e2e_ms = reduce_max([total_ms, e2e_ms], world)
     avg = {n: sum(v) / len(v) for n, v in marks.items()}
     return dict(cfg=cfg, total_ms=total_ms, e2e_ms=e2e_ms, avg=avg, clocks=clocks, status=status, h2d=h2d,
                 d2h=T * d * 2, x=x, layer=layer)
+
+
+def reduce_max(vals, world):
+    """Max over ranks of per-rank timings (the slowest rank sets the job's
+    time); a no-op for one rank.  Uses the process group's own device (CUDA
+    for NCCL, host for gloo)."""
+    import torch
+    if world <= 1:
+        return list(vals)
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(list(vals), dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def job_throughput(tokens_per_rank, steps, world, total_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time
+    (token sharding, weak scaling: each rank runs its own batch)."""
+    return tokens_per_rank * steps * world / (total_ms * 1e-3)
+
+
+def rank_seed(seed, rank):
+    """Each rank draws its own batch (and its own replica weights)."""
+    return seed + rank
 
 
 def rooflines(cfg, avg, peaks):
@@ -400,7 +421,7 @@ def main():
     ap.add_argument("--workload", default="large")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=256, help="token sample of the CPU baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=1024, help="token sample of the CPU baseline")
     ap.add_argument("--ref-tokens", type=int, default=32, help="token sample per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dispatch-combine", action="store_true")
@@ -447,9 +468,8 @@ def main():
     peaks = _peaks()
     r = run_gpu(args, rank, world)
     cfg = r["cfg"]
-    tokens = cfg.T * args.steps * world
-    value = tokens / (r["total_ms"] * 1e-3)
-    e2e = tokens / (r["e2e_ms"] * 1e-3)
+    value = job_throughput(cfg.T, args.steps, world, r["total_ms"])
+    e2e = job_throughput(cfg.T, args.steps, world, r["e2e_ms"])
     ffn, extra = rooflines(cfg, r["avg"], peaks)
     launches = sum(KERNELS_PER_STEP[n] for n in ("quant", "dispatch", "ffn", "combine")) + 1
     out = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
