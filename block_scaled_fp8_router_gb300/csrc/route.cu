@@ -9,20 +9,18 @@
 // index, computed by one thread (a SIMT register-tiled GEMM, not the tensor
 // cores, whose accumulation order is not specified).
 //
-// route_topk_kernel: CTA = 128 threads, 32 tokens x all experts (passes of
-// 256); each thread owns 8 tokens x 8 experts of fp32 accumulators (6
-// shared-memory wavefronts per 64 FMAs per warp); bf16 tiles of x and W_r (32
-// deep) are widened to fp32 in shared memory with conflict-free stores, the
-// next tile is loaded into registers while the current one is consumed.
-// Logits never leave the SM: they go to shared memory, and each warp then
-// selects top-k for 8 tokens with k rounds of a (value, index) arg-max.
+// route_topk_kernel: one cluster of ceil(E/128) CTAs per 32 tokens; each
+// 128-thread CTA computes 32 tokens x 128 experts with 4 x 8 fp32
+// accumulators per thread (3 shared-memory wavefronts per 32 FMAs per warp),
+// bf16 tiles of x and W_r (32 deep) widened to fp32 in shared memory with
+// conflict-free stores while the next tile loads into registers.  Logits stay
+// on chip: each CTA selects its own top-k, CTA 0 merges the candidates it
+// receives through distributed shared memory.
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int RT_BT = 32;   // tokens per CTA
-constexpr int RT_EP = 256;  // experts per pass
-constexpr int RT_BK = 32;   // hidden indices per shared-memory tile
+constexpr int RT_BT = 32;   // replay: tokens per CTA
 constexpr int RR_BK = 256;  // replay: hidden indices per staged x chunk
 
 // Strict total order of the selection: larger value first, -0 == +0, NaN
@@ -73,134 +71,246 @@ __device__ __forceinline__ float warp_gate(int lane, int k, float my_l, int scor
     return g * route_scale;
 }
 
-__global__ void __launch_bounds__(128, 3) route_topk_kernel(const uint16_t *__restrict__ x,
-                                                            const uint16_t *__restrict__ wr, int T, int d, int E,
-                                                            int k, int score_fn, int renorm, float route_scale,
-                                                            int32_t *__restrict__ ids, float *__restrict__ gates,
-                                                            int32_t *__restrict__ capture,
-                                                            float *__restrict__ logits_out)
+// ---- cluster helpers (route_topk runs one cluster per 32 tokens, one CTA
+// per 128 experts) ----
+__device__ __forceinline__ uint32_t cl_rank()
 {
-    extern __shared__ float4 smem4[];
-    float *xs = reinterpret_cast<float *>(smem4);   // [RT_BK][RT_BT]
-    float *ws = xs + RT_BK * RT_BT;                  // [RT_BK][RT_EP]
-    float *lg = ws + RT_BK * RT_EP;                  // [RT_BT][Epad]
-    const int Epad = (E + 31) & ~31;
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cl_size()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cl_id()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cl_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank)
+{
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(out)
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+    return out;
+}
+__device__ __forceinline__ void cl_st_f2(uint32_t addr, float a, float b)
+{
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * RT_BT;
-    const int tt = (lane >> 3) * 8;                // my 8 tokens in the tile
-    const int ee = warp * 64 + (lane & 7) * 8;     // my 8 experts in the pass
-
-    // tile loaders: x chunk (token = tid & 31, 8-wide part = tid >> 5) and
-    // 8 W_r chunks (expert = tid + 128 (r & 1), part = r >> 1); consecutive
-    // lanes write consecutive shared-memory words (no bank conflicts)
-    const int xt = tid & 31, xp = tid >> 5;
-    for (int e0 = 0; e0 < E; e0 += RT_EP) {
-        float acc[8][8];
+// k rounds of a warp-wide arg-max under ranks_before over the candidates
+// lane l holds (vals[m], idxs[m]) for m < nm (idx < 0 = no candidate); lane j
+// ends with the j-th pick in (out_v, out_i) (out_i = -1 if there were fewer).
+template <int NM>
+__device__ __forceinline__ void warp_topk(const float *vals, const int *idxs, int k, int lane, float &out_v,
+                                          int &out_i)
+{
+    uint32_t taken = 0;
+    out_v = 0.0f;
+    out_i = -1;
+    for (int j = 0; j < k; j++) {
+        float bv = 0.0f;
+        int bi = -1, bm = -1;
 #pragma unroll
-        for (int a = 0; a < 8; a++)
-#pragma unroll
-            for (int b = 0; b < 8; b++) acc[a][b] = 0.0f;
-
-        uint4 rx, rw[8];
-        auto load_tile = [&](int k0) {
-            const int t = t0 + xt;
-            rx = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 8))
-                       : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int r = 0; r < 8; r++) {
-                const int e = e0 + tid + 128 * (r & 1), p = r >> 1;
-                rw[r] = e < E ? __ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + k0 + p * 8))
-                              : make_uint4(0, 0, 0, 0);
-            }
-        };
-        load_tile(0);
-        for (int k0 = 0; k0 < d; k0 += RT_BK) {
-            __syncthreads();
-            {
-                float f[8];
-                unpack_bf16x8(rx, f);
-#pragma unroll
-                for (int j = 0; j < 8; j++) xs[(xp * 8 + j) * RT_BT + xt] = f[j];
-#pragma unroll
-                for (int r = 0; r < 8; r++) {
-                    const int e = tid + 128 * (r & 1), p = r >> 1;
-                    unpack_bf16x8(rw[r], f);
-#pragma unroll
-                    for (int j = 0; j < 8; j++) ws[(p * 8 + j) * RT_EP + e] = f[j];
-                }
-            }
-            __syncthreads();
-            if (k0 + RT_BK < d) load_tile(k0 + RT_BK);
-#pragma unroll
-            for (int i = 0; i < RT_BK; i++) {
-                const float4 x0 = *reinterpret_cast<const float4 *>(&xs[i * RT_BT + tt]);
-                const float4 x1 = *reinterpret_cast<const float4 *>(&xs[i * RT_BT + tt + 4]);
-                const float4 w0 = *reinterpret_cast<const float4 *>(&ws[i * RT_EP + ee]);
-                const float4 w1 = *reinterpret_cast<const float4 *>(&ws[i * RT_EP + ee + 4]);
-                const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                for (int a = 0; a < 8; a++)
-#pragma unroll
-                    for (int b = 0; b < 8; b++) acc[a][b] = fmaf(xa[a], wb[b], acc[a][b]);
+        for (int m = 0; m < NM; m++) {
+            if ((taken >> m) & 1u) continue;
+            const int e = idxs[m];
+            if (e < 0) continue;
+            if (bi < 0 || ranks_before(vals[m], e, bv, bi)) {
+                bv = vals[m];
+                bi = e;
+                bm = m;
             }
         }
+        float wv = bv;
+        int wi = bi;
 #pragma unroll
-        for (int a = 0; a < 8; a++)
-#pragma unroll
-            for (int b = 0; b < 8; b++) {
-                const int e = e0 + ee + b;
-                if (e < E) lg[(tt + a) * Epad + e] = acc[a][b];
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, wv, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, wi, o);
+            if (oi >= 0 && (wi < 0 || ranks_before(ov, oi, wv, wi))) {
+                wv = ov;
+                wi = oi;
             }
+        }
+        if (wi >= 0 && bi == wi && bm >= 0) taken |= 1u << bm;  // the winning lane retires its entry
+        if (lane == j) {
+            out_v = wv;
+            out_i = wi;
+        }
+    }
+}
+
+constexpr int RC_BT = 32;           // tokens per cluster
+constexpr int RC_EC = 128;          // experts per CTA
+constexpr int RC_BK = 32;           // hidden indices per shared-memory tile
+constexpr int RC_LGS = RC_EC + 4;   // logits row stride (floats)
+
+// One cluster of ceil(E/128) CTAs per 32 tokens.  CTA r computes the logits
+// of experts 128r .. 128r+127 for the 32 tokens (128 threads, 4 tokens x 8
+// experts of fp32 fma-chain accumulators each), keeps them in shared memory,
+// selects its own top-k per token and sends those (value, index) candidates
+// to CTA 0 of the cluster through distributed shared memory; CTA 0 merges
+// them into the top-k over all experts (every member of the global top-k is
+// in its own CTA's top-k, and the order is a strict total order, so the merge
+// is exact) and writes ids, gates and the capture.
+__global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restrict__ x,
+                                                         const uint16_t *__restrict__ wr, int T, int d, int E,
+                                                         int k, int score_fn, int renorm, float route_scale,
+                                                         int32_t *__restrict__ ids, float *__restrict__ gates,
+                                                         int32_t *__restrict__ capture,
+                                                         float *__restrict__ logits_out)
+{
+    extern __shared__ float4 smem4[];
+    const int ncta = (int)cl_size();
+    const int rank = (int)cl_rank();
+    float *xs = reinterpret_cast<float *>(smem4);   // [RC_BK][RC_BT]
+    float *ws = xs + RC_BK * RC_BT;                  // [RC_BK][RC_EC]
+    float *lg = ws + RC_BK * RC_EC;                  // [RC_BT][RC_LGS]
+    float2 *cand = reinterpret_cast<float2 *>(lg + RC_BT * RC_LGS);  // CTA 0: [RC_BT][ncta*k]
+    float2 *msum = cand + RC_BT * ncta * k;                           // CTA 0: [RC_BT][ncta]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = (int)cl_id() * RC_BT;
+    const int e0 = rank * RC_EC;
+    const int tt = (lane >> 2) * 4;                 // my 4 tokens in the tile
+    const int ee = warp * 32 + (lane & 3) * 8;      // my 8 experts of this CTA's 128
+
+    // tile loaders: x chunk (token tid & 31, 8-wide part tid >> 5) and four
+    // W_r chunks (expert tid, part r); consecutive lanes write consecutive
+    // shared-memory words
+    const int xt = tid & 31, xp = tid >> 5;
+    float acc[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; a++)
+#pragma unroll
+        for (int b = 0; b < 8; b++) acc[a][b] = 0.0f;
+    uint4 rx, rw[4];
+    auto load_tile = [&](int k0) {
+        const int t = t0 + xt;
+        rx = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 8))
+                   : make_uint4(0, 0, 0, 0);
+        const int e = e0 + tid;
+#pragma unroll
+        for (int r = 0; r < 4; r++)
+            rw[r] = e < E ? __ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + k0 + r * 8))
+                          : make_uint4(0, 0, 0, 0);
+    };
+    load_tile(0);
+    for (int k0 = 0; k0 < d; k0 += RC_BK) {
+        __syncthreads();
+        {
+            float f[8];
+            unpack_bf16x8(rx, f);
+#pragma unroll
+            for (int j = 0; j < 8; j++) xs[(xp * 8 + j) * RC_BT + xt] = f[j];
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+                unpack_bf16x8(rw[r], f);
+#pragma unroll
+                for (int j = 0; j < 8; j++) ws[(r * 8 + j) * RC_EC + tid] = f[j];
+            }
+        }
+        __syncthreads();
+        if (k0 + RC_BK < d) load_tile(k0 + RC_BK);
+#pragma unroll
+        for (int i = 0; i < RC_BK; i++) {
+            const float4 xv = *reinterpret_cast<const float4 *>(&xs[i * RC_BT + tt]);
+            const float4 w0 = *reinterpret_cast<const float4 *>(&ws[i * RC_EC + ee]);
+            const float4 w1 = *reinterpret_cast<const float4 *>(&ws[i * RC_EC + ee + 4]);
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+            const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int a = 0; a < 4; a++)
+#pragma unroll
+                for (int b = 0; b < 8; b++) acc[a][b] = fmaf(xa[a], wb[b], acc[a][b]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; a++) {
+        *reinterpret_cast<float4 *>(&lg[(tt + a) * RC_LGS + ee]) =
+            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        *reinterpret_cast<float4 *>(&lg[(tt + a) * RC_LGS + ee + 4]) =
+            make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
     }
     __syncthreads();
+    const int ne = min(RC_EC, E - e0);   // experts of this CTA
+    if (logits_out)
+        for (int i = tid; i < RC_BT * ne; i += blockDim.x) {
+            const int tl = i / ne, el = i - tl * ne;
+            if (t0 + tl < T) logits_out[(int64_t)(t0 + tl) * E + e0 + el] = lg[tl * RC_LGS + el];
+        }
 
-    // ---- top-k + gates: warp w handles tokens 8w .. 8w+7 of the tile ----
+    // ---- per-CTA top-k of each token over its 128 experts; candidates to CTA 0 ----
+    const int nc = ncta * k;
+    for (int tl = warp * 8; tl < warp * 8 + 8; tl++) {
+        if (t0 + tl >= T) break;
+        float vals[4];
+        int idx[4];
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const int el = m * 32 + lane;
+            vals[m] = el < ne ? lg[tl * RC_LGS + el] : 0.0f;
+            idx[m] = el < ne ? e0 + el : -1;
+        }
+        float v;
+        int i;
+        warp_topk<4>(vals, idx, k, lane, v, i);
+        if (lane < k) cl_st_f2(cl_map(&cand[tl * nc + rank * k + lane], 0), v, __int_as_float(i));
+        if (score_fn == MOE_SCORE_SOFTMAX && !renorm) {
+            // this CTA's share of the full softmax denominator, as (max, sum exp(l - max))
+            float mloc = -INFINITY;
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+                if (idx[m] >= 0) mloc = fmaxf(mloc, vals[m]);
+            mloc = warp_max(mloc);
+            float sloc = 0.0f;
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+                if (idx[m] >= 0) sloc += expf(vals[m] - mloc);
+            sloc = warp_sum(sloc);
+            if (lane == 0) cl_st_f2(cl_map(&msum[tl * ncta + rank], 0), mloc, sloc);
+        }
+    }
+    cl_sync();  // every candidate has reached CTA 0; nothing is written remotely after this
+    if (rank != 0) return;
+
+    // ---- CTA 0: merge the clusters' candidates, gates, outputs ----
     for (int tl = warp * 8; tl < warp * 8 + 8; tl++) {
         const int t = t0 + tl;
         if (t >= T) break;
-        const float *row = lg + tl * Epad;
-        if (logits_out)
-            for (int e = lane; e < E; e += 32) logits_out[(int64_t)t * E + e] = row[e];
-        uint32_t taken = 0;
-        int my_id = -1;
-        float my_l = 0.0f;
-        for (int j = 0; j < k; j++) {
-            float bv = 0.0f;
-            int bi = -1;
-            for (int m = 0; m * 32 + lane < E; m++) {
-                if (taken & (1u << m)) continue;
-                const int e = m * 32 + lane;
-                const float v = row[e];
-                if (bi < 0 || ranks_before(v, e, bv, bi)) {
-                    bv = v;
-                    bi = e;
-                }
-            }
+        float vals[8];
+        int idx[8];
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-                if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == j) {
-                my_id = bi;
-                my_l = bv;
-            }
+        for (int m = 0; m < 8; m++) {
+            const int c = m * 32 + lane;
+            const float2 cv = c < nc ? cand[tl * nc + c] : make_float2(0.0f, __int_as_float(-1));
+            vals[m] = cv.x;
+            idx[m] = __float_as_int(cv.y);
         }
+        float my_l;
+        int my_id;
+        warp_topk<8>(vals, idx, k, lane, my_l, my_id);
         float full_max = 0.0f, full_sum = 0.0f;
         if (score_fn == MOE_SCORE_SOFTMAX && !renorm) {
-            full_max = __shfl_sync(0xFFFFFFFFu, my_l, 0);
-            float s = 0.0f;
-            for (int e = lane; e < E; e += 32) s += expf(row[e] - full_max);
-            full_sum = warp_sum(s);
+            float M = -INFINITY;
+            for (int r = 0; r < ncta; r++) M = fmaxf(M, msum[tl * ncta + r].x);
+            float S = 0.0f;
+            for (int r = 0; r < ncta; r++) S += msum[tl * ncta + r].y * expf(msum[tl * ncta + r].x - M);
+            full_max = M;
+            full_sum = S;
         }
-        const float g = warp_gate(lane, k, my_l, score_fn, renorm, route_scale, full_max, full_sum);
+        const float g = warp_gate(lane, k, lane < k ? my_l : 0.0f, score_fn, renorm, route_scale, full_max, full_sum);
         if (lane < k) {
             ids[(int64_t)t * k + lane] = my_id;
             gates[(int64_t)t * k + lane] = g;
@@ -329,15 +439,27 @@ MOE_API moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, i
     if (T == 0) return MOE_OK;
     if (!x || !w_router || !topk_ids || !topk_gates) return MOE_ERR_NULL;
     if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_ALIGN;
-    const int Epad = (E + 31) & ~31;
-    const size_t smem = sizeof(float) * (RT_BK * RT_BT + RT_BK * RT_EP + (size_t)RT_BT * Epad);
+    const int ncta = (E + RC_EC - 1) / RC_EC;  // <= 8: a portable cluster size
+    const size_t smem = sizeof(float) * (RC_BK * RC_BT + RC_BK * RC_EC + (size_t)RC_BT * RC_LGS) +
+                        sizeof(float2) * ((size_t)RC_BT * ncta * k + (size_t)RC_BT * ncta);
     if (cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
-    const int grid = (T + RT_BT - 1) / RT_BT;
-    route_topk_kernel<<<grid, 128, smem, as_stream(stream)>>>(x, w_router, T, d, E, k, score_fn, renorm,
-                                                               route_scale, topk_ids, topk_gates, capture_kT,
-                                                               logits_out);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ncta;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(((T + RC_BT - 1) / RC_BT) * ncta));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = as_stream(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, route_topk_kernel, x, w_router, T, d, E, k, score_fn, renorm, route_scale,
+                           topk_ids, topk_gates, capture_kT, logits_out) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return launch_status();
 }
 
