@@ -20,8 +20,6 @@
 
 namespace moe {
 
-constexpr int RT_BT = 32;   // replay: tokens per CTA
-constexpr int RR_BK = 256;  // replay: hidden indices per staged x chunk
 
 // Strict total order of the selection: larger value first, -0 == +0, NaN
 // below every number, equal keys by lower index.
@@ -319,11 +317,16 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
     }
 }
 
-// Replay: CTA = 32 tokens.  Copies the layer slab [k, T] to [T, k], checks
-// ids, and (if x is given) evaluates the router logits of the replayed
-// experts -- one fma chain per (token, slot), as in route_topk_kernel -- for
-// the gates.
-__global__ void __launch_bounds__(256) route_replay_kernel(const int32_t *__restrict__ replay_kT,
+// Replay.  CTA = 256 threads = 256/TP tokens, TP = threads per token (2, 4
+// or 8, a power of two with TP * 4 >= k).  Copies the layer slab [k, T] to
+// [T, k] and checks the ids; if x is given, thread (token, part q) evaluates
+// the router logits of the token's slots q*SP .. q*SP+SP-1 (SP = ceil(k/TP)
+// <= 4) -- one fma chain per slot in ascending hidden index, as in
+// route_topk_kernel -- so every x value it loads feeds SP chains.  x and the
+// replayed W_r rows are read straight from L1/L2, 8 bf16 per load, one step
+// of 8 ahead.  Gates come from warp_gate, the routing kernel's code.
+template <int TP>
+__global__ void __launch_bounds__(256, 2) route_replay_kernel(const int32_t *__restrict__ replay_kT,
                                                            const uint16_t *__restrict__ x,
                                                            const uint16_t *__restrict__ wr, int T, int d, int E,
                                                            int k, int score_fn, int renorm, float route_scale,
@@ -331,16 +334,16 @@ __global__ void __launch_bounds__(256) route_replay_kernel(const int32_t *__rest
                                                            float *__restrict__ gates,
                                                            int32_t *__restrict__ dev_status)
 {
-    __shared__ int32_t sid[RT_BT * 32];
-    __shared__ float slg[RT_BT * 32];
-    __shared__ int sbad[RT_BT];
-    __shared__ float xs[RT_BT * (RR_BK + 1)];
+    constexpr int TPC = 256 / TP;  // tokens per CTA
+    __shared__ int32_t sid[TPC * 32];
+    __shared__ float slg[TPC * 32];
+    __shared__ int sbad[TPC];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * RT_BT;
-    const int nt = min(RT_BT, T - t0);
+    const int t0 = blockIdx.x * TPC;
+    const int nt = min(TPC, T - t0);
 
-    for (int idx = tid; idx < RT_BT * k; idx += blockDim.x) {
-        const int j = idx / RT_BT, tl = idx % RT_BT;
+    for (int idx = tid; idx < TPC * k; idx += blockDim.x) {
+        const int j = idx / TPC, tl = idx % TPC;
         if (tl < nt) {
             const int32_t v = replay_kT[(int64_t)j * T + t0 + tl];
             sid[tl * k + j] = v;
@@ -361,59 +364,59 @@ __global__ void __launch_bounds__(256) route_replay_kernel(const int32_t *__rest
     }
     if (x == nullptr) return;
 
-    // logits of the replayed experts: pair p = (tl, j), p = tid + 256 r
-    constexpr int MAXP = (RT_BT * 32) / 256;  // k <= 32
-    float acc[MAXP];
+    const int SP = (k + TP - 1) / TP;
+    const int tl = tid / TP, q = tid % TP;
+    const bool tok_ok = tl < nt;
+    const uint16_t *xrow = x + (int64_t)(t0 + (tok_ok ? tl : 0)) * d;
+    const uint16_t *wrow[4];
+    bool on[4];
 #pragma unroll
-    for (int r = 0; r < MAXP; r++) acc[r] = 0.0f;
-    const int npairs = nt * k;
-    for (int c0 = 0; c0 < d; c0 += RR_BK) {
-        __syncthreads();
-        for (int idx = tid; idx < RT_BT * (RR_BK / 8); idx += blockDim.x) {
-            const int tl = idx / (RR_BK / 8), p = idx % (RR_BK / 8);
-            float f[8];
-            if (tl < nt) {
-                unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(x + (int64_t)(t0 + tl) * d + c0 + p * 8)), f);
-            } else {
+    for (int u = 0; u < 4; u++) {
+        const int j = q * SP + u;
+        const int32_t e = (tok_ok && u < SP && j < k) ? sid[tl * k + j] : -1;
+        on[u] = e >= 0 && e < E;
+        wrow[u] = wr + (int64_t)(on[u] ? e : 0) * d;
+    }
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (tok_ok) {
+        uint4 cx = __ldg(reinterpret_cast<const uint4 *>(xrow)), cw[4];
 #pragma unroll
-                for (int j = 0; j < 8; j++) f[j] = 0.0f;
+        for (int u = 0; u < 4; u++) cw[u] = on[u] ? __ldg(reinterpret_cast<const uint4 *>(wrow[u])) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < d; i += 8) {
+            uint4 nx = make_uint4(0, 0, 0, 0), nw[4];
+            const bool more = i + 8 < d;
+            if (more) nx = __ldg(reinterpret_cast<const uint4 *>(xrow + i + 8));
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                nw[u] = (more && on[u]) ? __ldg(reinterpret_cast<const uint4 *>(wrow[u] + i + 8)) : make_uint4(0, 0, 0, 0);
+            float xf[8];
+            unpack_bf16x8(cx, xf);
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                if (!on[u]) continue;
+                float wf[8];
+                unpack_bf16x8(cw[u], wf);
+                float a = acc[u];
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) a = fmaf(xf[jj], wf[jj], a);
+                acc[u] = a;
             }
+            cx = nx;
 #pragma unroll
-            for (int j = 0; j < 8; j++) xs[tl * (RR_BK + 1) + p * 8 + j] = f[j];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < MAXP; r++) {
-            const int p = tid + 256 * r;
-            if (p < npairs) {
-                const int tl = p / k;
-                const int32_t e = sid[p];
-                if (e >= 0 && e < E) {
-                    const uint16_t *wrow = wr + (int64_t)e * d + c0;
-                    const float *xrow = xs + tl * (RR_BK + 1);
-                    float a = acc[r];
-                    for (int i = 0; i < RR_BK; i += 8) {
-                        float f[8];
-                        unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(wrow + i)), f);
-#pragma unroll
-                        for (int j = 0; j < 8; j++) a = fmaf(xrow[i + j], f[j], a);
-                    }
-                    acc[r] = a;
-                }
-            }
+            for (int u = 0; u < 4; u++) cw[u] = nw[u];
         }
     }
 #pragma unroll
-    for (int r = 0; r < MAXP; r++) {
-        const int p = tid + 256 * r;
-        if (p < npairs) slg[p] = acc[r];
+    for (int u = 0; u < 4; u++) {
+        const int j = q * SP + u;
+        if (tok_ok && u < SP && j < k) slg[tl * k + j] = acc[u];
     }
     __syncthreads();
-    for (int tl = warp; tl < nt; tl += 8) {
-        const float my_l = lane < k ? slg[tl * k + lane] : 0.0f;
+    for (int t = warp; t < nt; t += 8) {
+        const float my_l = lane < k ? slg[t * k + lane] : 0.0f;
         float g = warp_gate(lane, k, my_l, score_fn, renorm, route_scale, 0.0f, 0.0f);
-        if (sbad[tl]) g = 0.0f;
-        if (lane < k) gates[(int64_t)(t0 + tl) * k + lane] = g;
+        if (sbad[t]) g = 0.0f;
+        if (lane < k) gates[(int64_t)(t0 + t) * k + lane] = g;
     }
 }
 
@@ -474,9 +477,19 @@ MOE_API moe_status moe_route_replay(const int32_t *replay_kT, const uint16_t *x,
     if (!replay_kT || !topk_ids) return MOE_ERR_NULL;
     if (x && (!w_router || !topk_gates)) return MOE_ERR_NULL;
     if (x && (!aligned16(x) || !aligned16(w_router))) return MOE_ERR_ALIGN;
-    const int grid = (T + RT_BT - 1) / RT_BT;
-    route_replay_kernel<<<grid, 256, 0, as_stream(stream)>>>(replay_kT, x, w_router, T, d, E, k, score_fn,
-                                                              renorm, route_scale, topk_ids, topk_gates,
-                                                              dev_status);
+    cudaStream_t st = as_stream(stream);
+    if (k <= 8) {
+        route_replay_kernel<2><<<(T + 127) / 128, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k, score_fn,
+                                                                 renorm, route_scale, topk_ids, topk_gates,
+                                                                 dev_status);
+    } else if (k <= 16) {
+        route_replay_kernel<4><<<(T + 63) / 64, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k, score_fn,
+                                                               renorm, route_scale, topk_ids, topk_gates,
+                                                               dev_status);
+    } else {
+        route_replay_kernel<8><<<(T + 31) / 32, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k, score_fn,
+                                                               renorm, route_scale, topk_ids, topk_gates,
+                                                               dev_status);
+    }
     return launch_status();
 }
