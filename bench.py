@@ -41,6 +41,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
+# DRAM bytes (read + write) per routed row of the grouped FFN at d=7168, F=2048,
+# ~256 rows per expert: ncu capture of grouped_gemm_kernel<1> and <2> on the
+# large_e64 profiling shape (A = 16384 rows): 2.778e9 + 0.055e9 + 0.975e9 +
+# 0.217e9 bytes.  Valid for the kernel that capture measured.
+FFN_DRAM_BYTES_PER_ROW = (2.778e9 + 0.0554e9 + 0.975e9 + 0.2168e9) / 16384
 KERNELS_PER_STEP = {"route": 1, "replay": 1, "quant": 1, "dispatch": 4, "ffn": 2, "combine": 1}
 
 
@@ -132,14 +137,17 @@ def build_workload(cfg, dev, seed):
     return layer, x, replay
 
 
-def run_gpu(args, rank, world):
+def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None):
     import torch
     from block_scaled_fp8_router_gb300 import moe_r3 as Lb
     from block_scaled_fp8_router_gb300 import synthetic as S
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    cfg = S.CONFIGS[args.workload]
+    cfg = S.CONFIGS[workload or args.workload]
+    if cfg.layers > 1:
+        cfg = cfg.with_(layers=1)   # one layer of a stacked workload per step
+    steps = steps or args.steps
     layer, x, replay = build_workload(cfg, dev, rank_seed(args.seed, rank))
     T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
     A = T * k
@@ -184,7 +192,7 @@ def run_gpu(args, rank, world):
     with Clocks(dev.index) as clk:
         t0, t1 = ev(), ev()
         t0.record()
-        per = [step(True) for _ in range(args.steps)]
+        per = [step(True) for _ in range(steps)]
         t1.record()
         barrier()
     clocks = clk.summary()
@@ -194,32 +202,43 @@ def run_gpu(args, rank, world):
             marks[n].append(e[i].elapsed_time(e[i + 1]))
     status = Lb.check_status(layer.dev_status)
 
-    # ---- end to end through the public layer API: pinned host x in, y out ----
+    if not with_e2e:
+        avg = {n: sum(v) / len(v) for n, v in marks.items()}
+        total_ms = reduce_max([total_ms], world)[0]
+        return dict(cfg=cfg, total_ms=total_ms, avg=avg, clocks=clocks, status=status, steps=steps)
+
+    # ---- end to end through the public layer API: pinned host x in, y out,
+    # copies overlapped with compute by HostStreamer (two copy streams) ----
+    from block_scaled_fp8_router_gb300.layer import HostStreamer
     xh = torch.empty((T, d), dtype=torch.bfloat16, pin_memory=True)
     xh.copy_(x.cpu())
-    yh = torch.empty((T, d), dtype=torch.bfloat16, pin_memory=True)
-    xd = torch.empty_like(x)
+    yhs = [torch.empty((T, d), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
     rh = None
     if replay is not None:
         rh = torch.empty(replay.shape, dtype=torch.int32, pin_memory=True)
         rh.copy_(replay.cpu())
-        rd = torch.empty_like(replay)
+    streamer = HostStreamer(layer, T)
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
+    def e2e_run(n):
+        # the same pinned input batch every step (one batch of synthetic tokens)
+        reps = None
         if rh is not None:
+            rd = torch.empty_like(replay)
             rd.copy_(rh, non_blocking=True)
-        y = layer.forward(xd, replay_kT=rd if rh is not None else None)
-        yh.copy_(y, non_blocking=True)
+            reps = [rd] * n
+        streamer.run([xh] * n, [yhs[i & 1] for i in range(n)], reps)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    e2e_run(max(1, args.warmup))
+    streamer.synchronize()
     barrier()
     a, b = ev(), ev()
     a.record()
-    for _ in range(args.steps):
-        e2e_step()
+    streamer.h2d.wait_event(a)
+    streamer.d2h.wait_event(a)
+    e2e_run(steps)
+    torch.cuda.current_stream().wait_stream(streamer.d2h)
     b.record()
+    streamer.synchronize()
     barrier()
     e2e_ms = a.elapsed_time(b)
     h2d = T * d * 2 + (rh.numel() * 4 if rh is not None else 0)
@@ -263,7 +282,10 @@ def rooflines(cfg, avg, peaks):
     ffn = {"bound": "tensor", "kernel": "moe_grouped_ffn_fp8 (GEMM1+SwiGLU+requant, GEMM2)",
            "achieved": flops_ffn / (avg["ffn"] * 1e-3) / 1e12, "peak": fp8_peak, "unit": "TFLOP/s",
            "peak_note": "FP8 dense = 2 x measured bf16 burst (nominal FP8:BF16 ratio)" if peaks["source"] == "measured"
-           else "FP8 dense = 2 x fallback bf16", "traffic": None}
+           else "FP8 dense = 2 x fallback bf16",
+           "traffic": FFN_DRAM_BYTES_PER_ROW * A if cfg.d == 7168 and cfg.F == 2048 else None,
+           "traffic_note": "dram read+write bytes of both GEMM kernels from one ncu capture of the profiling shape "
+                           "(large_e64: same per-expert shape, 1/4 of the experts), scaled by routed rows"}
     ffn["frac"] = ffn["achieved"] / ffn["peak"]
     hbm = peaks["hbm_gbs"]
     row = d + 4 * d / 128                       # one FP8 row with its 1x128 scales
@@ -425,6 +447,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=32, help="token sample per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dispatch-combine", action="store_true")
+    ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -480,9 +503,23 @@ def main():
                    "d2h_bytes_per_step": r["d2h"]},
            "roofline": ffn, "extra": extra, "gpu_launches": launches * args.steps, "clocks": r["clocks"],
            "dev_status": r["status"], "peaks_source": peaks["source"]}
-    if cfg.name == "large" and not args.no_dispatch_combine:
+    if cfg.name == "large" and not args.no_replay:
         import torch
         del r
+        torch.cuda.empty_cache()
+        rr = run_gpu(args, rank, world, workload="multilayer_replay", with_e2e=False, steps=max(3, args.steps // 2))
+        rcfg = rr["cfg"]
+        rffn, rextra = rooflines(rcfg, rr["avg"], peaks)
+        out["replay_layer"] = {
+            "workload": f"multilayer_replay (one layer): T={rcfg.T} d={rcfg.d} E={rcfg.E} top_k={rcfg.k} "
+                        f"F={rcfg.F}, replayed payload with 8 hot and 8 empty experts, sigmoid gates",
+            "tokens/s": job_throughput(rcfg.T, rr["steps"], world, rr["total_ms"]),
+            "ms_per_step": rr["total_ms"] / rr["steps"], "ffn_TFLOP/s": rffn["achieved"],
+            "ffn_frac": rffn["frac"], "steps": rextra, "dev_status": rr["status"]}
+        del rr
+        torch.cuda.empty_cache()
+    if cfg.name == "large" and not args.no_dispatch_combine:
+        import torch
         torch.cuda.empty_cache()
         out["dispatch_combine"] = run_dispatch_combine(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
                                                        args.seed + rank, max(3, args.steps // 2), 3, peaks)

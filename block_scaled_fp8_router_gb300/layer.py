@@ -111,3 +111,65 @@ class MoELayerFP8:
                               dev_status=self.dev_status)
         y = self.y[:T] if y is None else y
         return L.moe_combine(self.out_sorted[:A], self.sl2[:A], gates, y=y)
+
+
+class HostStreamer:
+    """Forward of a sequence of host batches with the copies overlapped.
+
+    Batch i's x goes host -> device on one copy stream while batch i-1 runs
+    on the compute stream, and batch i-1's y goes device -> host on a second
+    copy stream while batch i runs; device x / y are double-buffered and
+    CUDA events order the three streams.  Host buffers should be pinned.
+    Only stream plumbing: every computation is the layer's kernels.
+    """
+
+    def __init__(self, layer: MoELayerFP8, T: int):
+        self.layer = layer
+        dev = layer.y.device
+        d = layer.w.d
+        self.T = T
+        self.xd = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.yd = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        self.x_ready = [torch.cuda.Event() for _ in range(2)]
+        self.y_ready = [torch.cuda.Event() for _ in range(2)]
+        self.y_drained = [torch.cuda.Event() for _ in range(2)]
+
+    def run(self, xs_host, ys_host, replays_device=None):
+        """xs_host[i] -> forward -> ys_host[i] for every i; returns when all
+        copies are enqueued (synchronise the compute / copy streams to wait)."""
+        compute = torch.cuda.current_stream()
+        n = len(xs_host)
+        fresh = [True, True]
+
+        def enqueue_h2d(i):
+            b = i & 1
+            with torch.cuda.stream(self.h2d):
+                if not fresh[b]:
+                    self.h2d.wait_event(self.y_ready[b])      # batch i-2 is done reading xd[b]
+                self.xd[b].copy_(xs_host[i], non_blocking=True)
+                self.x_ready[b].record(self.h2d)
+
+        if n:
+            enqueue_h2d(0)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                enqueue_h2d(i + 1)
+            compute.wait_event(self.x_ready[b])
+            if not fresh[b]:
+                compute.wait_event(self.y_drained[b])         # batch i-2's y has left yd[b]
+            replay = None if replays_device is None else replays_device[i]
+            self.layer.forward(self.xd[b], replay_kT=replay, y=self.yd[b])
+            self.y_ready[b].record(compute)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.y_ready[b])
+                ys_host[i].copy_(self.yd[b], non_blocking=True)
+                self.y_drained[b].record(self.d2h)
+            fresh[b] = False
+
+    def synchronize(self):
+        torch.cuda.current_stream().synchronize()
+        self.h2d.synchronize()
+        self.d2h.synchronize()
