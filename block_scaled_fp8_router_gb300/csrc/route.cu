@@ -149,14 +149,15 @@ __device__ __forceinline__ void warp_topk(const float *vals, const int *idxs, in
     }
 }
 
-constexpr int RC_BT = 32;           // tokens per cluster
+constexpr int RC_BT = 64;           // tokens per cluster
 constexpr int RC_EC = 128;          // experts per CTA
 constexpr int RC_BK = 32;           // hidden indices per shared-memory tile
 constexpr int RC_LGS = RC_EC + 4;   // logits row stride (floats)
 
-// One cluster of ceil(E/128) CTAs per 32 tokens.  CTA r computes the logits
-// of experts 128r .. 128r+127 for the 32 tokens (128 threads, 4 tokens x 8
-// experts of fp32 fma-chain accumulators each), keeps them in shared memory,
+// One cluster of ceil(E/128) CTAs per 64 tokens.  CTA r computes the logits
+// of experts 128r .. 128r+127 for the 64 tokens (128 threads, 8 tokens x 8
+// experts of fp32 fma-chain accumulators each: four 16-byte shared-memory
+// loads feed 64 fmas), keeps them in shared memory,
 // selects its own top-k per token and sends those (value, index) candidates
 // to CTA 0 of the cluster through distributed shared memory; CTA 0 merges
 // them into the top-k over all experts (every member of the global top-k is
@@ -181,23 +182,25 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = (int)cl_id() * RC_BT;
     const int e0 = rank * RC_EC;
-    const int tt = (lane >> 2) * 4;                 // my 4 tokens in the tile
+    const int tt = (lane >> 2) * 8;                 // my 8 tokens in the tile
     const int ee = warp * 32 + (lane & 3) * 8;      // my 8 experts of this CTA's 128
 
-    // tile loaders: x chunk (token tid & 31, 8-wide part tid >> 5) and four
-    // W_r chunks (expert tid, part r); consecutive lanes write consecutive
-    // shared-memory words
-    const int xt = tid & 31, xp = tid >> 5;
-    float acc[4][8];
+    // tile loaders: two x chunks (token tid & 63, 16-wide part tid >> 6) and
+    // four W_r chunks (expert tid, part r); consecutive lanes write
+    // consecutive shared-memory words
+    const int xt = tid & 63, xp = tid >> 6;
+    float acc[8][8];
 #pragma unroll
-    for (int a = 0; a < 4; a++)
+    for (int a = 0; a < 8; a++)
 #pragma unroll
         for (int b = 0; b < 8; b++) acc[a][b] = 0.0f;
-    uint4 rx, rw[4];
+    uint4 rx[2], rw[4];
     auto load_tile = [&](int k0) {
         const int t = t0 + xt;
-        rx = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 8))
-                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < 2; r++)
+            rx[r] = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 16 + r * 8))
+                          : make_uint4(0, 0, 0, 0);
         const int e = e0 + tid;
 #pragma unroll
         for (int r = 0; r < 4; r++)
@@ -209,9 +212,12 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
         __syncthreads();
         {
             float f[8];
-            unpack_bf16x8(rx, f);
 #pragma unroll
-            for (int j = 0; j < 8; j++) xs[(xp * 8 + j) * RC_BT + xt] = f[j];
+            for (int r = 0; r < 2; r++) {
+                unpack_bf16x8(rx[r], f);
+#pragma unroll
+                for (int j = 0; j < 8; j++) xs[(xp * 16 + r * 8 + j) * RC_BT + xt] = f[j];
+            }
 #pragma unroll
             for (int r = 0; r < 4; r++) {
                 unpack_bf16x8(rw[r], f);
@@ -223,19 +229,20 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
         if (k0 + RC_BK < d) load_tile(k0 + RC_BK);
 #pragma unroll
         for (int i = 0; i < RC_BK; i++) {
-            const float4 xv = *reinterpret_cast<const float4 *>(&xs[i * RC_BT + tt]);
+            const float4 x0 = *reinterpret_cast<const float4 *>(&xs[i * RC_BT + tt]);
+            const float4 x1 = *reinterpret_cast<const float4 *>(&xs[i * RC_BT + tt + 4]);
             const float4 w0 = *reinterpret_cast<const float4 *>(&ws[i * RC_EC + ee]);
             const float4 w1 = *reinterpret_cast<const float4 *>(&ws[i * RC_EC + ee + 4]);
-            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+            const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int a = 0; a < 4; a++)
+            for (int a = 0; a < 8; a++)
 #pragma unroll
                 for (int b = 0; b < 8; b++) acc[a][b] = fmaf(xa[a], wb[b], acc[a][b]);
         }
     }
 #pragma unroll
-    for (int a = 0; a < 4; a++) {
+    for (int a = 0; a < 8; a++) {
         *reinterpret_cast<float4 *>(&lg[(tt + a) * RC_LGS + ee]) =
             make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         *reinterpret_cast<float4 *>(&lg[(tt + a) * RC_LGS + ee + 4]) =
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
 
     // ---- per-CTA top-k of each token over its 128 experts; candidates to CTA 0 ----
     const int nc = ncta * k;
-    for (int tl = warp * 8; tl < warp * 8 + 8; tl++) {
+    for (int tl = warp * (RC_BT / 4); tl < (warp + 1) * (RC_BT / 4); tl++) {
         if (t0 + tl >= T) break;
         float vals[4];
         int idx[4];
@@ -284,7 +291,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
     if (rank != 0) return;
 
     // ---- CTA 0: merge the clusters' candidates, gates, outputs ----
-    for (int tl = warp * 8; tl < warp * 8 + 8; tl++) {
+    for (int tl = warp * (RC_BT / 4); tl < (warp + 1) * (RC_BT / 4); tl++) {
         const int t = t0 + tl;
         if (t >= T) break;
         float vals[8];
