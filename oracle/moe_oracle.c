@@ -15,7 +15,8 @@
  *   - section "Parallelism", "Expert parallelism (EP)": tokens are dispatched
  *     to experts and combined back.
  * What the pages leave open (score function, tie-break, SwiGLU, layouts,
- * accumulation order) is fixed by the plainest reading, listed in the design doc.
+ * accumulation order) is fixed by the plainest reading, stated in the
+ * comment of the routine that takes it.
  *
  * Every routine below computes the definition directly: no tiling, no
  * fusion, no reordering beyond what the definition states.  Floating point
@@ -313,6 +314,32 @@ int64_t or_replay(const int32_t *payload_kT, int64_t T, int E, int k, int32_t *i
             bad++;
     }
     return bad;
+}
+
+/* Compact the routed-experts payload to one byte per id ("Router replay":
+ * the captured [num_layers, top_k, seq_len] payload is large and is moved as
+ * an opaque tensor).  With E <= 256 every valid id fits a byte:
+ * out[i] = ids[i] for 0 <= ids[i] < E.  An id outside [0, E) is stored as
+ * 0xFF and counted; returns the number of such ids. */
+int64_t or_payload_pack_u8(const int32_t *ids, int64_t n, int E, uint8_t *out)
+{
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; i++) {
+        if (ids[i] >= 0 && ids[i] < E && ids[i] <= 255) {
+            out[i] = (uint8_t)ids[i];
+        } else {
+            out[i] = 0xFF;
+            bad++;
+        }
+    }
+    return bad;
+}
+
+/* Widen a one-byte payload back to int32 ids: out[i] = in[i]. */
+void or_payload_unpack_u8(const uint8_t *in, int64_t n, int32_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = (int32_t)in[i];
 }
 
 /* ------------------------------------------------------------------ */

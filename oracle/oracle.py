@@ -61,6 +61,8 @@ def _load():
                 "or_topk": (None, [P, I64, I, I, P]),
                 "or_gates": (None, [P, P, P, I64, I, I, I, I, F, P]),
                 "or_replay": (I64, [P, I64, I, I, P, P]),
+                "or_payload_pack_u8": (I64, [P, I64, I, P]),
+                "or_payload_unpack_u8": (None, [P, I64, P]),
                 "or_dispatch": (I64, [P, I64, I, I, P, P, P, P]),
                 "or_gather_rows": (None, [P, I64, P, I64, I, P]),
                 "or_fp8_gemm": (None, [P, P, I64, P, P, I64, I64, P]),
@@ -180,6 +182,22 @@ def replay(payload_kT: np.ndarray, E: int):
     valid = np.empty((T,), np.uint8)
     bad = _load().or_replay(_p(p), T, E, k, _p(ids), _p(valid))
     return ids, valid, int(bad)
+
+
+def payload_pack_u8(ids: np.ndarray, E: int):
+    """int32 payload (any shape) -> (uint8 payload of the same shape, number of ids outside [0, E))."""
+    a = _c(ids, np.int32)
+    out = np.empty(a.shape, np.uint8)
+    bad = _load().or_payload_pack_u8(_p(a), a.size, E, _p(out))
+    return out, int(bad)
+
+
+def payload_unpack_u8(p: np.ndarray) -> np.ndarray:
+    """uint8 payload (any shape) -> int32 payload of the same shape."""
+    a = _c(p, np.uint8)
+    out = np.empty(a.shape, np.int32)
+    _load().or_payload_unpack_u8(_p(a), a.size, _p(out))
+    return out
 
 
 def dispatch(ids: np.ndarray, E: int):
