@@ -363,6 +363,60 @@ def run_dispatch_combine(dev, seed, steps, warmup, peaks):
     return out
 
 
+def run_payload(dev, seed, steps, warmup, peaks):
+    """The routed-experts payload at one byte per id: a [64, 8, 131072] int32
+    payload (64 layers x top-8 x 128K tokens, 268 MB, replayed-id
+    distribution) packed to uint8 and unpacked again on the device, one
+    layer slab replayed from bytes and from int32 (ids only), and the
+    payload's host->device copy from pinned memory at both widths."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    cfg = S.CONFIGS["long_dispatch"].with_(layers=64)
+    L_, k, T, E = cfg.layers, cfg.k, cfg.T, cfg.E
+    n = L_ * k * T
+    payload = S.make_replay_payload(cfg, dev, seed)            # [L, k, T] int32
+    packed = torch.empty_like(payload, dtype=torch.uint8)
+    back = torch.empty_like(payload)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    h32 = torch.empty(payload.shape, dtype=torch.int32, pin_memory=True)
+    h8 = torch.empty(payload.shape, dtype=torch.uint8, pin_memory=True)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    t_pack = timed(lambda: Lb.moe_payload_pack_u8(payload, E, out=packed, dev_status=st))
+    t_unpack = timed(lambda: Lb.moe_payload_unpack_u8(packed, out=back))
+    exact = bool(torch.equal(back, payload))
+    t_r32 = timed(lambda: Lb.moe_route_replay(payload[7], E, topk_ids=ids, dev_status=st))
+    t_r8 = timed(lambda: Lb.moe_route_replay(packed[7], E, topk_ids=ids, dev_status=st))
+    t_h32 = timed(lambda: payload.copy_(h32, non_blocking=True))
+    t_h8 = timed(lambda: packed.copy_(h8, non_blocking=True))
+    gbs = lambda b, t: b / (t * 1e-3) / 1e9
+    out = {"workload": f"routed-experts payload [{L_}, {k}, {T}] (E={E}), replayed-id distribution",
+           "ids": n, "bytes_int32": 4 * n, "bytes_u8": n,
+           "pack_ms": t_pack, "pack_GB/s": gbs(5 * n, t_pack), "pack_frac_hbm": gbs(5 * n, t_pack) / peaks["hbm_gbs"],
+           "unpack_ms": t_unpack, "unpack_GB/s": gbs(5 * n, t_unpack),
+           "unpack_frac_hbm": gbs(5 * n, t_unpack) / peaks["hbm_gbs"], "round_trip_exact": exact,
+           "replay_layer_ids_only_ms": {"int32": t_r32, "u8": t_r8},
+           "h2d_ms": {"int32": t_h32, "u8": t_h8}, "h2d_GB/s": {"int32": gbs(4 * n, t_h32), "u8": gbs(n, t_h8)},
+           "status": Lb.check_status(st)}
+    del payload, packed, back, h32, h8
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 class OracleSample:
@@ -523,6 +577,9 @@ def main():
         torch.cuda.empty_cache()
         out["dispatch_combine"] = run_dispatch_combine(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
                                                        args.seed + rank, max(3, args.steps // 2), 3, peaks)
+    if cfg.name == "large" and not args.no_dispatch_combine:
+        out["payload"] = run_payload(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
+                                     args.seed + rank, max(3, args.steps // 2), 3, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, args.seed, args.cpu_tokens, "cuda")
     if rank == 0:

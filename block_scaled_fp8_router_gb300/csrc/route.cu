@@ -332,8 +332,9 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
 // route_topk_kernel -- so every x value it loads feeds SP chains.  x and the
 // replayed W_r rows are read straight from L1/L2, 8 bf16 per load, one step
 // of 8 ahead.  Gates come from warp_gate, the routing kernel's code.
-template <int TP>
-__global__ void __launch_bounds__(256, 2) route_replay_kernel(const int32_t *__restrict__ replay_kT,
+// IdT is the payload's id type: int32 or one byte (the compacted payload).
+template <int TP, typename IdT>
+__global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restrict__ replay_kT,
                                                            const uint16_t *__restrict__ x,
                                                            const uint16_t *__restrict__ wr, int T, int d, int E,
                                                            int k, int score_fn, int renorm, float route_scale,
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(256, 2) route_replay_kernel(const int32_t *__r
     for (int idx = tid; idx < TPC * k; idx += blockDim.x) {
         const int j = idx / TPC, tl = idx % TPC;
         if (tl < nt) {
-            const int32_t v = replay_kT[(int64_t)j * T + t0 + tl];
+            const int32_t v = (int32_t)replay_kT[(int64_t)j * T + t0 + tl];
             sid[tl * k + j] = v;
             ids[(int64_t)(t0 + tl) * k + j] = v;
         }
@@ -473,9 +474,12 @@ MOE_API moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, i
     return launch_status();
 }
 
-MOE_API moe_status moe_route_replay(const int32_t *replay_kT, const uint16_t *x, const uint16_t *w_router,
-                                    int T, int d, int E, int k, int score_fn, int renorm, float route_scale,
-                                    int32_t *topk_ids, float *topk_gates, int32_t *dev_status, void *stream)
+namespace moe {
+
+template <typename IdT>
+static moe_status replay_launch(const IdT *replay_kT, const uint16_t *x, const uint16_t *w_router, int T, int d,
+                                int E, int k, int score_fn, int renorm, float route_scale, int32_t *topk_ids,
+                                float *topk_gates, int32_t *dev_status, void *stream)
 {
     moe_status s = check_route_args(T, d, E, k, score_fn);
     if (s != MOE_OK) return s;
@@ -486,17 +490,35 @@ MOE_API moe_status moe_route_replay(const int32_t *replay_kT, const uint16_t *x,
     if (x && (!aligned16(x) || !aligned16(w_router))) return MOE_ERR_ALIGN;
     cudaStream_t st = as_stream(stream);
     if (k <= 8) {
-        route_replay_kernel<2><<<(T + 127) / 128, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k, score_fn,
-                                                                 renorm, route_scale, topk_ids, topk_gates,
-                                                                 dev_status);
+        route_replay_kernel<2, IdT><<<(T + 127) / 128, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
+                                                                      score_fn, renorm, route_scale, topk_ids,
+                                                                      topk_gates, dev_status);
     } else if (k <= 16) {
-        route_replay_kernel<4><<<(T + 63) / 64, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k, score_fn,
-                                                               renorm, route_scale, topk_ids, topk_gates,
-                                                               dev_status);
+        route_replay_kernel<4, IdT><<<(T + 63) / 64, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
+                                                                    score_fn, renorm, route_scale, topk_ids,
+                                                                    topk_gates, dev_status);
     } else {
-        route_replay_kernel<8><<<(T + 31) / 32, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k, score_fn,
-                                                               renorm, route_scale, topk_ids, topk_gates,
-                                                               dev_status);
+        route_replay_kernel<8, IdT><<<(T + 31) / 32, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
+                                                                    score_fn, renorm, route_scale, topk_ids,
+                                                                    topk_gates, dev_status);
     }
     return launch_status();
+}
+
+} // namespace moe
+
+MOE_API moe_status moe_route_replay(const int32_t *replay_kT, const uint16_t *x, const uint16_t *w_router,
+                                    int T, int d, int E, int k, int score_fn, int renorm, float route_scale,
+                                    int32_t *topk_ids, float *topk_gates, int32_t *dev_status, void *stream)
+{
+    return replay_launch(replay_kT, x, w_router, T, d, E, k, score_fn, renorm, route_scale, topk_ids, topk_gates,
+                         dev_status, stream);
+}
+
+MOE_API moe_status moe_route_replay_u8(const uint8_t *replay_kT, const uint16_t *x, const uint16_t *w_router,
+                                       int T, int d, int E, int k, int score_fn, int renorm, float route_scale,
+                                       int32_t *topk_ids, float *topk_gates, int32_t *dev_status, void *stream)
+{
+    return replay_launch(replay_kT, x, w_router, T, d, E, k, score_fn, renorm, route_scale, topk_ids, topk_gates,
+                         dev_status, stream);
 }

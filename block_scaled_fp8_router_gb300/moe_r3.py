@@ -30,6 +30,9 @@ _SIGS = {
     "moe_status_str": (ctypes.c_char_p, [I]),
     "moe_route_topk": (I, [P, P, I, I, I, I, I, I, F, P, P, P, P, P]),
     "moe_route_replay": (I, [P, P, P, I, I, I, I, I, I, F, P, P, P, P]),
+    "moe_route_replay_u8": (I, [P, P, P, I, I, I, I, I, I, F, P, P, P, P]),
+    "moe_payload_pack_u8": (I, [P, I64, I, P, P, P]),
+    "moe_payload_unpack_u8": (I, [P, I64, P, P]),
     "fp8_block_quant": (I, [P, I64, I64, I64, I, P, P, P]),
     "moe_dispatch_workspace_size": (SZ, [I, I, I]),
     "moe_dispatch": (I, [P, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, SZ, P, P]),
@@ -122,9 +125,15 @@ def moe_route_topk(x, w_router, k, score_fn, renorm=1, route_scale=1.0, topk_ids
 def moe_route_replay(replay_kT, E, x=None, w_router=None, score_fn=MOE_SCORE_SOFTMAX, renorm=1,
                      route_scale=1.0, topk_ids=None, topk_gates=None, dev_status=None, stream=None):
     """Replay one [k, T] layer slab of the routed-experts payload -> ids [T,k]
-    (exact copy) and, when x is given, gates [T,k] from the router logits."""
+    (exact copy) and, when x is given, gates [T,k] from the router logits.
+    An int32 slab calls moe_route_replay, a uint8 slab moe_route_replay_u8."""
     k, T = replay_kT.shape
-    _want(replay_kT, torch.int32, (k, T), "replay_kT")
+    if replay_kT.dtype == torch.uint8:
+        _want(replay_kT, torch.uint8, (k, T), "replay_kT")
+        fn_name = "moe_route_replay_u8"
+    else:
+        _want(replay_kT, torch.int32, (k, T), "replay_kT")
+        fn_name = "moe_route_replay"
     topk_ids = _empty((T, k), torch.int32, replay_kT) if topk_ids is None else topk_ids
     _want(topk_ids, torch.int32, (T, k), "topk_ids")
     d = 128
@@ -136,10 +145,44 @@ def moe_route_replay(replay_kT, E, x=None, w_router=None, score_fn=MOE_SCORE_SOF
         _want(topk_gates, torch.float32, (T, k), "topk_gates")
     if dev_status is not None:
         _want(dev_status, torch.int32, (1,), "dev_status")
-    _check("moe_route_replay", _lib.moe_route_replay(
+    _check(fn_name, getattr(_lib, fn_name)(
         _ptr(replay_kT), _ptr(x), _ptr(w_router), T, d, E, k, score_fn, renorm, route_scale, _ptr(topk_ids),
         _ptr(topk_gates), _ptr(dev_status), _stream(stream)))
     return topk_ids, topk_gates
+
+
+def moe_route_replay_u8(replay_kT, E, **kw):
+    """moe_route_replay on a one-byte [k, T] layer slab."""
+    if replay_kT.dtype != torch.uint8:
+        raise ValueError("replay_kT: uint8 payload slab expected")
+    return moe_route_replay(replay_kT, E, **kw)
+
+
+def moe_payload_pack_u8(ids, E, out=None, dev_status=None, stream=None):
+    """int32 routed-experts payload (any shape, contiguous) -> uint8 payload of
+    the same shape; out-of-range ids become 0xFF and set MOE_DEV_BAD_IDS in
+    dev_status (allocated and zeroed here when not given)."""
+    if ids.dtype != torch.int32 or not ids.is_cuda or not ids.is_contiguous():
+        raise ValueError("ids: contiguous int32 CUDA tensor")
+    out = _empty(tuple(ids.shape), torch.uint8, ids) if out is None else out
+    _want(out, torch.uint8, tuple(ids.shape), "out")
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=ids.device)
+    _want(dev_status, torch.int32, (1,), "dev_status")
+    _check("moe_payload_pack_u8", _lib.moe_payload_pack_u8(
+        _ptr(ids), ids.numel(), E, _ptr(out), _ptr(dev_status), _stream(stream)))
+    return out, dev_status
+
+
+def moe_payload_unpack_u8(packed, out=None, stream=None):
+    """uint8 payload (any shape, contiguous) -> int32 payload of the same shape."""
+    if packed.dtype != torch.uint8 or not packed.is_cuda or not packed.is_contiguous():
+        raise ValueError("packed: contiguous uint8 CUDA tensor")
+    out = _empty(tuple(packed.shape), torch.int32, packed) if out is None else out
+    _want(out, torch.int32, tuple(packed.shape), "out")
+    _check("moe_payload_unpack_u8", _lib.moe_payload_unpack_u8(
+        _ptr(packed), packed.numel(), _ptr(out), _stream(stream)))
+    return out
 
 
 def fp8_block_quant(src, block_rows, q=None, scales=None, stream=None):

@@ -109,6 +109,40 @@ moe_status moe_route_replay(const int32_t *replay_kT, const uint16_t *x, const u
                             int32_t *topk_ids, float *topk_gates, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * moe_route_replay_u8 -- moe_route_replay from a one-byte payload slab
+ * ("Router replay": the routed-experts payload moved at one byte per id,
+ * see moe_payload_pack_u8).
+ *
+ *   Identical to moe_route_replay with replay_kT[j*T + t] widened from
+ *   uint8_t: same copy, same validation (ids in [0,E), distinct per token,
+ *   MOE_DEV_BAD_IDS otherwise), same gates.  replay_kT needs no alignment.
+ * Errors: NULL, SHAPE, ALIGN (x, w_router), UNSUPPORTED (as moe_route_replay).
+ * ---------------------------------------------------------------------- */
+moe_status moe_route_replay_u8(const uint8_t *replay_kT, const uint16_t *x, const uint16_t *w_router,
+                               int T, int d, int E, int k, int score_fn, int renorm, float route_scale,
+                               int32_t *topk_ids, float *topk_gates, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_payload_pack_u8 / moe_payload_unpack_u8 -- the routed-experts payload
+ * at one byte per id ("Router replay": the [num_layers, top_k, seq_len]
+ * payload is large enough to strain its transport; with E <= 256 every id
+ * fits a byte, a 4x smaller payload).
+ *
+ *   pack:   out[i] = (uint8_t)ids[i] for 0 <= ids[i] < E, i in [0, n).  An id
+ *           outside [0, E) is stored as 0xFF and sets MOE_DEV_BAD_IDS in the
+ *           caller-zeroed *dev_status (device memory, required).
+ *   unpack: out[i] = in[i] widened to int32.
+ * Any flat layout: a whole [L, k, T] payload or one [k, T] layer slab, n
+ * elements.  Device buffers, caller-owned, need no alignment (16-byte
+ * aligned buffers take the vector path).  n may be 0.
+ * Errors: pack -- SHAPE (n < 0, E < 1), UNSUPPORTED (E > 256), NULL;
+ *         unpack -- SHAPE (n < 0), NULL.
+ * ---------------------------------------------------------------------- */
+moe_status moe_payload_pack_u8(const int32_t *ids, int64_t n, int E, uint8_t *out, int32_t *dev_status,
+                               void *stream);
+moe_status moe_payload_unpack_u8(const uint8_t *in, int64_t n, int32_t *out, void *stream);
+
+/* ------------------------------------------------------------------------
  * fp8_block_quant -- block-scaled E4M3 quantisation ("FP8 training",
  * DeepSeek-V3 recipe).
  *

@@ -62,6 +62,15 @@ def test_host_side_errors(lib):
     assert fws > 0
     assert L.moe_grouped_ffn_fp8(x, x, x, 1000, 8, 200, 512, x, x, x, x, x, x, fws, null, null) in (2, 6)
     assert L.moe_grouped_ffn_fp8(x, x, x, 1000, 8, 256, 512, x, x, x, x, x, x, fws - 1, null, null) in (4, 6)
+    assert L.moe_payload_pack_u8(x, -1, 8, x, x, null) == 2          # n < 0
+    assert L.moe_payload_pack_u8(x, 16, 0, x, x, null) == 2          # E < 1
+    assert L.moe_payload_pack_u8(x, 16, 257, x, x, null) == 6        # ids need more than a byte
+    assert L.moe_payload_pack_u8(x, 16, 8, x, null, null) == 1       # dev_status required
+    assert L.moe_payload_pack_u8(null, 0, 8, null, null, null) == 0  # empty
+    assert L.moe_payload_unpack_u8(x, -1, x, null) == 2
+    assert L.moe_payload_unpack_u8(null, 16, x, null) == 1
+    assert L.moe_route_replay_u8(null, null, null, 10, 100, 8, 2, 1, 1, 1.0, null, null, null, null) == 2
+    assert L.moe_route_replay_u8(null, null, null, 10, 128, 8, 2, 1, 1, 1.0, null, null, null, null) == 1
     assert L.moe_debug_bounded_wait(1000, null, null) == 1
     for s in range(7):
         assert lib.moe_status_str(s)
