@@ -113,7 +113,7 @@ class Clocks:
 
 # ------------------------------------------------------------------ workload
 
-def build_workload(cfg, dev, seed):
+def build_workload(cfg, dev, seed, gathered=False):
     import torch
     from block_scaled_fp8_router_gb300 import synthetic as S
     from block_scaled_fp8_router_gb300.layer import MoELayerFP8, MoEWeightsFP8, quantize_weights
@@ -131,7 +131,7 @@ def build_workload(cfg, dev, seed):
         w2 = torch.stack([S.make_w2_expert(cfg, e, dev, seed) for e in range(e0, e0 + n)])
         quantize_weights(w13, w2, out=w, e0=e0)
         del w13, w2
-    layer = MoELayerFP8(w, cfg.T, cfg.k, cfg.score_fn, cfg.renorm, cfg.route_scale)
+    layer = MoELayerFP8(w, cfg.T, cfg.k, cfg.score_fn, cfg.renorm, cfg.route_scale, gathered=gathered)
     x = S.make_x(cfg, dev, seed)
     replay = S.make_replay_payload(cfg.with_(layers=1), dev, seed)[0] if cfg.mode == "replay" else None
     return layer, x, replay
@@ -148,7 +148,8 @@ def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None):
     if cfg.layers > 1:
         cfg = cfg.with_(layers=1)   # one layer of a stacked workload per step
     steps = steps or args.steps
-    layer, x, replay = build_workload(cfg, dev, rank_seed(args.seed, rank))
+    gathered = args.form == "gathered"
+    layer, x, replay = build_workload(cfg, dev, rank_seed(args.seed, rank), gathered)
     T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
     A = T * k
     stream = torch.cuda.current_stream()
@@ -164,16 +165,31 @@ def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None):
         if record: e[1].record()
         Lb.fp8_block_quant(x, 1, q=layer.xq[:T], scales=layer.xs[:T])
         if record: e[2].record()
-        Lb.moe_dispatch(layer.ids[:T], E, rows=layer.xq[:T], row_scales=layer.xs[:T], expert_counts=layer.counts,
-                        expert_offsets=layer.offsets, sorted_to_slot=layer.s2s[:A], slot_to_sorted=layer.sl2[:A],
-                        rows_sorted=layer.xq_sorted[:A], scales_sorted=layer.xs_sorted[:A],
-                        workspace=layer.dsp_ws, dev_status=layer.dev_status)
+        if gathered:
+            Lb.moe_dispatch(layer.ids[:T], E, expert_counts=layer.counts, expert_offsets=layer.offsets,
+                            sorted_to_slot=layer.s2s[:A], slot_to_sorted=layer.sl2[:A], workspace=layer.dsp_ws,
+                            dev_status=layer.dev_status)
+        else:
+            Lb.moe_dispatch(layer.ids[:T], E, rows=layer.xq[:T], row_scales=layer.xs[:T],
+                            expert_counts=layer.counts, expert_offsets=layer.offsets,
+                            sorted_to_slot=layer.s2s[:A], slot_to_sorted=layer.sl2[:A],
+                            rows_sorted=layer.xq_sorted[:A], scales_sorted=layer.xs_sorted[:A],
+                            workspace=layer.dsp_ws, dev_status=layer.dev_status)
         if record: e[3].record()
-        Lb.moe_grouped_ffn_fp8(layer.xq_sorted[:A], layer.xs_sorted[:A], layer.offsets, layer.w.w13_q,
-                               layer.w.w13_s, layer.w.w2_q, layer.w.w2_s, out_sorted=layer.out_sorted[:A],
-                               workspace=layer.ffn_ws, dev_status=layer.dev_status)
+        if gathered:
+            Lb.moe_grouped_ffn_fp8_gathered(layer.xq[:T], layer.xs[:T], k, layer.s2s[:A], layer.offsets,
+                                            layer.w.w13_q, layer.w.w13_s, layer.w.w2_q, layer.w.w2_s,
+                                            out_slots=layer.out_sorted[:A], workspace=layer.ffn_ws,
+                                            dev_status=layer.dev_status)
+        else:
+            Lb.moe_grouped_ffn_fp8(layer.xq_sorted[:A], layer.xs_sorted[:A], layer.offsets, layer.w.w13_q,
+                                   layer.w.w13_s, layer.w.w2_q, layer.w.w2_s, out_sorted=layer.out_sorted[:A],
+                                   workspace=layer.ffn_ws, dev_status=layer.dev_status)
         if record: e[4].record()
-        Lb.moe_combine(layer.out_sorted[:A], layer.sl2[:A], layer.gates[:T], y=layer.y[:T])
+        if gathered:
+            Lb.moe_combine_slots(layer.out_sorted[:A], layer.sl2[:A], layer.gates[:T], y=layer.y[:T])
+        else:
+            Lb.moe_combine(layer.out_sorted[:A], layer.sl2[:A], layer.gates[:T], y=layer.y[:T])
         if record:
             e[5].record()
             return e
@@ -274,12 +290,13 @@ def rank_seed(seed, rank):
     return seed + rank
 
 
-def rooflines(cfg, avg, peaks):
+def rooflines(cfg, avg, peaks, gathered=False):
     T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
     A = T * k
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     flops_ffn = 6.0 * A * d * F
-    ffn = {"bound": "tensor", "kernel": "moe_grouped_ffn_fp8 (GEMM1+SwiGLU+requant, GEMM2)",
+    ffn = {"bound": "tensor", "kernel": ("moe_grouped_ffn_fp8_gathered" if gathered else "moe_grouped_ffn_fp8")
+                                         + " (GEMM1+SwiGLU+requant, GEMM2)",
            "achieved": flops_ffn / (avg["ffn"] * 1e-3) / 1e12, "peak": fp8_peak, "unit": "TFLOP/s",
            "peak_note": "FP8 dense = 2 x measured bf16 burst (nominal FP8:BF16 ratio)" if peaks["source"] == "measured"
            else "FP8 dense = 2 x fallback bf16",
@@ -290,7 +307,7 @@ def rooflines(cfg, avg, peaks):
     hbm = peaks["hbm_gbs"]
     row = d + 4 * d / 128                       # one FP8 row with its 1x128 scales
     bytes_quant = T * d * 2 + T * row
-    bytes_disp = A * 4 + 2 * A * 4 + T * row + A * row      # ids, two maps, rows in once, A rows out
+    bytes_disp = A * 4 + 2 * A * 4 + (0 if gathered else T * row + A * row)  # ids, two maps (+ row copy)
     bytes_comb = A * d * 2 + A * 4 + T * k * 4 + T * d * 2  # A bf16 rows + map + gates in, y out
     route_flops = 2.0 * T * d * E if cfg.mode == "route" else 2.0 * T * d * k
     extra = {
@@ -502,6 +519,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dispatch-combine", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
+    ap.add_argument("--form", default="sorted", choices=["sorted", "gathered"],
+                    help="sorted: dispatch copies rows into expert order; gathered: the FFN gathers its rows "
+                         "(tile::gather4) and stores outputs in slot order")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -512,7 +532,8 @@ def main():
     config = {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} top_k={cfg.k} F={cfg.F} "
                           f"{'sigmoid' if cfg.score_fn else 'softmax'} {cfg.mode}",
               "tokens_per_gpu": cfg.T, "parallelism": f"token-sharded x{world}" if world > 1 else "single GPU",
-              "l2": "inputs larger than L2 (FP8 expert weights streamed from HBM every step)"}
+              "l2": "inputs larger than L2 (FP8 expert weights streamed from HBM every step)",
+              "form": args.form}
     metric = "MoE-layer tokens/s (7168d/256e/top-8 FP8)" if cfg.name == "large" else f"MoE-layer tokens/s ({cfg.name})"
 
     if args.impl == "reference":
@@ -547,8 +568,9 @@ def main():
     cfg = r["cfg"]
     value = job_throughput(cfg.T, args.steps, world, r["total_ms"])
     e2e = job_throughput(cfg.T, args.steps, world, r["e2e_ms"])
-    ffn, extra = rooflines(cfg, r["avg"], peaks)
-    launches = sum(KERNELS_PER_STEP[n] for n in ("quant", "dispatch", "ffn", "combine")) + 1
+    gathered = args.form == "gathered"
+    ffn, extra = rooflines(cfg, r["avg"], peaks, gathered)
+    launches = sum(KERNELS_PER_STEP[n] for n in ("quant", "dispatch", "ffn", "combine")) + 1 - int(gathered)
     out = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 (GEMMs); fp32 router; bf16 io",
@@ -563,7 +585,7 @@ def main():
         torch.cuda.empty_cache()
         rr = run_gpu(args, rank, world, workload="multilayer_replay", with_e2e=False, steps=max(3, args.steps // 2))
         rcfg = rr["cfg"]
-        rffn, rextra = rooflines(rcfg, rr["avg"], peaks)
+        rffn, rextra = rooflines(rcfg, rr["avg"], peaks, gathered)
         out["replay_layer"] = {
             "workload": f"multilayer_replay (one layer): T={rcfg.T} d={rcfg.d} E={rcfg.E} top_k={rcfg.k} "
                         f"F={rcfg.F}, replayed payload with 8 hot and 8 empty experts, sigmoid gates",

@@ -218,6 +218,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint8_t *__restrict__
 // 16-byte column vectors (v, v + 32) per pass and has all 2 x 8 source loads
 // in flight before the first fma (16 x 16 B per lane keeps enough bytes in
 // flight to saturate HBM).  k > 8 runs the slots in groups of 8, in order.
+// SLOTS: the expert outputs are stored in slot order (row t*k + j), and
+// slot_to_sorted only says which slots were routed (>= 0).
+template <bool SLOTS>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ out_sorted,
                                                       const int32_t *__restrict__ slot_to_sorted,
                                                       const float *__restrict__ gates, int T, int k, int d,
@@ -228,7 +231,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t t = gw; t < T; t += nw) {
-        const int32_t my_src = lane < k ? __ldg(slot_to_sorted + t * k + lane) : -1;
+        int32_t my_src = lane < k ? __ldg(slot_to_sorted + t * k + lane) : -1;
+        if (SLOTS && my_src >= 0) my_src = (int32_t)(t * k + lane);
         const float my_g = lane < k ? __ldg(gates + t * k + lane) : 0.0f;
         for (int v0 = 0; v0 < nvec; v0 += 64) {
             float acc[2][8];
@@ -357,7 +361,21 @@ MOE_API moe_status moe_combine(const uint16_t *out_sorted, const int32_t *slot_t
     int64_t grid = ((int64_t)T + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (grid > cap) grid = cap;
-    combine_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(out_sorted, slot_to_sorted, gates, T, k, d, y);
+    combine_kernel<false><<<(unsigned)grid, 256, 0, as_stream(stream)>>>(out_sorted, slot_to_sorted, gates, T, k, d, y);
+    return launch_status();
+}
+
+MOE_API moe_status moe_combine_slots(const uint16_t *out_slots, const int32_t *slot_to_sorted, const float *gates,
+                                     int T, int k, int d, uint16_t *y, void *stream)
+{
+    if (T < 0 || k < 1 || k > 32 || d <= 0 || d % 8 != 0) return MOE_ERR_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!out_slots || !slot_to_sorted || !gates || !y) return MOE_ERR_NULL;
+    if (!aligned16(out_slots) || !aligned16(y)) return MOE_ERR_ALIGN;
+    int64_t grid = ((int64_t)T + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (grid > cap) grid = cap;
+    combine_kernel<true><<<(unsigned)grid, 256, 0, as_stream(stream)>>>(out_slots, slot_to_sorted, gates, T, k, d, y);
     return launch_status();
 }
 

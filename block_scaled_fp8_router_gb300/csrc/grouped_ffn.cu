@@ -78,8 +78,10 @@ struct Params {
     float *act_s;               // GEMM1 out [max_rows, F/128]
     uint16_t *out;              // GEMM2 out [max_rows, d] bf16
     int32_t *dev_status;
+    const int32_t *sorted_to_slot;  // gathered form: sorted row -> slot t*top_k + j
     int64_t max_rows;
     int E, d, F;
+    int top_k;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -90,6 +92,19 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, in
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// four rows (r0..r3) of a one-row-box tensor map, 128 bytes from column x,
+// land as four consecutive 128-byte rows at dst with the map's swizzle, as
+// a four-row box would
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *tm, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -255,7 +270,13 @@ __device__ void build_schedule(Smem &s, const Params &p, int n_tiles)
 
 // ------------------------------------------------------------------ kernel
 
-template <int MODE>
+// GATHER (the gathered form): GEMM1 loads its A rows straight from the
+// token-major activation codes (row = sorted_to_slot[r] / top_k, four rows
+// per tile::gather4, one per producer lane) and takes their scales from the
+// token-major scale array; GEMM2 writes each output row to its slot
+// (row sorted_to_slot[r] of a [T*top_k, d] array) instead of its sorted
+// position.
+template <int MODE, bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                         const Params p)
@@ -294,20 +315,40 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == PRODUCER_WARP) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
+        // lane 0 alone, or the whole warp when it gathers A rows
+        constexpr bool GA = GATHER && MODE == 1;
+        if (GA || lane == 0) {
             uint32_t j = 0;
             uint32_t issued = 0;  // per-stage "has an outstanding load" bits
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 const Tile tl = decode_tile(s, p.E, n_tiles, t);
+                int tok[4] = {0, 0, 0, 0};  // token rows of this lane's four A rows (0 past the tile's rows)
+                if (GA) {
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int r = 4 * lane + i;
+                        if (r < tl.rows) tok[i] = __ldg(p.sorted_to_slot + tl.row0 + r) / p.top_k;
+                    }
+                }
                 for (int kb = 0; kb < nkb; kb++, j++) {
                     const int st = j % STAGES;
-                    if (!wait_or_abort(&s.empty[st], ((j / STAGES) & 1) ^ 1, abort_flag, p.dev_status)) {
+                    bool w = true;
+                    if (lane == 0) w = wait_or_abort(&s.empty[st], ((j / STAGES) & 1) ^ 1, abort_flag, p.dev_status);
+                    if (GA) w = __shfl_sync(0xFFFFFFFFu, w, 0);
+                    if (!w) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
-                    tma_load_2d(s.a[st], &tm_a, kb * BK, tl.row0, &s.full[st]);
+                    if (GA) {
+                        if (lane == 0) mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+                        __syncwarp();
+                        tma_gather4(s.a[st] + 512 * lane, &tm_a, kb * BK, tok[0], tok[1], tok[2], tok[3], &s.full[st]);
+                        if (lane != 0) continue;
+                    } else {
+                        mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+                        tma_load_2d(s.a[st], &tm_a, kb * BK, tl.row0, &s.full[st]);
+                    }
                     if (MODE == 1) {
                         const int wrow = tl.e * 2 * p.F + tl.n_blk * 128;
                         tma_load_2d(s.b[st], &tm_b, kb * BK, wrow, &s.full[st]);
@@ -319,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             // drain: wait for the last load issued into every stage
-            for (int i = 0; i < STAGES; i++) {
+            for (int i = 0; i < STAGES && lane == 0; i++) {
                 if (!(issued & (1u << i)) || j == 0) continue;
                 // last use of stage i was at the largest j' < j with j' % STAGES == i
                 const uint32_t last = j - 1 - ((j - 1 - i) % STAGES);
@@ -370,6 +411,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Tile tl = decode_tile(s, p.E, n_tiles, t);
             const bool row_ok = r_in < tl.rows;
             const int64_t row = (int64_t)tl.row0 + r_in;
+            // gathered form: GEMM1 scales by token, GEMM2 stores by slot
+            int64_t srow = row, orow = row;
+            if (GATHER && row_ok) {
+                const int32_t slot = __ldg(p.sorted_to_slot + row);
+                if (MODE == 1) srow = slot / p.top_k;
+                else orow = slot;
+            }
             // accumulator columns of this thread: two 32-wide halves (GEMM1:
             // gate 32cg.., up 128+32cg..) or one 64-wide run (GEMM2: 64cg..)
             const int col0 = MODE == 1 ? 32 * cg : 64 * cg;
@@ -382,11 +430,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             float acc0[32], acc1[32];
 #pragma unroll
             for (int i = 0; i < 32; i++) acc0[i] = acc1[i] = 0.0f;
-            float sa_next = row_ok ? __ldg(p.a_scales + row * nkb_a) : 0.0f;
+            float sa_next = row_ok ? __ldg(p.a_scales + srow * nkb_a) : 0.0f;
             for (int kb = 0; kb < nkb; kb++, j++) {
                 const int buf = j & 1;
                 const float sa = sa_next;
-                if (kb + 1 < nkb) sa_next = row_ok ? __ldg(p.a_scales + row * nkb_a + kb + 1) : 0.0f;
+                if (kb + 1 < nkb) sa_next = row_ok ? __ldg(p.a_scales + srow * nkb_a + kb + 1) : 0.0f;
                 const float sb0 = nb_ok ? __ldg(p.b_scales + nb0 * nkb + kb) : 0.0f;
                 const float sb1 = nb_ok ? __ldg(p.b_scales + nb1 * nkb + kb) : 0.0f;
                 const float c0 = sa * sb0, c1 = sa * sb1;
@@ -442,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 const int c_glob = tl.n_blk * BN + 64 * cg;
                 if (row_ok && !aborted && c_glob < p.d) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * p.d + c_glob);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * p.d + c_glob);
 #pragma unroll
                     for (int i = 0; i < 4; i++)
                         dst[i] = make_uint4(pack_bf16x2(acc0[8 * i], acc0[8 * i + 1]),
@@ -510,11 +558,17 @@ MOE_API size_t moe_grouped_ffn_workspace_size(int64_t max_rows, int d, int F)
     return align256((size_t)max_rows * F) + align256((size_t)max_rows * (F / 128) * sizeof(float));
 }
 
-MOE_API moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs_sorted,
-                                       const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
-                                       const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q,
-                                       const float *w2_s, uint16_t *out_sorted, void *workspace,
-                                       size_t workspace_bytes, int32_t *dev_status, void *stream)
+namespace moe {
+namespace ffn {
+
+// both GEMMs; GATHER: A rows of GEMM1 from the token-major x (T rows) by
+// sorted_to_slot / top_k, outputs of GEMM2 to their slots
+template <bool GATHER>
+static moe_status ffn_launch(const uint8_t *xq, int64_t x_rows, const float *xs, const int32_t *sorted_to_slot,
+                             int top_k, const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                             const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q, const float *w2_s,
+                             uint16_t *out, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                             void *stream)
 {
     if (max_rows < 0 || max_rows >= (1LL << 31) || E < 1 || E > MAX_E || d <= 0 || F <= 0 || d % 128 != 0 ||
         F % 128 != 0)
@@ -523,9 +577,9 @@ MOE_API moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs
     const size_t need = moe_grouped_ffn_workspace_size(max_rows, d, F);
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
     if (max_rows == 0) return MOE_OK;
-    if (!xq_sorted || !xs_sorted || !expert_offsets || !w13_q || !w13_s || !w2_q || !w2_s || !out_sorted)
-        return MOE_ERR_NULL;
-    if (!aligned16(xq_sorted) || !aligned16(w13_q) || !aligned16(w2_q) || !aligned16(out_sorted) ||
+    if (!xq || !xs || !expert_offsets || !w13_q || !w13_s || !w2_q || !w2_s || !out) return MOE_ERR_NULL;
+    if (GATHER && !sorted_to_slot) return MOE_ERR_NULL;
+    if (!aligned16(xq) || !aligned16(w13_q) || !aligned16(w2_q) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
         return MOE_ERR_ALIGN;
     auto enc = encode_fn();
@@ -533,7 +587,7 @@ MOE_API moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs
     uint8_t *act_q = reinterpret_cast<uint8_t *>(workspace);
     float *act_s = reinterpret_cast<float *>(reinterpret_cast<char *>(workspace) + align256((size_t)max_rows * F));
     CUtensorMap ma1, mb1, ma2, mb2;
-    if (!make_map(enc, &ma1, xq_sorted, d, max_rows, 128) || !make_map(enc, &mb1, w13_q, d, (uint64_t)E * 2 * F, 128) ||
+    if (!make_map(enc, &ma1, xq, d, x_rows, GATHER ? 1 : 128) || !make_map(enc, &mb1, w13_q, d, (uint64_t)E * 2 * F, 128) ||
         !make_map(enc, &ma2, act_q, F, max_rows, 128) || !make_map(enc, &mb2, w2_q, F, (uint64_t)E * d, 256))
         return MOE_ERR_CUDA;
     Params prm;
@@ -541,26 +595,54 @@ MOE_API moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs
     prm.offsets = expert_offsets;
     prm.act_q = act_q;
     prm.act_s = act_s;
-    prm.out = out_sorted;
+    prm.out = out;
     prm.dev_status = dev_status;
+    prm.sorted_to_slot = sorted_to_slot;
     prm.max_rows = max_rows;
     prm.E = E;
     prm.d = d;
     prm.F = F;
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    prm.top_k = top_k;
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<1, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(grouped_gemm_kernel<2, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return MOE_ERR_CUDA;
     const int grid = sm_count();
     cudaStream_t st = as_stream(stream);
     Params p1 = prm;
-    p1.a_scales = xs_sorted;
+    p1.a_scales = xs;
     p1.b_scales = w13_s;
-    grouped_gemm_kernel<1><<<grid, THREADS, SMEM_BYTES, st>>>(ma1, mb1, p1);
+    grouped_gemm_kernel<1, GATHER><<<grid, THREADS, SMEM_BYTES, st>>>(ma1, mb1, p1);
     Params p2 = prm;
     p2.a_scales = act_s;
     p2.b_scales = w2_s;
-    grouped_gemm_kernel<2><<<grid, THREADS, SMEM_BYTES, st>>>(ma2, mb2, p2);
+    grouped_gemm_kernel<2, GATHER><<<grid, THREADS, SMEM_BYTES, st>>>(ma2, mb2, p2);
     return launch_status();
+}
+
+} // namespace ffn
+} // namespace moe
+
+MOE_API moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs_sorted,
+                                       const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                                       const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q,
+                                       const float *w2_s, uint16_t *out_sorted, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    return ffn_launch<false>(xq_sorted, max_rows, xs_sorted, nullptr, 1, expert_offsets, max_rows, E, d, F, w13_q,
+                             w13_s, w2_q, w2_s, out_sorted, workspace, workspace_bytes, dev_status, stream);
+}
+
+MOE_API moe_status moe_grouped_ffn_fp8_gathered(const uint8_t *xq, const float *xs, int T, int k,
+                                                const int32_t *sorted_to_slot, const int32_t *expert_offsets,
+                                                int E, int d, int F, const uint8_t *w13_q, const float *w13_s,
+                                                const uint8_t *w2_q, const float *w2_s, uint16_t *out_slots,
+                                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                                void *stream)
+{
+    if (T < 0 || k < 1 || k > 32 || (int64_t)T * k >= (1LL << 31)) return MOE_ERR_SHAPE;
+    if (T == 0) return MOE_OK;
+    return ffn_launch<true>(xq, T, xs, sorted_to_slot, k, expert_offsets, (int64_t)T * k, E, d, F, w13_q, w13_s,
+                            w2_q, w2_s, out_slots, workspace, workspace_bytes, dev_status, stream);
 }

@@ -56,11 +56,19 @@ def quantize_weights(w13: torch.Tensor, w2: torch.Tensor, out: MoEWeightsFP8 | N
 
 
 class MoELayerFP8:
-    """Forward of one MoE layer on one GPU with preallocated buffers."""
+    """Forward of one MoE layer on one GPU with preallocated buffers.
+
+    gathered=False: dispatch copies the quantised rows into expert order,
+    the grouped FFN reads them there and combine gathers the outputs back.
+    gathered=True: dispatch builds the maps only, the FFN gathers its A rows
+    from the token-major codes (tile::gather4) and stores its outputs in slot
+    order, and combine reads each token's k rows contiguously.  Same bits.
+    """
 
     def __init__(self, weights: MoEWeightsFP8, T_max: int, k: int, score_fn: int, renorm: int = 1,
-                 route_scale: float = 1.0, device=None):
+                 route_scale: float = 1.0, device=None, gathered: bool = False):
         self.w = weights
+        self.gathered = gathered
         self.k, self.score_fn, self.renorm, self.route_scale = k, score_fn, renorm, route_scale
         dev = weights.w13_q.device if device is None else device
         E, d, F = weights.E, weights.d, weights.F
@@ -75,9 +83,9 @@ class MoELayerFP8:
         self.offsets = e((E + 1,), torch.int32)
         self.s2s = e((A,), torch.int32)
         self.sl2 = e((A,), torch.int32)
-        self.xq_sorted = e((A, d), torch.uint8)
-        self.xs_sorted = e((A, d // 128), torch.float32)
-        self.out_sorted = e((A, d), torch.bfloat16)
+        self.xq_sorted = None if gathered else e((A, d), torch.uint8)
+        self.xs_sorted = None if gathered else e((A, d // 128), torch.float32)
+        self.out_sorted = e((A, d), torch.bfloat16)     # slot order when gathered
         self.y = e((T_max, d), torch.bfloat16)
         self.dsp_ws = e((L.moe_dispatch_workspace_size(T_max, k, E),), torch.uint8)
         self.ffn_ws = e((L.moe_grouped_ffn_workspace_size(A, d, F),), torch.uint8)
@@ -102,6 +110,15 @@ class MoELayerFP8:
         A = T * self.k
         ids, gates = self.route(x, replay_kT, capture_kT)
         xq, xs = L.fp8_block_quant(x, 1, q=self.xq[:T], scales=self.xs[:T])
+        y = self.y[:T] if y is None else y
+        if self.gathered:
+            L.moe_dispatch(ids, self.w.E, expert_counts=self.counts, expert_offsets=self.offsets,
+                           sorted_to_slot=self.s2s[:A], slot_to_sorted=self.sl2[:A], workspace=self.dsp_ws,
+                           dev_status=self.dev_status)
+            L.moe_grouped_ffn_fp8_gathered(xq, xs, self.k, self.s2s[:A], self.offsets, self.w.w13_q, self.w.w13_s,
+                                           self.w.w2_q, self.w.w2_s, out_slots=self.out_sorted[:A],
+                                           workspace=self.ffn_ws, dev_status=self.dev_status)
+            return L.moe_combine_slots(self.out_sorted[:A], self.sl2[:A], gates, y=y)
         L.moe_dispatch(ids, self.w.E, rows=xq, row_scales=xs, expert_counts=self.counts,
                        expert_offsets=self.offsets, sorted_to_slot=self.s2s[:A], slot_to_sorted=self.sl2[:A],
                        rows_sorted=self.xq_sorted[:A], scales_sorted=self.xs_sorted[:A], workspace=self.dsp_ws,
@@ -109,7 +126,6 @@ class MoELayerFP8:
         L.moe_grouped_ffn_fp8(self.xq_sorted[:A], self.xs_sorted[:A], self.offsets, self.w.w13_q, self.w.w13_s,
                               self.w.w2_q, self.w.w2_s, out_sorted=self.out_sorted[:A], workspace=self.ffn_ws,
                               dev_status=self.dev_status)
-        y = self.y[:T] if y is None else y
         return L.moe_combine(self.out_sorted[:A], self.sl2[:A], gates, y=y)
 
 

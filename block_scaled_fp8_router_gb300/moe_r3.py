@@ -40,6 +40,8 @@ _SIGS = {
     "moe_grouped_ffn_workspace_size": (SZ, [I64, I, I]),
     "moe_grouped_ffn_fp8": (I, [P, P, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_combine": (I, [P, P, P, I, I, I, P, P]),
+    "moe_grouped_ffn_fp8_gathered": (I, [P, P, I, I, P, P, I, I, I, P, P, P, P, P, P, SZ, P, P]),
+    "moe_combine_slots": (I, [P, P, P, I, I, I, P, P]),
     "moe_debug_bounded_wait": (I, [I64, P, P]),
     "moe_device_sm_count": (I, []),
 }
@@ -316,6 +318,47 @@ def moe_grouped_ffn_fp8(xq_sorted, xs_sorted, expert_offsets, w13_q, w13_s, w2_q
         _ptr(w2_q), _ptr(w2_s), _ptr(out_sorted), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream)))
     return out_sorted
+
+
+def moe_grouped_ffn_fp8_gathered(xq, xs, top_k, sorted_to_slot, expert_offsets, w13_q, w13_s, w2_q, w2_s,
+                                 out_slots=None, workspace=None, dev_status=None, stream=None):
+    """The grouped FFN reading token-major xq [T, d] / xs [T, d/128] through
+    sorted_to_slot and writing out_slots [T*top_k, d] bf16 in slot order."""
+    T, d = xq.shape
+    k = top_k
+    E, twoF, _ = w13_q.shape
+    F = twoF // 2
+    _want(xq, torch.uint8, (T, d), "xq")
+    _want(xs, torch.float32, (T, d // 128), "xs")
+    _want(sorted_to_slot, torch.int32, (T * k,), "sorted_to_slot")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(w13_q, torch.uint8, (E, 2 * F, d), "w13_q")
+    _want(w13_s, torch.float32, (E, 2 * F // 128, d // 128), "w13_s")
+    _want(w2_q, torch.uint8, (E, d, F), "w2_q")
+    _want(w2_s, torch.float32, (E, d // 128, F // 128), "w2_s")
+    out_slots = _empty((T * k, d), torch.bfloat16, xq) if out_slots is None else out_slots
+    _want(out_slots, torch.bfloat16, (T * k, d), "out_slots")
+    if workspace is None:
+        workspace = _empty((moe_grouped_ffn_workspace_size(T * k, d, F),), torch.uint8, xq)
+    _check("moe_grouped_ffn_fp8_gathered", _lib.moe_grouped_ffn_fp8_gathered(
+        _ptr(xq), _ptr(xs), T, k, _ptr(sorted_to_slot), _ptr(expert_offsets), E, d, F, _ptr(w13_q), _ptr(w13_s),
+        _ptr(w2_q), _ptr(w2_s), _ptr(out_slots), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))
+    return out_slots
+
+
+def moe_combine_slots(out_slots, slot_to_sorted, gates, y=None, stream=None):
+    """moe_combine over expert rows stored in slot order [T*k, d]."""
+    T, k = gates.shape
+    d = out_slots.shape[1]
+    _want(out_slots, torch.bfloat16, (T * k, d), "out_slots")
+    _want(slot_to_sorted, torch.int32, (T * k,), "slot_to_sorted")
+    _want(gates, torch.float32, (T, k), "gates")
+    y = _empty((T, d), torch.bfloat16, out_slots) if y is None else y
+    _want(y, torch.bfloat16, (T, d), "y")
+    _check("moe_combine_slots", _lib.moe_combine_slots(
+        _ptr(out_slots), _ptr(slot_to_sorted), _ptr(gates), T, k, d, _ptr(y), _stream(stream)))
+    return y
 
 
 def moe_combine(out_sorted, slot_to_sorted, gates, y=None, stream=None):

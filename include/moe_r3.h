@@ -246,6 +246,31 @@ moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs_sorted,
                                size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * moe_grouped_ffn_fp8_gathered -- moe_grouped_ffn_fp8 with the dispatch
+ * row gather fused into GEMM1's operand load and the un-permute fused into
+ * GEMM2's store ("FP8 inference": FP8 with DeepEP dispatch/combine and
+ * DeepGEMM kernels; "Expert parallelism": dispatch and combine).
+ *
+ *   Same arithmetic as moe_grouped_ffn_fp8 for sorted row r of expert e, but
+ *   the row's codes and scales are read from the token-major quantised
+ *   activations, xq[t] and xs[t] with t = sorted_to_slot[r] / k (tile::gather4
+ *   TMA loads, four rows per copy), and its output goes to
+ *   out_slots[sorted_to_slot[r], :] -- slot order, row t*k + j -- so the
+ *   permuted activation copy of moe_dispatch (its rows output) is not needed
+ *   and moe_combine_slots reads each token's k rows contiguously.
+ * xq [T, d] e4m3, xs [T, d/128] fp32, sorted_to_slot and expert_offsets from
+ * moe_dispatch (maps only); out_slots [T*k, d] bf16 (rows of unrouted slots
+ * are not written); workspace: moe_grouped_ffn_workspace_size(T*k, d, F).
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
+ * ---------------------------------------------------------------------- */
+moe_status moe_grouped_ffn_fp8_gathered(const uint8_t *xq, const float *xs, int T, int k,
+                                        const int32_t *sorted_to_slot, const int32_t *expert_offsets, int E,
+                                        int d, int F, const uint8_t *w13_q, const float *w13_s,
+                                        const uint8_t *w2_q, const float *w2_s, uint16_t *out_slots,
+                                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                        void *stream);
+
+/* ------------------------------------------------------------------------
  * moe_combine -- gate-weighted sum back to token order ("Expert
  * parallelism": combine).
  *
@@ -257,6 +282,19 @@ moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs_sorted,
  * ---------------------------------------------------------------------- */
 moe_status moe_combine(const uint16_t *out_sorted, const int32_t *slot_to_sorted, const float *gates,
                        int T, int k, int d, uint16_t *y, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_combine_slots -- moe_combine over expert outputs stored in slot order
+ * (as moe_grouped_ffn_fp8_gathered writes them).
+ *
+ *   y[t,c] = bf16( sum_j gates[t,j] * out_slots[t*k+j, c] ) over the slots
+ *   with slot_to_sorted[t*k+j] >= 0, the same fma chain in slot order as
+ *   moe_combine (so both give the same bits for the same expert outputs).
+ * out_slots [T*k, d] bf16; other arguments as moe_combine.
+ * Errors: NULL, SHAPE, ALIGN.
+ * ---------------------------------------------------------------------- */
+moe_status moe_combine_slots(const uint16_t *out_slots, const int32_t *slot_to_sorted, const float *gates,
+                             int T, int k, int d, uint16_t *y, void *stream);
 
 /* ------------------------------------------------------------------------
  * moe_debug_bounded_wait -- exercises the bounded device wait that every
