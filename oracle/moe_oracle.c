@@ -185,6 +185,56 @@ void or_quant_128x128(const uint16_t *src, int64_t rows, int64_t cols, int64_t l
     }
 }
 
+/* Power-of-two (UE8M0) variant of the block scale: s = 2^p with p the
+ * smallest integer such that amax <= 448 * 2^p, so that no code saturates;
+ * stored as the biased exponent e = p + 127 (one byte, s = 2^(e-127)).  An
+ * all-zero block takes e = 127 (s = 1).  p is clamped to [-127, 127]; the
+ * upper clamp is never reached by a finite bf16 input. */
+static int ue8m0_exponent(float amax)
+{
+    if (amax == 0.0f)
+        return 127;
+    int ex;
+    frexp((double)amax, &ex);
+    int p = ex - 10;                        /* 448 * 2^(ex-10) < 2^(ex-1) <= amax */
+    while (ldexp(448.0, p) < (double)amax)
+        p++;
+    if (p < -127)
+        p = -127;
+    if (p > 127)
+        p = 127;
+    return p + 127;
+}
+
+/* Block quantisation with power-of-two scales: blocks of block_rows (1 or
+ * 128) x 128 elements, code = e4m3(v / 2^(e-127)) (an exact division),
+ * e [rows/block_rows, cols/128] biased exponents. */
+void or_quant_ue8m0(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src, int block_rows,
+                    uint8_t *q, uint8_t *e)
+{
+    int64_t nbr = rows / block_rows, nbc = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t br = 0; br < nbr; br++) {
+        for (int64_t bc = 0; bc < nbc; bc++) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < block_rows; i++)
+                for (int64_t j = 0; j < 128; j++) {
+                    float a = fabsf(or_bf16_to_f32(src[(br * block_rows + i) * ld_src + bc * 128 + j]));
+                    if (a > amax)
+                        amax = a;
+                }
+            int ebias = ue8m0_exponent(amax);
+            e[br * nbc + bc] = (uint8_t)ebias;
+            float sc = (float)ldexp(1.0, ebias - 127);
+            for (int64_t i = 0; i < block_rows; i++)
+                for (int64_t j = 0; j < 128; j++) {
+                    int64_t r = br * block_rows + i, c = bc * 128 + j;
+                    q[r * cols + c] = or_e4m3_encode(or_bf16_to_f32(src[r * ld_src + c]) / sc);
+                }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* routing ("Router replay": the decision that is captured)             */
 /* ------------------------------------------------------------------ */
@@ -454,10 +504,12 @@ void or_fp8_gemm(const uint8_t *a, const float *sa, int64_t M, const uint8_t *w,
  *   w2_q  [*, d, F],                                 w2_s  [*, d/128, F/128]
  * h = X W13^T (block-scaled), act = silu(h_gate) * h_up in double rounded to
  * binary32, act re-quantised 1x128 along F, out = bf16(act_q W2^T).
- * act_f (nullable) [n, F], act_q [n, F], act_s [n, F/128], out [n, d]. */
-void or_expert_ffn(const uint8_t *xq, const float *xs, int64_t n, const int32_t *row_expert, int d, int F,
-                   const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q, const float *w2_s,
-                   float *act_f, uint8_t *act_q, float *act_s, uint16_t *out)
+ * act_f (nullable) [n, F], act_q [n, F], act_s [n, F/128], out [n, d].
+ * ue8m0 = 0: act scales amax/448 (fp32); 1: power-of-two scales as
+ * or_quant_ue8m0 (act_s holds their values). */
+void or_expert_ffn_rule(const uint8_t *xq, const float *xs, int64_t n, const int32_t *row_expert, int d,
+                        int F, const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q, const float *w2_s,
+                        int ue8m0, float *act_f, uint8_t *act_q, float *act_s, uint16_t *out)
 {
     double dec[256];
     for (int c = 0; c < 256; c++)
@@ -480,7 +532,7 @@ void or_expert_ffn(const uint8_t *xq, const float *xs, int64_t n, const int32_t 
             for (int i = 0; i < 128; i++)
                 if (fabsf(act[b * 128 + i]) > amax)
                     amax = fabsf(act[b * 128 + i]);
-            float sc = block_scale(amax);
+            float sc = ue8m0 ? (float)ldexp(1.0, ue8m0_exponent(amax) - 127) : block_scale(amax);
             act_s[r * nkf + b] = sc;
             for (int i = 0; i < 128; i++)
                 act_q[r * F + b * 128 + i] = or_e4m3_encode(act[b * 128 + i] / sc);
@@ -495,6 +547,14 @@ void or_expert_ffn(const uint8_t *xq, const float *xs, int64_t n, const int32_t 
         free(o);
         free(act);
     }
+}
+
+/* The recipe's FFN: fp32 amax/448 scales for the act re-quantisation. */
+void or_expert_ffn(const uint8_t *xq, const float *xs, int64_t n, const int32_t *row_expert, int d, int F,
+                   const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q, const float *w2_s,
+                   float *act_f, uint8_t *act_q, float *act_s, uint16_t *out)
+{
+    or_expert_ffn_rule(xq, xs, n, row_expert, d, F, w13_q, w13_s, w2_q, w2_s, 0, act_f, act_q, act_s, out);
 }
 
 /* ------------------------------------------------------------------ */

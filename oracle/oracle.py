@@ -67,6 +67,8 @@ def _load():
                 "or_gather_rows": (None, [P, I64, P, I64, I, P]),
                 "or_fp8_gemm": (None, [P, P, I64, P, P, I64, I64, P]),
                 "or_expert_ffn": (None, [P, P, I64, P, I, I, P, P, P, P, P, P, P, P]),
+                "or_expert_ffn_rule": (None, [P, P, I64, P, I, I, P, P, P, P, I, P, P, P, P]),
+                "or_quant_ue8m0": (None, [P, I64, I64, I64, I, P, P]),
                 "or_combine": (None, [P, P, P, I64, I, I, P]),
                 "or_num_threads": (I, []),
                 "or_set_num_threads": (None, [I]),
@@ -139,6 +141,23 @@ def quant_128x128(w_bf16: np.ndarray):
     s = np.empty((rows // 128, cols // 128), np.float32)
     _load().or_quant_128x128(_p(w), rows, cols, cols, _p(q), _p(s))
     return q, s
+
+
+def quant_ue8m0(x_bf16: np.ndarray, block_rows: int):
+    """[rows, cols] bf16 bits -> (codes uint8 [rows, cols], biased exponents uint8 [rows/block_rows, cols/128]);
+    block scale 2^(e-127), the smallest power of two with amax <= 448 * scale."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    assert cols % 128 == 0 and rows % block_rows == 0 and block_rows in (1, 128)
+    q = np.empty((rows, cols), np.uint8)
+    e = np.empty((rows // block_rows, cols // 128), np.uint8)
+    _load().or_quant_ue8m0(_p(x), rows, cols, cols, block_rows, _p(q), _p(e))
+    return q, e
+
+
+def ue8m0_value(e: np.ndarray) -> np.ndarray:
+    """Biased exponent bytes -> their scale values 2^(e-127) as fp32 (exact)."""
+    return np.ldexp(np.float32(1.0), np.asarray(e, np.int32) - 127).astype(np.float32)
 
 
 def router_logits(x_bf16: np.ndarray, wr_bf16: np.ndarray) -> np.ndarray:
@@ -239,8 +258,9 @@ def fp8_gemm(a_q: np.ndarray, a_s: np.ndarray, w_q: np.ndarray, w_s: np.ndarray)
 
 
 def expert_ffn(xq: np.ndarray, xs: np.ndarray, row_expert: np.ndarray,
-               w13_q: np.ndarray, w13_s: np.ndarray, w2_q: np.ndarray, w2_s: np.ndarray):
-    """SwiGLU FFN on sorted rows.  Returns (act_f [n,F] f32, act_q [n,F], act_s [n,F/128], out bf16 [n,d])."""
+               w13_q: np.ndarray, w13_s: np.ndarray, w2_q: np.ndarray, w2_s: np.ndarray, ue8m0: bool = False):
+    """SwiGLU FFN on sorted rows.  Returns (act_f [n,F] f32, act_q [n,F], act_s [n,F/128], out bf16 [n,d]).
+    ue8m0: the act re-quantisation takes power-of-two scales (or_quant_ue8m0's rule)."""
     xq = _c(xq, np.uint8)
     xs = _c(xs, np.float32)
     re = _c(row_expert, np.int32)
@@ -260,7 +280,8 @@ def expert_ffn(xq: np.ndarray, xs: np.ndarray, row_expert: np.ndarray,
     act_q = np.empty((n, F), np.uint8)
     act_s = np.empty((n, F // 128), np.float32)
     out = np.empty((n, d), np.uint16)
-    _load().or_expert_ffn(_p(xq), _p(xs), n, _p(re), d, F, _p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s),
+    _load().or_expert_ffn_rule(_p(xq), _p(xs), n, _p(re), d, F, _p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s),
+                               int(ue8m0),
                           _p(act_f), _p(act_q), _p(act_s), _p(out))
     return act_f, act_q, act_s, out
 
