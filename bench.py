@@ -113,17 +113,18 @@ class Clocks:
 
 # ------------------------------------------------------------------ workload
 
-def build_workload(cfg, dev, seed, gathered=False):
+def build_workload(cfg, dev, seed, gathered=False, ue8m0=False):
     import torch
     from block_scaled_fp8_router_gb300 import synthetic as S
     from block_scaled_fp8_router_gb300.layer import MoELayerFP8, MoEWeightsFP8, quantize_weights
 
     E, d, F = cfg.E, cfg.d, cfg.F
+    sdt = torch.uint8 if ue8m0 else torch.float32     # power-of-two exponents or fp32 scales
     w = MoEWeightsFP8(S.make_router_w(cfg, dev, seed),
                       torch.empty((E, 2 * F, d), dtype=torch.uint8, device=dev),
-                      torch.empty((E, 2 * F // 128, d // 128), dtype=torch.float32, device=dev),
+                      torch.empty((E, 2 * F // 128, d // 128), dtype=sdt, device=dev),
                       torch.empty((E, d, F), dtype=torch.uint8, device=dev),
-                      torch.empty((E, d // 128, F // 128), dtype=torch.float32, device=dev))
+                      torch.empty((E, d // 128, F // 128), dtype=sdt, device=dev))
     chunk = 16
     for e0 in range(0, E, chunk):
         n = min(chunk, E - e0)
@@ -137,7 +138,7 @@ def build_workload(cfg, dev, seed, gathered=False):
     return layer, x, replay
 
 
-def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None):
+def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None, ue8m0=False):
     import torch
     from block_scaled_fp8_router_gb300 import moe_r3 as Lb
     from block_scaled_fp8_router_gb300 import synthetic as S
@@ -148,8 +149,8 @@ def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None):
     if cfg.layers > 1:
         cfg = cfg.with_(layers=1)   # one layer of a stacked workload per step
     steps = steps or args.steps
-    gathered = args.form == "gathered"
-    layer, x, replay = build_workload(cfg, dev, rank_seed(args.seed, rank), gathered)
+    gathered = args.form == "gathered" and not ue8m0
+    layer, x, replay = build_workload(cfg, dev, rank_seed(args.seed, rank), gathered, ue8m0)
     T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
     A = T * k
     stream = torch.cuda.current_stream()
@@ -163,9 +164,16 @@ def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None):
             e[0].record()
         layer.route(x, replay)
         if record: e[1].record()
-        Lb.fp8_block_quant(x, 1, q=layer.xq[:T], scales=layer.xs[:T])
+        if ue8m0:
+            Lb.fp8_block_quant_ue8m0(x, 1, q=layer.xq[:T], scale_exp=layer.xs[:T])
+        else:
+            Lb.fp8_block_quant(x, 1, q=layer.xq[:T], scales=layer.xs[:T])
         if record: e[2].record()
-        if gathered:
+        if ue8m0:
+            Lb.moe_dispatch(layer.ids[:T], E, rows=layer.xq[:T], expert_counts=layer.counts,
+                            expert_offsets=layer.offsets, sorted_to_slot=layer.s2s[:A], slot_to_sorted=layer.sl2[:A],
+                            rows_sorted=layer.xq_sorted[:A], workspace=layer.dsp_ws, dev_status=layer.dev_status)
+        elif gathered:
             Lb.moe_dispatch(layer.ids[:T], E, expert_counts=layer.counts, expert_offsets=layer.offsets,
                             sorted_to_slot=layer.s2s[:A], slot_to_sorted=layer.sl2[:A], workspace=layer.dsp_ws,
                             dev_status=layer.dev_status)
@@ -176,7 +184,11 @@ def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None):
                             rows_sorted=layer.xq_sorted[:A], scales_sorted=layer.xs_sorted[:A],
                             workspace=layer.dsp_ws, dev_status=layer.dev_status)
         if record: e[3].record()
-        if gathered:
+        if ue8m0:
+            Lb.moe_grouped_ffn_mx(layer.xq_sorted[:A], layer.xs[:T], layer.s2s[:A], k, layer.offsets, layer.w.w13_q,
+                                  layer.w.w13_s, layer.w.w2_q, layer.w.w2_s, out_sorted=layer.out_sorted[:A],
+                                  workspace=layer.ffn_ws, dev_status=layer.dev_status)
+        elif gathered:
             Lb.moe_grouped_ffn_fp8_gathered(layer.xq[:T], layer.xs[:T], k, layer.s2s[:A], layer.offsets,
                                             layer.w.w13_q, layer.w.w13_s, layer.w.w2_q, layer.w.w2_s,
                                             out_slots=layer.out_sorted[:A], workspace=layer.ffn_ws,
@@ -290,7 +302,7 @@ def rank_seed(seed, rank):
     return seed + rank
 
 
-def rooflines(cfg, avg, peaks, gathered=False):
+def rooflines(cfg, avg, peaks, gathered=False, ue8m0=False):
     T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
     A = T * k
     fp8_peak = 2.0 * peaks["bf16_tflops"]
@@ -305,8 +317,10 @@ def rooflines(cfg, avg, peaks, gathered=False):
                            "(large_e64: same per-expert shape, 1/4 of the experts), scaled by routed rows"}
     ffn["frac"] = ffn["achieved"] / ffn["peak"]
     hbm = peaks["hbm_gbs"]
-    row = d + 4 * d / 128                       # one FP8 row with its 1x128 scales
+    row = d + (1 if ue8m0 else 4) * d / 128     # one FP8 row with its 1x128 scales (fp32 or exponent bytes)
     bytes_quant = T * d * 2 + T * row
+    if ue8m0:
+        row = d                                 # dispatch moves the codes only (the exponents stay token-major)
     bytes_disp = A * 4 + 2 * A * 4 + (0 if gathered else T * row + A * row)  # ids, two maps (+ row copy)
     bytes_comb = A * d * 2 + A * 4 + T * k * 4 + T * d * 2  # A bf16 rows + map + gates in, y out
     route_flops = 2.0 * T * d * E if cfg.mode == "route" else 2.0 * T * d * k
@@ -519,6 +533,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dispatch-combine", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
+    ap.add_argument("--no-mx", action="store_true", help="skip the power-of-two-scale (block-scaled MMA) line")
     ap.add_argument("--form", default="sorted", choices=["sorted", "gathered"],
                     help="sorted: dispatch copies rows into expert order; gathered: the FFN gathers its rows "
                          "(tile::gather4) and stores outputs in slot order")
@@ -593,6 +608,19 @@ def main():
             "ms_per_step": rr["total_ms"] / rr["steps"], "ffn_TFLOP/s": rffn["achieved"],
             "ffn_frac": rffn["frac"], "steps": rextra, "dev_status": rr["status"]}
         del rr
+        torch.cuda.empty_cache()
+    if cfg.name == "large" and not args.no_mx:
+        import torch
+        torch.cuda.empty_cache()
+        rm = run_gpu(args, rank, world, workload=cfg.name, with_e2e=False, steps=max(3, args.steps // 2), ue8m0=True)
+        mffn, mextra = rooflines(cfg, rm["avg"], peaks, ue8m0=True)
+        mffn["kernel"] = "moe_grouped_ffn_mx (block-scaled MMA, GEMM1+SwiGLU+requant, GEMM2)"
+        mffn["traffic"] = None
+        out["mx_layer"] = {
+            "workload": config["workload"] + ", power-of-two (UE8M0) block scales on the block-scaled MMA",
+            "tokens/s": job_throughput(cfg.T, rm["steps"], world, rm["total_ms"]),
+            "ms_per_step": rm["total_ms"] / rm["steps"], "ffn": mffn, "steps": mextra, "dev_status": rm["status"]}
+        del rm
         torch.cuda.empty_cache()
     if cfg.name == "large" and not args.no_dispatch_combine:
         import torch

@@ -157,6 +157,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 TMEM lanes x 16 columns into r[0..15], completion left to tmem_wait_ld32
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t *r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+}
+
+// wait for this thread's TMEM loads; the 32 registers are tied to the wait
+// so that no use of them is scheduled before it
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t *r)
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
 // barrier over the 16 epilogue warps that also ORs a predicate across them
 __device__ __forceinline__ bool epi_bar_or(bool pred)
 {
@@ -218,7 +243,8 @@ struct Tile {
     int rows;       // valid rows in this tile (1..128)
 };
 
-__device__ __forceinline__ Tile decode_tile(const Smem &s, int E, int n_tiles, int t)
+template <typename SmemT>
+__device__ __forceinline__ Tile decode_tile(const SmemT &s, int E, int n_tiles, int t)
 {
     int lo = 0, hi = E;  // largest e with tile_prefix[e] <= t
     while (hi - lo > 1) {
@@ -238,7 +264,8 @@ __device__ __forceinline__ Tile decode_tile(const Smem &s, int E, int n_tiles, i
 }
 
 // per-CTA tile table from the device offsets, by warp 0
-__device__ void build_schedule(Smem &s, const Params &p, int n_tiles)
+template <typename SmemT, typename ParamsT>
+__device__ void build_schedule(SmemT &s, const ParamsT &p, int n_tiles)
 {
     const int lane = threadIdx.x & 31;
     int32_t carry = 0;
@@ -545,6 +572,347 @@ static bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, cons
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// ============================================================================
+// Power-of-two scales (UE8M0): the hardware block-scaled MMA
+// ============================================================================
+//
+// With power-of-two block scales (fp8_block_quant_ue8m0) the scales need no
+// software promotion: tcgen05.mma.kind::mxf8f6f4.block_scale multiplies each
+// 32-deep K slice by 2^(ea-127) * 2^(eb-127) (one exponent byte per row of A
+// and per row of B, read from tensor memory) and accumulates the whole K
+// extent in TMEM.  One 128 x 256 fp32 accumulator per tile (256 columns;
+// the scale factors of each pipeline stage take 12 more), read once per
+// tile by the epilogue warps, which release it before the SwiGLU /
+// re-quantisation / store so that the next tile's MMAs start early.
+//
+// Scale factors: per K block the producer warp writes, for the A tile,
+// a 512-byte block of 32 rows x 16 bytes whose row r holds the exponent
+// words of A rows r, r+32, r+64, r+96 (each word = the row's exponent byte
+// repeated for the four 32-deep slices of the 128-deep block), and one
+// such block per 128-row half of the B tile; tcgen05.cp (32x128b, copied
+// into all four 32-lane quadrants) moves them to TMEM, where A row i finds
+// its word in lane i, column (i / 32) of its 4-column group, and the MMA's
+// scale-factor id picks the slice's byte (all four are equal here).
+
+constexpr int SFA_BYTES = 512;          // one 128-row scale-factor block
+constexpr int SFB_BYTES = 1024;         // two of them: B rows 0..127, 128..255
+constexpr int SF_COL0 = 256;            // TMEM column of stage 0's scale factors
+constexpr int SF_COLS_PER_STAGE = 16;   // A: 4 columns, B: 8 (+4 unused)
+
+struct SmemMX {
+    uint8_t a[STAGES][A_BYTES];
+    uint8_t b[STAGES][B_BYTES];
+    uint8_t sfa[STAGES][SFA_BYTES];
+    uint8_t sfb[STAGES][SFB_BYTES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull;                     // the tile's accumulator is complete
+    uint64_t tempty;                    // the epilogue has read it (16 arrivals)
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    float red[4][BM];
+    int32_t tile_prefix[MAX_E + 1];
+    int32_t row_lo[MAX_E + 1];
+};
+constexpr size_t SMEM_MX_BYTES = sizeof(SmemMX) + 1024;
+
+struct ParamsMX {
+    const uint8_t *a_exp;       // GEMM1: token-major [T, d/128]; GEMM2: sorted [max_rows, F/128]
+    const uint8_t *b_exp;       // GEMM1 [E, 2F/128, d/128]; GEMM2 [E, d/128, F/128]
+    const int32_t *offsets;     // [E+1]
+    const int32_t *sorted_to_slot;
+    uint8_t *act_q;             // GEMM1 out [max_rows, F]
+    uint8_t *act_e;             // GEMM1 out [max_rows, F/128]
+    uint16_t *out;              // GEMM2 out [max_rows, d] bf16
+    int32_t *dev_status;
+    int64_t max_rows;
+    int E, d, F;
+    int top_k;
+};
+
+// instruction descriptor of the block-scaled kind: fp32 accumulate, A = B =
+// E4M3, both K-major, N, UE8M0 scale factors, M, scale-factor ids of A, B
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t a_sf_id, uint32_t b_sf_id)
+{
+    return (b_sf_id << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | (a_sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
+                 "p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                 : "memory");
+}
+
+// shared-memory source of a 32 x 16-byte block, no swizzle: 8-row core
+// matrices of 128 contiguous bytes, 128 bytes apart
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr)
+{
+    uint64_t desc = 0;
+    desc |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    desc |= (uint64_t)(128u >> 4) << 16;
+    desc |= (uint64_t)(128u >> 4) << 32;
+    desc |= (uint64_t)1 << 46;
+    return desc;
+}
+
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ue8m0_exp_of(float amax)
+{
+    const uint32_t bits = __float_as_uint(amax);
+    const int32_t ef = (int32_t)(bits >> 23);
+    if (amax == 0.0f) return 127u;
+    if (ef == 0) return 0u;
+    const int32_t e = ef - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return (uint32_t)(e < 0 ? 0 : (e > 254 ? 254 : e));
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                           const ParamsMX p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SmemMX &s = *reinterpret_cast<SmemMX *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = MODE == 1 ? p.d : p.F;
+    const int nkb = K / BK;
+    const int n_tiles = MODE == 1 ? p.F / 128 : (p.d + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; i++) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        mbar_init(&s.tfull, 1);
+        mbar_init(&s.tempty, EPI_WARPS);
+        mbar_init(&s.mma_done, 1);
+        s.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) build_schedule(s, p, n_tiles);
+    if (warp == MMA_WARP) tmem_alloc(&s.tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+    const int total = s.tile_prefix[p.E];
+    volatile int *abort_flag = &s.abort_flag;
+
+    if (warp == PRODUCER_WARP) {
+        // ---------------- TMA producer + scale-factor blocks (whole warp) ----------------
+        uint32_t j = 0;
+        uint32_t issued = 0;
+        bool ok = true;
+        const int nka = K / 128;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const Tile tl = decode_tile(s, p.E, n_tiles, t);
+            // exponent rows of A rows lane + 32q (token rows for GEMM1); -1 past the tile
+            int64_t arow[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int r = lane + 32 * q;
+                arow[q] = -1;
+                if (r < tl.rows) {
+                    const int64_t row = (int64_t)tl.row0 + r;
+                    arow[q] = MODE == 1 ? (int64_t)(__ldg(p.sorted_to_slot + row) / p.top_k) : row;
+                }
+            }
+            // exponent rows of the B tile's two 128-row halves
+            const int64_t nb0 = MODE == 1 ? (int64_t)tl.e * (2 * p.F / 128) + tl.n_blk
+                                          : (int64_t)tl.e * (p.d / 128) + tl.n_blk * 2;
+            const int64_t nb1 = MODE == 1 ? nb0 + p.F / 128 : nb0 + 1;
+            const bool nb1_ok = MODE == 1 || (tl.n_blk * 2 + 1) < p.d / 128;
+            // exponent bytes of K block kb, fetched one block ahead so their
+            // latency hides behind the wait for the stage
+            auto fetch = [&](int kb, uint32_t *ea, uint32_t &eb0, uint32_t &eb1) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) ea[q] = arow[q] >= 0 ? (uint32_t)__ldg(p.a_exp + arow[q] * nka + kb) : 0u;
+                eb0 = (uint32_t)__ldg(p.b_exp + nb0 * nkb + kb);
+                eb1 = nb1_ok ? (uint32_t)__ldg(p.b_exp + nb1 * nkb + kb) : 0u;
+            };
+            uint32_t ea[4], eb0, eb1;
+            fetch(0, ea, eb0, eb1);
+            for (int kb = 0; kb < nkb; kb++, j++) {
+                const int st = j % STAGES;
+                uint32_t na[4] = {0u, 0u, 0u, 0u}, nb0e = 0u, nb1e = 0u;
+                if (kb + 1 < nkb) fetch(kb + 1, na, nb0e, nb1e);
+                bool w = true;
+                if (lane == 0) w = wait_or_abort(&s.empty[st], ((j / STAGES) & 1) ^ 1, abort_flag, p.dev_status);
+                w = __shfl_sync(0xFFFFFFFFu, w, 0);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                *reinterpret_cast<uint4 *>(s.sfa[st] + 16 * lane) =
+                    make_uint4(ea[0] * 0x01010101u, ea[1] * 0x01010101u, ea[2] * 0x01010101u, ea[3] * 0x01010101u);
+                const uint32_t wb0 = eb0 * 0x01010101u, wb1 = eb1 * 0x01010101u;
+                *reinterpret_cast<uint4 *>(s.sfb[st] + 16 * lane) = make_uint4(wb0, wb0, wb0, wb0);
+                *reinterpret_cast<uint4 *>(s.sfb[st] + SFA_BYTES + 16 * lane) = make_uint4(wb1, wb1, wb1, wb1);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+                    tma_load_2d(s.a[st], &tm_a, kb * BK, tl.row0, &s.full[st]);
+                    if (MODE == 1) {
+                        const int wrow = tl.e * 2 * p.F + tl.n_blk * 128;
+                        tma_load_2d(s.b[st], &tm_b, kb * BK, wrow, &s.full[st]);
+                        tma_load_2d(s.b[st] + B_BYTES / 2, &tm_b, kb * BK, wrow + p.F, &s.full[st]);
+                    } else {
+                        tma_load_2d(s.b[st], &tm_b, kb * BK, tl.e * p.d + tl.n_blk * BN, &s.full[st]);
+                    }
+                    issued |= 1u << st;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; q++) ea[q] = na[q];
+                eb0 = nb0e;
+                eb1 = nb1e;
+            }
+        }
+        if (lane == 0) {
+            for (int i = 0; i < STAGES; i++) {
+                if (!(issued & (1u << i)) || j == 0) continue;
+                const uint32_t last = j - 1 - ((j - 1 - i) % STAGES);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&s.full[i], (last / STAGES) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t j = 0, tcount = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x, tcount++) {
+                // the previous tile's accumulator must have been read out
+                if (!wait_or_abort(&s.tempty, (tcount & 1) ^ 1, abort_flag, p.dev_status)) break;
+                for (int kb = 0; kb < nkb; kb++, j++) {
+                    const int st = j % STAGES;
+                    if (!wait_or_abort(&s.full[st], (j / STAGES) & 1, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + SF_COL0 + SF_COLS_PER_STAGE * st;
+                    const uint32_t sfb_t = sfa_t + 4;
+                    tmem_cp_sf(sfa_t, sf_desc(smem_u32(s.sfa[st])));
+                    tmem_cp_sf(sfb_t, sf_desc(smem_u32(s.sfb[st])));
+                    tmem_cp_sf(sfb_t + 4, sf_desc(smem_u32(s.sfb[st] + SFA_BYTES)));
+                    const uint64_t adesc = sw128_desc(smem_u32(s.a[st]));
+                    const uint64_t bdesc = sw128_desc(smem_u32(s.b[st]));
+#pragma unroll
+                    for (int ks = 0; ks < BK / 32; ks++)
+                        // the four bytes of every scale word are equal (one exponent per
+                        // 128-deep block), so scale-factor id 0 serves all four slices
+                        mma_mx(tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc_mx(BM, BN, 0, 0), sfa_t, sfb_t,
+                               (kb > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&s.empty[st]);
+                }
+                if (ok) mma_commit(&s.tfull);
+            }
+            mma_commit(&s.mma_done);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&s.mma_done, 0) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 0..15): one accumulator read per tile ----------------
+        const int q = warp & 3;
+        const int cg = warp >> 2;
+        const int r_in = q * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        uint32_t tcount = 0;
+        bool aborted = false;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, tcount++) {
+            const Tile tl = decode_tile(s, p.E, n_tiles, t);
+            const bool row_ok = r_in < tl.rows;
+            const int64_t row = (int64_t)tl.row0 + r_in;
+            const int col0 = MODE == 1 ? 32 * cg : 64 * cg;
+            const int col1 = MODE == 1 ? 128 + 32 * cg : 64 * cg + 32;
+            float acc0[32], acc1[32];
+            if (!aborted && !wait_or_abort(&s.tfull, tcount & 1, abort_flag, p.dev_status)) aborted = true;
+            if (!aborted) {
+                tc_fence_after();
+                const uint32_t base = tmem + lane_addr;
+                uint32_t r0[32], r1[32];
+                tmem_ld16_nowait(base + col0, r0);
+                tmem_ld16_nowait(base + col0 + 16, r0 + 16);
+                tmem_ld16_nowait(base + col1, r1);
+                tmem_ld16_nowait(base + col1 + 16, r1 + 16);
+                tmem_wait_ld32(r0);   // one wait for all four loads; the operands
+                tmem_wait_ld32(r1);   // order every use of the values after it
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    acc0[i] = __uint_as_float(r0[i]);
+                    acc1[i] = __uint_as_float(r1[i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.tempty);
+            }
+            if (MODE == 1) {
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    const float g = acc0[i];
+                    acc0[i] = __fdiv_rn(g, 1.0f + expf(-g)) * acc1[i];
+                    amax = fmaxf(amax, fabsf(acc0[i]));
+                }
+                s.red[cg][r_in] = amax;
+                epi_bar();
+                amax = fmaxf(fmaxf(s.red[0][r_in], s.red[1][r_in]), fmaxf(s.red[2][r_in], s.red[3][r_in]));
+                const uint32_t e8 = ue8m0_exp_of(amax);
+                const float sc = e8 == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e8 << 23);
+                if (row_ok && !aborted) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++)
+                        w[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i], sc), __fdiv_rn(acc0[4 * i + 1], sc)) |
+                               ((uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sc),
+                                                      __fdiv_rn(acc0[4 * i + 3], sc))
+                                << 16);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.act_q + row * p.F + tl.n_blk * 128 + 32 * cg);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    if (cg == 0) p.act_e[row * (p.F / 128) + tl.n_blk] = (uint8_t)e8;
+                }
+            } else {
+                const int c_glob = tl.n_blk * BN + 64 * cg;
+                if (row_ok && !aborted && c_glob < p.d) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * p.d + c_glob);
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        dst[i] = make_uint4(pack_bf16x2(acc0[8 * i], acc0[8 * i + 1]),
+                                            pack_bf16x2(acc0[8 * i + 2], acc0[8 * i + 3]),
+                                            pack_bf16x2(acc0[8 * i + 4], acc0[8 * i + 5]),
+                                            pack_bf16x2(acc0[8 * i + 6], acc0[8 * i + 7]));
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        dst[4 + i] = make_uint4(pack_bf16x2(acc1[8 * i], acc1[8 * i + 1]),
+                                                pack_bf16x2(acc1[8 * i + 2], acc1[8 * i + 3]),
+                                                pack_bf16x2(acc1[8 * i + 4], acc1[8 * i + 5]),
+                                                pack_bf16x2(acc1[8 * i + 6], acc1[8 * i + 7]));
+                }
+            }
+            if (epi_bar_or(aborted || *abort_flag)) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+}
+
 } // namespace ffn
 } // namespace moe
 
@@ -645,4 +1013,68 @@ MOE_API moe_status moe_grouped_ffn_fp8_gathered(const uint8_t *xq, const float *
     if (T == 0) return MOE_OK;
     return ffn_launch<true>(xq, T, xs, sorted_to_slot, k, expert_offsets, (int64_t)T * k, E, d, F, w13_q, w13_s,
                             w2_q, w2_s, out_slots, workspace, workspace_bytes, dev_status, stream);
+}
+
+MOE_API size_t moe_grouped_ffn_mx_workspace_size(int64_t max_rows, int d, int F)
+{
+    (void)d;
+    if (max_rows < 0 || F <= 0) return 0;
+    return align256((size_t)max_rows * F) + align256((size_t)max_rows * (F / 128));
+}
+
+MOE_API moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, const int32_t *sorted_to_slot,
+                                      int T, int k, const int32_t *expert_offsets, int64_t max_rows, int E, int d,
+                                      int F, const uint8_t *w13_q, const uint8_t *w13_exp, const uint8_t *w2_q,
+                                      const uint8_t *w2_exp, uint16_t *out_sorted, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    if (max_rows < 0 || max_rows >= (1LL << 31) || E < 1 || E > MAX_E || d <= 0 || F <= 0 || d % 128 != 0 ||
+        F % 128 != 0 || T < 0 || k < 1 || k > 32)
+        return MOE_ERR_SHAPE;
+    if ((int64_t)E * 2 * F >= (1LL << 31) || (int64_t)E * d >= (1LL << 31)) return MOE_ERR_SHAPE;
+    const size_t need = moe_grouped_ffn_mx_workspace_size(max_rows, d, F);
+    if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    if (max_rows == 0 || T == 0) return MOE_OK;
+    if (!xq_sorted || !x_exp || !sorted_to_slot || !expert_offsets || !w13_q || !w13_exp || !w2_q || !w2_exp ||
+        !out_sorted)
+        return MOE_ERR_NULL;
+    if (!aligned16(xq_sorted) || !aligned16(w13_q) || !aligned16(w2_q) || !aligned16(out_sorted) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return MOE_ERR_ALIGN;
+    auto enc = encode_fn();
+    if (!enc) return MOE_ERR_CUDA;
+    uint8_t *act_q = reinterpret_cast<uint8_t *>(workspace);
+    uint8_t *act_e = reinterpret_cast<uint8_t *>(workspace) + align256((size_t)max_rows * F);
+    CUtensorMap ma1, mb1, ma2, mb2;
+    if (!make_map(enc, &ma1, xq_sorted, d, max_rows, 128) || !make_map(enc, &mb1, w13_q, d, (uint64_t)E * 2 * F, 128) ||
+        !make_map(enc, &ma2, act_q, F, max_rows, 128) || !make_map(enc, &mb2, w2_q, F, (uint64_t)E * d, 256))
+        return MOE_ERR_CUDA;
+    ParamsMX prm;
+    prm.offsets = expert_offsets;
+    prm.sorted_to_slot = sorted_to_slot;
+    prm.act_q = act_q;
+    prm.act_e = act_e;
+    prm.out = out_sorted;
+    prm.dev_status = dev_status;
+    prm.max_rows = max_rows;
+    prm.E = E;
+    prm.d = d;
+    prm.F = F;
+    prm.top_k = k;
+    if (cudaFuncSetAttribute(grouped_gemm_mx_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_MX_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(grouped_gemm_mx_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_MX_BYTES) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int grid = sm_count();
+    cudaStream_t st = as_stream(stream);
+    ParamsMX p1 = prm;
+    p1.a_exp = x_exp;
+    p1.b_exp = w13_exp;
+    grouped_gemm_mx_kernel<1><<<grid, THREADS, SMEM_MX_BYTES, st>>>(ma1, mb1, p1);
+    ParamsMX p2 = prm;
+    p2.a_exp = act_e;
+    p2.b_exp = w2_exp;
+    grouped_gemm_mx_kernel<2><<<grid, THREADS, SMEM_MX_BYTES, st>>>(ma2, mb2, p2);
+    return launch_status();
 }

@@ -10,13 +10,56 @@
 // is 16 lanes of one half-warp (amax by 4 shuffles), a 128x128 block is one
 // 256-thread CTA holding its 64 values per thread in registers between the
 // amax pass and the encode pass (the block is read from HBM once).
+//
+// MX = true is the power-of-two variant (the scale format of the hardware
+// block-scaled MMA, UE8M0): the block scale is the smallest power of two
+// 2^p with amax <= 448 * 2^p, stored as the biased exponent byte p + 127;
+// codes are v / 2^p (an exact division), so none saturates.
 #include "common.cuh"
 
 namespace moe {
 
+// biased exponent of the UE8M0 block scale, read off amax's bits:
+// amax = 1.m * 2^E needs p = E - 8 (448 = 1.75 * 2^8), one more when
+// 1.m > 1.75; subnormal amax clamps to p = -127 (exponent byte 0)
+__device__ __forceinline__ uint32_t ue8m0_exp(float amax)
+{
+    const uint32_t bits = __float_as_uint(amax);
+    const int32_t ef = (int32_t)(bits >> 23);
+    if (amax == 0.0f) return 127u;
+    if (ef == 0) return 0u;
+    int32_t e = ef - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return (uint32_t)(e < 0 ? 0 : (e > 254 ? 254 : e));
+}
+
+__device__ __forceinline__ float ue8m0_value(uint32_t e)
+{
+    return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);   // 2^(e-127)
+}
+
+// the block's scale value; *stored is the fp32 scale or the exponent byte
+template <bool MX>
+__device__ __forceinline__ float rule_scale(float amax, uint32_t &e8)
+{
+    if (MX) {
+        e8 = ue8m0_exp(amax);
+        return ue8m0_value(e8);
+    }
+    e8 = 0;
+    return block_scale(amax);
+}
+
+template <bool MX>
+__device__ __forceinline__ void store_scale(void *scales, int64_t i, float s, uint32_t e8)
+{
+    if (MX) reinterpret_cast<uint8_t *>(scales)[i] = (uint8_t)e8;
+    else reinterpret_cast<float *>(scales)[i] = s;
+}
+
+template <bool MX>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t *__restrict__ src, int64_t rows,
                                                           int64_t cols, int64_t ld, uint8_t *__restrict__ q,
-                                                          float *__restrict__ scales)
+                                                          void *__restrict__ scales)
 {
     const int64_t nbc = cols >> 7;
     const int64_t nblocks = rows * nbc;
@@ -35,20 +78,22 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t *__rest
         for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o, 16));
-        const float s = block_scale(amax);
+        uint32_t e8;
+        const float s = rule_scale<MX>(amax, e8);
         uint2 out;
         out.x = (uint32_t)pack_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
                 ((uint32_t)pack_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
         out.y = (uint32_t)pack_e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) |
                 ((uint32_t)pack_e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
         *reinterpret_cast<uint2 *>(q + r * cols + cb * 128 + sub * 8) = out;
-        if (sub == 0) scales[b] = s;
+        if (sub == 0) store_scale<MX>(scales, b, s, e8);
     }
 }
 
+template <bool MX>
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t *__restrict__ src, int64_t cols,
                                                             int64_t ld, uint8_t *__restrict__ q,
-                                                            float *__restrict__ scales)
+                                                            void *__restrict__ scales)
 {
     __shared__ float warp_amax[8];
     const int64_t nbc = cols >> 7;
@@ -76,7 +121,8 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t *__re
     amax = warp_amax[0];
 #pragma unroll
     for (int w = 1; w < 8; w++) amax = fmaxf(amax, warp_amax[w]);
-    const float s = block_scale(amax);
+    uint32_t e8;
+    const float s = rule_scale<MX>(amax, e8);
 #pragma unroll
     for (int i = 0; i < 8; i++) {
         float v[8];
@@ -89,15 +135,18 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t *__re
         const int64_t r = br * 128 + tr + 16 * i;
         *reinterpret_cast<uint2 *>(q + r * cols + bc * 128 + tc * 8) = out;
     }
-    if (tid == 0) scales[b] = s;
+    if (tid == 0) store_scale<MX>(scales, b, s, e8);
 }
 
 } // namespace moe
 
 using namespace moe;
 
-MOE_API moe_status fp8_block_quant(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
-                                   int block_rows, uint8_t *q, float *scales, void *stream)
+namespace moe {
+
+template <bool MX>
+static moe_status quant_launch(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src, int block_rows,
+                               uint8_t *q, void *scales, void *stream)
 {
     if (rows < 0 || cols <= 0 || cols % 128 != 0 || ld_src < cols) return MOE_ERR_SHAPE;
     if (block_rows != 1 && block_rows != 128) return MOE_ERR_SHAPE;
@@ -111,11 +160,25 @@ MOE_API moe_status fp8_block_quant(const uint16_t *src, int64_t rows, int64_t co
         int64_t grid = (nblocks + 15) / 16;
         const int64_t cap = (int64_t)sm_count() * 16;
         if (grid > cap) grid = cap;
-        quant_1x128_kernel<<<(unsigned)grid, 256, 0, st>>>(src, rows, cols, ld_src, q, scales);
+        quant_1x128_kernel<MX><<<(unsigned)grid, 256, 0, st>>>(src, rows, cols, ld_src, q, scales);
     } else {
         const int64_t nblocks = (rows / 128) * (cols / 128);
         if (nblocks > 0x7FFFFFFFLL) return MOE_ERR_SHAPE;
-        quant_128x128_kernel<<<(unsigned)nblocks, 256, 0, st>>>(src, cols, ld_src, q, scales);
+        quant_128x128_kernel<MX><<<(unsigned)nblocks, 256, 0, st>>>(src, cols, ld_src, q, scales);
     }
     return launch_status();
+}
+
+} // namespace moe
+
+MOE_API moe_status fp8_block_quant(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
+                                   int block_rows, uint8_t *q, float *scales, void *stream)
+{
+    return quant_launch<false>(src, rows, cols, ld_src, block_rows, q, scales, stream);
+}
+
+MOE_API moe_status fp8_block_quant_ue8m0(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
+                                         int block_rows, uint8_t *q, uint8_t *scale_exp, void *stream)
+{
+    return quant_launch<true>(src, rows, cols, ld_src, block_rows, q, scale_exp, stream);
 }

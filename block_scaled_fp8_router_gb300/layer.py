@@ -20,9 +20,14 @@ from . import moe_r3 as L
 class MoEWeightsFP8:
     w_router: torch.Tensor   # [E, d] bf16
     w13_q: torch.Tensor      # [E, 2F, d] e4m3 codes (rows 0..F-1 gate, F..2F-1 up)
-    w13_s: torch.Tensor      # [E, 2F/128, d/128] fp32
+    w13_s: torch.Tensor      # [E, 2F/128, d/128] fp32 scales, or uint8 power-of-two exponents (UE8M0)
     w2_q: torch.Tensor       # [E, d, F] e4m3 codes
-    w2_s: torch.Tensor       # [E, d/128, F/128] fp32
+    w2_s: torch.Tensor       # [E, d/128, F/128] fp32, or uint8 exponents
+
+    @property
+    def ue8m0(self) -> bool:
+        """Power-of-two block scales (the block-scaled-MMA variant)."""
+        return self.w13_s.dtype == torch.uint8
 
     @property
     def E(self) -> int:
@@ -37,21 +42,30 @@ class MoEWeightsFP8:
         return self.w13_q.shape[1] // 2
 
 
-def quantize_weights(w13: torch.Tensor, w2: torch.Tensor, out: MoEWeightsFP8 | None = None, e0: int = 0):
+def quantize_weights(w13: torch.Tensor, w2: torch.Tensor, out: MoEWeightsFP8 | None = None, e0: int = 0,
+                     ue8m0: bool = False):
     """128x128 block quantisation of bf16 expert weights (once per weight
-    update).  w13 [n, 2F, d], w2 [n, d, F] -> codes and scales; with `out`,
-    writes experts e0 .. e0+n-1 of it in place."""
+    update).  w13 [n, 2F, d], w2 [n, d, F] -> codes and scales (fp32, or
+    power-of-two exponent bytes with ue8m0 / an `out` holding uint8 scales);
+    with `out`, writes experts e0 .. e0+n-1 of it in place."""
     n, twoF, d = w13.shape
     F = twoF // 2
+    if out is not None:
+        ue8m0 = out.ue8m0
+    if ue8m0:
+        def quant(src, q=None, s=None):
+            return L.fp8_block_quant_ue8m0(src, 128, q=q, scale_exp=s)
+    else:
+        def quant(src, q=None, s=None):
+            return L.fp8_block_quant(src, 128, q=q, scales=s)
     if out is None:
-        w13_q, w13_s = L.fp8_block_quant(w13.reshape(n * twoF, d), 128)
-        w2_q, w2_s = L.fp8_block_quant(w2.reshape(n * d, F), 128)
+        w13_q, w13_s = quant(w13.reshape(n * twoF, d))
+        w2_q, w2_s = quant(w2.reshape(n * d, F))
         return (w13_q.view(n, twoF, d), w13_s.view(n, twoF // 128, d // 128),
                 w2_q.view(n, d, F), w2_s.view(n, d // 128, F // 128))
-    L.fp8_block_quant(w13.reshape(n * twoF, d), 128, q=out.w13_q[e0:e0 + n].view(n * twoF, d),
-                      scales=out.w13_s[e0:e0 + n].view(n * twoF // 128, d // 128))
-    L.fp8_block_quant(w2.reshape(n * d, F), 128, q=out.w2_q[e0:e0 + n].view(n * d, F),
-                      scales=out.w2_s[e0:e0 + n].view(n * d // 128, F // 128))
+    quant(w13.reshape(n * twoF, d), out.w13_q[e0:e0 + n].view(n * twoF, d),
+          out.w13_s[e0:e0 + n].view(n * twoF // 128, d // 128))
+    quant(w2.reshape(n * d, F), out.w2_q[e0:e0 + n].view(n * d, F), out.w2_s[e0:e0 + n].view(n * d // 128, F // 128))
     return out
 
 
@@ -63,12 +77,18 @@ class MoELayerFP8:
     gathered=True: dispatch builds the maps only, the FFN gathers its A rows
     from the token-major codes (tile::gather4) and stores its outputs in slot
     order, and combine reads each token's k rows contiguously.  Same bits.
+    Weights with power-of-two (UE8M0) scales select the block-scaled-MMA
+    variant: x is quantised with power-of-two scales and the FFN is
+    moe_grouped_ffn_mx (sorted form).
     """
 
     def __init__(self, weights: MoEWeightsFP8, T_max: int, k: int, score_fn: int, renorm: int = 1,
                  route_scale: float = 1.0, device=None, gathered: bool = False):
         self.w = weights
         self.gathered = gathered
+        self.mx = weights.ue8m0
+        if self.mx and gathered:
+            raise ValueError("the power-of-two variant runs in the sorted form")
         self.k, self.score_fn, self.renorm, self.route_scale = k, score_fn, renorm, route_scale
         dev = weights.w13_q.device if device is None else device
         E, d, F = weights.E, weights.d, weights.F
@@ -78,17 +98,18 @@ class MoELayerFP8:
         self.ids = e((T_max, k), torch.int32)
         self.gates = e((T_max, k), torch.float32)
         self.xq = e((T_max, d), torch.uint8)
-        self.xs = e((T_max, d // 128), torch.float32)
+        self.xs = e((T_max, d // 128), torch.uint8 if self.mx else torch.float32)
         self.counts = e((E,), torch.int32)
         self.offsets = e((E + 1,), torch.int32)
         self.s2s = e((A,), torch.int32)
         self.sl2 = e((A,), torch.int32)
         self.xq_sorted = None if gathered else e((A, d), torch.uint8)
-        self.xs_sorted = None if gathered else e((A, d // 128), torch.float32)
+        self.xs_sorted = None if (gathered or self.mx) else e((A, d // 128), torch.float32)
         self.out_sorted = e((A, d), torch.bfloat16)     # slot order when gathered
         self.y = e((T_max, d), torch.bfloat16)
         self.dsp_ws = e((L.moe_dispatch_workspace_size(T_max, k, E),), torch.uint8)
-        self.ffn_ws = e((L.moe_grouped_ffn_workspace_size(A, d, F),), torch.uint8)
+        ws = L.moe_grouped_ffn_mx_workspace_size(A, d, F) if self.mx else L.moe_grouped_ffn_workspace_size(A, d, F)
+        self.ffn_ws = e((ws,), torch.uint8)
         self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
 
     def route(self, x: torch.Tensor, replay_kT: torch.Tensor | None = None, capture_kT: torch.Tensor | None = None):
@@ -109,8 +130,17 @@ class MoELayerFP8:
             raise ValueError(f"T={T} exceeds T_max={self.T_max}")
         A = T * self.k
         ids, gates = self.route(x, replay_kT, capture_kT)
-        xq, xs = L.fp8_block_quant(x, 1, q=self.xq[:T], scales=self.xs[:T])
         y = self.y[:T] if y is None else y
+        if self.mx:
+            xq, xe = L.fp8_block_quant_ue8m0(x, 1, q=self.xq[:T], scale_exp=self.xs[:T])
+            L.moe_dispatch(ids, self.w.E, rows=xq, expert_counts=self.counts, expert_offsets=self.offsets,
+                           sorted_to_slot=self.s2s[:A], slot_to_sorted=self.sl2[:A], rows_sorted=self.xq_sorted[:A],
+                           workspace=self.dsp_ws, dev_status=self.dev_status)
+            L.moe_grouped_ffn_mx(self.xq_sorted[:A], xe, self.s2s[:A], self.k, self.offsets, self.w.w13_q,
+                                 self.w.w13_s, self.w.w2_q, self.w.w2_s, out_sorted=self.out_sorted[:A],
+                                 workspace=self.ffn_ws, dev_status=self.dev_status)
+            return L.moe_combine(self.out_sorted[:A], self.sl2[:A], gates, y=y)
+        xq, xs = L.fp8_block_quant(x, 1, q=self.xq[:T], scales=self.xs[:T])
         if self.gathered:
             L.moe_dispatch(ids, self.w.E, expert_counts=self.counts, expert_offsets=self.offsets,
                            sorted_to_slot=self.s2s[:A], slot_to_sorted=self.sl2[:A], workspace=self.dsp_ws,

@@ -34,6 +34,7 @@ _SIGS = {
     "moe_payload_pack_u8": (I, [P, I64, I, P, P, P]),
     "moe_payload_unpack_u8": (I, [P, I64, P, P]),
     "fp8_block_quant": (I, [P, I64, I64, I64, I, P, P, P]),
+    "fp8_block_quant_ue8m0": (I, [P, I64, I64, I64, I, P, P, P]),
     "moe_dispatch_workspace_size": (SZ, [I, I, I]),
     "moe_dispatch": (I, [P, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_dispatch_noalloc": (I, [P, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, P]),
@@ -42,6 +43,8 @@ _SIGS = {
     "moe_combine": (I, [P, P, P, I, I, I, P, P]),
     "moe_grouped_ffn_fp8_gathered": (I, [P, P, I, I, P, P, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_combine_slots": (I, [P, P, P, I, I, I, P, P]),
+    "moe_grouped_ffn_mx_workspace_size": (SZ, [I64, I, I]),
+    "moe_grouped_ffn_mx": (I, [P, P, P, I, I, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_debug_bounded_wait": (I, [I64, P, P]),
     "moe_device_sm_count": (I, []),
 }
@@ -185,6 +188,23 @@ def moe_payload_unpack_u8(packed, out=None, stream=None):
     _check("moe_payload_unpack_u8", _lib.moe_payload_unpack_u8(
         _ptr(packed), packed.numel(), _ptr(out), _stream(stream)))
     return out
+
+
+def fp8_block_quant_ue8m0(src, block_rows, q=None, scale_exp=None, stream=None):
+    """bf16 [rows, cols] -> (E4M3 codes uint8 [rows, cols], power-of-two
+    scale exponents uint8 [rows/block_rows, cols/128], scale = 2^(e-127))."""
+    if src.dim() != 2:
+        raise ValueError("src must be 2-D")
+    rows, cols = src.shape
+    if src.dtype != torch.bfloat16 or not src.is_cuda or src.stride(1) != 1:
+        raise ValueError("src: bf16 CUDA tensor with unit column stride")
+    q = _empty((rows, cols), torch.uint8, src) if q is None else q
+    scale_exp = _empty((rows // block_rows, cols // 128), torch.uint8, src) if scale_exp is None else scale_exp
+    _want(q, torch.uint8, (rows, cols), "q")
+    _want(scale_exp, torch.uint8, (rows // block_rows, cols // 128), "scale_exp")
+    _check("fp8_block_quant_ue8m0", _lib.fp8_block_quant_ue8m0(
+        _ptr(src), rows, cols, src.stride(0), block_rows, _ptr(q), _ptr(scale_exp), _stream(stream)))
+    return q, scale_exp
 
 
 def fp8_block_quant(src, block_rows, q=None, scales=None, stream=None):
@@ -345,6 +365,37 @@ def moe_grouped_ffn_fp8_gathered(xq, xs, top_k, sorted_to_slot, expert_offsets, 
         _ptr(w2_q), _ptr(w2_s), _ptr(out_slots), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream)))
     return out_slots
+
+
+def moe_grouped_ffn_mx_workspace_size(max_rows: int, d: int, F: int) -> int:
+    return int(_lib.moe_grouped_ffn_mx_workspace_size(max_rows, d, F))
+
+
+def moe_grouped_ffn_mx(xq_sorted, x_exp, sorted_to_slot, top_k, expert_offsets, w13_q, w13_exp, w2_q, w2_exp,
+                       out_sorted=None, workspace=None, dev_status=None, stream=None):
+    """Grouped SwiGLU FFN with power-of-two block scales on the block-scaled
+    MMA -> out_sorted [max_rows, d] bf16.  x_exp is token-major [T, d/128]."""
+    max_rows, d = xq_sorted.shape
+    T = x_exp.shape[0]
+    E, twoF, _ = w13_q.shape
+    F = twoF // 2
+    _want(xq_sorted, torch.uint8, (max_rows, d), "xq_sorted")
+    _want(x_exp, torch.uint8, (T, d // 128), "x_exp")
+    _want(sorted_to_slot, torch.int32, (sorted_to_slot.numel(),), "sorted_to_slot")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(w13_q, torch.uint8, (E, 2 * F, d), "w13_q")
+    _want(w13_exp, torch.uint8, (E, 2 * F // 128, d // 128), "w13_exp")
+    _want(w2_q, torch.uint8, (E, d, F), "w2_q")
+    _want(w2_exp, torch.uint8, (E, d // 128, F // 128), "w2_exp")
+    out_sorted = _empty((max_rows, d), torch.bfloat16, xq_sorted) if out_sorted is None else out_sorted
+    _want(out_sorted, torch.bfloat16, (max_rows, d), "out_sorted")
+    if workspace is None:
+        workspace = _empty((moe_grouped_ffn_mx_workspace_size(max_rows, d, F),), torch.uint8, xq_sorted)
+    _check("moe_grouped_ffn_mx", _lib.moe_grouped_ffn_mx(
+        _ptr(xq_sorted), _ptr(x_exp), _ptr(sorted_to_slot), T, top_k, _ptr(expert_offsets), max_rows, E, d, F,
+        _ptr(w13_q), _ptr(w13_exp), _ptr(w2_q), _ptr(w2_exp), _ptr(out_sorted), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+    return out_sorted
 
 
 def moe_combine_slots(out_slots, slot_to_sorted, gates, y=None, stream=None):

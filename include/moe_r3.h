@@ -159,6 +159,20 @@ moe_status fp8_block_quant(const uint16_t *src, int64_t rows, int64_t cols, int6
                            int block_rows, uint8_t *q, float *scales, void *stream);
 
 /* ------------------------------------------------------------------------
+ * fp8_block_quant_ue8m0 -- fp8_block_quant with power-of-two block scales
+ * (the UE8M0 scale format of MXFP8 and of the hardware block-scaled MMA; a
+ * variant of the "FP8 training" recipe, whose scales are arbitrary fp32).
+ *
+ * Per block (1 x 128 or 128 x 128 as fp8_block_quant): amax = max |v|; the
+ * scale is 2^p for the smallest integer p with amax <= 448 * 2^p (p clamped
+ * to [-127, 127]; an all-zero block takes p = 0); scale_exp holds p + 127;
+ * q = E4M3(v / 2^p), round to nearest even (no code saturates).
+ * scale_exp [rows/block_rows, cols/128] uint8.  Errors as fp8_block_quant.
+ * ---------------------------------------------------------------------- */
+moe_status fp8_block_quant_ue8m0(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src,
+                                 int block_rows, uint8_t *q, uint8_t *scale_exp, void *stream);
+
+/* ------------------------------------------------------------------------
  * moe_dispatch -- permute token rows into expert-contiguous order
  * ("Expert parallelism": dispatch).
  *
@@ -269,6 +283,31 @@ moe_status moe_grouped_ffn_fp8_gathered(const uint8_t *xq, const float *xs, int 
                                         const uint8_t *w2_q, const float *w2_s, uint16_t *out_slots,
                                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                         void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_ffn_mx -- the grouped SwiGLU FFN with power-of-two (UE8M0)
+ * block scales on the hardware block-scaled MMA
+ * (tcgen05.mma.kind::mxf8f6f4.block_scale): a variant of the "FP8
+ * training" recipe whose scales are powers of two, so no per-block software
+ * promotion is needed.
+ *
+ *   h[r,n] = sum over K of (xq * 2^(x_exp-127)) (w13_q * 2^(w13_exp-127)),
+ *            accumulated in fp32 by the tensor core; act = silu(gate) * up,
+ *            re-quantised 1x128 along F with power-of-two scales (the rule of
+ *            fp8_block_quant_ue8m0); out_sorted = bf16 of act_q W2^T likewise.
+ * xq_sorted [max_rows, d] e4m3 (moe_dispatch rows); x_exp [T, d/128] uint8,
+ * token-major (row r's exponents are x_exp[sorted_to_slot[r] / k]);
+ * w13_q [E, 2F, d], w13_exp [E, 2F/128, d/128]; w2_q [E, d, F],
+ * w2_exp [E, d/128, F/128]; workspace moe_grouped_ffn_mx_workspace_size
+ * bytes (act_q and its exponents), 256-byte aligned.
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
+ * ---------------------------------------------------------------------- */
+size_t moe_grouped_ffn_mx_workspace_size(int64_t max_rows, int d, int F);
+moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, const int32_t *sorted_to_slot,
+                              int T, int k, const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                              const uint8_t *w13_q, const uint8_t *w13_exp, const uint8_t *w2_q,
+                              const uint8_t *w2_exp, uint16_t *out_sorted, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * moe_combine -- gate-weighted sum back to token order ("Expert
