@@ -534,6 +534,8 @@ def main():
     ap.add_argument("--no-dispatch-combine", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
     ap.add_argument("--no-mx", action="store_true", help="skip the power-of-two-scale (block-scaled MMA) line")
+    ap.add_argument("--scales", default="fp32", choices=["fp32", "ue8m0"],
+                    help="block scales of the timed layer: fp32 (the recipe) or power-of-two (block-scaled MMA)")
     ap.add_argument("--form", default="sorted", choices=["sorted", "gathered"],
                     help="sorted: dispatch copies rows into expert order; gathered: the FFN gathers its rows "
                          "(tile::gather4) and stores outputs in slot order")
@@ -548,7 +550,7 @@ def main():
                           f"{'sigmoid' if cfg.score_fn else 'softmax'} {cfg.mode}",
               "tokens_per_gpu": cfg.T, "parallelism": f"token-sharded x{world}" if world > 1 else "single GPU",
               "l2": "inputs larger than L2 (FP8 expert weights streamed from HBM every step)",
-              "form": args.form}
+              "form": args.form, "scales": args.scales}
     metric = "MoE-layer tokens/s (7168d/256e/top-8 FP8)" if cfg.name == "large" else f"MoE-layer tokens/s ({cfg.name})"
 
     if args.impl == "reference":
@@ -579,12 +581,16 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     peaks = _peaks()
-    r = run_gpu(args, rank, world)
+    main_mx = args.scales == "ue8m0"
+    r = run_gpu(args, rank, world, ue8m0=main_mx)
     cfg = r["cfg"]
     value = job_throughput(cfg.T, args.steps, world, r["total_ms"])
     e2e = job_throughput(cfg.T, args.steps, world, r["e2e_ms"])
-    gathered = args.form == "gathered"
-    ffn, extra = rooflines(cfg, r["avg"], peaks, gathered)
+    gathered = args.form == "gathered" and not main_mx
+    ffn, extra = rooflines(cfg, r["avg"], peaks, gathered, main_mx)
+    if main_mx:
+        ffn["kernel"] = "moe_grouped_ffn_mx (block-scaled MMA, GEMM1+SwiGLU+requant, GEMM2)"
+        ffn["traffic"] = None
     launches = sum(KERNELS_PER_STEP[n] for n in ("quant", "dispatch", "ffn", "combine")) + 1 - int(gathered)
     out = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
@@ -609,7 +615,7 @@ def main():
             "ffn_frac": rffn["frac"], "steps": rextra, "dev_status": rr["status"]}
         del rr
         torch.cuda.empty_cache()
-    if cfg.name == "large" and not args.no_mx:
+    if cfg.name == "large" and not args.no_mx and not main_mx:
         import torch
         torch.cuda.empty_cache()
         rm = run_gpu(args, rank, world, workload=cfg.name, with_e2e=False, steps=max(3, args.steps // 2), ue8m0=True)
