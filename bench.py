@@ -448,6 +448,74 @@ def run_payload(dev, seed, steps, warmup, peaks):
     return out
 
 
+def run_hbm_kernels(dev, seed, steps, warmup, peaks):
+    """The HBM-bound kernels alone on a profiling shape larger than L2 and a
+    few GB in total: T=16384 tokens, d=7168, E=256, top-8, replayed uniform
+    ids.  1x128 quantiser (235 MB of x), dispatch with FP8 rows + scales
+    (940 MB of rows), combine of bf16 expert rows (1.9 GB), one-byte payload
+    pack/unpack of a [64, 8, 131072] payload (268 MB)."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    cfg = S.CONFIGS["long_dispatch"].with_(T=16384)
+    T, k, d, E = cfg.T, cfg.k, cfg.d, cfg.E
+    A = T * k
+    x = S.make_x(cfg, dev, seed)
+    ids = S.make_replay_payload(cfg, dev, seed)[0].t().contiguous()
+    gates = S.make_dirichlet_gates(cfg, dev, seed)
+    q = torch.empty((T, d), dtype=torch.uint8, device=dev)
+    sc = torch.empty((T, d // 128), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    s2s = torch.empty(A, dtype=torch.int32, device=dev)
+    sl2 = torch.empty(A, dtype=torch.int32, device=dev)
+    rows = torch.empty((A, d), dtype=torch.uint8, device=dev)
+    rsc = torch.empty((A, d // 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(Lb.moe_dispatch_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    out = torch.empty((A, d), dtype=torch.bfloat16, device=dev).normal_(0.0, 0.1, generator=torch.Generator(device=dev).manual_seed(seed))
+    y = torch.empty_like(x)
+    pl = S.make_replay_payload(S.CONFIGS["long_dispatch"].with_(layers=64), dev, seed)
+    packed = torch.empty_like(pl, dtype=torch.uint8)
+    back = torch.empty_like(pl)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    gbs = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9
+    row = d + 4 * d / 128
+    res = {}
+    t = timed(lambda: Lb.fp8_block_quant(x, 1, q=q, scales=sc))
+    res["quant_1x128"] = {"ms": t, "bytes": T * d * 2 + T * row, "GB/s": gbs(T * d * 2 + T * row, t)}
+    t = timed(lambda: Lb.moe_dispatch(ids, E, rows=q, row_scales=sc, expert_counts=counts, expert_offsets=offs,
+                                      sorted_to_slot=s2s, slot_to_sorted=sl2, rows_sorted=rows, scales_sorted=rsc,
+                                      workspace=ws, dev_status=st))
+    nb = A * 4 + 2 * A * 4 + T * row + A * row
+    res["dispatch_fp8_rows"] = {"ms": t, "bytes": nb, "GB/s": gbs(nb, t)}
+    t = timed(lambda: Lb.moe_combine(out, sl2, gates, y=y))
+    nb = A * d * 2 + A * 4 + A * 4 + T * d * 2
+    res["combine"] = {"ms": t, "bytes": nb, "GB/s": gbs(nb, t)}
+    n = pl.numel()
+    t = timed(lambda: Lb.moe_payload_pack_u8(pl, E, out=packed, dev_status=st))
+    res["payload_pack_u8"] = {"ms": t, "bytes": 5 * n, "GB/s": gbs(5 * n, t)}
+    t = timed(lambda: Lb.moe_payload_unpack_u8(packed, out=back))
+    res["payload_unpack_u8"] = {"ms": t, "bytes": 5 * n, "GB/s": gbs(5 * n, t)}
+    for v in res.values():
+        v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+    return {"workload": f"HBM kernels: T={T} d={d} E={E} top_k={k} (replayed uniform ids); payload [64, 8, 131072]",
+            "peak_GB/s": peaks["hbm_gbs"], "kernels": res, "status": Lb.check_status(st)}
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 class OracleSample:
@@ -534,6 +602,8 @@ def main():
     ap.add_argument("--no-dispatch-combine", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
     ap.add_argument("--no-mx", action="store_true", help="skip the power-of-two-scale (block-scaled MMA) line")
+    ap.add_argument("--hbm-kernels", action="store_true",
+                    help="time only the HBM-bound kernels on a profiling shape (T=16384) and print their line")
     ap.add_argument("--scales", default="fp32", choices=["fp32", "ue8m0"],
                     help="block scales of the timed layer: fp32 (the recipe) or power-of-two (block-scaled MMA)")
     ap.add_argument("--form", default="sorted", choices=["sorted", "gathered"],
@@ -552,6 +622,14 @@ def main():
               "l2": "inputs larger than L2 (FP8 expert weights streamed from HBM every step)",
               "form": args.form, "scales": args.scales}
     metric = "MoE-layer tokens/s (7168d/256e/top-8 FP8)" if cfg.name == "large" else f"MoE-layer tokens/s ({cfg.name})"
+
+    if args.hbm_kernels:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        print(json.dumps(run_hbm_kernels(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))), args.seed,
+                                         args.steps, args.warmup, _peaks())))
+        return
 
     if args.impl == "reference":
         if rank != 0:
