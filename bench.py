@@ -516,6 +516,52 @@ def run_hbm_kernels(dev, seed, steps, warmup, peaks):
             "peak_GB/s": peaks["hbm_gbs"], "kernels": res, "status": Lb.check_status(st)}
 
 
+def run_router_kernels(dev, seed, steps, warmup):
+    """The router kernels alone (no expert weights on the device): route_topk
+    on the large layer's shape (T=8192, d=7168, E=256, top-8, sigmoid) and
+    route_replay of one layer of the replay workload (T=16384, skewed
+    replayed ids, gates from the router logits)."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    res = {}
+    c = S.CONFIGS["large"]
+    x = S.make_x(c, dev, seed)
+    wr = S.make_router_w(c, dev, seed)
+    ids = torch.empty((c.T, c.k), dtype=torch.int32, device=dev)
+    g = torch.empty((c.T, c.k), dtype=torch.float32, device=dev)
+    t = timed(lambda: Lb.moe_route_topk(x, wr, c.k, c.score_fn, c.renorm, c.route_scale, topk_ids=ids, topk_gates=g))
+    res["route_topk"] = {"workload": f"T={c.T} d={c.d} E={c.E} top_k={c.k}", "ms": t,
+                         "fp32 TFLOP/s": 2.0 * c.T * c.d * c.E / (t * 1e-3) / 1e12}
+    del x
+    r = S.CONFIGS["multilayer_replay"]
+    x = S.make_x(r, dev, seed)
+    payload = S.make_replay_payload(r.with_(layers=1), dev, seed)[0]
+    ids = torch.empty((r.T, r.k), dtype=torch.int32, device=dev)
+    g = torch.empty((r.T, r.k), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    t = timed(lambda: Lb.moe_route_replay(payload, r.E, x, wr, r.score_fn, r.renorm, r.route_scale, topk_ids=ids,
+                                          topk_gates=g, dev_status=st))
+    res["route_replay"] = {"workload": f"T={r.T} d={r.d} E={r.E} top_k={r.k}", "ms": t,
+                           "fp32 TFLOP/s": 2.0 * r.T * r.d * r.k / (t * 1e-3) / 1e12,
+                           "W_r row bytes read from L2 per launch": r.T * r.k * r.d * 2}
+    return {"kernels": res, "status": Lb.check_status(st)}
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 class OracleSample:
@@ -602,6 +648,8 @@ def main():
     ap.add_argument("--no-dispatch-combine", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
     ap.add_argument("--no-mx", action="store_true", help="skip the power-of-two-scale (block-scaled MMA) line")
+    ap.add_argument("--router-kernels", action="store_true",
+                    help="time only the router kernels (route_topk, route_replay) and print their line")
     ap.add_argument("--hbm-kernels", action="store_true",
                     help="time only the HBM-bound kernels on a profiling shape (T=16384) and print their line")
     ap.add_argument("--scales", default="fp32", choices=["fp32", "ue8m0"],
@@ -622,6 +670,14 @@ def main():
               "l2": "inputs larger than L2 (FP8 expert weights streamed from HBM every step)",
               "form": args.form, "scales": args.scales}
     metric = "MoE-layer tokens/s (7168d/256e/top-8 FP8)" if cfg.name == "large" else f"MoE-layer tokens/s ({cfg.name})"
+
+    if args.router_kernels:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        print(json.dumps(run_router_kernels(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))), args.seed,
+                                            args.steps, args.warmup)))
+        return
 
     if args.hbm_kernels:
         import torch
