@@ -227,12 +227,20 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
         }
         __syncthreads();
         if (k0 + RC_BK < d) load_tile(k0 + RC_BK);
+        // operands of hidden index i+1 are loaded while the fmas of i run
+        float4 nx0 = *reinterpret_cast<const float4 *>(&xs[tt]);
+        float4 nx1 = *reinterpret_cast<const float4 *>(&xs[tt + 4]);
+        float4 nw0 = *reinterpret_cast<const float4 *>(&ws[ee]);
+        float4 nw1 = *reinterpret_cast<const float4 *>(&ws[ee + 4]);
 #pragma unroll
         for (int i = 0; i < RC_BK; i++) {
-            const float4 x0 = *reinterpret_cast<const float4 *>(&xs[i * RC_BT + tt]);
-            const float4 x1 = *reinterpret_cast<const float4 *>(&xs[i * RC_BT + tt + 4]);
-            const float4 w0 = *reinterpret_cast<const float4 *>(&ws[i * RC_EC + ee]);
-            const float4 w1 = *reinterpret_cast<const float4 *>(&ws[i * RC_EC + ee + 4]);
+            const float4 x0 = nx0, x1 = nx1, w0 = nw0, w1 = nw1;
+            if (i + 1 < RC_BK) {
+                nx0 = *reinterpret_cast<const float4 *>(&xs[(i + 1) * RC_BT + tt]);
+                nx1 = *reinterpret_cast<const float4 *>(&xs[(i + 1) * RC_BT + tt + 4]);
+                nw0 = *reinterpret_cast<const float4 *>(&ws[(i + 1) * RC_EC + ee]);
+                nw1 = *reinterpret_cast<const float4 *>(&ws[(i + 1) * RC_EC + ee + 4]);
+            }
             const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
