@@ -153,6 +153,10 @@ constexpr int RC_BT = 64;           // tokens per cluster
 constexpr int RC_EC = 128;          // experts per CTA
 constexpr int RC_BK = 32;           // hidden indices per shared-memory tile
 constexpr int RC_LGS = RC_EC + 4;   // logits row stride (floats)
+// shared floats before the candidate arrays: the double-buffered tiles, or
+// the logits that replace them after the last tile, whichever is larger
+constexpr int RC_TILE_FLOATS = (2 * RC_BK * (RC_BT + RC_EC) > RC_BT * RC_LGS) ? 2 * RC_BK * (RC_BT + RC_EC)
+                                                                              : RC_BT * RC_LGS;
 
 // One cluster of ceil(E/128) CTAs per 64 tokens.  CTA r computes the logits
 // of experts 128r .. 128r+127 for the 64 tokens (128 threads, 8 tokens x 8
@@ -173,10 +177,13 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
     extern __shared__ float4 smem4[];
     const int ncta = (int)cl_size();
     const int rank = (int)cl_rank();
-    float *xs = reinterpret_cast<float *>(smem4);   // [RC_BK][RC_BT]
-    float *ws = xs + RC_BK * RC_BT;                  // [RC_BK][RC_EC]
-    float *lg = ws + RC_BK * RC_EC;                  // [RC_BT][RC_LGS]
-    float2 *cand = reinterpret_cast<float2 *>(lg + RC_BT * RC_LGS);  // CTA 0: [RC_BT][ncta*k]
+    // two [RC_BK][RC_BT] x tiles and two [RC_BK][RC_EC] W_r tiles (one is
+    // filled while the other is read); the logits [RC_BT][RC_LGS] reuse the
+    // same space after the last tile
+    float *xs2 = reinterpret_cast<float *>(smem4);
+    float *ws2 = xs2 + 2 * RC_BK * RC_BT;
+    float *lg = xs2;
+    float2 *cand = reinterpret_cast<float2 *>(xs2 + RC_TILE_FLOATS);  // CTA 0: [RC_BT][ncta*k]
     float2 *msum = cand + RC_BT * ncta * k;                           // CTA 0: [RC_BT][ncta]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -208,8 +215,9 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
                           : make_uint4(0, 0, 0, 0);
     };
     load_tile(0);
-    for (int k0 = 0; k0 < d; k0 += RC_BK) {
-        __syncthreads();
+    for (int k0 = 0, buf = 0; k0 < d; k0 += RC_BK, buf ^= 1) {
+        float *xs = xs2 + buf * RC_BK * RC_BT;
+        float *ws = ws2 + buf * RC_BK * RC_EC;
         {
             float f[8];
 #pragma unroll
@@ -225,6 +233,8 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
                 for (int j = 0; j < 8; j++) ws[(r * 8 + j) * RC_EC + tid] = f[j];
             }
         }
+        // one barrier per tile: it publishes this tile and, since every
+        // thread has passed it, the tile read two steps ago is free
         __syncthreads();
         if (k0 + RC_BK < d) load_tile(k0 + RC_BK);
         // operands of hidden index i+1 are loaded while the fmas of i run
@@ -249,6 +259,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
                 for (int b = 0; b < 8; b++) acc[a][b] = fmaf(xa[a], wb[b], acc[a][b]);
         }
     }
+    __syncthreads();  // the logits overwrite the tiles
 #pragma unroll
     for (int a = 0; a < 8; a++) {
         *reinterpret_cast<float4 *>(&lg[(tt + a) * RC_LGS + ee]) =
@@ -459,7 +470,7 @@ MOE_API moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, i
     if (!x || !w_router || !topk_ids || !topk_gates) return MOE_ERR_NULL;
     if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_ALIGN;
     const int ncta = (E + RC_EC - 1) / RC_EC;  // <= 8: a portable cluster size
-    const size_t smem = sizeof(float) * (RC_BK * RC_BT + RC_BK * RC_EC + (size_t)RC_BT * RC_LGS) +
+    const size_t smem = sizeof(float) * (size_t)RC_TILE_FLOATS +
                         sizeof(float2) * ((size_t)RC_BT * ncta * k + (size_t)RC_BT * ncta);
     if (cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
