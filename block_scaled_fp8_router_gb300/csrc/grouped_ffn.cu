@@ -32,6 +32,11 @@
 //          output columns, stored as bf16.
 // Every mbarrier wait is bounded; on expiry the CTA flags MOE_DEV_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
+//
+// Also in this file: the gathered form of the same kernel (GATHER: GEMM1's
+// A rows fetched from the token-major codes by tile::gather4, GEMM2's rows
+// stored in slot order) and grouped_gemm_mx_kernel, the power-of-two-scale
+// variant on the hardware block-scaled MMA (described above it).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -9,13 +9,14 @@
 // index, computed by one thread (a SIMT register-tiled GEMM, not the tensor
 // cores, whose accumulation order is not specified).
 //
-// route_topk_kernel: one cluster of ceil(E/128) CTAs per 32 tokens; each
-// 128-thread CTA computes 32 tokens x 128 experts with 4 x 8 fp32
-// accumulators per thread (3 shared-memory wavefronts per 32 FMAs per warp),
-// bf16 tiles of x and W_r (32 deep) widened to fp32 in shared memory with
-// conflict-free stores while the next tile loads into registers.  Logits stay
-// on chip: each CTA selects its own top-k, CTA 0 merges the candidates it
-// receives through distributed shared memory.
+// route_topk_kernel: one cluster of ceil(E/128) CTAs per 64 tokens; each
+// 128-thread CTA computes 64 tokens x 128 experts with 8 x 8 fp32
+// accumulators per thread (four 16-byte shared loads per 64 FMAs, the next
+// hidden index's operands loaded while the current FMAs run), bf16 tiles of
+// x and W_r (32 deep) widened to fp32 in double-buffered shared memory with
+// conflict-free stores while the next tile loads into registers (one
+// barrier per tile).  Logits stay on chip: each CTA selects its own top-k,
+// CTA 0 merges the candidates it receives through distributed shared memory.
 #include "common.cuh"
 
 namespace moe {
