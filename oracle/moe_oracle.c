@@ -582,6 +582,165 @@ void or_combine(const uint16_t *out_sorted, const int32_t *slot_to_sorted, const
 }
 
 /* Number of OpenMP threads the parallel loops above use (1 without OpenMP). */
+/* ------------------------------------------------------------------ */
+/* backward of the expert path under replay (the trainer replays routing */
+/* to train; "Router replay", "FP8 training")                           */
+/* ------------------------------------------------------------------ */
+
+/* Combine backward.  y[t] = sum_j g[t,j] * out[r(t,j)], so for a routed slot
+ * the expert output's gradient is d_out[r] = g[t,j] * dy[t] (one binary32
+ * product per element) and the gate's gradient is d_g[t,j] = <dy[t], out[r]>
+ * (computed in double, rounded once); an unrouted slot gets d_g = 0.  d_out
+ * is then quantised 1 x 128 along d by the recipe's rule (fp32 scale
+ * amax/448, IEEE division) for the dgrad GEMM.  d_out_f (nullable) [A, d]
+ * receives the fp32 values before quantisation. */
+void or_combine_backward(const uint16_t *dy, const float *gates, const uint16_t *out_sorted,
+                         const int32_t *slot_to_sorted, int64_t T, int k, int d, int64_t A,
+                         float *d_out_f, uint8_t *d_out_q, float *d_out_s, float *d_gates)
+{
+    int64_t nb = d / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++) {
+        for (int j = 0; j < k; j++) {
+            int32_t r = slot_to_sorted[t * k + j];
+            if (r < 0 || r >= A) {
+                d_gates[t * k + j] = 0.0f;
+                continue;
+            }
+            float g = gates[t * k + j];
+            double dot = 0.0;
+            for (int c = 0; c < d; c++)
+                dot += (double)or_bf16_to_f32(dy[t * d + c]) * (double)or_bf16_to_f32(out_sorted[(int64_t)r * d + c]);
+            d_gates[t * k + j] = (float)dot;
+            for (int64_t b = 0; b < nb; b++) {
+                float v[128], amax = 0.0f;
+                for (int i = 0; i < 128; i++) {
+                    v[i] = g * or_bf16_to_f32(dy[t * d + b * 128 + i]);
+                    if (fabsf(v[i]) > amax)
+                        amax = fabsf(v[i]);
+                }
+                float sc = block_scale(amax);
+                d_out_s[(int64_t)r * nb + b] = sc;
+                for (int i = 0; i < 128; i++) {
+                    d_out_q[(int64_t)r * d + b * 128 + i] = or_e4m3_encode(v[i] / sc);
+                    if (d_out_f)
+                        d_out_f[(int64_t)r * d + b * 128 + i] = v[i];
+                }
+            }
+        }
+    }
+}
+
+/* Transposed copy of block-quantised weights: q [E, R, C] codes with scales
+ * [E, R/128, C/128] -> qt [E, C, R], st [E, C/128, R/128].  Block
+ * quantisation commutes with transposition, so this is the quantisation of
+ * the transposed weights (the operand layout of the dgrad GEMMs). */
+void or_weight_transpose(const uint8_t *q, const float *s, int64_t E, int64_t R, int64_t C, uint8_t *qt, float *st)
+{
+    for (int64_t e = 0; e < E; e++) {
+        for (int64_t r = 0; r < R; r++)
+            for (int64_t c = 0; c < C; c++)
+                qt[e * R * C + c * R + r] = q[e * R * C + r * C + c];
+        int64_t br = R / 128, bc = C / 128;
+        for (int64_t i = 0; i < br; i++)
+            for (int64_t j = 0; j < bc; j++)
+                st[e * br * bc + j * br + i] = s[e * br * bc + i * bc + j];
+    }
+}
+
+/* The forward's GEMM1 pre-activations h = [gate | up] [n, 2F] (fp32, the
+ * promotion of fp8_row_gemm), saved by the forward for the backward. */
+void or_expert_ffn_preact(const uint8_t *xq, const float *xs, int64_t n, const int32_t *row_expert, int d, int F,
+                          const uint8_t *w13_q, const float *w13_s, float *h)
+{
+    double dec[256];
+    for (int c = 0; c < 256; c++)
+        dec[c] = or_e4m3_decode((uint8_t)c);
+    int64_t nkd = d / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; r++) {
+        int64_t e = row_expert[r];
+        fp8_row_gemm(xq + r * d, xs + r * nkd, w13_q + e * 2 * F * (int64_t)d, w13_s + e * (2 * F / 128) * nkd,
+                     2 * F, d, dec, h + r * 2 * F);
+    }
+}
+
+/* Grouped block-scaled GEMM with bf16 output: out[r, :] = bf16(fp8_row_gemm(
+ * a[r], sa[r], b[row_expert[r]])) with b [E, N, K] codes, sb [E, N/128, K/128].
+ * The forward's GEMM2 is (K, N) = (F, d) with W2; the dgrad GEMMs are
+ * (d, F) with W2 transposed and (2F, d) with W13 transposed. */
+void or_grouped_gemm(const uint8_t *a, const float *sa, int64_t n, const int32_t *row_expert, int64_t K, int64_t N,
+                     const uint8_t *b, const float *sb, uint16_t *out)
+{
+    double dec[256];
+    for (int c = 0; c < 256; c++)
+        dec[c] = or_e4m3_decode((uint8_t)c);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; r++) {
+        int64_t e = row_expert[r];
+        float *o = malloc(sizeof(float) * (size_t)N);
+        fp8_row_gemm(a + r * K, sa + r * (K / 128), b + e * N * K, sb + e * (N / 128) * (K / 128), N, K, dec, o);
+        for (int64_t c = 0; c < N; c++)
+            out[r * N + c] = or_f32_to_bf16(o[c]);
+        free(o);
+    }
+}
+
+/* SwiGLU backward: act = silu(g) * u with silu(g) = g * sigma(g), so
+ *   d_g = d_act * u * sigma(g) * (1 + g * (1 - sigma(g))),   d_u = d_act * silu(g)
+ * in double from the bf16 d_act and the saved fp32 h = [g | u], rounded to
+ * fp32 (dh_f, nullable), then quantised 1 x 128 along 2F by the recipe's
+ * rule: dh_q [n, 2F], dh_s [n, 2F/128]. */
+void or_swiglu_backward(const uint16_t *d_act, const float *h, int64_t n, int F, float *dh_f, uint8_t *dh_q,
+                        float *dh_s)
+{
+    int64_t nb = 2 * (int64_t)F / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; r++) {
+        float *dh = malloc(sizeof(float) * 2 * (size_t)F);
+        for (int64_t c = 0; c < F; c++) {
+            double da = or_bf16_to_f32(d_act[r * F + c]);
+            double g = h[r * 2 * F + c], u = h[r * 2 * F + F + c];
+            double sg = 1.0 / (1.0 + exp(-g));
+            dh[c] = (float)(da * u * sg * (1.0 + g * (1.0 - sg)));
+            dh[F + c] = (float)(da * g * sg);
+        }
+        for (int64_t b = 0; b < nb; b++) {
+            float amax = 0.0f;
+            for (int i = 0; i < 128; i++)
+                if (fabsf(dh[b * 128 + i]) > amax)
+                    amax = fabsf(dh[b * 128 + i]);
+            float sc = block_scale(amax);
+            dh_s[r * nb + b] = sc;
+            for (int i = 0; i < 128; i++)
+                dh_q[r * 2 * F + b * 128 + i] = or_e4m3_encode(dh[b * 128 + i] / sc);
+        }
+        if (dh_f)
+            memcpy(dh_f + r * 2 * F, dh, sizeof(float) * 2 * (size_t)F);
+        free(dh);
+    }
+}
+
+/* Dispatch backward: the input rows' gradient is the sum of their sorted
+ * copies' gradients, dx[t] = bf16( sum_j dx_sorted[r(t,j)] ), a binary32
+ * chain over j in slot order from +0 (unrouted slots skipped). */
+void or_dispatch_backward(const uint16_t *dx_sorted, const int32_t *slot_to_sorted, int64_t T, int k, int d,
+                          uint16_t *dx)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++)
+        for (int c = 0; c < d; c++) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; j++) {
+                int32_t r = slot_to_sorted[t * k + j];
+                if (r < 0)
+                    continue;
+                acc = acc + or_bf16_to_f32(dx_sorted[(int64_t)r * d + c]);
+            }
+            dx[t * d + c] = or_f32_to_bf16(acc);
+        }
+}
+
 #ifdef _OPENMP
 #include <omp.h>
 int or_num_threads(void) { return omp_get_max_threads(); }

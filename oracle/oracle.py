@@ -62,6 +62,12 @@ def _load():
                 "or_gates": (None, [P, P, P, I64, I, I, I, I, F, P]),
                 "or_replay": (I64, [P, I64, I, I, P, P]),
                 "or_payload_pack_u8": (I64, [P, I64, I, P]),
+                "or_combine_backward": (None, [P, P, P, P, I64, I, I, I64, P, P, P, P]),
+                "or_weight_transpose": (None, [P, P, I64, I64, I64, P, P]),
+                "or_expert_ffn_preact": (None, [P, P, I64, P, I, I, P, P, P]),
+                "or_grouped_gemm": (None, [P, P, I64, P, I64, I64, P, P, P]),
+                "or_swiglu_backward": (None, [P, P, I64, I, P, P, P]),
+                "or_dispatch_backward": (None, [P, P, I64, I, I, P]),
                 "or_payload_unpack_u8": (None, [P, I64, P]),
                 "or_dispatch": (I64, [P, I64, I, I, P, P, P, P]),
                 "or_gather_rows": (None, [P, I64, P, I64, I, P]),
@@ -217,6 +223,85 @@ def payload_unpack_u8(p: np.ndarray) -> np.ndarray:
     out = np.empty(a.shape, np.int32)
     _load().or_payload_unpack_u8(_p(a), a.size, _p(out))
     return out
+
+
+def combine_backward(dy_bf16: np.ndarray, gates: np.ndarray, out_sorted_bf16: np.ndarray, slot_to_sorted: np.ndarray):
+    """Gradients of y = sum_j g * out: (d_out_f [A,d] f32, d_out_q [A,d], d_out_s [A,d/128], d_gates [T,k])."""
+    dy = _c(dy_bf16, np.uint16)
+    g = _c(gates, np.float32)
+    out = _c(out_sorted_bf16, np.uint16)
+    sl2 = _c(slot_to_sorted, np.int32)
+    T, d = dy.shape
+    k = g.shape[1]
+    A = out.shape[0]
+    d_out_f = np.zeros((A, d), np.float32)
+    d_out_q = np.zeros((A, d), np.uint8)
+    d_out_s = np.ones((A, d // 128), np.float32)
+    d_g = np.empty((T, k), np.float32)
+    _load().or_combine_backward(_p(dy), _p(g), _p(out), _p(sl2), T, k, d, A, _p(d_out_f), _p(d_out_q), _p(d_out_s),
+                                _p(d_g))
+    return d_out_f, d_out_q, d_out_s, d_g
+
+
+def weight_transpose(q: np.ndarray, s: np.ndarray):
+    """[E, R, C] codes + [E, R/128, C/128] scales -> the transposed pair."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    E, R, C = q.shape
+    qt = np.empty((E, C, R), np.uint8)
+    st = np.empty((E, C // 128, R // 128), np.float32)
+    _load().or_weight_transpose(_p(q), _p(s), E, R, C, _p(qt), _p(st))
+    return qt, st
+
+
+def expert_ffn_preact(xq: np.ndarray, xs: np.ndarray, row_expert: np.ndarray, w13_q: np.ndarray, w13_s: np.ndarray):
+    """GEMM1 pre-activations h = [gate | up] [n, 2F] fp32."""
+    xq = _c(xq, np.uint8)
+    xs = _c(xs, np.float32)
+    re = _c(row_expert, np.int32)
+    w13_q = _c(w13_q, np.uint8)
+    w13_s = _c(w13_s, np.float32)
+    n, d = xq.shape
+    F = w13_q.shape[1] // 2
+    h = np.empty((n, 2 * F), np.float32)
+    _load().or_expert_ffn_preact(_p(xq), _p(xs), n, _p(re), d, F, _p(w13_q), _p(w13_s), _p(h))
+    return h
+
+
+def grouped_gemm(a_q: np.ndarray, a_s: np.ndarray, row_expert: np.ndarray, b_q: np.ndarray, b_s: np.ndarray):
+    """out [n, N] bf16 bits = a (rows of expert row_expert[r]) x b[e]^T, b [E, N, K], block-scaled."""
+    a_q = _c(a_q, np.uint8)
+    a_s = _c(a_s, np.float32)
+    re = _c(row_expert, np.int32)
+    b_q = _c(b_q, np.uint8)
+    b_s = _c(b_s, np.float32)
+    n, K = a_q.shape
+    N = b_q.shape[1]
+    out = np.empty((n, N), np.uint16)
+    _load().or_grouped_gemm(_p(a_q), _p(a_s), n, _p(re), K, N, _p(b_q), _p(b_s), _p(out))
+    return out
+
+
+def swiglu_backward(d_act_bf16: np.ndarray, h: np.ndarray):
+    """(dh_f [n, 2F] f32, dh_q [n, 2F], dh_s [n, 2F/128]) from the bf16 d_act [n, F] and saved h [n, 2F]."""
+    da = _c(d_act_bf16, np.uint16)
+    h = _c(h, np.float32)
+    n, F = da.shape
+    dh_f = np.empty((n, 2 * F), np.float32)
+    dh_q = np.empty((n, 2 * F), np.uint8)
+    dh_s = np.empty((n, 2 * F // 128), np.float32)
+    _load().or_swiglu_backward(_p(da), _p(h), n, F, _p(dh_f), _p(dh_q), _p(dh_s))
+    return dh_f, dh_q, dh_s
+
+
+def dispatch_backward(dx_sorted_bf16: np.ndarray, slot_to_sorted: np.ndarray, T: int, k: int):
+    """dx [T, d] bf16 bits = per token the sum of its routed rows' gradients."""
+    dxs = _c(dx_sorted_bf16, np.uint16)
+    sl2 = _c(slot_to_sorted, np.int32)
+    d = dxs.shape[1]
+    dx = np.empty((T, d), np.uint16)
+    _load().or_dispatch_backward(_p(dxs), _p(sl2), T, k, d, _p(dx))
+    return dx
 
 
 def dispatch(ids: np.ndarray, E: int):
