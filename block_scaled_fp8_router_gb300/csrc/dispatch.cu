@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     for (int64_t t = gw; t < T; t += nw) {
         int32_t my_src = lane < k ? __ldg(slot_to_sorted + t * k + lane) : -1;
         if (SLOTS && my_src >= 0) my_src = (int32_t)(t * k + lane);
-        const float my_g = lane < k ? __ldg(gates + t * k + lane) : 0.0f;
+        const float my_g = lane < k ? (gates ? __ldg(gates + t * k + lane) : 1.0f) : 0.0f;  // no gates: unit
         for (int v0 = 0; v0 < nvec; v0 += 64) {
             float acc[2][8];
 #pragma unroll
@@ -362,6 +362,22 @@ MOE_API moe_status moe_combine(const uint16_t *out_sorted, const int32_t *slot_t
     const int64_t cap = (int64_t)sm_count() * 8;
     if (grid > cap) grid = cap;
     combine_kernel<false><<<(unsigned)grid, 256, 0, as_stream(stream)>>>(out_sorted, slot_to_sorted, gates, T, k, d, y);
+    return launch_status();
+}
+
+MOE_API moe_status moe_dispatch_backward(const uint16_t *dx_sorted, const int32_t *slot_to_sorted, int T, int k,
+                                         int d, uint16_t *dx, void *stream)
+{
+    if (T < 0 || k < 1 || k > 32 || d <= 0 || d % 8 != 0) return MOE_ERR_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!dx_sorted || !slot_to_sorted || !dx) return MOE_ERR_NULL;
+    if (!aligned16(dx_sorted) || !aligned16(dx)) return MOE_ERR_ALIGN;
+    int64_t grid = ((int64_t)T + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (grid > cap) grid = cap;
+    // the combine with unit gates: fma(1, v, acc) is the binary32 sum in slot order
+    combine_kernel<false><<<(unsigned)grid, 256, 0, as_stream(stream)>>>(dx_sorted, slot_to_sorted, nullptr, T, k, d,
+                                                                         dx);
     return launch_status();
 }
 

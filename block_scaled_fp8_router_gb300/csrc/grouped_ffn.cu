@@ -84,6 +84,7 @@ struct Params {
     uint16_t *out;              // GEMM2 out [max_rows, d] bf16
     int32_t *dev_status;
     const int32_t *sorted_to_slot;  // gathered form: sorted row -> slot t*top_k + j
+    float *h_out;                   // GEMM1, nullable: pre-activations [max_rows, 2F] for the backward
     int64_t max_rows;
     int E, d, F;
     int top_k;
@@ -494,6 +495,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (MODE == 1) {
+                if (p.h_out != nullptr && row_ok && !aborted) {
+                    // the pre-activations, kept for the backward: gate then up columns
+                    float4 *hg = reinterpret_cast<float4 *>(p.h_out + row * 2 * p.F + tl.n_blk * 128 + 32 * cg);
+                    float4 *hu = reinterpret_cast<float4 *>(p.h_out + row * 2 * p.F + p.F + tl.n_blk * 128 + 32 * cg);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        hg[i] = make_float4(acc0[4 * i], acc0[4 * i + 1], acc0[4 * i + 2], acc0[4 * i + 3]);
+                        hu[i] = make_float4(acc1[4 * i], acc1[4 * i + 1], acc1[4 * i + 2], acc1[4 * i + 3]);
+                    }
+                }
                 // act = silu(gate) * up for 32 of the tile's 128 act columns
                 float amax = 0.0f;
 #pragma unroll
@@ -941,7 +952,7 @@ static moe_status ffn_launch(const uint8_t *xq, int64_t x_rows, const float *xs,
                              int top_k, const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
                              const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q, const float *w2_s,
                              uint16_t *out, void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                             void *stream)
+                             void *stream, float *h_out = nullptr)
 {
     if (max_rows < 0 || max_rows >= (1LL << 31) || E < 1 || E > MAX_E || d <= 0 || F <= 0 || d % 128 != 0 ||
         F % 128 != 0)
@@ -971,6 +982,7 @@ static moe_status ffn_launch(const uint8_t *xq, int64_t x_rows, const float *xs,
     prm.out = out;
     prm.dev_status = dev_status;
     prm.sorted_to_slot = sorted_to_slot;
+    prm.h_out = nullptr;
     prm.max_rows = max_rows;
     prm.E = E;
     prm.d = d;
@@ -986,6 +998,7 @@ static moe_status ffn_launch(const uint8_t *xq, int64_t x_rows, const float *xs,
     Params p1 = prm;
     p1.a_scales = xs;
     p1.b_scales = w13_s;
+    p1.h_out = h_out;
     grouped_gemm_kernel<1, GATHER><<<grid, THREADS, SMEM_BYTES, st>>>(ma1, mb1, p1);
     Params p2 = prm;
     p2.a_scales = act_s;
@@ -1005,6 +1018,56 @@ MOE_API moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs
 {
     return ffn_launch<false>(xq_sorted, max_rows, xs_sorted, nullptr, 1, expert_offsets, max_rows, E, d, F, w13_q,
                              w13_s, w2_q, w2_s, out_sorted, workspace, workspace_bytes, dev_status, stream);
+}
+
+MOE_API moe_status moe_grouped_ffn_fp8_train(const uint8_t *xq_sorted, const float *xs_sorted,
+                                             const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                                             const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q,
+                                             const float *w2_s, uint16_t *out_sorted, float *h_out, void *workspace,
+                                             size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    if (!h_out) return MOE_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(h_out) & 15) return MOE_ERR_ALIGN;
+    return ffn_launch<false>(xq_sorted, max_rows, xs_sorted, nullptr, 1, expert_offsets, max_rows, E, d, F, w13_q,
+                             w13_s, w2_q, w2_s, out_sorted, workspace, workspace_bytes, dev_status, stream, h_out);
+}
+
+MOE_API moe_status moe_grouped_gemm_fp8(const uint8_t *a_q, const float *a_s, const int32_t *expert_offsets,
+                                        int64_t max_rows, int E, int K, int N, const uint8_t *b_q, const float *b_s,
+                                        uint16_t *out, int32_t *dev_status, void *stream)
+{
+    if (max_rows < 0 || max_rows >= (1LL << 31) || E < 1 || E > MAX_E || K <= 0 || N <= 0 || K % 128 != 0 ||
+        N % 128 != 0 || (int64_t)E * N >= (1LL << 31))
+        return MOE_ERR_SHAPE;
+    if (max_rows == 0) return MOE_OK;
+    if (!a_q || !a_s || !expert_offsets || !b_q || !b_s || !out) return MOE_ERR_NULL;
+    if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(out)) return MOE_ERR_ALIGN;
+    auto enc = encode_fn();
+    if (!enc) return MOE_ERR_CUDA;
+    CUtensorMap ma, mb;
+    if (!make_map(enc, &ma, a_q, K, max_rows, 128) || !make_map(enc, &mb, b_q, K, (uint64_t)E * N, 256))
+        return MOE_ERR_CUDA;
+    // the GEMM2 form of the kernel with (K, N) in place of (F, d)
+    Params prm;
+    prm.a_scales = a_s;
+    prm.b_scales = b_s;
+    prm.offsets = expert_offsets;
+    prm.act_q = nullptr;
+    prm.act_s = nullptr;
+    prm.out = out;
+    prm.dev_status = dev_status;
+    prm.sorted_to_slot = nullptr;
+    prm.h_out = nullptr;
+    prm.max_rows = max_rows;
+    prm.E = E;
+    prm.d = N;
+    prm.F = K;
+    prm.top_k = 1;
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    grouped_gemm_kernel<2, false><<<sm_count(), THREADS, SMEM_BYTES, as_stream(stream)>>>(ma, mb, prm);
+    return launch_status();
 }
 
 MOE_API moe_status moe_grouped_ffn_fp8_gathered(const uint8_t *xq, const float *xs, int T, int k,

@@ -33,6 +33,15 @@ class MoEWeightsFP8:
     def E(self) -> int:
         return self.w13_q.shape[0]
 
+    def transposed(self):
+        """(w2t_q [E, F, d], w2t_s, w13t_q [E, d, 2F], w13t_s): the dgrad GEMMs'
+        operands, made once per weight update and cached."""
+        if getattr(self, "_t", None) is None:
+            w2t = L.fp8_weight_transpose(self.w2_q, self.w2_s)
+            w13t = L.fp8_weight_transpose(self.w13_q, self.w13_s)
+            self._t = (*w2t, *w13t)
+        return self._t
+
     @property
     def d(self) -> int:
         return self.w13_q.shape[2]
@@ -124,7 +133,9 @@ class MoELayerFP8:
         return ids, gates
 
     def forward(self, x: torch.Tensor, replay_kT: torch.Tensor | None = None,
-                capture_kT: torch.Tensor | None = None, y: torch.Tensor | None = None) -> torch.Tensor:
+                capture_kT: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                train: bool = False) -> torch.Tensor:
+        """train=True also keeps GEMM1's pre-activations for backward()."""
         T = x.shape[0]
         if T > self.T_max:
             raise ValueError(f"T={T} exceeds T_max={self.T_max}")
@@ -153,10 +164,49 @@ class MoELayerFP8:
                        expert_offsets=self.offsets, sorted_to_slot=self.s2s[:A], slot_to_sorted=self.sl2[:A],
                        rows_sorted=self.xq_sorted[:A], scales_sorted=self.xs_sorted[:A], workspace=self.dsp_ws,
                        dev_status=self.dev_status)
-        L.moe_grouped_ffn_fp8(self.xq_sorted[:A], self.xs_sorted[:A], self.offsets, self.w.w13_q, self.w.w13_s,
-                              self.w.w2_q, self.w.w2_s, out_sorted=self.out_sorted[:A], workspace=self.ffn_ws,
-                              dev_status=self.dev_status)
+        if train:
+            if getattr(self, "h", None) is None or self.h.shape[0] < A:
+                self.h = torch.empty((self.T_max * self.k, 2 * self.w.F), dtype=torch.float32, device=x.device)
+            L.moe_grouped_ffn_fp8_train(self.xq_sorted[:A], self.xs_sorted[:A], self.offsets, self.w.w13_q,
+                                        self.w.w13_s, self.w.w2_q, self.w.w2_s, self.h[:A],
+                                        out_sorted=self.out_sorted[:A], workspace=self.ffn_ws,
+                                        dev_status=self.dev_status)
+            self._T_train = T
+        else:
+            L.moe_grouped_ffn_fp8(self.xq_sorted[:A], self.xs_sorted[:A], self.offsets, self.w.w13_q, self.w.w13_s,
+                                  self.w.w2_q, self.w.w2_s, out_sorted=self.out_sorted[:A], workspace=self.ffn_ws,
+                                  dev_status=self.dev_status)
         return L.moe_combine(self.out_sorted[:A], self.sl2[:A], gates, y=y)
+
+    def backward(self, dy: torch.Tensor):
+        """Backward of the expert path of the last forward(train=True) with its
+        routing fixed (replayed): returns (dx [T, d] bf16 from the experts,
+        d_gates [T, k] fp32).  Weight gradients and the router's backward are
+        not computed."""
+        T = getattr(self, "_T_train", None)
+        if T is None or self.mx or self.gathered:
+            raise ValueError("backward needs a forward(train=True) of the fp32-scale sorted form")
+        A = T * self.k
+        E, d, F = self.w.E, self.w.d, self.w.F
+        dev = dy.device
+        if getattr(self, "_bw", None) is None:
+            e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+            Am = self.T_max * self.k
+            self._bw = dict(d_out_q=e((Am, d), torch.uint8), d_out_s=e((Am, d // 128), torch.float32),
+                            d_gates=e((self.T_max, self.k), torch.float32), d_act=e((Am, F), torch.bfloat16),
+                            dh_q=e((Am, 2 * F), torch.uint8), dh_s=e((Am, 2 * F // 128), torch.float32),
+                            dx_sorted=e((Am, d), torch.bfloat16), dx=e((self.T_max, d), torch.bfloat16))
+        b = self._bw
+        w2t_q, w2t_s, w13t_q, w13t_s = self.w.transposed()
+        L.moe_combine_backward(dy, self.gates[:T], self.out_sorted[:A], self.sl2[:A], d_out_q=b["d_out_q"][:A],
+                               d_out_s=b["d_out_s"][:A], d_gates=b["d_gates"][:T])
+        L.moe_grouped_gemm_fp8(b["d_out_q"][:A], b["d_out_s"][:A], self.offsets, w2t_q, w2t_s, out=b["d_act"][:A],
+                               dev_status=self.dev_status)
+        L.moe_swiglu_backward(b["d_act"][:A], self.h[:A], dh_q=b["dh_q"][:A], dh_s=b["dh_s"][:A])
+        L.moe_grouped_gemm_fp8(b["dh_q"][:A], b["dh_s"][:A], self.offsets, w13t_q, w13t_s, out=b["dx_sorted"][:A],
+                               dev_status=self.dev_status)
+        dx = L.moe_dispatch_backward(b["dx_sorted"][:A], self.sl2[:A], T, self.k, dx=b["dx"][:T])
+        return dx, b["d_gates"][:T]
 
 
 class HostStreamer:

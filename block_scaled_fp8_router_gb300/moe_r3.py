@@ -44,6 +44,12 @@ _SIGS = {
     "moe_grouped_ffn_fp8_gathered": (I, [P, P, I, I, P, P, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_combine_slots": (I, [P, P, P, I, I, I, P, P]),
     "moe_grouped_ffn_mx_workspace_size": (SZ, [I64, I, I]),
+    "moe_grouped_ffn_fp8_train": (I, [P, P, P, I64, I, I, I, P, P, P, P, P, P, P, SZ, P, P]),
+    "moe_grouped_gemm_fp8": (I, [P, P, P, I64, I, I, I, P, P, P, P, P]),
+    "fp8_weight_transpose": (I, [P, P, I64, I64, I64, P, P, P]),
+    "moe_combine_backward": (I, [P, P, P, P, I, I, I, I64, P, P, P, P]),
+    "moe_swiglu_backward": (I, [P, P, I64, I, P, P, P]),
+    "moe_dispatch_backward": (I, [P, P, I, I, I, P, P]),
     "moe_grouped_ffn_mx": (I, [P, P, P, I, I, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_debug_bounded_wait": (I, [I64, P, P]),
     "moe_device_sm_count": (I, []),
@@ -396,6 +402,106 @@ def moe_grouped_ffn_mx(xq_sorted, x_exp, sorted_to_slot, top_k, expert_offsets, 
         _ptr(w13_q), _ptr(w13_exp), _ptr(w2_q), _ptr(w2_exp), _ptr(out_sorted), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
     return out_sorted
+
+
+def moe_grouped_ffn_fp8_train(xq_sorted, xs_sorted, expert_offsets, w13_q, w13_s, w2_q, w2_s, h_out,
+                              out_sorted=None, workspace=None, dev_status=None, stream=None):
+    """moe_grouped_ffn_fp8 that also writes GEMM1's pre-activations h [max_rows, 2F] fp32."""
+    max_rows, d = xq_sorted.shape
+    E, twoF, _ = w13_q.shape
+    F = twoF // 2
+    _want(xq_sorted, torch.uint8, (max_rows, d), "xq_sorted")
+    _want(xs_sorted, torch.float32, (max_rows, d // 128), "xs_sorted")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(h_out, torch.float32, (max_rows, 2 * F), "h_out")
+    out_sorted = _empty((max_rows, d), torch.bfloat16, xq_sorted) if out_sorted is None else out_sorted
+    _want(out_sorted, torch.bfloat16, (max_rows, d), "out_sorted")
+    if workspace is None:
+        workspace = _empty((moe_grouped_ffn_workspace_size(max_rows, d, F),), torch.uint8, xq_sorted)
+    _check("moe_grouped_ffn_fp8_train", _lib.moe_grouped_ffn_fp8_train(
+        _ptr(xq_sorted), _ptr(xs_sorted), _ptr(expert_offsets), max_rows, E, d, F, _ptr(w13_q), _ptr(w13_s),
+        _ptr(w2_q), _ptr(w2_s), _ptr(out_sorted), _ptr(h_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+    return out_sorted
+
+
+def moe_grouped_gemm_fp8(a_q, a_s, expert_offsets, b_q, b_s, out=None, dev_status=None, stream=None):
+    """Grouped block-scaled FP8 GEMM, bf16 out [max_rows, N] = a [max_rows, K] x b[e]^T, b [E, N, K]."""
+    max_rows, K = a_q.shape
+    E, N, _ = b_q.shape
+    _want(a_q, torch.uint8, (max_rows, K), "a_q")
+    _want(a_s, torch.float32, (max_rows, K // 128), "a_s")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(b_q, torch.uint8, (E, N, K), "b_q")
+    _want(b_s, torch.float32, (E, N // 128, K // 128), "b_s")
+    out = _empty((max_rows, N), torch.bfloat16, a_q) if out is None else out
+    _want(out, torch.bfloat16, (max_rows, N), "out")
+    _check("moe_grouped_gemm_fp8", _lib.moe_grouped_gemm_fp8(
+        _ptr(a_q), _ptr(a_s), _ptr(expert_offsets), max_rows, E, K, N, _ptr(b_q), _ptr(b_s), _ptr(out),
+        _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def fp8_weight_transpose(q, s, qt=None, st=None, stream=None):
+    """[E, R, C] codes + [E, R/128, C/128] scales -> transposed [E, C, R] / [E, C/128, R/128]."""
+    E, R, C = q.shape
+    _want(q, torch.uint8, (E, R, C), "q")
+    _want(s, torch.float32, (E, R // 128, C // 128), "s")
+    qt = _empty((E, C, R), torch.uint8, q) if qt is None else qt
+    st = _empty((E, C // 128, R // 128), torch.float32, q) if st is None else st
+    _want(qt, torch.uint8, (E, C, R), "qt")
+    _want(st, torch.float32, (E, C // 128, R // 128), "st")
+    _check("fp8_weight_transpose", _lib.fp8_weight_transpose(_ptr(q), _ptr(s), E, R, C, _ptr(qt), _ptr(st),
+                                                             _stream(stream)))
+    return qt, st
+
+
+def moe_combine_backward(dy, gates, out_sorted, slot_to_sorted, d_out_q=None, d_out_s=None, d_gates=None,
+                         stream=None):
+    """-> (d_out_q [A, d] e4m3, d_out_s [A, d/128], d_gates [T, k])."""
+    T, k = gates.shape
+    A, d = out_sorted.shape
+    _want(dy, torch.bfloat16, (T, d), "dy")
+    _want(gates, torch.float32, (T, k), "gates")
+    _want(out_sorted, torch.bfloat16, (A, d), "out_sorted")
+    _want(slot_to_sorted, torch.int32, (T * k,), "slot_to_sorted")
+    d_out_q = _empty((A, d), torch.uint8, dy) if d_out_q is None else d_out_q
+    d_out_s = _empty((A, d // 128), torch.float32, dy) if d_out_s is None else d_out_s
+    d_gates = _empty((T, k), torch.float32, dy) if d_gates is None else d_gates
+    _want(d_out_q, torch.uint8, (A, d), "d_out_q")
+    _want(d_out_s, torch.float32, (A, d // 128), "d_out_s")
+    _want(d_gates, torch.float32, (T, k), "d_gates")
+    _check("moe_combine_backward", _lib.moe_combine_backward(
+        _ptr(dy), _ptr(gates), _ptr(out_sorted), _ptr(slot_to_sorted), T, k, d, A, _ptr(d_out_q), _ptr(d_out_s),
+        _ptr(d_gates), _stream(stream)))
+    return d_out_q, d_out_s, d_gates
+
+
+def moe_swiglu_backward(d_act, h, dh_q=None, dh_s=None, stream=None):
+    """bf16 d_act [rows, F], fp32 h [rows, 2F] -> (dh_q [rows, 2F] e4m3, dh_s [rows, 2F/128])."""
+    rows, F = d_act.shape
+    _want(d_act, torch.bfloat16, (rows, F), "d_act")
+    _want(h, torch.float32, (rows, 2 * F), "h")
+    dh_q = _empty((rows, 2 * F), torch.uint8, d_act) if dh_q is None else dh_q
+    dh_s = _empty((rows, 2 * F // 128), torch.float32, d_act) if dh_s is None else dh_s
+    _want(dh_q, torch.uint8, (rows, 2 * F), "dh_q")
+    _want(dh_s, torch.float32, (rows, 2 * F // 128), "dh_s")
+    _check("moe_swiglu_backward", _lib.moe_swiglu_backward(_ptr(d_act), _ptr(h), rows, F, _ptr(dh_q), _ptr(dh_s),
+                                                           _stream(stream)))
+    return dh_q, dh_s
+
+
+def moe_dispatch_backward(dx_sorted, slot_to_sorted, T, k, dx=None, stream=None):
+    """dx [T, d] bf16 = per token the sum of its routed rows' gradients."""
+    A, d = dx_sorted.shape
+    if dx_sorted.dtype != torch.bfloat16 or not dx_sorted.is_contiguous():
+        raise ValueError("dx_sorted: contiguous bf16")
+    _want(slot_to_sorted, torch.int32, (T * k,), "slot_to_sorted")
+    dx = _empty((T, d), torch.bfloat16, dx_sorted) if dx is None else dx
+    _want(dx, torch.bfloat16, (T, d), "dx")
+    _check("moe_dispatch_backward", _lib.moe_dispatch_backward(_ptr(dx_sorted), _ptr(slot_to_sorted), T, k, d,
+                                                               _ptr(dx), _stream(stream)))
+    return dx
 
 
 def moe_combine_slots(out_slots, slot_to_sorted, gates, y=None, stream=None):

@@ -310,6 +310,53 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
                               size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Backward of the expert path under replay ("Router replay": the trainer
+ * replays the captured routing and trains through the layer; "FP8 training":
+ * its GEMMs are block-scaled FP8).  With the ids fixed, given dy [T, d]:
+ *   moe_combine_backward   d_out[r] = g[t,j] * dy[t] (binary32 product),
+ *                          quantised 1x128 along d as fp8_block_quant, to the
+ *                          slot's sorted row r = slot_to_sorted[t*k+j];
+ *                          d_gates[t,j] = <dy[t], out_sorted[r]> (fp32
+ *                          accumulation), 0 for an unrouted slot.
+ *   moe_grouped_gemm_fp8   with W2 transposed: d_act = d_out W2 (bf16).
+ *   moe_swiglu_backward    from the saved pre-activations h = [g | u]:
+ *                          d_g = d_act * u * s(g) * (1 + g (1 - s(g))),
+ *                          d_u = d_act * g * s(g) (s the logistic sigmoid),
+ *                          quantised 1x128 along 2F.
+ *   moe_grouped_gemm_fp8   with W13 transposed: dx_sorted = dh W13 (bf16).
+ *   moe_dispatch_backward  dx[t] = bf16(sum_j dx_sorted[r(t,j)]), a binary32
+ *                          sum in slot order.
+ * moe_grouped_ffn_fp8_train is moe_grouped_ffn_fp8 that also writes h
+ * [max_rows, 2F] fp32 (GEMM1's promoted accumulators, gate columns then up
+ * columns).  fp8_weight_transpose turns [E, R, C] codes with [E, R/128,
+ * C/128] scales into [E, C, R] / [E, C/128, R/128] (block quantisation
+ * commutes with transposition), once per weight update.
+ * moe_grouped_gemm_fp8 is the block-scaled grouped GEMM with bf16 output:
+ * out[r, :] = bf16(a[r] b[e]^T) for the rows of expert e, a [max_rows, K]
+ * e4m3 with [max_rows, K/128] fp32 scales, b [E, N, K] with [E, N/128,
+ * K/128]; K, N multiples of 128 (the forward's GEMM2 is K = F, N = d).
+ * Weight gradients and the router's backward are not provided.
+ * Errors: NULL, SHAPE, ALIGN, CUDA (WORKSPACE for the _train call).
+ * ---------------------------------------------------------------------- */
+moe_status moe_grouped_ffn_fp8_train(const uint8_t *xq_sorted, const float *xs_sorted,
+                                     const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                                     const uint8_t *w13_q, const float *w13_s, const uint8_t *w2_q,
+                                     const float *w2_s, uint16_t *out_sorted, float *h_out, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_status, void *stream);
+moe_status moe_grouped_gemm_fp8(const uint8_t *a_q, const float *a_s, const int32_t *expert_offsets,
+                                int64_t max_rows, int E, int K, int N, const uint8_t *b_q, const float *b_s,
+                                uint16_t *out, int32_t *dev_status, void *stream);
+moe_status fp8_weight_transpose(const uint8_t *q, const float *s, int64_t E, int64_t R, int64_t C, uint8_t *qt,
+                                float *st, void *stream);
+moe_status moe_combine_backward(const uint16_t *dy, const float *gates, const uint16_t *out_sorted,
+                                const int32_t *slot_to_sorted, int T, int k, int d, int64_t A, uint8_t *d_out_q,
+                                float *d_out_s, float *d_gates, void *stream);
+moe_status moe_swiglu_backward(const uint16_t *d_act, const float *h, int64_t rows, int F, uint8_t *dh_q,
+                               float *dh_s, void *stream);
+moe_status moe_dispatch_backward(const uint16_t *dx_sorted, const int32_t *slot_to_sorted, int T, int k, int d,
+                                 uint16_t *dx, void *stream);
+
+/* ------------------------------------------------------------------------
  * moe_combine -- gate-weighted sum back to token order ("Expert
  * parallelism": combine).
  *

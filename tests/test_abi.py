@@ -22,7 +22,7 @@ def lib():
 def _declared():
     src = open(os.path.join(ROOT, "include", "moe_r3.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_\w+|fp8_block_quant\w*)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_\w+|fp8_\w+)\s*\(", src)))
 
 
 def test_header_symbols_exported(lib):

@@ -1,0 +1,145 @@
+"""GPU parity of the expert path's backward under replay against the CPU
+oracle, through the C ABI: combine backward (quantised gradient rows and
+scales bit-exact, gate gradients to fp32 accumulation), the weight
+transpose and the dispatch backward bit-exact, the saved GEMM1
+pre-activations and both dgrad GEMMs within the layer's 2e-2 row bar, the
+SwiGLU backward within rounding (code flips < 1%), and the composed
+backward of the layer against the oracle's chain, every token on the tiny
+and replay workloads and a token sample of the 8192-token layer."""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_router_gb300 import synthetic as S
+from tests.helpers import bf16_bits, bf16_to_f64, e4m3_to_f64, row_rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_scaled_fp8_router_gb300 import moe_r3
+    return moe_r3
+
+
+def _layer(cfg, T=None):
+    from block_scaled_fp8_router_gb300.layer import MoELayerFP8, MoEWeightsFP8, quantize_weights
+    wr = S.make_router_w(cfg, DEV)
+    w13, w2 = S.make_w13(cfg, DEV), S.make_w2(cfg, DEV)
+    w = MoEWeightsFP8(wr, *quantize_weights(w13, w2))
+    return MoELayerFP8(w, T or cfg.T, cfg.k, cfg.score_fn, cfg.renorm, cfg.route_scale)
+
+
+def _deq_rows(q, s):
+    return e4m3_to_f64(q) * np.repeat(s.astype(np.float64), 128, axis=1)
+
+
+@pytest.mark.parametrize("T,k,d", [(37, 3, 256), (300, 8, 384), (5, 1, 128)])
+def test_combine_backward_against_oracle(L, oracle, T, k, d):
+    g = torch.Generator(device=DEV).manual_seed(T + d)
+    A = T * k
+    sl2 = torch.randperm(A, generator=g, device=DEV).to(torch.int32)
+    sl2[::7] = -1
+    out = torch.randn((A, d), generator=g, device=DEV).to(torch.bfloat16)
+    dy = torch.randn((T, d), generator=g, device=DEV).to(torch.bfloat16)
+    gates = torch.rand((T, k), generator=g, device=DEV)
+    dq, ds, dg = L.moe_combine_backward(dy, gates, out, sl2)
+    rf, rq, rs, rg = oracle.combine_backward(bf16_bits(dy), gates.cpu().numpy(), bf16_bits(out), sl2.cpu().numpy())
+    s = sl2.cpu().numpy()
+    routed = s[s >= 0]
+    np.testing.assert_array_equal(dq.cpu().numpy()[routed], rq[routed])
+    np.testing.assert_array_equal(ds.cpu().numpy()[routed], rs[routed])
+    idx = np.where(s >= 0, s, 0)
+    mag = (np.abs(bf16_to_f64(bf16_bits(dy)))[:, None, :] *
+           np.abs(bf16_to_f64(bf16_bits(out)))[idx].reshape(T, k, d)).sum(2)
+    assert np.all(np.abs(dg.cpu().numpy() - rg) <= mag * 1e-6 + 1e-30)
+    assert np.all(dg.cpu().numpy().reshape(-1)[s < 0] == 0)
+
+
+def test_weight_transpose_bit_exact(L, oracle):
+    cfg = S.CONFIGS["tiny"]
+    from block_scaled_fp8_router_gb300.layer import quantize_weights
+    w13, w2 = S.make_w13(cfg, DEV), S.make_w2(cfg, DEV)
+    w13q, w13s, w2q, w2s = quantize_weights(w13, w2)
+    for q, s_ in ((w13q, w13s), (w2q, w2s)):
+        qt, st = L.fp8_weight_transpose(q, s_)
+        rq, rs = oracle.weight_transpose(q.cpu().numpy(), s_.cpu().numpy())
+        np.testing.assert_array_equal(qt.cpu().numpy(), rq)
+        np.testing.assert_array_equal(st.cpu().numpy(), rs)
+
+
+def test_dispatch_backward_bit_exact(L, oracle):
+    g = torch.Generator(device=DEV).manual_seed(3)
+    T, k, d = 211, 8, 384
+    A = T * k
+    sl2 = torch.randperm(A, generator=g, device=DEV).to(torch.int32)
+    sl2[::11] = -1
+    rows = torch.randn((A, d), generator=g, device=DEV).to(torch.bfloat16)
+    dx = L.moe_dispatch_backward(rows, sl2, T, k)
+    ref = oracle.dispatch_backward(bf16_bits(rows), sl2.cpu().numpy(), T, k)
+    np.testing.assert_array_equal(bf16_bits(dx), ref)
+
+
+def _oracle_backward(oracle, layer, x, dy, T, k):
+    """The oracle's chain on the layer's own routing: every sorted row."""
+    E, d, F = layer.w.E, layer.w.d, layer.w.F
+    A = T * k
+    xq, xs = oracle.quant_1x128(bf16_bits(x))
+    s2s = layer.s2s[:A].cpu().numpy()
+    sl2 = layer.sl2[:A].cpu().numpy()
+    counts = layer.counts.cpu().numpy()
+    row_e = np.repeat(np.arange(E, dtype=np.int32), counts)
+    rows_q = oracle.gather_rows(xq, s2s, A, k)
+    rows_s = oracle.gather_rows(xs, s2s, A, k)
+    w13q, w13s = layer.w.w13_q.cpu().numpy(), layer.w.w13_s.cpu().numpy()
+    w2q, w2s = layer.w.w2_q.cpu().numpy(), layer.w.w2_s.cpu().numpy()
+    h = oracle.expert_ffn_preact(rows_q, rows_s, row_e, w13q, w13s)
+    _, _, _, out = oracle.expert_ffn(rows_q, rows_s, row_e, w13q, w13s, w2q, w2s)
+    _, dq, ds, dg = oracle.combine_backward(bf16_bits(dy), layer.gates[:T].cpu().numpy(), out, sl2)
+    w2tq, w2ts = oracle.weight_transpose(w2q, w2s)
+    w13tq, w13ts = oracle.weight_transpose(w13q, w13s)
+    d_act = oracle.grouped_gemm(dq, ds, row_e, w2tq, w2ts)
+    _, dhq, dhs = oracle.swiglu_backward(d_act, h)
+    dxs = oracle.grouped_gemm(dhq, dhs, row_e, w13tq, w13ts)
+    dx = oracle.dispatch_backward(dxs, sl2, T, k)
+    return dict(h=h, d_out_q=dq, d_out_s=ds, d_gates=dg, d_act=d_act, dh_q=dhq, dh_s=dhs, dx_sorted=dxs, dx=dx)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("replay", 500)])
+def test_layer_backward_against_oracle(L, oracle, name, T):
+    cfg = S.CONFIGS[name]
+    if T:
+        cfg = cfg.with_(T=T)
+    layer = _layer(cfg)
+    x = S.make_x(cfg, DEV)
+    replay = S.make_replay_payload(cfg.with_(layers=1), DEV)[0] if cfg.mode == "replay" else None
+    y_ref_form = layer.forward(x, replay_kT=replay).clone()
+    y = layer.forward(x, replay_kT=replay, train=True)
+    assert torch.equal(y.view(torch.int16), y_ref_form.view(torch.int16))       # saving h changes nothing
+    g = torch.Generator(device=DEV).manual_seed(5)
+    dy = torch.randn((cfg.T, cfg.d), generator=g, device=DEV).to(torch.bfloat16)
+    dx, d_gates = layer.backward(dy)
+    torch.cuda.synchronize()
+    assert L.check_status(layer.dev_status) == 0
+    A = cfg.T * cfg.k
+    r = _oracle_backward(oracle, layer, x, dy, cfg.T, cfg.k)
+    b = layer._bw
+    assert row_rel_err(layer.h[:A].cpu().numpy().astype(np.float64), r["h"].astype(np.float64)).max() <= 1e-5
+    np.testing.assert_array_equal(b["d_out_q"][:A].cpu().numpy(), r["d_out_q"])  # g * dy only: same gates, same codes
+    e_act = row_rel_err(bf16_to_f64(bf16_bits(b["d_act"][:A])), bf16_to_f64(r["d_act"]))
+    assert e_act.max() <= TOL, e_act.max()
+    g_dh = _deq_rows(b["dh_q"][:A].cpu().numpy(), b["dh_s"][:A].cpu().numpy())
+    r_dh = _deq_rows(r["dh_q"], r["dh_s"])
+    assert row_rel_err(g_dh, r_dh).max() <= TOL
+    assert (b["dh_q"][:A].cpu().numpy() != r["dh_q"]).mean() < 1e-2
+    e_dxs = row_rel_err(bf16_to_f64(bf16_bits(b["dx_sorted"][:A])), bf16_to_f64(r["dx_sorted"]))
+    assert e_dxs.max() <= TOL, e_dxs.max()
+    e_dx = row_rel_err(bf16_to_f64(bf16_bits(dx)), bf16_to_f64(r["dx"]))
+    assert e_dx.max() <= TOL, e_dx.max()
+    mag = np.abs(r["d_gates"]).max()
+    assert np.abs(d_gates.cpu().numpy() - r["d_gates"]).max() <= 2e-2 * mag
+    print(f"{name}: backward max row rel err d_act {e_act.max():.2e} dx_sorted {e_dxs.max():.2e} dx {e_dx.max():.2e}")
