@@ -394,6 +394,75 @@ def run_dispatch_combine(dev, seed, steps, warmup, peaks):
     return out
 
 
+def run_backward(cfg, dev, seed, steps, warmup, peaks):
+    """Backward of the expert path with the routing fixed (as the trainer
+    replays it): forward(train=True) once, then per step combine backward ->
+    dgrad GEMM (W2^T) -> SwiGLU backward -> dgrad GEMM (W13^T) -> dispatch
+    backward, timed by CUDA events between the calls."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    layer, x, replay = build_workload(cfg, dev, seed)
+    layer.forward(x, replay_kT=replay, train=True)
+    layer.backward(torch.zeros_like(x))               # allocates the gradient buffers and the W^T copies
+    torch.cuda.synchronize()
+    T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
+    A = T * k
+    dy = torch.empty_like(x).normal_(0.0, 1.0, generator=torch.Generator(device=dev).manual_seed(seed + 1))
+    b = layer._bw
+    w2t_q, w2t_s, w13t_q, w13t_s = layer.w.transposed()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    names = ("combine_bwd", "dgrad_gemm2", "swiglu_bwd", "dgrad_gemm1", "dispatch_bwd")
+
+    def step(e=None):
+        if e: e[0].record()
+        Lb.moe_combine_backward(dy, layer.gates[:T], layer.out_sorted[:A], layer.sl2[:A], d_out_q=b["d_out_q"][:A],
+                                d_out_s=b["d_out_s"][:A], d_gates=b["d_gates"][:T])
+        if e: e[1].record()
+        Lb.moe_grouped_gemm_fp8(b["d_out_q"][:A], b["d_out_s"][:A], layer.offsets, w2t_q, w2t_s, out=b["d_act"][:A],
+                                dev_status=layer.dev_status)
+        if e: e[2].record()
+        Lb.moe_swiglu_backward(b["d_act"][:A], layer.h[:A], dh_q=b["dh_q"][:A], dh_s=b["dh_s"][:A])
+        if e: e[3].record()
+        Lb.moe_grouped_gemm_fp8(b["dh_q"][:A], b["dh_s"][:A], layer.offsets, w13t_q, w13t_s,
+                                out=b["dx_sorted"][:A], dev_status=layer.dev_status)
+        if e: e[4].record()
+        Lb.moe_dispatch_backward(b["dx_sorted"][:A], layer.sl2[:A], T, k, dx=b["dx"][:T])
+        if e: e[5].record()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    evs = [[ev() for _ in range(6)] for _ in range(steps)]
+    t0.record()
+    for e in evs:
+        step(e)
+    t1.record()
+    torch.cuda.synchronize()
+    total = t0.elapsed_time(t1) / steps
+    split = {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / steps for i, n in enumerate(names)}
+    gemm_ms = split["dgrad_gemm2"] + split["dgrad_gemm1"]
+    flops = 6.0 * A * d * F
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    hbm = peaks["hbm_gbs"]
+    row = d + 4 * d / 128
+    b_comb = T * d * 2 + A * d * 2 + A * row + A * 4 + T * k * 8
+    b_swi = A * F * 2 + A * 2 * F * 4 + A * 2 * F * (1 + 4 / 128)
+    b_disp = A * d * 2 + A * 4 + T * d * 2
+    out = {"workload": f"{cfg.name}: T={T} d={d} E={E} top_k={k} F={F}, expert-path backward (dgrad) with the "
+                       "routing fixed", "tokens/s": T / (total * 1e-3), "ms_per_step": total,
+           "steps": {n: {"ms": v} for n, v in split.items()},
+           "dgrad_gemms": {"ms": gemm_ms, "TFLOP/s": flops / (gemm_ms * 1e-3) / 1e12,
+                           "frac": flops / (gemm_ms * 1e-3) / 1e12 / fp8_peak, "peak": fp8_peak},
+           "status": Lb.check_status(layer.dev_status)}
+    for n, nb in (("combine_bwd", b_comb), ("swiglu_bwd", b_swi), ("dispatch_bwd", b_disp)):
+        out["steps"][n]["GB/s"] = nb / (split[n] * 1e-3) / 1e9
+        out["steps"][n]["frac_hbm"] = out["steps"][n]["GB/s"] / hbm
+    del layer, x, b
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_payload(dev, seed, steps, warmup, peaks):
     """The routed-experts payload at one byte per id: a [64, 8, 131072] int32
     payload (64 layers x top-8 x 128K tokens, 268 MB, replayed-id
@@ -648,6 +717,7 @@ def main():
     ap.add_argument("--no-dispatch-combine", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
     ap.add_argument("--no-mx", action="store_true", help="skip the power-of-two-scale (block-scaled MMA) line")
+    ap.add_argument("--no-backward", action="store_true", help="skip the expert-path backward line")
     ap.add_argument("--router-kernels", action="store_true",
                     help="time only the router kernels (route_topk, route_replay) and print their line")
     ap.add_argument("--hbm-kernels", action="store_true",
@@ -749,6 +819,11 @@ def main():
             "ffn_frac": rffn["frac"], "steps": rextra, "dev_status": rr["status"]}
         del rr
         torch.cuda.empty_cache()
+    if cfg.name == "large" and not args.no_backward and not main_mx:
+        import torch
+        torch.cuda.empty_cache()
+        out["backward_layer"] = run_backward(cfg, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
+                                             rank_seed(args.seed, rank), max(3, args.steps // 2), 3, peaks)
     if cfg.name == "large" and not args.no_mx and not main_mx:
         import torch
         torch.cuda.empty_cache()

@@ -143,3 +143,52 @@ def test_layer_backward_against_oracle(L, oracle, name, T):
     mag = np.abs(r["d_gates"]).max()
     assert np.abs(d_gates.cpu().numpy() - r["d_gates"]).max() <= 2e-2 * mag
     print(f"{name}: backward max row rel err d_act {e_act.max():.2e} dx_sorted {e_dxs.max():.2e} dx {e_dx.max():.2e}")
+
+
+def test_backward_full_size_sampled(L, oracle):
+    """The 8192-token large layer (d=7168, E=256, top-8, F=2048): forward with
+    the pre-activations kept, backward of the expert path, and the oracle's
+    chain on 64 sampled tokens (every row is independent given its routing)."""
+    cfg = S.CONFIGS["large"]
+    from tests.test_gpu_fullsize import _layer as big_layer
+    layer = big_layer(cfg)
+    x = S.make_x(cfg, DEV)
+    layer.forward(x, train=True)
+    g = torch.Generator(device=DEV).manual_seed(9)
+    dy = torch.randn((cfg.T, cfg.d), generator=g, device=DEV).to(torch.bfloat16)
+    dx, d_gates = layer.backward(dy)
+    torch.cuda.synchronize()
+    assert L.check_status(layer.dev_status) == 0
+    rng = np.random.default_rng(2)
+    tokens = np.sort(np.concatenate([[0, cfg.T - 1], rng.choice(np.arange(1, cfg.T - 1), 62, replace=False)]))
+    k = cfg.k
+    n = len(tokens)
+    tt = torch.as_tensor(tokens, device=DEV)
+    ids = layer.ids[tt].cpu().numpy()
+    used = np.unique(ids)
+    remap = {int(e): i for i, e in enumerate(used)}
+    row_e = np.array([remap[int(e)] for e in ids.reshape(-1)], np.int32)
+    w13q = layer.w.w13_q[torch.as_tensor(used, device=DEV)].cpu().numpy()
+    w13s = layer.w.w13_s[torch.as_tensor(used, device=DEV)].cpu().numpy()
+    w2q = layer.w.w2_q[torch.as_tensor(used, device=DEV)].cpu().numpy()
+    w2s = layer.w.w2_s[torch.as_tensor(used, device=DEV)].cpu().numpy()
+    xq, xs = oracle.quant_1x128(bf16_bits(x[tt]))
+    rq, rs = np.repeat(xq, k, axis=0), np.repeat(xs, k, axis=0)
+    h = oracle.expert_ffn_preact(rq, rs, row_e, w13q, w13s)
+    _, _, _, out = oracle.expert_ffn(rq, rs, row_e, w13q, w13s, w2q, w2s)
+    loc = np.arange(n * k, dtype=np.int32)
+    _, dq, ds, dg = oracle.combine_backward(bf16_bits(dy[tt]), layer.gates[tt].cpu().numpy(), out, loc)
+    w2tq, w2ts = oracle.weight_transpose(w2q, w2s)
+    w13tq, w13ts = oracle.weight_transpose(w13q, w13s)
+    d_act = oracle.grouped_gemm(dq, ds, row_e, w2tq, w2ts)
+    _, dhq, dhs = oracle.swiglu_backward(d_act, h)
+    dxs = oracle.grouped_gemm(dhq, dhs, row_e, w13tq, w13ts)
+    dx_ref = oracle.dispatch_backward(dxs, loc, n, k)
+    # the GPU's quantised gradient rows of the sampled slots are bit-exact
+    sl2 = layer.sl2.cpu().numpy().reshape(cfg.T, k)[tokens].reshape(-1)
+    np.testing.assert_array_equal(layer._bw["d_out_q"][torch.as_tensor(sl2, device=DEV)].cpu().numpy(), dq)
+    err = row_rel_err(bf16_to_f64(bf16_bits(dx[tt])), bf16_to_f64(dx_ref))
+    assert err.max() <= TOL, err.max()
+    mag = np.abs(dg).max()
+    assert np.abs(d_gates[tt].cpu().numpy() - dg).max() <= 2e-2 * mag
+    print(f"large backward: {n} sampled tokens, max row rel err dx {err.max():.2e}")
