@@ -721,6 +721,79 @@ void or_swiglu_backward(const uint16_t *d_act, const float *h, int64_t n, int F,
     }
 }
 
+/* Padded segment offsets of the weight-gradient layouts: expert e's rows
+ * [offsets[e], offsets[e+1]) start at pad[e] = sum_{e'<e} roundup128(rows_e')
+ * so that every 128-row block holds rows of one expert; pad[E] is the total. */
+void or_pad_offsets(const int32_t *offsets, int E, int32_t *pad)
+{
+    int64_t acc = 0;
+    for (int e = 0; e < E; e++) {
+        pad[e] = (int32_t)acc;
+        int64_t rows = offsets[e + 1] - offsets[e];
+        acc += (rows + 127) / 128 * 128;
+    }
+    pad[E] = (int32_t)acc;
+}
+
+/* 128 x 1 quantisation for the weight-gradient GEMMs (the contraction runs
+ * over tokens): src [A, C] fp32 rows in expert order; for every expert's
+ * 128-row block and every channel c, amax over the block's real rows, scale
+ * amax / 448 (1 if 0), codes e4m3(v / s); written transposed, channel-major:
+ * q [C, pad[E]] (zero codes in the padding rows), s [C, pad[E] / 128]. */
+void or_quant_128x1(const float *src, const int32_t *offsets, const int32_t *pad, int E, int64_t C,
+                    uint8_t *q, float *s)
+{
+    int64_t P = pad[E], nbk = P / 128;
+    memset(q, 0, (size_t)(C * P));
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < C; c++) {
+        for (int e = 0; e < E; e++) {
+            int64_t r0 = offsets[e], rows = offsets[e + 1] - offsets[e];
+            for (int64_t b = 0; b * 128 < rows; b++) {
+                int64_t n = rows - b * 128 < 128 ? rows - b * 128 : 128;
+                float amax = 0.0f;
+                for (int64_t i = 0; i < n; i++) {
+                    float v = fabsf(src[(r0 + b * 128 + i) * C + c]);
+                    if (v > amax)
+                        amax = v;
+                }
+                float sc = block_scale(amax);
+                int64_t kb = pad[e] / 128 + b;
+                s[c * nbk + kb] = sc;
+                for (int64_t i = 0; i < n; i++)
+                    q[c * P + pad[e] + b * 128 + i] = or_e4m3_encode(src[(r0 + b * 128 + i) * C + c] / sc);
+            }
+        }
+    }
+}
+
+/* Weight gradient of one grouped GEMM: out[e] [M, N] fp32 =
+ * sum over expert e's 128-row blocks kb of (sa[m, kb] * sb[n, kb]) * P_kb(m, n),
+ * P_kb the exact 128-term dot of the two channel rows (rounded to binary32),
+ * a binary32 fma chain in ascending kb (the forward's promotion, with the
+ * contraction over tokens).  a [M, P] codes with sa [M, P/128], b [N, P] with
+ * sb [N, P/128] (the 128 x 1 layouts above). */
+void or_wgrad(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, const int32_t *pad, int E,
+              int64_t M, int64_t N, float *out)
+{
+    double dec[256];
+    for (int c = 0; c < 256; c++)
+        dec[c] = or_e4m3_decode((uint8_t)c);
+    int64_t P = pad[E], nbk = P / 128;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t em = 0; em < (int64_t)E * M; em++) {
+        int64_t e = em / M, m = em % M;
+        for (int64_t n = 0; n < N; n++) {
+            float acc = 0.0f;
+            for (int64_t kb = pad[e] / 128; kb < pad[e + 1] / 128; kb++) {
+                float pk = (float)e4m3_block_dot(a + m * P + kb * 128, b + n * P + kb * 128, dec);
+                acc = fmaf(sa[m * nbk + kb] * sb[n * nbk + kb], pk, acc);
+            }
+            out[(e * M + m) * N + n] = acc;
+        }
+    }
+}
+
 /* Dispatch backward: the input rows' gradient is the sum of their sorted
  * copies' gradients, dx[t] = bf16( sum_j dx_sorted[r(t,j)] ), a binary32
  * chain over j in slot order from +0 (unrouted slots skipped). */

@@ -68,6 +68,9 @@ def _load():
                 "or_grouped_gemm": (None, [P, P, I64, P, I64, I64, P, P, P]),
                 "or_swiglu_backward": (None, [P, P, I64, I, P, P, P]),
                 "or_dispatch_backward": (None, [P, P, I64, I, I, P]),
+                "or_pad_offsets": (None, [P, I, P]),
+                "or_quant_128x1": (None, [P, P, P, I, I64, P, P]),
+                "or_wgrad": (None, [P, P, P, P, P, I, I64, I64, P]),
                 "or_payload_unpack_u8": (None, [P, I64, P]),
                 "or_dispatch": (I64, [P, I64, I, I, P, P, P, P]),
                 "or_gather_rows": (None, [P, I64, P, I64, I, P]),
@@ -302,6 +305,43 @@ def dispatch_backward(dx_sorted_bf16: np.ndarray, slot_to_sorted: np.ndarray, T:
     dx = np.empty((T, d), np.uint16)
     _load().or_dispatch_backward(_p(dxs), _p(sl2), T, k, d, _p(dx))
     return dx
+
+
+def pad_offsets(offsets: np.ndarray) -> np.ndarray:
+    """Expert segments rounded up to 128 rows: pad [E+1] int32."""
+    o = _c(offsets, np.int32)
+    E = o.shape[0] - 1
+    pad = np.empty((E + 1,), np.int32)
+    _load().or_pad_offsets(_p(o), E, _p(pad))
+    return pad
+
+
+def quant_128x1(src: np.ndarray, offsets: np.ndarray):
+    """fp32 rows [A, C] in expert order -> (codes [C, P] channel-major, scales [C, P/128], pad [E+1])."""
+    x = _c(src, np.float32)
+    o = _c(offsets, np.int32)
+    pad = pad_offsets(o)
+    E = o.shape[0] - 1
+    C = x.shape[1]
+    P = int(pad[E])
+    q = np.empty((C, P), np.uint8)
+    s = np.ones((C, P // 128), np.float32)
+    _load().or_quant_128x1(_p(x), _p(o), _p(pad), E, C, _p(q), _p(s))
+    return q, s, pad
+
+
+def wgrad(a_q: np.ndarray, a_s: np.ndarray, b_q: np.ndarray, b_s: np.ndarray, pad: np.ndarray):
+    """Per-expert weight gradient [E, M, N] fp32 from the 128 x 1 layouts a [M, P], b [N, P]."""
+    a_q = _c(a_q, np.uint8)
+    a_s = _c(a_s, np.float32)
+    b_q = _c(b_q, np.uint8)
+    b_s = _c(b_s, np.float32)
+    pad = _c(pad, np.int32)
+    E = pad.shape[0] - 1
+    M, N = a_q.shape[0], b_q.shape[0]
+    out = np.empty((E, M, N), np.float32)
+    _load().or_wgrad(_p(a_q), _p(a_s), _p(b_q), _p(b_s), _p(pad), E, M, N, _p(out))
+    return out
 
 
 def dispatch(ids: np.ndarray, E: int):

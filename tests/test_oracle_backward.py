@@ -168,3 +168,82 @@ def test_expert_backward_dense_against_autograd(oracle):
     ref_da = (Dq @ W2).numpy()
     got = bf16_to_f64(d_act)
     assert np.all(np.abs(got - ref_da) <= np.abs(ref_da) * 2.0 ** -8 + 1e-6 * np.abs(ref_da).max())
+
+
+# ------------------------------------------------------------------ weight gradients
+
+def test_pad_offsets_hand_example(oracle):
+    pad = oracle.pad_offsets(np.array([0, 1, 1, 129, 385, 512], np.int32))
+    assert list(pad) == [0, 128, 128, 256, 512, 640]
+
+
+def test_quant_128x1_against_torch(oracle):
+    g = torch.Generator().manual_seed(13)
+    offsets = np.array([0, 5, 5, 200, 330], np.int32)
+    A, C = 330, 256
+    x = (torch.randn(A, C, generator=g) * torch.exp2(torch.randint(-8, 8, (1, C), generator=g).float())).float()
+    x[5:133, 7] = 0.0                                   # an all-zero block of one channel
+    q, s, pad = oracle.quant_128x1(x.numpy(), offsets)
+    assert q.shape == (C, int(pad[-1])) and s.shape == (C, int(pad[-1]) // 128)
+    for e in range(4):
+        r0, rows = offsets[e], offsets[e + 1] - offsets[e]
+        for b in range((rows + 127) // 128):
+            n = min(128, rows - 128 * b)
+            v = x[r0 + 128 * b: r0 + 128 * b + n].t()       # [C, n]
+            amax = v.abs().amax(1)
+            sref = amax / torch.tensor(448.0)
+            sref[sref == 0] = 1.0
+            kb = pad[e] // 128 + b
+            np.testing.assert_array_equal(s[:, kb], sref.numpy())
+            qref = (v / sref[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            np.testing.assert_array_equal(q[:, pad[e] + 128 * b: pad[e] + 128 * b + n], qref)
+            assert np.all(q[:, pad[e] + 128 * b + n: pad[e] + 128 * b + 128] == 0)   # padding rows
+    assert s[7, pad[2] // 128] == 1.0                 # the zero block of channel 7 (expert 2, first block)
+
+
+def test_wgrad_against_float64(oracle):
+    g = torch.Generator().manual_seed(17)
+    offsets = np.array([0, 70, 70, 300], np.int32)
+    A, M, N = 300, 256, 384
+    a = torch.randn(A, M, generator=g).float()
+    b = torch.randn(A, N, generator=g).float()
+    aq, as_, pad = oracle.quant_128x1(a.numpy(), offsets)
+    bq, bs, _ = oracle.quant_128x1(b.numpy(), offsets)
+    out = oracle.wgrad(aq, as_, bq, bs, pad)
+    deq = lambda q, s: e4m3_to_f64(q) * np.repeat(s.astype(np.float64), 128, axis=1)
+    Ad, Bd = deq(aq, as_), deq(bq, bs)
+    for e in range(3):
+        seg = slice(pad[e], pad[e + 1])
+        ref = Ad[:, seg] @ Bd[:, seg].T
+        mag = np.abs(Ad[:, seg]) @ np.abs(Bd[:, seg]).T
+        assert np.all(np.abs(out[e] - ref) <= mag * 2.0 ** -20 + 1e-30)
+    assert np.all(out[1] == 0)                          # the expert with no rows
+
+
+def test_weight_gradients_dense_against_autograd(oracle):
+    """E = 1: dW2 = d_out^T act and dW13 = dh^T x of a dense SwiGLU layer,
+    from the 128 x 1 quantised operands, against float64 autograd."""
+    cfg = S.CONFIGS["tiny"]
+    n = 200
+    g = torch.Generator().manual_seed(19)
+    x = torch.randn(n, cfg.d, generator=g).double()
+    W13 = (torch.randn(2 * cfg.F, cfg.d, generator=g) * 0.02).double().requires_grad_(True)
+    W2 = (torch.randn(cfg.d, cfg.F, generator=g) * 0.02).double().requires_grad_(True)
+    h = x @ W13.T
+    act = torch.nn.functional.silu(h[:, :cfg.F]) * h[:, cfg.F:]
+    act.retain_grad()
+    h.retain_grad()
+    y = act @ W2.T
+    dy = torch.randn(n, cfg.d, generator=g).double()
+    y.backward(dy)
+    offsets = np.array([0, n], np.int32)
+    dq, ds, pad = oracle.quant_128x1(dy.float().numpy(), offsets)
+    aq, as_, _ = oracle.quant_128x1(act.detach().float().numpy(), offsets)
+    dW2 = oracle.wgrad(dq, ds, aq, as_, pad)[0]
+    hq, hs, _ = oracle.quant_128x1(h.grad.float().numpy(), offsets)
+    xq, xs, _ = oracle.quant_128x1(x.float().numpy(), offsets)
+    dW13 = oracle.wgrad(hq, hs, xq, xs, pad)[0]
+    rel = lambda a, b: np.abs(a - b).max() / np.abs(b).max()
+    # two e4m3 operands per product: a few percent of the largest entry
+    assert rel(dW2, W2.grad.numpy()) < 5e-2, rel(dW2, W2.grad.numpy())
+    assert rel(dW13, W13.grad.numpy()) < 5e-2, rel(dW13, W13.grad.numpy())
