@@ -183,6 +183,125 @@ __global__ void transpose_scales_kernel(const float *__restrict__ s, int64_t E, 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Weight gradients.  dW2[e] = d_out^T act and dW13[e] = dh^T x over expert
+// e's rows: the contraction runs over tokens, so both operands are
+// re-quantised 128 x 1 (one scale per channel per 128-row block of the
+// expert) and stored channel-major with each expert's rows padded to a
+// multiple of 128: q [C, ld], s [C, ld/128] with the rows of expert e at
+// columns pad[e] .. (ld is a host-known bound of pad[E], so that tensor
+// maps can be built without reading pad back).
+
+// pad[e] = sum of the 128-rounded row counts of experts before e (one CTA)
+__global__ void pad_offsets_kernel(const int32_t *__restrict__ offsets, int E, int32_t *__restrict__ pad)
+{
+    if (threadIdx.x != 0) return;
+    int32_t acc = 0;
+    for (int e = 0; e < E; e++) {
+        pad[e] = acc;
+        acc += ((offsets[e + 1] - offsets[e] + 127) / 128) * 128;
+    }
+    pad[E] = acc;
+}
+
+// the operand's value at sorted row r, channel c (fp32)
+enum { SRC_GDY = 0, SRC_ACT = 1, SRC_DH = 2, SRC_X = 3 };
+struct WgSrc {
+    const uint16_t *dy;          // SRC_GDY: [T, C] bf16, with gates [T*k] and the slot map
+    const float *gates;
+    const uint16_t *x;           // SRC_X: [T, C] bf16
+    const int32_t *sorted_to_slot;
+    const float *h;              // SRC_ACT, SRC_DH: [A, 2F] fp32 pre-activations (C = F or 2F)
+    const uint16_t *d_act;       // SRC_DH: [A, F] bf16
+    int k, F;
+};
+
+template <int SRC>
+__device__ __forceinline__ float wg_value(const WgSrc &w, int64_t r, int64_t c, int64_t C)
+{
+    if (SRC == SRC_GDY) {
+        const int32_t slot = __ldg(w.sorted_to_slot + r);
+        return __ldg(w.gates + slot) * bf16_bits_to_f32(__ldg(w.dy + (int64_t)(slot / w.k) * C + c));
+    } else if (SRC == SRC_X) {
+        const int32_t slot = __ldg(w.sorted_to_slot + r);
+        return bf16_bits_to_f32(__ldg(w.x + (int64_t)(slot / w.k) * C + c));
+    } else if (SRC == SRC_ACT) {
+        const float g = __ldg(w.h + r * 2 * w.F + c), u = __ldg(w.h + r * 2 * w.F + w.F + c);
+        return __fdiv_rn(g, 1.0f + expf(-g)) * u;
+    } else {
+        const int64_t f = c < w.F ? c : c - w.F;
+        const float da = bf16_bits_to_f32(__ldg(w.d_act + r * w.F + f));
+        const float g = __ldg(w.h + r * 2 * w.F + f), u = __ldg(w.h + r * 2 * w.F + w.F + f);
+        const float sg = __fdiv_rn(1.0f, 1.0f + expf(-g));
+        return c < w.F ? da * u * sg * (1.0f + g * (1.0f - sg)) : da * (g * sg);
+    }
+}
+
+// One CTA per (64 channels, padded 128-row block): the block's values are
+// staged in shared memory, each channel's amax over the expert's rows is a
+// 4-thread reduction, and each thread writes 32 codes of one channel (the
+// 128 codes of a channel are one contiguous 128-byte run of q).
+// Scales channel-major sc[c * ld/128 + kb] (the GEMM's A side: one scale per
+// row of the MMA tile per K block) or block-major sc[kb * C + c] (the B side:
+// the 64 columns a promotion thread needs for one K block are contiguous).
+template <int SRC>
+__global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t *__restrict__ offsets,
+                                                          const int32_t *__restrict__ pad, int E, int64_t C,
+                                                          int64_t ld, bool kb_major, uint8_t *__restrict__ q,
+                                                          float *__restrict__ sc)
+{
+    __shared__ float tile[128][65];
+    __shared__ int s_e;
+    const int64_t P = pad[E];
+    const int64_t kb = blockIdx.y;
+    if (kb * 128 >= P || kb * 128 >= ld) return;
+    if (threadIdx.x == 0) {
+        int lo = 0, hi = E;  // expert with pad[e] <= 128 kb < pad[e+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pad[mid] <= kb * 128) lo = mid; else hi = mid;
+        }
+        s_e = lo;
+    }
+    __syncthreads();
+    const int e = s_e;
+    const int64_t r0 = offsets[e] + (kb * 128 - pad[e]);       // first sorted row of the block
+    const int64_t rend = offsets[e + 1];
+    const int64_t c0 = (int64_t)blockIdx.x * 64;
+    const int tid = threadIdx.x;
+    {
+        const int rr = tid >> 1, ch = (tid & 1) * 32;
+        const int64_t r = r0 + rr;
+#pragma unroll 4
+        for (int i = 0; i < 32; i++) {
+            const int64_t c = c0 + ch + i;
+            tile[rr][ch + i] = (r < rend && c < C) ? wg_value<SRC>(w, r, c, C) : 0.0f;
+        }
+    }
+    __syncthreads();
+    const int cc = tid >> 2, part = tid & 3;
+    float amax = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(tile[part * 32 + i][cc]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    const float s = block_scale(amax);
+    const int64_t c = c0 + cc;
+    if (c < C) {
+        uint32_t wds[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const float *t4 = &tile[part * 32 + 4 * i][cc];
+            wds[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(t4[0], s), __fdiv_rn(t4[65], s)) |
+                     ((uint32_t)pack_e4m3x2(__fdiv_rn(t4[130], s), __fdiv_rn(t4[195], s)) << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(q + c * ld + kb * 128 + part * 32);
+        dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+        dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+        if (part == 0) sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
+    }
+}
+
 } // namespace moe
 
 using namespace moe;
@@ -231,5 +350,41 @@ MOE_API moe_status fp8_weight_transpose(const uint8_t *q, const float *s, int64_
     const int64_t ns = E * (R / 128) * (C / 128);
     transpose_scales_kernel<<<(unsigned)((ns + 255) / 256 < 4096 ? (ns + 255) / 256 : 4096), 256, 0, stm>>>(
         s, E, R / 128, C / 128, st);
+    return launch_status();
+}
+
+MOE_API moe_status moe_wgrad_pad_offsets(const int32_t *expert_offsets, int E, int32_t *pad, void *stream)
+{
+    if (E < 1 || E > 1024) return MOE_ERR_SHAPE;
+    if (!expert_offsets || !pad) return MOE_ERR_NULL;
+    pad_offsets_kernel<<<1, 32, 0, as_stream(stream)>>>(expert_offsets, E, pad);
+    return launch_status();
+}
+
+MOE_API moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gates, const uint16_t *x,
+                                   const int32_t *sorted_to_slot, int k, const float *h, const uint16_t *d_act,
+                                   int F, const int32_t *expert_offsets, const int32_t *pad, int E, int64_t C,
+                                   int64_t max_pad, int scales_kb_major, uint8_t *q, float *scales, void *stream)
+{
+    if (E < 1 || E > 1024 || C <= 0 || C % 128 != 0 || max_pad < 0 || max_pad % 128 != 0 || k < 1 || k > 32)
+        return MOE_ERR_SHAPE;
+    if (!expert_offsets || !pad || !q || !scales) return MOE_ERR_NULL;
+    WgSrc w{dy, gates, x, sorted_to_slot, h, d_act, k, F};
+    if ((src == SRC_GDY && (!dy || !gates || !sorted_to_slot)) || (src == SRC_X && (!x || !sorted_to_slot)) ||
+        (src == SRC_ACT && (!h || F <= 0 || C != F)) || (src == SRC_DH && (!h || !d_act || F <= 0 || C != 2 * F)))
+        return src < 0 || src > 3 ? MOE_ERR_SHAPE : MOE_ERR_NULL;
+    if (!aligned16(q)) return MOE_ERR_ALIGN;
+    if (max_pad == 0) return MOE_OK;
+    // one CTA per (64 channels, 128-row block) of the largest possible padded
+    // extent; blocks past pad[E] (known on the device only) return at once
+    const dim3 grid((unsigned)((C + 63) / 64), (unsigned)(max_pad / 128));
+    cudaStream_t st = as_stream(stream);
+    switch (src) {
+    case SRC_GDY: quant_128x1_kernel<SRC_GDY><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
+    case SRC_ACT: quant_128x1_kernel<SRC_ACT><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
+    case SRC_DH: quant_128x1_kernel<SRC_DH><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
+    case SRC_X: quant_128x1_kernel<SRC_X><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
+    default: return MOE_ERR_SHAPE;
+    }
     return launch_status();
 }

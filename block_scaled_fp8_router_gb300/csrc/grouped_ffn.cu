@@ -589,6 +589,235 @@ static bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, cons
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // ============================================================================
+// Weight gradients: per expert e, out[e] [M, N] fp32 = sum over e's padded
+// 128-row blocks kb of (sa[m, kb] * sb[n, kb]) * P_kb(m, n), the same 128-deep
+// block MMAs and fp32 promotion as the forward with the contraction over the
+// expert's tokens.  A = [M, ld] codes (the 128 x 1 layout of d_out or dh,
+// channel-major scales sa [M, ld/128]), B = [N, ld] (act or x, block-major
+// scales sbT [ld/128, N]: the 64 column scales a promotion thread needs for
+// one K block are contiguous).  Tiles are (expert, N block, M block), M
+// fastest; experts without rows have no tiles (their out is zeroed apart).
+// ============================================================================
+
+struct ParamsWG {
+    const float *sa;            // [M, ld/128]
+    const float *sbT;           // [ld/128, N]
+    const int32_t *pad;         // [E+1]
+    float *out;                 // [E, M, N]
+    int32_t *dev_status;
+    int64_t ld;
+    int E, M, N;
+};
+
+struct SmemWG {
+    uint8_t a[STAGES][A_BYTES];
+    uint8_t b[STAGES][B_BYTES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int32_t tile_prefix[MAX_E + 1];
+};
+constexpr size_t SMEM_WG_BYTES = sizeof(SmemWG) + 1024;
+
+struct TileWG {
+    int e, m_blk, n_blk;
+    int kb0, nkb;   // first global K block and count
+};
+
+__device__ __forceinline__ TileWG decode_tile_wg(const SmemWG &s, const ParamsWG &p, int t)
+{
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s.tile_prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    TileWG tl;
+    tl.e = lo;
+    const int m_tiles = p.M / BM;
+    const int local = t - s.tile_prefix[lo];
+    tl.n_blk = local / m_tiles;
+    tl.m_blk = local - tl.n_blk * m_tiles;
+    const int32_t p0 = __ldg(p.pad + lo), p1 = __ldg(p.pad + lo + 1);
+    tl.kb0 = p0 / 128;
+    tl.nkb = (p1 - p0) / 128;
+    return tl;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                         const ParamsWG p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SmemWG &s = *reinterpret_cast<SmemWG *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_per_e = (p.M / BM) * ((p.N + BN - 1) / BN);   // N % 256 == 128: a half last N tile
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; i++) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&s.tfull[i], 1);
+            mbar_init(&s.tempty[i], EPI_WARPS);
+        }
+        mbar_init(&s.mma_done, 1);
+        s.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        // tile prefix over experts with rows (warp-wide scan)
+        int32_t carry = 0;
+        for (int base = 0; base <= p.E; base += 32) {
+            const int e = base + lane;
+            const int32_t tiles = (e < p.E && __ldg(p.pad + e + 1) > __ldg(p.pad + e)) ? tiles_per_e : 0;
+            int32_t incl = tiles;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (e <= p.E) s.tile_prefix[e] = carry + incl - tiles;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+    }
+    if (warp == MMA_WARP) tmem_alloc(&s.tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+    const int total = s.tile_prefix[p.E];
+    volatile int *abort_flag = &s.abort_flag;
+
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            uint32_t j = 0, issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileWG tl = decode_tile_wg(s, p, t);
+                for (int kb = 0; kb < tl.nkb; kb++, j++) {
+                    const int st = j % STAGES;
+                    if (!wait_or_abort(&s.empty[st], ((j / STAGES) & 1) ^ 1, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
+                    tma_load_2d(s.a[st], &tm_a, (tl.kb0 + kb) * BK, tl.m_blk * BM, &s.full[st]);
+                    tma_load_2d(s.b[st], &tm_b, (tl.kb0 + kb) * BK, tl.n_blk * BN, &s.full[st]);
+                    issued |= 1u << st;
+                }
+            }
+            for (int i = 0; i < STAGES; i++) {
+                if (!(issued & (1u << i)) || j == 0) continue;
+                const uint32_t last = j - 1 - ((j - 1 - i) % STAGES);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&s.full[i], (last / STAGES) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_f8(BM, BN);
+            uint32_t j = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileWG tl = decode_tile_wg(s, p, t);
+                for (int kb = 0; kb < tl.nkb; kb++, j++) {
+                    const int st = j % STAGES;
+                    const int buf = j & 1;
+                    if (!wait_or_abort(&s.tempty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.dev_status) ||
+                        !wait_or_abort(&s.full[st], (j / STAGES) & 1, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(smem_u32(s.a[st]));
+                    const uint64_t bdesc = sw128_desc(smem_u32(s.b[st]));
+#pragma unroll
+                    for (int ks = 0; ks < BK / 32; ks++)
+                        mma_f8(tmem + buf * BN, adesc + 2 * ks, bdesc + 2 * ks, IDESC, ks > 0);
+                    mma_commit(&s.empty[st]);
+                    mma_commit(&s.tfull[buf]);
+                }
+            }
+            mma_commit(&s.mma_done);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&s.mma_done, 0) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+        }
+        __syncwarp();
+    } else if (warp < EPI_WARPS) {
+        const int q = warp & 3, cg = warp >> 2;
+        const int r_in = q * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        const int64_t nbk = p.ld / 128;
+        uint32_t j = 0;
+        bool aborted = false;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const TileWG tl = decode_tile_wg(s, p, t);
+            const int64_t m = (int64_t)tl.m_blk * BM + r_in;
+            const int64_t n0 = (int64_t)tl.n_blk * BN + 64 * cg;
+            const bool n_ok = n0 < p.N;    // past N only in the half last tile (B rows zero-filled there)
+            float acc[64];
+#pragma unroll
+            for (int i = 0; i < 64; i++) acc[i] = 0.0f;
+            for (int kb = 0; kb < tl.nkb; kb++, j++) {
+                const int buf = j & 1;
+                const int64_t kg = tl.kb0 + kb;
+                const float sa = __ldg(p.sa + m * nbk + kg);
+                const float4 *sb4 = reinterpret_cast<const float4 *>(p.sbT + kg * p.N + (n_ok ? n0 : 0));
+                if (!aborted && !wait_or_abort(&s.tfull[buf], (j >> 1) & 1, abort_flag, p.dev_status))
+                    aborted = true;
+                if (!aborted) {
+                    tc_fence_after();
+                    const uint32_t base = tmem + lane_addr + buf * BN + 64 * cg;
+                    float v[16];
+#pragma unroll
+                    for (int h = 0; h < 4; h++) {
+                        tmem_ld16(base + 16 * h, v);
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; i4++) {
+                            const float4 b = n_ok ? __ldg(sb4 + 4 * h + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            acc[16 * h + 4 * i4 + 0] = fmaf(sa * b.x, v[4 * i4 + 0], acc[16 * h + 4 * i4 + 0]);
+                            acc[16 * h + 4 * i4 + 1] = fmaf(sa * b.y, v[4 * i4 + 1], acc[16 * h + 4 * i4 + 1]);
+                            acc[16 * h + 4 * i4 + 2] = fmaf(sa * b.z, v[4 * i4 + 2], acc[16 * h + 4 * i4 + 2]);
+                            acc[16 * h + 4 * i4 + 3] = fmaf(sa * b.w, v[4 * i4 + 3], acc[16 * h + 4 * i4 + 3]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.tempty[buf]);
+                }
+            }
+            if (!aborted && n_ok) {
+                float4 *dst = reinterpret_cast<float4 *>(p.out + ((int64_t)tl.e * p.M + m) * p.N + n0);
+#pragma unroll
+                for (int i = 0; i < 16; i++)
+                    dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+            }
+            if (epi_bar_or(aborted || *abort_flag)) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// zero out[e] of the experts without rows (the GEMM has no tiles for them)
+__global__ void wgrad_zero_empty_kernel(const int32_t *__restrict__ pad, int64_t MN, float *__restrict__ out)
+{
+    const int e = blockIdx.y;
+    if (__ldg(pad + e + 1) != __ldg(pad + e)) return;
+    float4 *o = reinterpret_cast<float4 *>(out + (int64_t)e * MN);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < MN / 4; i += (int64_t)gridDim.x * blockDim.x)
+        o[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+}
+
+// ============================================================================
 // Power-of-two scales (UE8M0): the hardware block-scaled MMA
 // ============================================================================
 //
@@ -1144,5 +1373,37 @@ MOE_API moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x
     p2.a_exp = act_e;
     p2.b_exp = w2_exp;
     grouped_gemm_mx_kernel<2><<<grid, THREADS, SMEM_MX_BYTES, st>>>(ma2, mb2, p2);
+    return launch_status();
+}
+
+MOE_API moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_s, const uint8_t *b_q, const float *b_sT,
+                                  const int32_t *pad, int E, int M, int N, int64_t ld, float *out,
+                                  int32_t *dev_status, void *stream)
+{
+    if (E < 1 || E > MAX_E || M <= 0 || N <= 0 || M % BM != 0 || N % 128 != 0 || ld <= 0 || ld % 128 != 0 ||
+        ld >= (1LL << 31) || (int64_t)M >= (1LL << 31) || (int64_t)N >= (1LL << 31))
+        return MOE_ERR_SHAPE;
+    if (!a_q || !a_s || !b_q || !b_sT || !pad || !out) return MOE_ERR_NULL;
+    if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(out) || !aligned16(b_sT)) return MOE_ERR_ALIGN;
+    auto enc = encode_fn();
+    if (!enc) return MOE_ERR_CUDA;
+    CUtensorMap ma, mb;
+    if (!make_map(enc, &ma, a_q, ld, M, 128) || !make_map(enc, &mb, b_q, ld, N, 256)) return MOE_ERR_CUDA;
+    ParamsWG prm;
+    prm.sa = a_s;
+    prm.sbT = b_sT;
+    prm.pad = pad;
+    prm.out = out;
+    prm.dev_status = dev_status;
+    prm.ld = ld;
+    prm.E = E;
+    prm.M = M;
+    prm.N = N;
+    if (cudaFuncSetAttribute(grouped_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_WG_BYTES) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    cudaStream_t st = as_stream(stream);
+    wgrad_zero_empty_kernel<<<dim3(64, (unsigned)E), 256, 0, st>>>(pad, (int64_t)M * N, out);
+    grouped_wgrad_kernel<<<sm_count(), THREADS, SMEM_WG_BYTES, st>>>(ma, mb, prm);
     return launch_status();
 }

@@ -172,17 +172,18 @@ class MoELayerFP8:
                                         out_sorted=self.out_sorted[:A], workspace=self.ffn_ws,
                                         dev_status=self.dev_status)
             self._T_train = T
+            self._x_train = x
         else:
             L.moe_grouped_ffn_fp8(self.xq_sorted[:A], self.xs_sorted[:A], self.offsets, self.w.w13_q, self.w.w13_s,
                                   self.w.w2_q, self.w.w2_s, out_sorted=self.out_sorted[:A], workspace=self.ffn_ws,
                                   dev_status=self.dev_status)
         return L.moe_combine(self.out_sorted[:A], self.sl2[:A], gates, y=y)
 
-    def backward(self, dy: torch.Tensor):
+    def backward(self, dy: torch.Tensor, weight_grads: bool = False):
         """Backward of the expert path of the last forward(train=True) with its
         routing fixed (replayed): returns (dx [T, d] bf16 from the experts,
-        d_gates [T, k] fp32).  Weight gradients and the router's backward are
-        not computed."""
+        d_gates [T, k] fp32), and with weight_grads also (dW13 [E, 2F, d],
+        dW2 [E, d, F]) fp32.  The router's backward is not computed."""
         T = getattr(self, "_T_train", None)
         if T is None or self.mx or self.gathered:
             raise ValueError("backward needs a forward(train=True) of the fp32-scale sorted form")
@@ -206,7 +207,41 @@ class MoELayerFP8:
         L.moe_grouped_gemm_fp8(b["dh_q"][:A], b["dh_s"][:A], self.offsets, w13t_q, w13t_s, out=b["dx_sorted"][:A],
                                dev_status=self.dev_status)
         dx = L.moe_dispatch_backward(b["dx_sorted"][:A], self.sl2[:A], T, self.k, dx=b["dx"][:T])
-        return dx, b["d_gates"][:T]
+        if not weight_grads:
+            return dx, b["d_gates"][:T]
+        return (dx, b["d_gates"][:T], *self._weight_grads(dy, T))
+
+    def _weight_grads(self, dy: torch.Tensor, T: int):
+        A = T * self.k
+        E, d, F = self.w.E, self.w.d, self.w.F
+        dev = dy.device
+        ld = L.wgrad_ld(self.T_max * self.k, E)
+        if getattr(self, "_wg", None) is None:
+            e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+            self._wg = dict(pad=e((E + 1,), torch.int32),
+                            aq=e((max(d, 2 * F), ld), torch.uint8), as_=e((max(d, 2 * F) * (ld // 128),), torch.float32),
+                            bq=e((max(F, d), ld), torch.uint8), bs=e((max(F, d) * (ld // 128),), torch.float32),
+                            dW2=e((E, d, F), torch.float32), dW13=e((E, 2 * F, d), torch.float32))
+        w = self._wg
+        b = self._bw
+        pad = L.moe_wgrad_pad_offsets(self.offsets, pad=w["pad"])
+        s2s = self.s2s[:A]
+        # dW2 = d_out^T act
+        aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_GDY, self.offsets, pad, d, ld, False, dy=dy, gates=self.gates[:T],
+                                    sorted_to_slot=s2s, k=self.k, q=w["aq"][:d],
+                                    scales=w["as_"][:d * (ld // 128)].view(d, ld // 128))
+        bq, bs = L.moe_wgrad_quant(L.WGRAD_SRC_ACT, self.offsets, pad, F, ld, True, h=self.h, F=F, q=w["bq"][:F],
+                                   scales=w["bs"][:F * (ld // 128)].view(ld // 128, F))
+        L.moe_wgrad_gemm(aq, as_, bq, bs, pad, out=w["dW2"], dev_status=self.dev_status)
+        # dW13 = dh^T x
+        aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_DH, self.offsets, pad, 2 * F, ld, False, h=self.h,
+                                    d_act=b["d_act"], F=F, q=w["aq"][:2 * F],
+                                    scales=w["as_"][:2 * F * (ld // 128)].view(2 * F, ld // 128))
+        bq, bs = L.moe_wgrad_quant(L.WGRAD_SRC_X, self.offsets, pad, d, ld, True, x=self._x_train,
+                                   sorted_to_slot=s2s, k=self.k, q=w["bq"][:d],
+                                   scales=w["bs"][:d * (ld // 128)].view(ld // 128, d))
+        L.moe_wgrad_gemm(aq, as_, bq, bs, pad, out=w["dW13"], dev_status=self.dev_status)
+        return w["dW13"], w["dW2"]
 
 
 class HostStreamer:

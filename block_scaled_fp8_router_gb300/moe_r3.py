@@ -50,6 +50,9 @@ _SIGS = {
     "moe_combine_backward": (I, [P, P, P, P, I, I, I, I64, P, P, P, P]),
     "moe_swiglu_backward": (I, [P, P, I64, I, P, P, P]),
     "moe_dispatch_backward": (I, [P, P, I, I, I, P, P]),
+    "moe_wgrad_pad_offsets": (I, [P, I, P, P]),
+    "moe_wgrad_quant": (I, [I, P, P, P, P, I, P, P, I, P, P, I, I64, I64, I, P, P, P]),
+    "moe_wgrad_gemm": (I, [P, P, P, P, P, I, I, I, I64, P, P, P]),
     "moe_grouped_ffn_mx": (I, [P, P, P, I, I, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_debug_bounded_wait": (I, [I64, P, P]),
     "moe_device_sm_count": (I, []),
@@ -502,6 +505,54 @@ def moe_dispatch_backward(dx_sorted, slot_to_sorted, T, k, dx=None, stream=None)
     _check("moe_dispatch_backward", _lib.moe_dispatch_backward(_ptr(dx_sorted), _ptr(slot_to_sorted), T, k, d,
                                                                _ptr(dx), _stream(stream)))
     return dx
+
+
+WGRAD_SRC_GDY, WGRAD_SRC_ACT, WGRAD_SRC_DH, WGRAD_SRC_X = 0, 1, 2, 3
+
+
+def wgrad_ld(max_rows: int, E: int) -> int:
+    """A host-side bound of the padded row extent (multiple of 128)."""
+    return ((max_rows + 127) // 128 + E) * 128
+
+
+def moe_wgrad_pad_offsets(expert_offsets, pad=None, stream=None):
+    E = expert_offsets.numel() - 1
+    pad = _empty((E + 1,), torch.int32, expert_offsets) if pad is None else pad
+    _want(pad, torch.int32, (E + 1,), "pad")
+    _check("moe_wgrad_pad_offsets", _lib.moe_wgrad_pad_offsets(_ptr(expert_offsets), E, _ptr(pad), _stream(stream)))
+    return pad
+
+
+def moe_wgrad_quant(src, expert_offsets, pad, C, ld, kb_major, dy=None, gates=None, x=None, sorted_to_slot=None,
+                    k=1, h=None, d_act=None, F=0, q=None, scales=None, stream=None):
+    """One weight-gradient operand, 128 x 1 quantised, channel-major: (q [C, ld], scales)."""
+    E = expert_offsets.numel() - 1
+    dev = expert_offsets.device
+    q = torch.empty((C, ld), dtype=torch.uint8, device=dev) if q is None else q
+    sshape = (ld // 128, C) if kb_major else (C, ld // 128)
+    scales = torch.empty(sshape, dtype=torch.float32, device=dev) if scales is None else scales
+    _want(q, torch.uint8, (C, ld), "q")
+    _want(scales, torch.float32, sshape, "scales")
+    _check("moe_wgrad_quant", _lib.moe_wgrad_quant(
+        src, _ptr(dy), _ptr(gates), _ptr(x), _ptr(sorted_to_slot), k, _ptr(h), _ptr(d_act), F,
+        _ptr(expert_offsets), _ptr(pad), E, C, ld, int(kb_major), _ptr(q), _ptr(scales), _stream(stream)))
+    return q, scales
+
+
+def moe_wgrad_gemm(a_q, a_s, b_q, b_sT, pad, out=None, dev_status=None, stream=None):
+    """out [E, M, N] fp32: per expert the weight gradient over its rows."""
+    M, ld = a_q.shape
+    N = b_q.shape[0]
+    E = pad.numel() - 1
+    _want(a_q, torch.uint8, (M, ld), "a_q")
+    _want(a_s, torch.float32, (M, ld // 128), "a_s")
+    _want(b_q, torch.uint8, (N, ld), "b_q")
+    _want(b_sT, torch.float32, (ld // 128, N), "b_sT")
+    out = _empty((E, M, N), torch.float32, a_q) if out is None else out
+    _want(out, torch.float32, (E, M, N), "out")
+    _check("moe_wgrad_gemm", _lib.moe_wgrad_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_sT), _ptr(pad), E, M, N, ld,
+                                                 _ptr(out), _ptr(dev_status), _stream(stream)))
+    return out
 
 
 def moe_combine_slots(out_slots, slot_to_sorted, gates, y=None, stream=None):

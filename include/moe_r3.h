@@ -335,7 +335,28 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  * out[r, :] = bf16(a[r] b[e]^T) for the rows of expert e, a [max_rows, K]
  * e4m3 with [max_rows, K/128] fp32 scales, b [E, N, K] with [E, N/128,
  * K/128]; K, N multiples of 128 (the forward's GEMM2 is K = F, N = d).
- * Weight gradients and the router's backward are not provided.
+ * Weight gradients (same section): dW2[e] = d_out^T act and dW13[e] =
+ * dh^T x over expert e's rows, with both operands re-quantised 128 x 1 (one
+ * fp32 scale, amax/448, per channel per 128-row block of the expert) because
+ * the contraction runs over tokens:
+ *   moe_wgrad_pad_offsets  pad[e] = sum of the 128-rounded row counts of the
+ *                          experts before e (device, [E+1]).
+ *   moe_wgrad_quant        one operand in the channel-major layout q [C, ld]
+ *                          (expert e's rows at columns pad[e].., zero codes in
+ *                          the padding), scales [C, ld/128] or, with
+ *                          scales_kb_major, [ld/128, C]; ld is a host-known
+ *                          bound of pad[E] (multiple of 128, e.g.
+ *                          (ceil(A/128) + E) * 128).  src selects the operand
+ *                          0: g * dy (d_out, C = d), 1: silu(g) * u from h
+ *                          (act, C = F), 2: dh from d_act and h (C = 2F),
+ *                          3: x (C = d); rows map to tokens by
+ *                          sorted_to_slot / k.
+ *   moe_wgrad_gemm         out[e] [M, N] fp32 = sum over e's blocks kb of
+ *                          (a_s[m, kb] * b_sT[kb, n]) * P_kb(m, n) (the
+ *                          forward's per-block promotion), a [M, ld], b [N,
+ *                          ld]; M, N multiples of 128; experts without rows
+ *                          get zeros.
+ * The router's backward is not provided (d_gates are returned for it).
  * Errors: NULL, SHAPE, ALIGN, CUDA (WORKSPACE for the _train call).
  * ---------------------------------------------------------------------- */
 moe_status moe_grouped_ffn_fp8_train(const uint8_t *xq_sorted, const float *xs_sorted,
@@ -355,6 +376,14 @@ moe_status moe_swiglu_backward(const uint16_t *d_act, const float *h, int64_t ro
                                float *dh_s, void *stream);
 moe_status moe_dispatch_backward(const uint16_t *dx_sorted, const int32_t *slot_to_sorted, int T, int k, int d,
                                  uint16_t *dx, void *stream);
+moe_status moe_wgrad_pad_offsets(const int32_t *expert_offsets, int E, int32_t *pad, void *stream);
+moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gates, const uint16_t *x,
+                           const int32_t *sorted_to_slot, int k, const float *h, const uint16_t *d_act, int F,
+                           const int32_t *expert_offsets, const int32_t *pad, int E, int64_t C, int64_t ld,
+                           int scales_kb_major, uint8_t *q, float *scales, void *stream);
+moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_s, const uint8_t *b_q, const float *b_sT,
+                          const int32_t *pad, int E, int M, int N, int64_t ld, float *out, int32_t *dev_status,
+                          void *stream);
 
 /* ------------------------------------------------------------------------
  * moe_combine -- gate-weighted sum back to token order ("Expert

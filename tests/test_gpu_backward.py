@@ -192,3 +192,70 @@ def test_backward_full_size_sampled(L, oracle):
     mag = np.abs(dg).max()
     assert np.abs(d_gates[tt].cpu().numpy() - dg).max() <= 2e-2 * mag
     print(f"large backward: {n} sampled tokens, max row rel err dx {err.max():.2e}")
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("replay", 500)])
+def test_weight_gradients_against_oracle(L, oracle, name, T):
+    """dW2 = d_out^T act and dW13 = dh^T x per expert from 128 x 1 operands:
+    the d_out and x operands bit-exact (same values on both sides), act and
+    dh within rounding (code flips < 1%), and both gradients within 2e-2 of
+    each expert matrix's largest entry."""
+    cfg = S.CONFIGS[name]
+    if T:
+        cfg = cfg.with_(T=T)
+    layer = _layer(cfg)
+    x = S.make_x(cfg, DEV)
+    replay = S.make_replay_payload(cfg.with_(layers=1), DEV)[0] if cfg.mode == "replay" else None
+    layer.forward(x, replay_kT=replay, train=True)
+    g = torch.Generator(device=DEV).manual_seed(8)
+    dy = torch.randn((cfg.T, cfg.d), generator=g, device=DEV).to(torch.bfloat16)
+    dx, d_gates, dW13, dW2 = layer.backward(dy, weight_grads=True)
+    torch.cuda.synchronize()
+    assert L.check_status(layer.dev_status) == 0
+    E, d, F, k, Tn = cfg.E, cfg.d, cfg.F, cfg.k, cfg.T
+    A = Tn * k
+    offsets = layer.offsets.cpu().numpy()
+    s2s = layer.s2s[:A].cpu().numpy()
+    sl2 = layer.sl2[:A].cpu().numpy()
+    counts = layer.counts.cpu().numpy()
+    row_e = np.repeat(np.arange(E, dtype=np.int32), counts)
+    xq, xs = oracle.quant_1x128(bf16_bits(x))
+    rq, rs = oracle.gather_rows(xq, s2s, A, k), oracle.gather_rows(xs, s2s, A, k)
+    w13q, w13s = layer.w.w13_q.cpu().numpy(), layer.w.w13_s.cpu().numpy()
+    w2q, w2s = layer.w.w2_q.cpu().numpy(), layer.w.w2_s.cpu().numpy()
+    h = oracle.expert_ffn_preact(rq, rs, row_e, w13q, w13s)
+    act_f, _, _, out = oracle.expert_ffn(rq, rs, row_e, w13q, w13s, w2q, w2s)
+    d_out_f, dq, ds, _ = oracle.combine_backward(bf16_bits(dy), layer.gates[:Tn].cpu().numpy(), out, sl2)
+    w2tq, w2ts = oracle.weight_transpose(w2q, w2s)
+    d_act = oracle.grouped_gemm(dq, ds, row_e, w2tq, w2ts)
+    dh_f, _, _ = oracle.swiglu_backward(d_act, h)
+    x_rows = bf16_to_f64(bf16_bits(x)).astype(np.float32)[s2s // k]
+    # operands: d_out and x bit-exact against the oracle's 128 x 1 quantisation
+    pad = L.moe_wgrad_pad_offsets(layer.offsets)
+    ld = L.wgrad_ld(A, E)
+    gq, gs = L.moe_wgrad_quant(L.WGRAD_SRC_GDY, layer.offsets, pad, d, ld, False, dy=dy, gates=layer.gates[:Tn],
+                               sorted_to_slot=layer.s2s[:A], k=k)
+    oq, os_, opad = oracle.quant_128x1(d_out_f, offsets)
+    np.testing.assert_array_equal(pad.cpu().numpy(), opad)
+    P = int(opad[-1])
+    np.testing.assert_array_equal(gq.cpu().numpy()[:, :P], oq)
+    np.testing.assert_array_equal(gs.cpu().numpy()[:, :P // 128], os_)
+    xq2, xs2 = L.moe_wgrad_quant(L.WGRAD_SRC_X, layer.offsets, pad, d, ld, True, x=x, sorted_to_slot=layer.s2s[:A], k=k)
+    oxq, oxs, _ = oracle.quant_128x1(x_rows, offsets)
+    np.testing.assert_array_equal(xq2.cpu().numpy()[:, :P], oxq)
+    np.testing.assert_array_equal(xs2.cpu().numpy()[:P // 128].T, oxs)
+    aq2, _ = L.moe_wgrad_quant(L.WGRAD_SRC_ACT, layer.offsets, pad, F, ld, True, h=layer.h, F=F)
+    oaq, oas, _ = oracle.quant_128x1(act_f, offsets)
+    assert (aq2.cpu().numpy()[:, :P] != oaq).mean() < 1e-2
+    # the gradients
+    ohq, ohs, _ = oracle.quant_128x1(dh_f, offsets)
+    dW2_ref = oracle.wgrad(oq, os_, oaq, oas, opad)
+    dW13_ref = oracle.wgrad(ohq, ohs, oxq, oxs, opad)
+    for got, ref, nm in ((dW2.cpu().numpy(), dW2_ref, "dW2"), (dW13.cpu().numpy(), dW13_ref, "dW13")):
+        for e in range(E):
+            if counts[e] == 0:
+                assert np.all(got[e] == 0)
+                continue
+            err = np.abs(got[e] - ref[e]).max() / max(np.abs(ref[e]).max(), 1e-30)
+            assert err <= TOL, (nm, e, err)
+    print(f"{name}: weight gradients within {TOL} of each expert's largest entry")
