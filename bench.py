@@ -442,6 +442,17 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
     total = t0.elapsed_time(t1) / steps
     split = {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / steps for i, n in enumerate(names)}
     gemm_ms = split["dgrad_gemm2"] + split["dgrad_gemm1"]
+    # weight gradients (four 128 x 1 operand quantisations, two grouped GEMMs)
+    for _ in range(warmup):
+        layer._weight_grads(dy, T)
+    torch.cuda.synchronize()
+    a, bb = ev(), ev()
+    a.record()
+    for _ in range(steps):
+        layer._weight_grads(dy, T)
+    bb.record()
+    torch.cuda.synchronize()
+    wg_ms = a.elapsed_time(bb) / steps
     flops = 6.0 * A * d * F
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"]
@@ -454,6 +465,9 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
            "steps": {n: {"ms": v} for n, v in split.items()},
            "dgrad_gemms": {"ms": gemm_ms, "TFLOP/s": flops / (gemm_ms * 1e-3) / 1e12,
                            "frac": flops / (gemm_ms * 1e-3) / 1e12 / fp8_peak, "peak": fp8_peak},
+           "weight_grads": {"ms": wg_ms, "TFLOP/s (dW2 + dW13 GEMMs, algorithmic)": flops / (wg_ms * 1e-3) / 1e12,
+                            "note": "includes the four 128x1 operand quantisations and the fp32 dW writes "
+                                    f"({4 * 3 * E * d * F / 1e9:.1f} GB)"},
            "status": Lb.check_status(layer.dev_status)}
     for n, nb in (("combine_bwd", b_comb), ("swiglu_bwd", b_swi), ("dispatch_bwd", b_disp)):
         out["steps"][n]["GB/s"] = nb / (split[n] * 1e-3) / 1e9

@@ -259,3 +259,58 @@ def test_weight_gradients_against_oracle(L, oracle, name, T):
             err = np.abs(got[e] - ref[e]).max() / max(np.abs(ref[e]).max(), 1e-30)
             assert err <= TOL, (nm, e, err)
     print(f"{name}: weight gradients within {TOL} of each expert's largest entry")
+
+
+def test_weight_gradients_full_size_two_experts(L, oracle):
+    """The 8192-token large layer: dW2 and dW13 of two experts (the most and
+    the least loaded) against the oracle's chain on those experts' rows
+    (every expert's gradient depends only on its own rows)."""
+    cfg = S.CONFIGS["large"]
+    from tests.test_gpu_fullsize import _layer as big_layer
+    layer = big_layer(cfg)
+    x = S.make_x(cfg, DEV)
+    layer.forward(x, train=True)
+    g = torch.Generator(device=DEV).manual_seed(12)
+    dy = torch.randn((cfg.T, cfg.d), generator=g, device=DEV).to(torch.bfloat16)
+    _, _, dW13, dW2 = layer.backward(dy, weight_grads=True)
+    torch.cuda.synchronize()
+    assert L.check_status(layer.dev_status) == 0
+    k, d, F = cfg.k, cfg.d, cfg.F
+    counts = layer.counts.cpu().numpy()
+    offsets = layer.offsets.cpu().numpy()
+    nz = np.nonzero(counts)[0]
+    experts = [int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])]
+    s2s = layer.s2s.cpu().numpy()
+    sl2 = layer.sl2.cpu().numpy()
+    for e in experts:
+        rows = np.arange(offsets[e], offsets[e + 1])
+        n = len(rows)
+        tok = s2s[rows] // k
+        slots = s2s[rows]
+        xq, xs = oracle.quant_1x128(bf16_bits(x[torch.as_tensor(tok, device=DEV)]))
+        re0 = np.zeros(n, np.int32)
+        w13q, w13s = layer.w.w13_q[e:e + 1].cpu().numpy(), layer.w.w13_s[e:e + 1].cpu().numpy()
+        w2q, w2s = layer.w.w2_q[e:e + 1].cpu().numpy(), layer.w.w2_s[e:e + 1].cpu().numpy()
+        h = oracle.expert_ffn_preact(xq, xs, re0, w13q, w13s)
+        act_f, _, _, out = oracle.expert_ffn(xq, xs, re0, w13q, w13s, w2q, w2s)
+        gts = layer.gates.reshape(-1)[torch.as_tensor(slots, device=DEV)].cpu().numpy().reshape(n, 1)
+        loc = np.arange(n, dtype=np.int32)
+        d_out_f, dq, ds, _ = oracle.combine_backward(bf16_bits(dy[torch.as_tensor(tok, device=DEV)]), gts, out, loc)
+        w2tq, w2ts = oracle.weight_transpose(w2q, w2s)
+        d_act = oracle.grouped_gemm(dq, ds, re0, w2tq, w2ts)
+        dh_f, _, _ = oracle.swiglu_backward(d_act, h)
+        x_rows = bf16_to_f64(bf16_bits(x[torch.as_tensor(tok, device=DEV)])).astype(np.float32)
+        off1 = np.array([0, n], np.int32)
+        aq, as_, pad = oracle.quant_128x1(d_out_f, off1)
+        bq, bs, _ = oracle.quant_128x1(act_f, off1)
+        ref2 = oracle.wgrad(aq, as_, bq, bs, pad)[0]
+        aq, as_, _ = oracle.quant_128x1(dh_f, off1)
+        bq, bs, _ = oracle.quant_128x1(x_rows, off1)
+        ref13 = oracle.wgrad(aq, as_, bq, bs, pad)[0]
+        for got, ref, nm in ((dW2[e].cpu().numpy(), ref2, "dW2"), (dW13[e].cpu().numpy(), ref13, "dW13")):
+            err = np.abs(got - ref).max() / np.abs(ref).max()
+            assert err <= TOL, (nm, e, n, err)
+        print(f"large wgrad: expert {e} ({n} rows) within {TOL}")
+    empty = np.nonzero(counts == 0)[0]
+    if len(empty):
+        assert float(dW2[int(empty[0])].abs().max()) == 0.0
