@@ -216,24 +216,53 @@ struct WgSrc {
     int k, F;
 };
 
+// 32 consecutive channels c0 .. c0+31 of sorted row r (16-byte loads)
 template <int SRC>
-__device__ __forceinline__ float wg_value(const WgSrc &w, int64_t r, int64_t c, int64_t C)
+__device__ __forceinline__ void wg_row32(const WgSrc &w, int64_t r, int64_t c0, int64_t C, float *v)
 {
-    if (SRC == SRC_GDY) {
+    if (SRC == SRC_GDY || SRC == SRC_X) {
         const int32_t slot = __ldg(w.sorted_to_slot + r);
-        return __ldg(w.gates + slot) * bf16_bits_to_f32(__ldg(w.dy + (int64_t)(slot / w.k) * C + c));
-    } else if (SRC == SRC_X) {
-        const int32_t slot = __ldg(w.sorted_to_slot + r);
-        return bf16_bits_to_f32(__ldg(w.x + (int64_t)(slot / w.k) * C + c));
+        const float g = SRC == SRC_GDY ? __ldg(w.gates + slot) : 1.0f;
+        const uint4 *src = reinterpret_cast<const uint4 *>((SRC == SRC_GDY ? w.dy : w.x) + (int64_t)(slot / w.k) * C + c0);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            unpack_bf16x8(__ldg(src + i), v + 8 * i);
+            if (SRC == SRC_GDY) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) v[8 * i + j] = g * v[8 * i + j];
+            }
+        }
     } else if (SRC == SRC_ACT) {
-        const float g = __ldg(w.h + r * 2 * w.F + c), u = __ldg(w.h + r * 2 * w.F + w.F + c);
-        return __fdiv_rn(g, 1.0f + expf(-g)) * u;
+        const float4 *hg = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + c0);
+        const float4 *hu = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + w.F + c0);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const float4 g4 = __ldg(hg + i), u4 = __ldg(hu + i);
+            v[4 * i + 0] = __fdiv_rn(g4.x, 1.0f + expf(-g4.x)) * u4.x;
+            v[4 * i + 1] = __fdiv_rn(g4.y, 1.0f + expf(-g4.y)) * u4.y;
+            v[4 * i + 2] = __fdiv_rn(g4.z, 1.0f + expf(-g4.z)) * u4.z;
+            v[4 * i + 3] = __fdiv_rn(g4.w, 1.0f + expf(-g4.w)) * u4.w;
+        }
     } else {
-        const int64_t f = c < w.F ? c : c - w.F;
-        const float da = bf16_bits_to_f32(__ldg(w.d_act + r * w.F + f));
-        const float g = __ldg(w.h + r * 2 * w.F + f), u = __ldg(w.h + r * 2 * w.F + w.F + f);
-        const float sg = __fdiv_rn(1.0f, 1.0f + expf(-g));
-        return c < w.F ? da * u * sg * (1.0f + g * (1.0f - sg)) : da * (g * sg);
+        const bool up_half = c0 >= w.F;
+        const int64_t f0 = up_half ? c0 - w.F : c0;
+        float da[32];
+        const uint4 *a4 = reinterpret_cast<const uint4 *>(w.d_act + r * w.F + f0);
+#pragma unroll
+        for (int i = 0; i < 4; i++) unpack_bf16x8(__ldg(a4 + i), da + 8 * i);
+        const float4 *hg = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + f0);
+        const float4 *hu = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + w.F + f0);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const float4 g4 = __ldg(hg + i), u4 = __ldg(hu + i);
+            const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, uu[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const float g = gg[j], sg = __fdiv_rn(1.0f, 1.0f + expf(-g));
+                const float a = da[4 * i + j];
+                v[4 * i + j] = up_half ? a * (g * sg) : a * uu[j] * sg * (1.0f + g * (1.0f - sg));
+            }
+        }
     }
 }
 
@@ -272,11 +301,15 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t
     {
         const int rr = tid >> 1, ch = (tid & 1) * 32;
         const int64_t r = r0 + rr;
-#pragma unroll 4
-        for (int i = 0; i < 32; i++) {
-            const int64_t c = c0 + ch + i;
-            tile[rr][ch + i] = (r < rend && c < C) ? wg_value<SRC>(w, r, c, C) : 0.0f;
+        float v[32];
+        if (r < rend) {
+            wg_row32<SRC>(w, r, c0 + ch, C, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; i++) v[i] = 0.0f;
         }
+#pragma unroll
+        for (int i = 0; i < 32; i++) tile[rr][ch + i] = v[i];
     }
     __syncthreads();
     const int cc = tid >> 2, part = tid & 3;
@@ -373,7 +406,10 @@ MOE_API moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gat
     if ((src == SRC_GDY && (!dy || !gates || !sorted_to_slot)) || (src == SRC_X && (!x || !sorted_to_slot)) ||
         (src == SRC_ACT && (!h || F <= 0 || C != F)) || (src == SRC_DH && (!h || !d_act || F <= 0 || C != 2 * F)))
         return src < 0 || src > 3 ? MOE_ERR_SHAPE : MOE_ERR_NULL;
-    if (!aligned16(q)) return MOE_ERR_ALIGN;
+    // rows are read 16 bytes at a time
+    if (!aligned16(q) || (dy && !aligned16(dy)) || (x && !aligned16(x)) || (h && !aligned16(h)) ||
+        (d_act && !aligned16(d_act)))
+        return MOE_ERR_ALIGN;
     if (max_pad == 0) return MOE_OK;
     // one CTA per (64 channels, 128-row block) of the largest possible padded
     // extent; blocks past pad[E] (known on the device only) return at once

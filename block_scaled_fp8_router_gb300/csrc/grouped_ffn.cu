@@ -609,11 +609,15 @@ struct ParamsWG {
     int E, M, N;
 };
 
+constexpr int WG_STAGES = 3;           // a tile has few K blocks (an expert's rows / 128)
+constexpr int WG_STG = 20;              // floats per row of a warp's 32 x 16 store-staging tile
+
 struct SmemWG {
-    uint8_t a[STAGES][A_BYTES];
-    uint8_t b[STAGES][B_BYTES];
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint8_t a[WG_STAGES][A_BYTES];
+    uint8_t b[WG_STAGES][B_BYTES];
+    float stage[EPI_WARPS][32 * WG_STG];   // the epilogue writes its rows through these, 64 B per row segment
+    uint64_t full[WG_STAGES];
+    uint64_t empty[WG_STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t mma_done;
@@ -656,7 +660,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles_per_e = (p.M / BM) * ((p.N + BN - 1) / BN);   // N % 256 == 128: a half last N tile
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; i++) {
+        for (int i = 0; i < WG_STAGES; i++) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
         }
@@ -700,8 +704,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 const TileWG tl = decode_tile_wg(s, p, t);
                 for (int kb = 0; kb < tl.nkb; kb++, j++) {
-                    const int st = j % STAGES;
-                    if (!wait_or_abort(&s.empty[st], ((j / STAGES) & 1) ^ 1, abort_flag, p.dev_status)) {
+                    const int st = j % WG_STAGES;
+                    if (!wait_or_abort(&s.empty[st], ((j / WG_STAGES) & 1) ^ 1, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
@@ -711,11 +715,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     issued |= 1u << st;
                 }
             }
-            for (int i = 0; i < STAGES; i++) {
+            for (int i = 0; i < WG_STAGES; i++) {
                 if (!(issued & (1u << i)) || j == 0) continue;
-                const uint32_t last = j - 1 - ((j - 1 - i) % STAGES);
+                const uint32_t last = j - 1 - ((j - 1 - i) % WG_STAGES);
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&s.full[i], (last / STAGES) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+                while (!mbar_try_wait(&s.full[i], (last / WG_STAGES) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
             }
         }
     } else if (warp == MMA_WARP) {
@@ -726,10 +730,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 const TileWG tl = decode_tile_wg(s, p, t);
                 for (int kb = 0; kb < tl.nkb; kb++, j++) {
-                    const int st = j % STAGES;
+                    const int st = j % WG_STAGES;
                     const int buf = j & 1;
                     if (!wait_or_abort(&s.tempty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.dev_status) ||
-                        !wait_or_abort(&s.full[st], (j / STAGES) & 1, abort_flag, p.dev_status)) {
+                        !wait_or_abort(&s.full[st], (j / WG_STAGES) & 1, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
@@ -792,10 +796,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!aborted && n_ok) {
-                float4 *dst = reinterpret_cast<float4 *>(p.out + ((int64_t)tl.e * p.M + m) * p.N + n0);
+                // 16 columns at a time through the warp's staging tile, so that
+                // each store instruction writes 8 rows x 64 contiguous bytes
+                float *stg = s.stage[warp];
+                const int64_t row0 = (int64_t)tl.e * p.M + (int64_t)tl.m_blk * BM + q * 32;
 #pragma unroll
-                for (int i = 0; i < 16; i++)
-                    dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                for (int h = 0; h < 4; h++) {
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        *reinterpret_cast<float4 *>(stg + lane * WG_STG + 4 * i) =
+                            make_float4(acc[16 * h + 4 * i], acc[16 * h + 4 * i + 1], acc[16 * h + 4 * i + 2],
+                                        acc[16 * h + 4 * i + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 4; it++) {
+                        const int idx = it * 32 + lane, rr = idx >> 2, c4 = idx & 3;
+                        const float4 v4 = *reinterpret_cast<const float4 *>(stg + rr * WG_STG + 4 * c4);
+                        *reinterpret_cast<float4 *>(p.out + (row0 + rr) * p.N + n0 + 16 * h + 4 * c4) = v4;
+                    }
+                    __syncwarp();
+                }
             }
             if (epi_bar_or(aborted || *abort_flag)) break;
         }

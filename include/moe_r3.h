@@ -350,7 +350,8 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  *                          0: g * dy (d_out, C = d), 1: silu(g) * u from h
  *                          (act, C = F), 2: dh from d_act and h (C = 2F),
  *                          3: x (C = d); rows map to tokens by
- *                          sorted_to_slot / k.
+ *                          sorted_to_slot / k.  C a multiple of 128; q and
+ *                          the source buffers 16-byte aligned.
  *   moe_wgrad_gemm         out[e] [M, N] fp32 = sum over e's blocks kb of
  *                          (a_s[m, kb] * b_sT[kb, n]) * P_kb(m, n) (the
  *                          forward's per-block promotion), a [M, ld], b [N,
