@@ -833,7 +833,7 @@ def main():
             "ffn_frac": rffn["frac"], "steps": rextra, "dev_status": rr["status"]}
         del rr
         torch.cuda.empty_cache()
-    if cfg.name == "large" and not args.no_backward and not main_mx:
+    if cfg.name in ("large", "large_e16") and not args.no_backward and not main_mx:
         import torch
         torch.cuda.empty_cache()
         out["backward_layer"] = run_backward(cfg, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),

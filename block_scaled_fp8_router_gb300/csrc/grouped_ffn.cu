@@ -101,6 +101,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, in
         : "memory");
 }
 
+// contiguous bytes (a multiple of 16, both addresses 16-byte aligned)
+__device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // four rows (r0..r3) of a one-row-box tensor map, 128 bytes from column x,
 // land as four consecutive 128-byte rows at dst with the map's swizzle, as
 // a four-row box would
@@ -162,6 +171,40 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
+
+// 32 TMEM lanes x 32 columns (one load, one wait)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
+{
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+                   "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+                   "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// 2-D tile store from shared memory through a tensor map (bulk async group)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// this thread's bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // 32 TMEM lanes x 16 columns into r[0..15], completion left to tmem_wait_ld32
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t *r)
@@ -586,21 +629,35 @@ static bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, cons
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor [rows, cols] (row stride = 4 cols bytes) for 32 x 32 tile
+// stores from 128-byte-swizzled shared memory
+static bool make_map_f32_store(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, void *base, uint64_t cols,
+                               uint64_t rows)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // ============================================================================
 // Weight gradients: per expert e, out[e] [M, N] fp32 = sum over e's padded
 // 128-row blocks kb of (sa[m, kb] * sb[n, kb]) * P_kb(m, n), the same 128-deep
 // block MMAs and fp32 promotion as the forward with the contraction over the
-// expert's tokens.  A = [M, ld] codes (the 128 x 1 layout of d_out or dh,
-// channel-major scales sa [M, ld/128]), B = [N, ld] (act or x, block-major
-// scales sbT [ld/128, N]: the 64 column scales a promotion thread needs for
-// one K block are contiguous).  Tiles are (expert, N block, M block), M
-// fastest; experts without rows have no tiles (their out is zeroed apart).
+// expert's tokens.  A = [M, ld] codes (the 128 x 1 layout of d_out or dh),
+// B = [N, ld] (act or x), both scale arrays block-major (saT [ld/128, M],
+// sbT [ld/128, N]: a tile's 128 row and 128 column scales of one K block are
+// contiguous).  Tiles are (expert, N block, M block), M fastest; experts
+// without rows have no tiles (their out is zeroed apart).
 // ============================================================================
 
 struct ParamsWG {
-    const float *sa;            // [M, ld/128]
+    const float *saT;           // [ld/128, M]
     const float *sbT;           // [ld/128, N]
     const int32_t *pad;         // [E+1]
     float *out;                 // [E, M, N]
@@ -609,43 +666,62 @@ struct ParamsWG {
     int E, M, N;
 };
 
-constexpr int WG_STAGES = 3;           // a tile has few K blocks (an expert's rows / 128)
-constexpr int WG_STG = 20;              // floats per row of a warp's 32 x 16 store-staging tile
+// The contraction runs over an expert's rows (a few 128-row blocks per tile),
+// so the tile's output is large next to its MMA work and the kernel is bound
+// by its fp32 stores.  128 x 128 tiles keep the promoted accumulator at 32
+// values per epilogue thread (under the 18-warp register cap), and four
+// 128-column TMEM buffers let the MMAs of the next tile run while the
+// epilogue stores this one.  The K block's row and column scales travel with
+// it: the producer copies them into a ring of shared-memory slots (its own
+// full/empty barriers), so the epilogue reads them at shared-memory latency
+// while the stores keep L2 busy.  Each epilogue warp hands its 32 x 32 fp32
+// sub-tile to a TMA store (128-byte swizzled staging, conflict-free writes)
+// and goes on to the next tile while the copy drains.
+constexpr int WG_BN = 128;
+constexpr int WG_BUFS = 4;                 // TMEM accumulators (4 x 128 columns)
+constexpr int WG_STAGES = 4;
+constexpr int WG_B_BYTES = WG_BN * BK;     // 16 KB
+constexpr int WG_SLOTS = 8;                // scale slots (K blocks the producer may run ahead of the epilogue)
 
 struct SmemWG {
     uint8_t a[WG_STAGES][A_BYTES];
-    uint8_t b[WG_STAGES][B_BYTES];
-    float stage[EPI_WARPS][32 * WG_STG];   // the epilogue writes its rows through these, 64 B per row segment
+    uint8_t b[WG_STAGES][WG_B_BYTES];
+    float stage[EPI_WARPS][32 * 32];       // a warp's 32 x 32 sub-tile for its TMA store (128-byte swizzle)
+    float sa[WG_SLOTS][BM];                // scales of K block j in slot j % WG_SLOTS: the tile's rows
+    float sb[WG_SLOTS][WG_BN];             //   and the tile's columns
     uint64_t full[WG_STAGES];
     uint64_t empty[WG_STAGES];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tfull[WG_BUFS];
+    uint64_t tempty[WG_BUFS];
+    uint64_t sfull[WG_SLOTS];
+    uint64_t sempty[WG_SLOTS];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
     int32_t tile_prefix[MAX_E + 1];
+    int32_t pad[MAX_E + 1];
 };
 constexpr size_t SMEM_WG_BYTES = sizeof(SmemWG) + 1024;
+static_assert(SMEM_WG_BYTES <= 227 * 1024, "wgrad shared memory");
+static_assert(WG_BUFS * WG_BN <= TMEM_COLS, "wgrad TMEM buffers");
 
 struct TileWG {
     int e, m_blk, n_blk;
     int kb0, nkb;   // first global K block and count
 };
 
-__device__ __forceinline__ TileWG decode_tile_wg(const SmemWG &s, const ParamsWG &p, int t)
+// every role walks its tiles in increasing order, so the expert of tile t is
+// found by advancing e from the previous tile's
+__device__ __forceinline__ TileWG decode_tile_wg(const SmemWG &s, const ParamsWG &p, int t, int &e)
 {
-    int lo = 0, hi = p.E;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s.tile_prefix[mid] <= t) lo = mid; else hi = mid;
-    }
+    while (e + 1 < p.E && s.tile_prefix[e + 1] <= t) e++;
     TileWG tl;
-    tl.e = lo;
+    tl.e = e;
     const int m_tiles = p.M / BM;
-    const int local = t - s.tile_prefix[lo];
+    const int local = t - s.tile_prefix[e];
     tl.n_blk = local / m_tiles;
     tl.m_blk = local - tl.n_blk * m_tiles;
-    const int32_t p0 = __ldg(p.pad + lo), p1 = __ldg(p.pad + lo + 1);
+    const int32_t p0 = s.pad[e], p1 = s.pad[e + 1];
     tl.kb0 = p0 / 128;
     tl.nkb = (p1 - p0) / 128;
     return tl;
@@ -653,20 +729,24 @@ __device__ __forceinline__ TileWG decode_tile_wg(const SmemWG &s, const ParamsWG
 
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                         const ParamsWG p)
+                         const __grid_constant__ CUtensorMap tm_out, const ParamsWG p)
 {
     extern __shared__ uint8_t smem_raw[];
     SmemWG &s = *reinterpret_cast<SmemWG *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_per_e = (p.M / BM) * ((p.N + BN - 1) / BN);   // N % 256 == 128: a half last N tile
+    const int tiles_per_e = (p.M / BM) * (p.N / WG_BN);
     if (threadIdx.x == 0) {
         for (int i = 0; i < WG_STAGES; i++) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
         }
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < WG_BUFS; i++) {
             mbar_init(&s.tfull[i], 1);
             mbar_init(&s.tempty[i], EPI_WARPS);
+        }
+        for (int i = 0; i < WG_SLOTS; i++) {
+            mbar_init(&s.sfull[i], 1);
+            mbar_init(&s.sempty[i], EPI_WARPS);
         }
         mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
@@ -674,11 +754,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 0) {
-        // tile prefix over experts with rows (warp-wide scan)
+        // tile prefix over experts with rows (warp-wide scan); the scale
+        // copies are not bounds-checked, so offsets outside [0, ld] or off
+        // the 128-row grid run no tile at all and set MOE_DEV_ROWS
         int32_t carry = 0;
+        bool bad = false;
         for (int base = 0; base <= p.E; base += 32) {
             const int e = base + lane;
-            const int32_t tiles = (e < p.E && __ldg(p.pad + e + 1) > __ldg(p.pad + e)) ? tiles_per_e : 0;
+            int32_t tiles = 0;
+            if (e <= p.E) s.pad[e] = __ldg(p.pad + e);
+            if (e < p.E) {
+                const int32_t p0 = __ldg(p.pad + e), p1 = __ldg(p.pad + e + 1);
+                bad |= p0 < 0 || (int64_t)p1 > p.ld || (p0 & 127) != 0 || (p1 & 127) != 0;
+                tiles = p1 > p0 ? tiles_per_e : 0;
+            }
             int32_t incl = tiles;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -687,6 +776,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (e <= p.E) s.tile_prefix[e] = carry + incl - tiles;
             carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) {
+            s.tile_prefix[p.E] = 0;
+            if (blockIdx.x == 0) dev_flag(p.dev_status, MOE_DEV_ROWS);
         }
     }
     if (warp == MMA_WARP) tmem_alloc(&s.tmem_base, TMEM_COLS);
@@ -699,40 +792,54 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
-            uint32_t j = 0, issued = 0;
+            uint32_t j = 0;
+            int ecur = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileWG tl = decode_tile_wg(s, p, t);
+                const TileWG tl = decode_tile_wg(s, p, t, ecur);
                 for (int kb = 0; kb < tl.nkb; kb++, j++) {
-                    const int st = j % WG_STAGES;
-                    if (!wait_or_abort(&s.empty[st], ((j / WG_STAGES) & 1) ^ 1, abort_flag, p.dev_status)) {
+                    const int st = j % WG_STAGES, sl = j % WG_SLOTS;
+                    const int64_t kg = tl.kb0 + kb;
+                    // both waits come before any copy of block j, so that an
+                    // abort leaves exactly blocks 0 .. j-1 issued
+                    if (!wait_or_abort(&s.empty[st], ((j / WG_STAGES) & 1) ^ 1, abort_flag, p.dev_status) ||
+                        !wait_or_abort(&s.sempty[sl], ((j / WG_SLOTS) & 1) ^ 1, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES);
-                    tma_load_2d(s.a[st], &tm_a, (tl.kb0 + kb) * BK, tl.m_blk * BM, &s.full[st]);
-                    tma_load_2d(s.b[st], &tm_b, (tl.kb0 + kb) * BK, tl.n_blk * BN, &s.full[st]);
-                    issued |= 1u << st;
+                    mbar_arrive_expect_tx(&s.full[st], A_BYTES + WG_B_BYTES);
+                    tma_load_2d(s.a[st], &tm_a, (int)kg * BK, tl.m_blk * BM, &s.full[st]);
+                    tma_load_2d(s.b[st], &tm_b, (int)kg * BK, tl.n_blk * WG_BN, &s.full[st]);
+                    mbar_arrive_expect_tx(&s.sfull[sl], (BM + WG_BN) * 4);
+                    bulk_load_1d(s.sa[sl], p.saT + kg * p.M + (int64_t)tl.m_blk * BM, BM * 4, &s.sfull[sl]);
+                    bulk_load_1d(s.sb[sl], p.sbT + kg * p.N + (int64_t)tl.n_blk * WG_BN, WG_BN * 4, &s.sfull[sl]);
                 }
             }
-            for (int i = 0; i < WG_STAGES; i++) {
-                if (!(issued & (1u << i)) || j == 0) continue;
+            // no copy may still be in flight when the CTA exits: wait for the
+            // last block issued into each stage and each scale slot
+            for (int i = 0; i < WG_STAGES && (uint32_t)i < j; i++) {
                 const uint32_t last = j - 1 - ((j - 1 - i) % WG_STAGES);
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(&s.full[i], (last / WG_STAGES) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
             }
+            for (int i = 0; i < WG_SLOTS && (uint32_t)i < j; i++) {
+                const uint32_t last = j - 1 - ((j - 1 - i) % WG_SLOTS);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&s.sfull[i], (last / WG_SLOTS) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
+            }
         }
     } else if (warp == MMA_WARP) {
         if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_f8(BM, BN);
+            constexpr uint32_t IDESC = idesc_f8(BM, WG_BN);
             uint32_t j = 0;
+            int ecur = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileWG tl = decode_tile_wg(s, p, t);
+                const TileWG tl = decode_tile_wg(s, p, t, ecur);
                 for (int kb = 0; kb < tl.nkb; kb++, j++) {
                     const int st = j % WG_STAGES;
-                    const int buf = j & 1;
-                    if (!wait_or_abort(&s.tempty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.dev_status) ||
+                    const int buf = j % WG_BUFS;
+                    if (!wait_or_abort(&s.tempty[buf], ((j / WG_BUFS) & 1) ^ 1, abort_flag, p.dev_status) ||
                         !wait_or_abort(&s.full[st], (j / WG_STAGES) & 1, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
@@ -742,7 +849,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint64_t bdesc = sw128_desc(smem_u32(s.b[st]));
 #pragma unroll
                     for (int ks = 0; ks < BK / 32; ks++)
-                        mma_f8(tmem + buf * BN, adesc + 2 * ks, bdesc + 2 * ks, IDESC, ks > 0);
+                        mma_f8(tmem + buf * WG_BN, adesc + 2 * ks, bdesc + 2 * ks, IDESC, ks > 0);
                     mma_commit(&s.empty[st]);
                     mma_commit(&s.tfull[buf]);
                 }
@@ -753,72 +860,64 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
     } else if (warp < EPI_WARPS) {
+        // warp (q, cg): TMEM lanes 32q .. 32q+31 (the tile's rows), columns 32cg .. 32cg+31
         const int q = warp & 3, cg = warp >> 2;
-        const int r_in = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        const int64_t nbk = p.ld / 128;
+        float *stg = s.stage[warp];
         uint32_t j = 0;
+        int ecur = 0;
         bool aborted = false;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const TileWG tl = decode_tile_wg(s, p, t);
-            const int64_t m = (int64_t)tl.m_blk * BM + r_in;
-            const int64_t n0 = (int64_t)tl.n_blk * BN + 64 * cg;
-            const bool n_ok = n0 < p.N;    // past N only in the half last tile (B rows zero-filled there)
-            float acc[64];
+            const TileWG tl = decode_tile_wg(s, p, t, ecur);
+            float acc[32];
 #pragma unroll
-            for (int i = 0; i < 64; i++) acc[i] = 0.0f;
+            for (int i = 0; i < 32; i++) acc[i] = 0.0f;
             for (int kb = 0; kb < tl.nkb; kb++, j++) {
-                const int buf = j & 1;
-                const int64_t kg = tl.kb0 + kb;
-                const float sa = __ldg(p.sa + m * nbk + kg);
-                const float4 *sb4 = reinterpret_cast<const float4 *>(p.sbT + kg * p.N + (n_ok ? n0 : 0));
-                if (!aborted && !wait_or_abort(&s.tfull[buf], (j >> 1) & 1, abort_flag, p.dev_status))
+                const int buf = j % WG_BUFS, sl = j % WG_SLOTS;
+                if (!aborted && (!wait_or_abort(&s.sfull[sl], (j / WG_SLOTS) & 1, abort_flag, p.dev_status) ||
+                                 !wait_or_abort(&s.tfull[buf], (j / WG_BUFS) & 1, abort_flag, p.dev_status)))
                     aborted = true;
                 if (!aborted) {
                     tc_fence_after();
-                    const uint32_t base = tmem + lane_addr + buf * BN + 64 * cg;
-                    float v[16];
+                    float v[32];
+                    tmem_ld32(tmem + lane_addr + buf * WG_BN + 32 * cg, v);
+                    const float sa = s.sa[sl][q * 32 + lane];
+                    const float4 *sb4 = reinterpret_cast<const float4 *>(&s.sb[sl][32 * cg]);
 #pragma unroll
-                    for (int h = 0; h < 4; h++) {
-                        tmem_ld16(base + 16 * h, v);
-#pragma unroll
-                        for (int i4 = 0; i4 < 4; i4++) {
-                            const float4 b = n_ok ? __ldg(sb4 + 4 * h + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            acc[16 * h + 4 * i4 + 0] = fmaf(sa * b.x, v[4 * i4 + 0], acc[16 * h + 4 * i4 + 0]);
-                            acc[16 * h + 4 * i4 + 1] = fmaf(sa * b.y, v[4 * i4 + 1], acc[16 * h + 4 * i4 + 1]);
-                            acc[16 * h + 4 * i4 + 2] = fmaf(sa * b.z, v[4 * i4 + 2], acc[16 * h + 4 * i4 + 2]);
-                            acc[16 * h + 4 * i4 + 3] = fmaf(sa * b.w, v[4 * i4 + 3], acc[16 * h + 4 * i4 + 3]);
-                        }
+                    for (int i4 = 0; i4 < 8; i4++) {
+                        const float4 b = sb4[i4];
+                        acc[4 * i4 + 0] = fmaf(sa * b.x, v[4 * i4 + 0], acc[4 * i4 + 0]);
+                        acc[4 * i4 + 1] = fmaf(sa * b.y, v[4 * i4 + 1], acc[4 * i4 + 1]);
+                        acc[4 * i4 + 2] = fmaf(sa * b.z, v[4 * i4 + 2], acc[4 * i4 + 2]);
+                        acc[4 * i4 + 3] = fmaf(sa * b.w, v[4 * i4 + 3], acc[4 * i4 + 3]);
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&s.tempty[buf]);
+                    if (lane == 0) {
+                        mbar_arrive(&s.tempty[buf]);
+                        mbar_arrive(&s.sempty[sl]);
+                    }
                 }
             }
-            if (!aborted && n_ok) {
-                // 16 columns at a time through the warp's staging tile, so that
-                // each store instruction writes 8 rows x 64 contiguous bytes
-                float *stg = s.stage[warp];
-                const int64_t row0 = (int64_t)tl.e * p.M + (int64_t)tl.m_blk * BM + q * 32;
+            if (!aborted) {
+                // the previous tile's store has read the staging tile; row
+                // `lane` goes in with the 128-byte swizzle (16-byte chunk c of
+                // row r at chunk c ^ (r & 7)), then one TMA store of 32 x 32
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
 #pragma unroll
-                for (int h = 0; h < 4; h++) {
-#pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        *reinterpret_cast<float4 *>(stg + lane * WG_STG + 4 * i) =
-                            make_float4(acc[16 * h + 4 * i], acc[16 * h + 4 * i + 1], acc[16 * h + 4 * i + 2],
-                                        acc[16 * h + 4 * i + 3]);
-                    __syncwarp();
-#pragma unroll
-                    for (int it = 0; it < 4; it++) {
-                        const int idx = it * 32 + lane, rr = idx >> 2, c4 = idx & 3;
-                        const float4 v4 = *reinterpret_cast<const float4 *>(stg + rr * WG_STG + 4 * c4);
-                        *reinterpret_cast<float4 *>(p.out + (row0 + rr) * p.N + n0 + 16 * h + 4 * c4) = v4;
-                    }
-                    __syncwarp();
-                }
+                for (int i = 0; i < 8; i++)
+                    *reinterpret_cast<float4 *>(stg + lane * 32 + 4 * (i ^ (lane & 7))) =
+                        make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    tma_store_2d(&tm_out, stg, tl.n_blk * WG_BN + 32 * cg, tl.e * p.M + tl.m_blk * BM + q * 32);
             }
             if (epi_bar_or(aborted || *abort_flag)) break;
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -1396,21 +1495,25 @@ MOE_API moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x
     return launch_status();
 }
 
-MOE_API moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_s, const uint8_t *b_q, const float *b_sT,
+MOE_API moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_sT, const uint8_t *b_q, const float *b_sT,
                                   const int32_t *pad, int E, int M, int N, int64_t ld, float *out,
                                   int32_t *dev_status, void *stream)
 {
     if (E < 1 || E > MAX_E || M <= 0 || N <= 0 || M % BM != 0 || N % 128 != 0 || ld <= 0 || ld % 128 != 0 ||
         ld >= (1LL << 31) || (int64_t)M >= (1LL << 31) || (int64_t)N >= (1LL << 31))
         return MOE_ERR_SHAPE;
-    if (!a_q || !a_s || !b_q || !b_sT || !pad || !out) return MOE_ERR_NULL;
-    if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(out) || !aligned16(b_sT)) return MOE_ERR_ALIGN;
+    if (!a_q || !a_sT || !b_q || !b_sT || !pad || !out) return MOE_ERR_NULL;
+    if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(out) || !aligned16(a_sT) || !aligned16(b_sT))
+        return MOE_ERR_ALIGN;
     auto enc = encode_fn();
     if (!enc) return MOE_ERR_CUDA;
     CUtensorMap ma, mb;
-    if (!make_map(enc, &ma, a_q, ld, M, 128) || !make_map(enc, &mb, b_q, ld, N, 256)) return MOE_ERR_CUDA;
+    CUtensorMap mo;
+    if (!make_map(enc, &ma, a_q, ld, M, BM) || !make_map(enc, &mb, b_q, ld, N, WG_BN) ||
+        !make_map_f32_store(enc, &mo, out, (uint64_t)N, (uint64_t)E * M))
+        return MOE_ERR_CUDA;
     ParamsWG prm;
-    prm.sa = a_s;
+    prm.saT = a_sT;
     prm.sbT = b_sT;
     prm.pad = pad;
     prm.out = out;
@@ -1424,6 +1527,6 @@ MOE_API moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_s, const ui
         return MOE_ERR_CUDA;
     cudaStream_t st = as_stream(stream);
     wgrad_zero_empty_kernel<<<dim3(64, (unsigned)E), 256, 0, st>>>(pad, (int64_t)M * N, out);
-    grouped_wgrad_kernel<<<sm_count(), THREADS, SMEM_WG_BYTES, st>>>(ma, mb, prm);
+    grouped_wgrad_kernel<<<sm_count(), THREADS, SMEM_WG_BYTES, st>>>(ma, mb, mo, prm);
     return launch_status();
 }

@@ -227,16 +227,16 @@ class MoELayerFP8:
         pad = L.moe_wgrad_pad_offsets(self.offsets, pad=w["pad"])
         s2s = self.s2s[:A]
         # dW2 = d_out^T act
-        aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_GDY, self.offsets, pad, d, ld, False, dy=dy, gates=self.gates[:T],
+        aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_GDY, self.offsets, pad, d, ld, True, dy=dy, gates=self.gates[:T],
                                     sorted_to_slot=s2s, k=self.k, q=w["aq"][:d],
-                                    scales=w["as_"][:d * (ld // 128)].view(d, ld // 128))
+                                    scales=w["as_"][:d * (ld // 128)].view(ld // 128, d))
         bq, bs = L.moe_wgrad_quant(L.WGRAD_SRC_ACT, self.offsets, pad, F, ld, True, h=self.h, F=F, q=w["bq"][:F],
                                    scales=w["bs"][:F * (ld // 128)].view(ld // 128, F))
         L.moe_wgrad_gemm(aq, as_, bq, bs, pad, out=w["dW2"], dev_status=self.dev_status)
         # dW13 = dh^T x
-        aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_DH, self.offsets, pad, 2 * F, ld, False, h=self.h,
+        aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_DH, self.offsets, pad, 2 * F, ld, True, h=self.h,
                                     d_act=b["d_act"], F=F, q=w["aq"][:2 * F],
-                                    scales=w["as_"][:2 * F * (ld // 128)].view(2 * F, ld // 128))
+                                    scales=w["as_"][:2 * F * (ld // 128)].view(ld // 128, 2 * F))
         bq, bs = L.moe_wgrad_quant(L.WGRAD_SRC_X, self.offsets, pad, d, ld, True, x=self._x_train,
                                    sorted_to_slot=s2s, k=self.k, q=w["bq"][:d],
                                    scales=w["bs"][:d * (ld // 128)].view(ld // 128, d))

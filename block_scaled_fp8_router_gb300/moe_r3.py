@@ -539,18 +539,19 @@ def moe_wgrad_quant(src, expert_offsets, pad, C, ld, kb_major, dy=None, gates=No
     return q, scales
 
 
-def moe_wgrad_gemm(a_q, a_s, b_q, b_sT, pad, out=None, dev_status=None, stream=None):
-    """out [E, M, N] fp32: per expert the weight gradient over its rows."""
+def moe_wgrad_gemm(a_q, a_sT, b_q, b_sT, pad, out=None, dev_status=None, stream=None):
+    """out [E, M, N] fp32: per expert the weight gradient over its rows
+    (both operands' scales kb-major, [ld/128, M] and [ld/128, N])."""
     M, ld = a_q.shape
     N = b_q.shape[0]
     E = pad.numel() - 1
     _want(a_q, torch.uint8, (M, ld), "a_q")
-    _want(a_s, torch.float32, (M, ld // 128), "a_s")
+    _want(a_sT, torch.float32, (ld // 128, M), "a_sT")
     _want(b_q, torch.uint8, (N, ld), "b_q")
     _want(b_sT, torch.float32, (ld // 128, N), "b_sT")
     out = _empty((E, M, N), torch.float32, a_q) if out is None else out
     _want(out, torch.float32, (E, M, N), "out")
-    _check("moe_wgrad_gemm", _lib.moe_wgrad_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_sT), _ptr(pad), E, M, N, ld,
+    _check("moe_wgrad_gemm", _lib.moe_wgrad_gemm(_ptr(a_q), _ptr(a_sT), _ptr(b_q), _ptr(b_sT), _ptr(pad), E, M, N, ld,
                                                  _ptr(out), _ptr(dev_status), _stream(stream)))
     return out
 

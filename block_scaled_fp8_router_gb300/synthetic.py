@@ -73,6 +73,10 @@ CONFIGS = {
     # per expert, d=7168, F=2048) with a quarter of the experts and tokens, so
     # that a profiler capture holds ~3.5 GB instead of ~14 GB
     "large_e64": MoEConfig("large_e64", 2048, 7168, 64, 8, 2048, SIGMOID, "route", "router", w_std=0.006),
+    # weight-gradient profiling shape: the same per-expert shape with 16
+    # experts, so that dW13 [16, 4096, 7168] and dW2 [16, 7168, 2048] fp32
+    # hold ~2.8 GB
+    "large_e16": MoEConfig("large_e16", 512, 7168, 16, 8, 2048, SIGMOID, "route", "router", w_std=0.006),
 }
 
 

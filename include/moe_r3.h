@@ -353,10 +353,14 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  *                          sorted_to_slot / k.  C a multiple of 128; q and
  *                          the source buffers 16-byte aligned.
  *   moe_wgrad_gemm         out[e] [M, N] fp32 = sum over e's blocks kb of
- *                          (a_s[m, kb] * b_sT[kb, n]) * P_kb(m, n) (the
+ *                          (a_sT[kb, m] * b_sT[kb, n]) * P_kb(m, n) (the
  *                          forward's per-block promotion), a [M, ld], b [N,
- *                          ld]; M, N multiples of 128; experts without rows
- *                          get zeros.
+ *                          ld], both scale arrays kb-major [ld/128, *] (as
+ *                          moe_wgrad_quant writes them with scales_kb_major);
+ *                          M, N multiples of 128; experts without rows get
+ *                          zeros; pad entries outside [0, ld] or not
+ *                          multiples of 128 run no tile and set
+ *                          MOE_DEV_ROWS.
  * The router's backward is not provided (d_gates are returned for it).
  * Errors: NULL, SHAPE, ALIGN, CUDA (WORKSPACE for the _train call).
  * ---------------------------------------------------------------------- */
@@ -382,7 +386,7 @@ moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gates, cons
                            const int32_t *sorted_to_slot, int k, const float *h, const uint16_t *d_act, int F,
                            const int32_t *expert_offsets, const int32_t *pad, int E, int64_t C, int64_t ld,
                            int scales_kb_major, uint8_t *q, float *scales, void *stream);
-moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_s, const uint8_t *b_q, const float *b_sT,
+moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_sT, const uint8_t *b_q, const float *b_sT,
                           const int32_t *pad, int E, int M, int N, int64_t ld, float *out, int32_t *dev_status,
                           void *stream);
 

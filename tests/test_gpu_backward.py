@@ -235,11 +235,15 @@ def test_weight_gradients_against_oracle(L, oracle, name, T):
     ld = L.wgrad_ld(A, E)
     gq, gs = L.moe_wgrad_quant(L.WGRAD_SRC_GDY, layer.offsets, pad, d, ld, False, dy=dy, gates=layer.gates[:Tn],
                                sorted_to_slot=layer.s2s[:A], k=k)
+    gq2, gs2 = L.moe_wgrad_quant(L.WGRAD_SRC_GDY, layer.offsets, pad, d, ld, True, dy=dy, gates=layer.gates[:Tn],
+                                 sorted_to_slot=layer.s2s[:A], k=k)
     oq, os_, opad = oracle.quant_128x1(d_out_f, offsets)
     np.testing.assert_array_equal(pad.cpu().numpy(), opad)
     P = int(opad[-1])
     np.testing.assert_array_equal(gq.cpu().numpy()[:, :P], oq)
     np.testing.assert_array_equal(gs.cpu().numpy()[:, :P // 128], os_)
+    np.testing.assert_array_equal(gq2.cpu().numpy()[:, :P], oq)                  # both scale layouts
+    np.testing.assert_array_equal(gs2.cpu().numpy()[:P // 128].T, os_)
     xq2, xs2 = L.moe_wgrad_quant(L.WGRAD_SRC_X, layer.offsets, pad, d, ld, True, x=x, sorted_to_slot=layer.s2s[:A], k=k)
     oxq, oxs, _ = oracle.quant_128x1(x_rows, offsets)
     np.testing.assert_array_equal(xq2.cpu().numpy()[:, :P], oxq)
@@ -314,3 +318,21 @@ def test_weight_gradients_full_size_two_experts(L, oracle):
     empty = np.nonzero(counts == 0)[0]
     if len(empty):
         assert float(dW2[int(empty[0])].abs().max()) == 0.0
+
+
+def test_wgrad_gemm_rejects_offsets_past_ld(L):
+    """Padded offsets beyond the operands' ld are caught on the device: no
+    tile runs (nothing is read past the scale arrays) and MOE_DEV_ROWS is
+    set; the output of the experts with rows is left untouched."""
+    E, M, N, ld = 2, 128, 128, 256
+    a_q = torch.zeros((M, ld), dtype=torch.uint8, device=DEV)
+    b_q = torch.zeros((N, ld), dtype=torch.uint8, device=DEV)
+    a_sT = torch.ones((ld // 128, M), dtype=torch.float32, device=DEV)
+    b_sT = torch.ones((ld // 128, N), dtype=torch.float32, device=DEV)
+    pad = torch.tensor([0, 128, 384], dtype=torch.int32, device=DEV)
+    out = torch.full((E, M, N), 7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_wgrad_gemm(a_q, a_sT, b_q, b_sT, pad, out=out, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & L.MOE_DEV_ROWS
+    assert torch.all(out == 7.0)
