@@ -69,11 +69,12 @@ struct Smem {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
-    float red[4][BM];                   // GEMM1: per-column-group partial amax
+    float red[2][4][BM];                // GEMM1: per-column-group partial amax (by tile parity)
     int32_t tile_prefix[MAX_E + 1];     // tiles before expert e
     int32_t row_lo[MAX_E + 1];          // clipped expert row ranges
 };
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "GEMM shared memory");
 
 struct Params {
     const float *a_scales;      // [max_rows, K/128]
@@ -231,19 +232,18 @@ __device__ __forceinline__ void tmem_wait_ld32(uint32_t *r)
                  : "memory");
 }
 
-// barrier over the 16 epilogue warps that also ORs a predicate across them
-__device__ __forceinline__ bool epi_bar_or(bool pred)
+// barrier over the four epilogue warps of TMEM lane quarter q (warps q, q+4,
+// q+8, q+12; named barrier 2+q) that also ORs a predicate across them
+__device__ __forceinline__ bool quarter_bar_or(int q, bool pred)
 {
     uint32_t out;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-                 "barrier.cta.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+    asm volatile("{\n\t.reg .pred p, r;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "barrier.cta.red.or.pred r, %2, 128, p;\n\tselp.u32 %0, 1, 0, r;\n\t}"
                  : "=r"(out)
-                 : "r"((uint32_t)pred), "n"(EPI_WARPS * 32)
+                 : "r"((uint32_t)pred), "r"(2 + q)
                  : "memory");
     return out != 0;
 }
-
-__device__ __forceinline__ void epi_bar() { asm volatile("barrier.cta.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory"); }
 
 // K-major operand tile in shared memory written by TMA with 128-byte
 // swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked along
@@ -483,6 +483,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int nkb_a = K / 128;     // A scale row length
         uint32_t j = 0;
         bool aborted = false;
+        bool stop = false;     // GEMM1: abort decided at the row quarter's amax exchange
+        int red_par = 0;       // GEMM1: exchange buffer of this tile
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile tl = decode_tile(s, p.E, n_tiles, t);
             const bool row_ok = r_in < tl.rows;
@@ -519,18 +521,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!aborted) {
                     tc_fence_after();
                     const uint32_t base = tmem + lane_addr + buf * BN;
+                    // acc += c * v, two columns per packed instruction (each
+                    // lane of the pair rounded as the scalar fmaf)
+                    const float2 c02 = make_float2(c0, c0), c12 = make_float2(c1, c1);
                     float v[16];
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
                         tmem_ld16(base + col0 + 16 * h, v);
 #pragma unroll
-                        for (int i = 0; i < 16; i++) acc0[16 * h + i] = fmaf(c0, v[i], acc0[16 * h + i]);
+                        for (int i = 0; i < 16; i += 2) {
+                            const float2 r = __ffma2_rn(c02, make_float2(v[i], v[i + 1]),
+                                                        make_float2(acc0[16 * h + i], acc0[16 * h + i + 1]));
+                            acc0[16 * h + i] = r.x;
+                            acc0[16 * h + i + 1] = r.y;
+                        }
                     }
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
                         tmem_ld16(base + col1 + 16 * h, v);
 #pragma unroll
-                        for (int i = 0; i < 16; i++) acc1[16 * h + i] = fmaf(c1, v[i], acc1[16 * h + i]);
+                        for (int i = 0; i < 16; i += 2) {
+                            const float2 r = __ffma2_rn(c12, make_float2(v[i], v[i + 1]),
+                                                        make_float2(acc1[16 * h + i], acc1[16 * h + i + 1]));
+                            acc1[16 * h + i] = r.x;
+                            acc1[16 * h + i + 1] = r.y;
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -556,9 +571,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     acc0[i] = __fdiv_rn(g, 1.0f + expf(-g)) * acc1[i];
                     amax = fmaxf(amax, fabsf(acc0[i]));
                 }
-                s.red[cg][r_in] = amax;
-                epi_bar();
-                amax = fmaxf(fmaxf(s.red[0][r_in], s.red[1][r_in]), fmaxf(s.red[2][r_in], s.red[3][r_in]));
+                // the row's amax over the four column groups: the warps of
+                // row quarter q meet at their own barrier, which also ORs
+                // their abort state so that they leave together; the
+                // exchange buffer alternates by tile, so the next tile's
+                // writes never meet this tile's reads
+                s.red[red_par][cg][r_in] = amax;
+                stop = quarter_bar_or(q, aborted || *abort_flag);
+                amax = fmaxf(fmaxf(s.red[red_par][0][r_in], s.red[red_par][1][r_in]),
+                             fmaxf(s.red[red_par][2][r_in], s.red[red_par][3][r_in]));
+                red_par ^= 1;
                 const float sc = block_scale(amax);
                 if (row_ok && !aborted) {
                     uint32_t w[8];
@@ -591,9 +613,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                 pack_bf16x2(acc1[8 * i + 6], acc1[8 * i + 7]));
                 }
             }
-            // uniform decision across the epilogue warps (also separates the
-            // red[] reads of this tile from the writes of the next)
-            if (epi_bar_or(aborted || *abort_flag)) break;
+            // GEMM1 leaves by its row quarter's decision; GEMM2's warps share
+            // nothing within a tile and leave on their own (waits are bounded)
+            if (MODE == 1 ? stop : (aborted || *abort_flag)) break;
         }
     }
 
@@ -914,7 +936,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0)
                     tma_store_2d(&tm_out, stg, tl.n_blk * WG_BN + 32 * cg, tl.e * p.M + tl.m_blk * BM + q * 32);
             }
-            if (epi_bar_or(aborted || *abort_flag)) break;
+            // no barrier between the epilogue warps: they share no staging, so
+            // each runs ahead until the TMEM ring stops it, and leaves on its
+            // own abort (every wait is bounded)
+            if (aborted || *abort_flag) break;
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -975,11 +1000,12 @@ struct SmemMX {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
-    float red[4][BM];
+    float red[2][4][BM];
     int32_t tile_prefix[MAX_E + 1];
     int32_t row_lo[MAX_E + 1];
 };
 constexpr size_t SMEM_MX_BYTES = sizeof(SmemMX) + 1024;
+static_assert(SMEM_MX_BYTES <= 227 * 1024, "block-scaled GEMM shared memory");
 
 struct ParamsMX {
     const uint8_t *a_exp;       // GEMM1: token-major [T, d/128]; GEMM2: sorted [max_rows, F/128]
@@ -1196,6 +1222,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         uint32_t tcount = 0;
         bool aborted = false;
+        bool stop = false;     // GEMM1: abort decided at the row quarter's amax exchange
+        int red_par = 0;       // GEMM1: exchange buffer of this tile
         for (int t = blockIdx.x; t < total; t += gridDim.x, tcount++) {
             const Tile tl = decode_tile(s, p.E, n_tiles, t);
             const bool row_ok = r_in < tl.rows;
@@ -1231,9 +1259,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     acc0[i] = __fdiv_rn(g, 1.0f + expf(-g)) * acc1[i];
                     amax = fmaxf(amax, fabsf(acc0[i]));
                 }
-                s.red[cg][r_in] = amax;
-                epi_bar();
-                amax = fmaxf(fmaxf(s.red[0][r_in], s.red[1][r_in]), fmaxf(s.red[2][r_in], s.red[3][r_in]));
+                // the row's amax over the four column groups: the warps of
+                // row quarter q meet at their own barrier, which also ORs
+                // their abort state so that they leave together; the
+                // exchange buffer alternates by tile, so the next tile's
+                // writes never meet this tile's reads
+                s.red[red_par][cg][r_in] = amax;
+                stop = quarter_bar_or(q, aborted || *abort_flag);
+                amax = fmaxf(fmaxf(s.red[red_par][0][r_in], s.red[red_par][1][r_in]),
+                             fmaxf(s.red[red_par][2][r_in], s.red[red_par][3][r_in]));
+                red_par ^= 1;
                 const uint32_t e8 = ue8m0_exp_of(amax);
                 const float sc = e8 == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e8 << 23);
                 if (row_ok && !aborted) {
@@ -1267,7 +1302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                 pack_bf16x2(acc1[8 * i + 6], acc1[8 * i + 7]));
                 }
             }
-            if (epi_bar_or(aborted || *abort_flag)) break;
+            if (MODE == 1 ? stop : (aborted || *abort_flag)) break;
         }
     }
 
