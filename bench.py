@@ -43,9 +43,9 @@ sys.path.insert(0, ROOT)
 L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes (read + write) per routed row of the grouped FFN at d=7168, F=2048,
 # ~256 rows per expert: ncu capture of grouped_gemm_kernel<1> and <2> on the
-# large_e64 profiling shape (A = 16384 rows): 2.778e9 + 0.055e9 + 0.975e9 +
+# large_e64 profiling shape (A = 16384 rows): 2.649e9 + 0.051e9 + 0.975e9 +
 # 0.217e9 bytes.  Valid for the kernel that capture measured.
-FFN_DRAM_BYTES_PER_ROW = (2.778e9 + 0.0554e9 + 0.975e9 + 0.2168e9) / 16384
+FFN_DRAM_BYTES_PER_ROW = (2.6488e9 + 0.0510e9 + 0.9750e9 + 0.2169e9) / 16384
 KERNELS_PER_STEP = {"route": 1, "replay": 1, "quant": 1, "dispatch": 4, "ffn": 2, "combine": 1}
 
 
