@@ -266,40 +266,48 @@ __device__ __forceinline__ void wg_row32(const WgSrc &w, int64_t r, int64_t c0, 
     }
 }
 
+// the transpose tile: row stride 65 words, and each 32-row group shifted by 8
+// more words, so that the column reads (8 channels x 4 row groups per warp)
+// and the row writes (32 rows per warp) hit 32 distinct banks
+__device__ __forceinline__ int q1_idx(int r, int c) { return r * 65 + c + (r >> 5) * 8; }
+constexpr int Q1_TILE = 127 * 65 + 64 + 3 * 8;
+
 // One CTA per (64 channels, padded 128-row block): the block's values are
 // staged in shared memory, each channel's amax over the expert's rows is a
 // 4-thread reduction, and each thread writes 32 codes of one channel (the
 // 128 codes of a channel are one contiguous 128-byte run of q).
-// Scales channel-major sc[c * ld/128 + kb] (the GEMM's A side: one scale per
-// row of the MMA tile per K block) or block-major sc[kb * C + c] (the B side:
-// the 64 columns a promotion thread needs for one K block are contiguous).
+// Scales channel-major sc[c * ld/128 + kb] or block-major sc[kb * C + c] (the
+// layout the weight-gradient GEMM takes for both operands: a tile's 128
+// scales of one K block are one contiguous 512-byte run).
 template <int SRC>
 __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t *__restrict__ offsets,
                                                           const int32_t *__restrict__ pad, int E, int64_t C,
                                                           int64_t ld, bool kb_major, uint8_t *__restrict__ q,
                                                           float *__restrict__ sc)
 {
-    __shared__ float tile[128][65];
-    __shared__ int s_e;
-    const int64_t P = pad[E];
+    __shared__ float tile[Q1_TILE];
+    __shared__ int64_t s_r0, s_rend;
+    const int64_t P = __ldg(pad + E);
     const int64_t kb = blockIdx.y;
     if (kb * 128 >= P || kb * 128 >= ld) return;
-    if (threadIdx.x == 0) {
-        int lo = 0, hi = E;  // expert with pad[e] <= 128 kb < pad[e+1]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (pad[mid] <= kb * 128) lo = mid; else hi = mid;
+    // the expert with pad[e] <= 128 kb < pad[e+1] (E <= 1024: each thread
+    // checks up to four experts with independent loads; with offsets from
+    // moe_wgrad_pad_offsets exactly one matches, otherwise the block is empty)
+    if (threadIdx.x == 0) s_r0 = s_rend = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t p0 = __ldg(pad + e), p1 = __ldg(pad + e + 1);
+        if (p0 <= kb * 128 && kb * 128 < p1) {
+            s_r0 = __ldg(offsets + e) + (kb * 128 - p0);     // first sorted row of the block
+            s_rend = __ldg(offsets + e + 1);
         }
-        s_e = lo;
     }
     __syncthreads();
-    const int e = s_e;
-    const int64_t r0 = offsets[e] + (kb * 128 - pad[e]);       // first sorted row of the block
-    const int64_t rend = offsets[e + 1];
+    const int64_t r0 = s_r0, rend = s_rend;
     const int64_t c0 = (int64_t)blockIdx.x * 64;
     const int tid = threadIdx.x;
     {
-        const int rr = tid >> 1, ch = (tid & 1) * 32;
+        const int rr = tid & 127, ch = (tid >> 7) * 32;
         const int64_t r = r0 + rr;
         float v[32];
         if (r < rend) {
@@ -309,13 +317,13 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t
             for (int i = 0; i < 32; i++) v[i] = 0.0f;
         }
 #pragma unroll
-        for (int i = 0; i < 32; i++) tile[rr][ch + i] = v[i];
+        for (int i = 0; i < 32; i++) tile[q1_idx(rr, ch + i)] = v[i];
     }
     __syncthreads();
     const int cc = tid >> 2, part = tid & 3;
     float amax = 0.0f;
 #pragma unroll 8
-    for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(tile[part * 32 + i][cc]));
+    for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(tile[q1_idx(part * 32 + i, cc)]));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     const float s = block_scale(amax);
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t
         uint32_t wds[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            const float *t4 = &tile[part * 32 + 4 * i][cc];
+            const float *t4 = &tile[q1_idx(part * 32 + 4 * i, cc)];   // rows +1..+3 are +65 words each
             wds[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(t4[0], s), __fdiv_rn(t4[65], s)) |
                      ((uint32_t)pack_e4m3x2(__fdiv_rn(t4[130], s), __fdiv_rn(t4[195], s)) << 16);
         }
