@@ -191,12 +191,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
-// 2-D tile store from shared memory through a tensor map (bulk async group)
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *src, int x, int y)
+// 2-D tile store from shared memory through a tensor map (bulk async group),
+// its lines marked first for eviction from L2: the data is written once and
+// not read again by this kernel
+__device__ __forceinline__ void tma_store_2d_evict_first(const CUtensorMap *tm, const void *src, int x, int y)
 {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
                      reinterpret_cast<uint64_t>(tm)),
-                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 "r"(x), "r"(y), "r"(smem_u32(src)), "l"(pol)
                  : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -934,7 +938,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0)
-                    tma_store_2d(&tm_out, stg, tl.n_blk * WG_BN + 32 * cg, tl.e * p.M + tl.m_blk * BM + q * 32);
+                    tma_store_2d_evict_first(&tm_out, stg, tl.n_blk * WG_BN + 32 * cg,
+                                             tl.e * p.M + tl.m_blk * BM + q * 32);
             }
             // no barrier between the epilogue warps: they share no staging, so
             // each runs ahead until the TMEM ring stops it, and leaves on its
