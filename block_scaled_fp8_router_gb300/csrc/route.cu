@@ -10,8 +10,8 @@
 // cores, whose accumulation order is not specified).
 //
 // route_topk_kernel: one cluster of ceil(E/128) CTAs per 64 tokens; each
-// 128-thread CTA computes 64 tokens x 128 experts with 8 x 8 fp32
-// accumulators per thread (four 16-byte shared loads per 64 FMAs, the next
+// 256-thread CTA computes 64 tokens x 128 experts with 8 x 4 fp32
+// accumulators per thread (three 16-byte shared loads per 32 FMAs, the next
 // hidden index's operands loaded while the current FMAs run), bf16 tiles of
 // x and W_r (32 deep) widened to fp32 in double-buffered shared memory with
 // conflict-free stores while the next tile loads into registers (one
@@ -160,15 +160,16 @@ constexpr int RC_TILE_FLOATS = (2 * RC_BK * (RC_BT + RC_EC) > RC_BT * RC_LGS) ? 
                                                                               : RC_BT * RC_LGS;
 
 // One cluster of ceil(E/128) CTAs per 64 tokens.  CTA r computes the logits
-// of experts 128r .. 128r+127 for the 64 tokens (128 threads, 8 tokens x 8
-// experts of fp32 fma-chain accumulators each: four 16-byte shared-memory
-// loads feed 64 fmas), keeps them in shared memory,
+// of experts 128r .. 128r+127 for the 64 tokens (256 threads, 8 tokens x 4
+// experts of fp32 fma-chain accumulators each: three 16-byte shared-memory
+// loads feed 32 fmas; eight warps per CTA so that one CTA per SM already
+// hides the shared-memory latency), keeps them in shared memory,
 // selects its own top-k per token and sends those (value, index) candidates
 // to CTA 0 of the cluster through distributed shared memory; CTA 0 merges
 // them into the top-k over all experts (every member of the global top-k is
 // in its own CTA's top-k, and the order is a strict total order, so the merge
 // is exact) and writes ids, gates and the capture.
-__global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restrict__ x,
                                                          const uint16_t *__restrict__ wr, int T, int d, int E,
                                                          int k, int score_fn, int renorm, float route_scale,
                                                          int32_t *__restrict__ ids, float *__restrict__ gates,
@@ -191,28 +192,28 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
     const int t0 = (int)cl_id() * RC_BT;
     const int e0 = rank * RC_EC;
     const int tt = (lane >> 2) * 8;                 // my 8 tokens in the tile
-    const int ee = warp * 32 + (lane & 3) * 8;      // my 8 experts of this CTA's 128
+    const int ee = warp * 16 + (lane & 3) * 4;      // my 4 experts of this CTA's 128
+    const int nw = blockDim.x >> 5;
 
-    // tile loaders: two x chunks (token tid & 63, 16-wide part tid >> 6) and
-    // four W_r chunks (expert tid, part r); consecutive lanes write
-    // consecutive shared-memory words
-    const int xt = tid & 63, xp = tid >> 6;
-    float acc[8][8];
+    // tile loaders: one x chunk (token tid & 63, 8-wide part tid >> 6) and
+    // two W_r chunks (expert tid & 127, 16-wide part tid >> 7); consecutive
+    // lanes write consecutive shared-memory words
+    const int xt = tid & 63, xp = tid >> 6;          // token, 8-wide part 0..3
+    const int we = tid & 127, wp = tid >> 7;         // expert, 16-wide part 0..1
+    float acc[8][4];
 #pragma unroll
     for (int a = 0; a < 8; a++)
 #pragma unroll
-        for (int b = 0; b < 8; b++) acc[a][b] = 0.0f;
-    uint4 rx[2], rw[4];
+        for (int b = 0; b < 4; b++) acc[a][b] = 0.0f;
+    uint4 rx[1], rw[2];
     auto load_tile = [&](int k0) {
         const int t = t0 + xt;
+        rx[0] = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 8))
+                      : make_uint4(0, 0, 0, 0);
+        const int e = e0 + we;
 #pragma unroll
         for (int r = 0; r < 2; r++)
-            rx[r] = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 16 + r * 8))
-                          : make_uint4(0, 0, 0, 0);
-        const int e = e0 + tid;
-#pragma unroll
-        for (int r = 0; r < 4; r++)
-            rw[r] = e < E ? __ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + k0 + r * 8))
+            rw[r] = e < E ? __ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + k0 + wp * 16 + r * 8))
                           : make_uint4(0, 0, 0, 0);
     };
     load_tile(0);
@@ -221,17 +222,14 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
         float *ws = ws2 + buf * RC_BK * RC_EC;
         {
             float f[8];
+            unpack_bf16x8(rx[0], f);
+#pragma unroll
+            for (int j = 0; j < 8; j++) xs[(xp * 8 + j) * RC_BT + xt] = f[j];
 #pragma unroll
             for (int r = 0; r < 2; r++) {
-                unpack_bf16x8(rx[r], f);
-#pragma unroll
-                for (int j = 0; j < 8; j++) xs[(xp * 16 + r * 8 + j) * RC_BT + xt] = f[j];
-            }
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
                 unpack_bf16x8(rw[r], f);
 #pragma unroll
-                for (int j = 0; j < 8; j++) ws[(r * 8 + j) * RC_EC + tid] = f[j];
+                for (int j = 0; j < 8; j++) ws[(wp * 16 + r * 8 + j) * RC_EC + we] = f[j];
             }
         }
         // one barrier per tile: it publishes this tile and, since every
@@ -242,32 +240,27 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
         float4 nx0 = *reinterpret_cast<const float4 *>(&xs[tt]);
         float4 nx1 = *reinterpret_cast<const float4 *>(&xs[tt + 4]);
         float4 nw0 = *reinterpret_cast<const float4 *>(&ws[ee]);
-        float4 nw1 = *reinterpret_cast<const float4 *>(&ws[ee + 4]);
 #pragma unroll
         for (int i = 0; i < RC_BK; i++) {
-            const float4 x0 = nx0, x1 = nx1, w0 = nw0, w1 = nw1;
+            const float4 x0 = nx0, x1 = nx1, w0 = nw0;
             if (i + 1 < RC_BK) {
                 nx0 = *reinterpret_cast<const float4 *>(&xs[(i + 1) * RC_BT + tt]);
                 nx1 = *reinterpret_cast<const float4 *>(&xs[(i + 1) * RC_BT + tt + 4]);
                 nw0 = *reinterpret_cast<const float4 *>(&ws[(i + 1) * RC_EC + ee]);
-                nw1 = *reinterpret_cast<const float4 *>(&ws[(i + 1) * RC_EC + ee + 4]);
             }
             const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const float wb[4] = {w0.x, w0.y, w0.z, w0.w};
 #pragma unroll
             for (int a = 0; a < 8; a++)
 #pragma unroll
-                for (int b = 0; b < 8; b++) acc[a][b] = fmaf(xa[a], wb[b], acc[a][b]);
+                for (int b = 0; b < 4; b++) acc[a][b] = fmaf(xa[a], wb[b], acc[a][b]);
         }
     }
     __syncthreads();  // the logits overwrite the tiles
 #pragma unroll
-    for (int a = 0; a < 8; a++) {
+    for (int a = 0; a < 8; a++)
         *reinterpret_cast<float4 *>(&lg[(tt + a) * RC_LGS + ee]) =
             make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-        *reinterpret_cast<float4 *>(&lg[(tt + a) * RC_LGS + ee + 4]) =
-            make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
-    }
     __syncthreads();
     const int ne = min(RC_EC, E - e0);   // experts of this CTA
     if (logits_out)
@@ -278,7 +271,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
 
     // ---- per-CTA top-k of each token over its 128 experts; candidates to CTA 0 ----
     const int nc = ncta * k;
-    for (int tl = warp * (RC_BT / 4); tl < (warp + 1) * (RC_BT / 4); tl++) {
+    for (int tl = warp * (RC_BT / nw); tl < (warp + 1) * (RC_BT / nw); tl++) {
         if (t0 + tl >= T) break;
         float vals[4];
         int idx[4];
@@ -311,7 +304,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const uint16_t *__restr
     if (rank != 0) return;
 
     // ---- CTA 0: merge the clusters' candidates, gates, outputs ----
-    for (int tl = warp * (RC_BT / 4); tl < (warp + 1) * (RC_BT / 4); tl++) {
+    for (int tl = warp * (RC_BT / nw); tl < (warp + 1) * (RC_BT / nw); tl++) {
         const int t = t0 + tl;
         if (t >= T) break;
         float vals[8];
@@ -483,7 +476,7 @@ MOE_API moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, i
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(((T + RC_BT - 1) / RC_BT) * ncta));
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = as_stream(stream);
     cfg.attrs = attr;
