@@ -14,7 +14,9 @@
 // Kernel shape (one persistent CTA per SM, 576 threads):
 //   warps 0-15  epilogue: warp w reads TMEM lane quadrant w % 4 (32 rows),
 //               column group w / 4 (64 of the 256 accumulator columns);
-//               promotion per K block, then the tile epilogue
+//               promotion per K block (two columns per packed fp32x2 FMA),
+//               then the tile epilogue; the warps meet only in GEMM1, four
+//               at a time (one row quarter), to exchange the SwiGLU amax
 //   warp 16     TMA producer: A tile 128 x 128 B and B tile 256 x 128 B per
 //               K block into a 4-stage shared-memory ring (128-byte swizzle)
 //   warp 17     MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=32, E4M3 x E4M3
@@ -35,8 +37,10 @@
 //
 // Also in this file: the gathered form of the same kernel (GATHER: GEMM1's
 // A rows fetched from the token-major codes by tile::gather4, GEMM2's rows
-// stored in slot order) and grouped_gemm_mx_kernel, the power-of-two-scale
-// variant on the hardware block-scaled MMA (described above it).
+// stored in slot order), grouped_wgrad_kernel (the weight gradients, the
+// contraction over each expert's tokens) and grouped_gemm_mx_kernel, the
+// power-of-two-scale variant on the hardware block-scaled MMA (each
+// described above it).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
