@@ -411,9 +411,11 @@ MOE_API moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gat
         return MOE_ERR_SHAPE;
     if (!expert_offsets || !pad || !q || !scales) return MOE_ERR_NULL;
     WgSrc w{dy, gates, x, sorted_to_slot, h, d_act, k, F};
+    if (src < 0 || src > 3 || (src == SRC_ACT && (F <= 0 || C != F)) || (src == SRC_DH && (F <= 0 || C != 2 * F)))
+        return MOE_ERR_SHAPE;
     if ((src == SRC_GDY && (!dy || !gates || !sorted_to_slot)) || (src == SRC_X && (!x || !sorted_to_slot)) ||
-        (src == SRC_ACT && (!h || F <= 0 || C != F)) || (src == SRC_DH && (!h || !d_act || F <= 0 || C != 2 * F)))
-        return src < 0 || src > 3 ? MOE_ERR_SHAPE : MOE_ERR_NULL;
+        (src == SRC_ACT && !h) || (src == SRC_DH && (!h || !d_act)))
+        return MOE_ERR_NULL;
     // rows are read 16 bytes at a time
     if (!aligned16(q) || (dy && !aligned16(dy)) || (x && !aligned16(x)) || (h && !aligned16(h)) ||
         (d_act && !aligned16(d_act)))

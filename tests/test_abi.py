@@ -72,5 +72,38 @@ def test_host_side_errors(lib):
     assert L.moe_route_replay_u8(null, null, null, 10, 100, 8, 2, 1, 1, 1.0, null, null, null, null) == 2
     assert L.moe_route_replay_u8(null, null, null, 10, 128, 8, 2, 1, 1, 1.0, null, null, null, null) == 1
     assert L.moe_debug_bounded_wait(1000, null, null) == 1
+    # backward of the expert path
+    y = ctypes.c_void_p(0x1008)                                        # 8-byte aligned only
+    assert L.moe_combine_backward(x, x, x, x, 10, 2, 100, 20, x, x, x, null) == 2      # d % 128
+    assert L.moe_combine_backward(null, null, null, null, 0, 2, 128, 0, null, null, null, null) == 0   # empty
+    assert L.moe_combine_backward(x, x, x, null, 10, 2, 128, 20, x, x, x, null) == 1   # NULL
+    assert L.moe_combine_backward(y, x, x, x, 10, 2, 128, 20, x, x, x, null) == 3      # misaligned dy
+    assert L.moe_swiglu_backward(x, x, 10, 100, x, x, null) == 2                        # F % 128
+    assert L.moe_swiglu_backward(null, null, 0, 128, null, null, null) == 0             # empty
+    assert L.moe_swiglu_backward(x, x, 10, 128, y, x, null) == 3                        # misaligned dh_q
+    assert L.moe_dispatch_backward(x, x, 10, 33, 128, x, null) == 2                     # k > 32
+    assert L.moe_dispatch_backward(x, null, 10, 2, 128, x, null) == 1
+    assert L.fp8_weight_transpose(x, x, 2, 100, 128, x, x, null) == 2                   # R % 128
+    assert L.fp8_weight_transpose(x, x, 0, 128, 128, x, x, null) == 0                   # no experts
+    assert L.fp8_weight_transpose(x, x, 2, 128, 128, y, x, null) == 3
+    # weight gradients
+    assert L.moe_wgrad_pad_offsets(x, 0, x, null) == 2                                  # E < 1
+    assert L.moe_wgrad_pad_offsets(null, 4, x, null) == 1
+    assert L.moe_wgrad_quant(0, x, x, null, x, 2, null, null, 0, x, x, 4, 100, 256, 1, x, x, null) == 2   # C % 128
+    assert L.moe_wgrad_quant(0, x, x, null, x, 2, null, null, 0, x, x, 4, 128, 200, 1, x, x, null) == 2   # ld % 128
+    assert L.moe_wgrad_quant(0, x, x, null, x, 40, null, null, 0, x, x, 4, 128, 256, 1, x, x, null) == 2  # k > 32
+    assert L.moe_wgrad_quant(5, x, x, x, x, 2, x, x, 128, x, x, 4, 128, 256, 1, x, x, null) == 2          # source
+    assert L.moe_wgrad_quant(0, null, x, null, x, 2, null, null, 0, x, x, 4, 128, 256, 1, x, x, null) == 1  # no dy
+    assert L.moe_wgrad_quant(1, null, null, null, null, 1, x, null, 128, x, x, 4, 256, 256, 1, x, x, null) == 2  # C != F
+    assert L.moe_wgrad_quant(2, null, null, null, null, 1, x, null, 128, x, x, 4, 256, 256, 1, x, x, null) == 1  # no d_act
+    assert L.moe_wgrad_quant(2, null, null, null, null, 1, x, x, 128, x, x, 4, 256, 256, 1, y, x, null) == 3    # q
+    assert L.moe_wgrad_quant(3, null, null, y, x, 2, null, null, 0, x, x, 4, 128, 256, 1, x, x, null) == 3      # x
+    assert L.moe_wgrad_quant(3, null, null, x, x, 2, null, null, 0, x, x, 4, 128, 0, 1, x, x, null) == 0       # ld 0
+    assert L.moe_wgrad_gemm(x, x, x, x, x, 4, 200, 256, 256, x, null, null) == 2        # M % 128
+    assert L.moe_wgrad_gemm(x, x, x, x, x, 4, 256, 200, 256, x, null, null) == 2        # N % 128
+    assert L.moe_wgrad_gemm(x, x, x, x, x, 4, 256, 256, 200, x, null, null) == 2        # ld % 128
+    assert L.moe_wgrad_gemm(x, x, x, x, x, 2000, 256, 256, 256, x, null, null) == 2     # E > max
+    assert L.moe_wgrad_gemm(x, null, x, x, x, 4, 256, 256, 256, x, null, null) == 1
+    assert L.moe_wgrad_gemm(x, y, x, x, x, 4, 256, 256, 256, x, null, null) == 3        # a_sT for the bulk copy
     for s in range(7):
         assert lib.moe_status_str(s)
