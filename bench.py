@@ -453,6 +453,14 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
     bb.record()
     torch.cuda.synchronize()
     wg_ms = a.elapsed_time(bb) / steps
+    # the same calls split by events (pad offsets + d_out quantisation, act
+    # quantisation, dW2 GEMM, dh quantisation, x quantisation, dW13 GEMM)
+    wg_names = ("quant_d_out", "quant_act", "gemm_dW2", "quant_dh", "quant_x", "gemm_dW13")
+    wevs = [[ev() for _ in range(7)] for _ in range(steps)]
+    for e in wevs:
+        layer._weight_grads(dy, T, events=e)
+    torch.cuda.synchronize()
+    wg_split = {n: sum(e[i].elapsed_time(e[i + 1]) for e in wevs) / steps for i, n in enumerate(wg_names)}
     flops = 6.0 * A * d * F
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"]
@@ -467,11 +475,18 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
                            "frac": flops / (gemm_ms * 1e-3) / 1e12 / fp8_peak, "peak": fp8_peak},
            "weight_grads": {"ms": wg_ms, "TFLOP/s (dW2 + dW13 GEMMs, algorithmic)": flops / (wg_ms * 1e-3) / 1e12,
                             "note": "includes the four 128x1 operand quantisations and the fp32 dW writes "
-                                    f"({4 * 3 * E * d * F / 1e9:.1f} GB)"},
+                                    f"({4 * 3 * E * d * F / 1e9:.1f} GB)",
+                            "steps": {n: {"ms": v} for n, v in wg_split.items()}},
            "status": Lb.check_status(layer.dev_status)}
     for n, nb in (("combine_bwd", b_comb), ("swiglu_bwd", b_swi), ("dispatch_bwd", b_disp)):
         out["steps"][n]["GB/s"] = nb / (split[n] * 1e-3) / 1e9
         out["steps"][n]["frac_hbm"] = out["steps"][n]["GB/s"] / hbm
+    # the weight-gradient GEMMs are bound by their fp32 stores: output bytes
+    # per launch over the launch time, against the measured copy bandwidth
+    for n, nb in (("gemm_dW2", 4.0 * E * d * F), ("gemm_dW13", 4.0 * E * 2 * F * d)):
+        st = out["weight_grads"]["steps"][n]
+        st["store GB/s"] = nb / (st["ms"] * 1e-3) / 1e9
+        st["frac_hbm"] = st["store GB/s"] / hbm
     del layer, x, b
     torch.cuda.empty_cache()
     return out

@@ -211,7 +211,10 @@ class MoELayerFP8:
             return dx, b["d_gates"][:T]
         return (dx, b["d_gates"][:T], *self._weight_grads(dy, T))
 
-    def _weight_grads(self, dy: torch.Tensor, T: int):
+    def _weight_grads(self, dy: torch.Tensor, T: int, events=None):
+        """dW13, dW2 of the last train forward; `events` (seven CUDA events, for
+        timing) are recorded around the six library calls."""
+        rec = (lambda i: events[i].record()) if events else (lambda i: None)
         A = T * self.k
         E, d, F = self.w.E, self.w.d, self.w.F
         dev = dy.device
@@ -224,23 +227,30 @@ class MoELayerFP8:
                             dW2=e((E, d, F), torch.float32), dW13=e((E, 2 * F, d), torch.float32))
         w = self._wg
         b = self._bw
+        rec(0)
         pad = L.moe_wgrad_pad_offsets(self.offsets, pad=w["pad"])
         s2s = self.s2s[:A]
         # dW2 = d_out^T act
         aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_GDY, self.offsets, pad, d, ld, True, dy=dy, gates=self.gates[:T],
                                     sorted_to_slot=s2s, k=self.k, q=w["aq"][:d],
                                     scales=w["as_"][:d * (ld // 128)].view(ld // 128, d))
+        rec(1)
         bq, bs = L.moe_wgrad_quant(L.WGRAD_SRC_ACT, self.offsets, pad, F, ld, True, h=self.h, F=F, q=w["bq"][:F],
                                    scales=w["bs"][:F * (ld // 128)].view(ld // 128, F))
+        rec(2)
         L.moe_wgrad_gemm(aq, as_, bq, bs, pad, out=w["dW2"], dev_status=self.dev_status)
+        rec(3)
         # dW13 = dh^T x
         aq, as_ = L.moe_wgrad_quant(L.WGRAD_SRC_DH, self.offsets, pad, 2 * F, ld, True, h=self.h,
                                     d_act=b["d_act"], F=F, q=w["aq"][:2 * F],
                                     scales=w["as_"][:2 * F * (ld // 128)].view(ld // 128, 2 * F))
+        rec(4)
         bq, bs = L.moe_wgrad_quant(L.WGRAD_SRC_X, self.offsets, pad, d, ld, True, x=self._x_train,
                                    sorted_to_slot=s2s, k=self.k, q=w["bq"][:d],
                                    scales=w["bs"][:d * (ld // 128)].view(ld // 128, d))
+        rec(5)
         L.moe_wgrad_gemm(aq, as_, bq, bs, pad, out=w["dW13"], dev_status=self.dev_status)
+        rec(6)
         return w["dW13"], w["dW2"]
 
 
