@@ -238,6 +238,122 @@ void or_quant_ue8m0(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_
 /* ------------------------------------------------------------------ */
 /* routing ("Router replay": the decision that is captured)             */
 /* ------------------------------------------------------------------ */
+/* NVFP4: FP4 E2M1 values, 16-element blocks with E4M3 scales, and one  */
+/* fp32 scale per tensor (the FP4 variant the pages list as future work, */
+/* "RL at 1T Scale", closing section; the format is NVIDIA's published   */
+/* NVFP4, taken as the plainest reading)                                 */
+/* ------------------------------------------------------------------ */
+
+/* E2M1 (low 4 bits of code): sign bit 3, exponent bits 2..1 (bias 1),
+ * mantissa bit 0; exponent 0 is subnormal (m * 0.5).  Magnitudes of codes
+ * 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6.  No inf, no NaN. */
+double or_e2m1_decode(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Round a binary32 to E2M1, nearest with ties to even, saturating to +-6
+ * (a value whose rounding leaves the range becomes 6).  The sign is kept
+ * (-0 -> 0x8).  The grid spacing is 0.5 below 2, 1 in [2, 4) and 2 in
+ * [4, 8): dividing by it is exact in double and rint() rounds to the
+ * nearest integer with ties to even, which is the even-mantissa code.  NaN
+ * is outside the contract (the quantiser's inputs are finite). */
+uint8_t or_e2m1_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs((double)v);
+    double step = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+    double r = rint(a / step) * step;
+    if (r > 6.0)
+        r = 6.0;
+    uint8_t code;
+    if (r == 0.0)
+        code = 0;
+    else if (r < 1.0)
+        code = 1;                                    /* 0.5, subnormal */
+    else {
+        int ex;
+        frexp(r, &ex);                               /* r in [2^(ex-1), 2^ex) */
+        int e = ex - 1;                              /* 0, 1 or 2 */
+        int m = ldexp(r, -e) > 1.0 ? 1 : 0;          /* 1.5 * 2^e -> m = 1 */
+        code = (uint8_t)(((e + 1) << 1) | m);
+    }
+    return (uint8_t)(sign | code);
+}
+
+/* NVFP4 quantisation of a [rows, cols] bf16 tensor (row stride ld_src),
+ * blocks of 16 consecutive elements along each row (the contraction
+ * dimension of the GEMM that consumes it):
+ *   s_enc = (6 * 448) / amax over the whole tensor   (binary32 division;
+ *           an all-zero tensor takes s_enc = 1),
+ *   block scale byte sb = e4m3((amax_block / 6) * s_enc)  (binary32 division
+ *           and product, then round-to-nearest-even saturating E4M3),
+ *   per element: s_elem = s_enc / e4m3value(sb) (binary32; 0 when the scale
+ *           byte decodes to 0), code = e2m1(x * s_elem).
+ * Decoded value: e2m1value(code) * e4m3value(sb) / s_enc.
+ * q [rows, cols/2]: element 2i in the low nibble of byte i, 2i+1 in the high
+ * nibble; s [rows, cols/16] E4M3 bytes; *s_enc_out the tensor's s_enc. */
+void or_quant_nvfp4(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_src, uint8_t *q, uint8_t *s,
+                    float *s_enc_out)
+{
+    float amax_t = 0.0f;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++)
+            amax_t = fmaxf(amax_t, fabsf(or_bf16_to_f32(src[r * ld_src + c])));
+    const float s_enc = amax_t == 0.0f ? 1.0f : (6.0f * 448.0f) / amax_t;
+    *s_enc_out = s_enc;
+    const int64_t nb = cols / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint16_t *x = src + r * ld_src + b * 16;
+            float amax = 0.0f;
+            for (int i = 0; i < 16; i++)
+                amax = fmaxf(amax, fabsf(or_bf16_to_f32(x[i])));
+            const float bd = amax / 6.0f;
+            const uint8_t sb = or_e4m3_encode(bd * s_enc);
+            s[r * nb + b] = sb;
+            const float sbv = (float)or_e4m3_decode(sb);
+            const float s_elem = sbv == 0.0f ? 0.0f : s_enc / sbv;
+            for (int i = 0; i < 16; i += 2) {
+                const uint8_t lo = or_e2m1_encode(or_bf16_to_f32(x[i]) * s_elem);
+                const uint8_t hi = or_e2m1_encode(or_bf16_to_f32(x[i + 1]) * s_elem);
+                q[r * (cols / 2) + b * 8 + i / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+}
+
+/* out[m, n] = sum over k of dec(a[m, k]) * dec(b[n, k]) for NVFP4 operands
+ * a [M, K] and b [N, K] as or_quant_nvfp4 writes them (K a multiple of 16),
+ * computed as (sum over k, ascending, of e2m1(a) * e4m3(sa) * e2m1(b) *
+ * e4m3(sb)) / (a_enc * b_enc) in double.  Each product has at most 12
+ * significant bits and lies in [2^-20, 2^23], so the sum is exact for
+ * K <= 1024 (and rounded in ascending k beyond); a_enc * b_enc is exact;
+ * one division rounds.  The tensor-core result (fp32, order unspecified)
+ * is compared with this. */
+void or_gemm_nvfp4(const uint8_t *aq, const uint8_t *as, float a_enc, const uint8_t *bq, const uint8_t *bs,
+                   float b_enc, int64_t M, int64_t N, int64_t K, double *out)
+{
+    const double enc = (double)a_enc * (double)b_enc;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                const uint8_t ab = aq[m * (K / 2) + k / 2], bb = bq[n * (K / 2) + k / 2];
+                const double av = or_e2m1_decode((k & 1) ? (ab >> 4) : (ab & 15)) * or_e4m3_decode(as[m * (K / 16) + k / 16]);
+                const double bv = or_e2m1_decode((k & 1) ? (bb >> 4) : (bb & 15)) * or_e4m3_decode(bs[n * (K / 16) + k / 16]);
+                acc += av * bv;
+            }
+            out[m * N + n] = acc / enc;
+        }
+}
+
+/* ------------------------------------------------------------------ */
 
 /* l[t,e] = sum_i x[t,i] * Wr[e,i] as one binary32 fused-multiply-add chain in
  * ascending i, starting from +0. */

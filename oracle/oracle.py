@@ -55,6 +55,10 @@ def _load():
                 "or_f32_to_bf16": (ctypes.c_uint16, [F]),
                 "or_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
                 "or_e4m3_encode": (ctypes.c_uint8, [F]),
+                "or_e2m1_decode": (ctypes.c_double, [ctypes.c_uint8]),
+                "or_e2m1_encode": (ctypes.c_uint8, [F]),
+                "or_quant_nvfp4": (None, [P, I64, I64, I64, P, P, P]),
+                "or_gemm_nvfp4": (None, [P, P, F, P, P, F, I64, I64, I64, P]),
                 "or_quant_1x128": (None, [P, I64, I64, I64, P, P]),
                 "or_quant_128x128": (None, [P, I64, I64, I64, P, P]),
                 "or_router_logits": (None, [P, P, I64, I, I, P]),
@@ -167,6 +171,43 @@ def quant_ue8m0(x_bf16: np.ndarray, block_rows: int):
 def ue8m0_value(e: np.ndarray) -> np.ndarray:
     """Biased exponent bytes -> their scale values 2^(e-127) as fp32 (exact)."""
     return np.ldexp(np.float32(1.0), np.asarray(e, np.int32) - 127).astype(np.float32)
+
+
+def e2m1_decode(c: int) -> float:
+    """FP4 E2M1 code (low 4 bits) -> its value."""
+    return _load().or_e2m1_decode(c)
+
+
+def e2m1_encode(v: float) -> int:
+    """binary32 -> E2M1 code, nearest with ties to even, saturating to +-6."""
+    return _load().or_e2m1_encode(v)
+
+
+def quant_nvfp4(x_bf16: np.ndarray):
+    """[rows, cols] bf16 bits -> (packed codes uint8 [rows, cols/2], E4M3 block scales uint8 [rows, cols/16],
+    s_enc float): 16-element blocks along each row, one fp32 scale for the tensor."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    q = np.empty((rows, cols // 2), np.uint8)
+    s = np.empty((rows, cols // 16), np.uint8)
+    enc = ctypes.c_float(0.0)
+    _load().or_quant_nvfp4(_p(x), rows, cols, cols, _p(q), _p(s), ctypes.byref(enc))
+    return q, s, enc.value
+
+
+def gemm_nvfp4(aq: np.ndarray, as_: np.ndarray, a_enc: float, bq: np.ndarray, bs: np.ndarray, b_enc: float):
+    """out [M, N] float64 = a (NVFP4 [M, K]) x b (NVFP4 [N, K])^T from the quant_nvfp4 layouts."""
+    aq = _c(aq, np.uint8)
+    as_ = _c(as_, np.uint8)
+    bq = _c(bq, np.uint8)
+    bs = _c(bs, np.uint8)
+    M, K = aq.shape[0], aq.shape[1] * 2
+    N = bq.shape[0]
+    assert bq.shape[1] * 2 == K and as_.shape == (M, K // 16) and bs.shape == (N, K // 16)
+    out = np.empty((M, N), np.float64)
+    _load().or_gemm_nvfp4(_p(aq), _p(as_), a_enc, _p(bq), _p(bs), b_enc, M, N, K, _p(out))
+    return out
 
 
 def router_logits(x_bf16: np.ndarray, wr_bf16: np.ndarray) -> np.ndarray:
