@@ -53,6 +53,7 @@ _SIGS = {
     "moe_wgrad_pad_offsets": (I, [P, I, P, P]),
     "moe_wgrad_quant": (I, [I, P, P, P, P, I, P, P, I, P, P, I, I64, I64, I, P, P, P]),
     "moe_wgrad_gemm": (I, [P, P, P, P, P, I, I, I, I64, P, P, P]),
+    "fp8_quant_nvfp4": (I, [P, I64, I64, P, P, P, P]),
     "moe_grouped_ffn_mx": (I, [P, P, P, I, I, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_debug_bounded_wait": (I, [I64, P, P]),
     "moe_device_sm_count": (I, []),
@@ -214,6 +215,25 @@ def fp8_block_quant_ue8m0(src, block_rows, q=None, scale_exp=None, stream=None):
     _check("fp8_block_quant_ue8m0", _lib.fp8_block_quant_ue8m0(
         _ptr(src), rows, cols, src.stride(0), block_rows, _ptr(q), _ptr(scale_exp), _stream(stream)))
     return q, scale_exp
+
+
+def fp8_quant_nvfp4(src, q=None, scales=None, tensor_scale=None, stream=None):
+    """bf16 [rows, cols] -> (packed E2M1 codes uint8 [rows, cols/2], E4M3 block
+    scales uint8 [rows, cols/16], tensor_scale float32 [2] = (s_enc, amax))."""
+    if src.dim() != 2:
+        raise ValueError("src must be 2-D")
+    rows, cols = src.shape
+    if src.dtype != torch.bfloat16 or not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src: contiguous bf16 CUDA tensor")
+    q = _empty((rows, cols // 2), torch.uint8, src) if q is None else q
+    scales = _empty((rows, cols // 16), torch.uint8, src) if scales is None else scales
+    tensor_scale = _empty((2,), torch.float32, src) if tensor_scale is None else tensor_scale
+    _want(q, torch.uint8, (rows, cols // 2), "q")
+    _want(scales, torch.uint8, (rows, cols // 16), "scales")
+    _want(tensor_scale, torch.float32, (2,), "tensor_scale")
+    _check("fp8_quant_nvfp4", _lib.fp8_quant_nvfp4(_ptr(src), rows, cols, _ptr(q), _ptr(scales), _ptr(tensor_scale),
+                                                   _stream(stream)))
+    return q, scales, tensor_scale
 
 
 def fp8_block_quant(src, block_rows, q=None, scales=None, stream=None):

@@ -159,6 +159,28 @@ moe_status fp8_block_quant(const uint16_t *src, int64_t rows, int64_t cols, int6
                            int block_rows, uint8_t *q, float *scales, void *stream);
 
 /* ------------------------------------------------------------------------
+ * fp8_quant_nvfp4 -- NVFP4 quantisation (the FP4 variant listed as future
+ * work for training and inference in "RL at 1T Scale", closing section;
+ * NVIDIA's NVFP4 format): FP4 E2M1 values, 16-element blocks along each row
+ * with E4M3 block scales, one fp32 scale for the tensor.
+ *
+ *   s_enc = (6 * 448) / amax over the tensor (binary32; 1 if amax is 0),
+ *   per block: scale byte = E4M3((amax_block / 6) * s_enc), round to
+ *     nearest even, saturating; per element: code = E2M1(x * (s_enc /
+ *     scale)), nearest even, saturating to +-6 (0 where the scale byte
+ *     decodes to 0); decoded value = e2m1 * scale / s_enc.
+ * src [rows, cols] bf16 (row stride cols); q [rows, cols/2] (element 2i in
+ * the low nibble of byte i, 2i+1 in the high nibble); scales [rows, cols/16]
+ * E4M3 bytes; tensor_scale: two device floats, [0] = s_enc (written), [1] =
+ * the tensor amax (written; scratch of the first pass).  Two launches (amax,
+ * then the blocks) and a memset on `stream`.
+ * rows may be 0.  Errors: NULL, SHAPE (cols % 16), ALIGN (src, q not
+ * 16-byte aligned), CUDA.  NaN inputs are outside the contract.
+ * ---------------------------------------------------------------------- */
+moe_status fp8_quant_nvfp4(const uint16_t *src, int64_t rows, int64_t cols, uint8_t *q, uint8_t *scales,
+                           float *tensor_scale, void *stream);
+
+/* ------------------------------------------------------------------------
  * fp8_block_quant_ue8m0 -- fp8_block_quant with power-of-two block scales
  * (the UE8M0 scale format of MXFP8 and of the hardware block-scaled MMA; a
  * variant of the "FP8 training" recipe, whose scales are arbitrary fp32).

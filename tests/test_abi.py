@@ -105,5 +105,10 @@ def test_host_side_errors(lib):
     assert L.moe_wgrad_gemm(x, x, x, x, x, 2000, 256, 256, 256, x, null, null) == 2     # E > max
     assert L.moe_wgrad_gemm(x, null, x, x, x, 4, 256, 256, 256, x, null, null) == 1
     assert L.moe_wgrad_gemm(x, y, x, x, x, 4, 256, 256, 256, x, null, null) == 3        # a_sT for the bulk copy
+    # NVFP4 quantiser
+    assert L.fp8_quant_nvfp4(x, 4, 40, x, x, x, null) == 2                              # cols % 16
+    assert L.fp8_quant_nvfp4(x, 4, 64, x, x, null, null) == 1                           # tensor scale
+    assert L.fp8_quant_nvfp4(null, 4, 64, x, x, x, null) == 1                           # src
+    assert L.fp8_quant_nvfp4(y, 4, 64, x, x, x, null) == 3                              # misaligned src
     for s in range(7):
         assert lib.moe_status_str(s)
