@@ -492,6 +492,33 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
     return out
 
 
+def run_nvfp4_quant(cfg, dev, seed, steps, warmup, peaks):
+    """The NVFP4 quantiser (fp8_quant_nvfp4: tensor amax pass, then E4M3 block
+    scales and packed E2M1 codes) on the layer's activations [T, d] bf16."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    x = S.make_x(cfg, dev, seed)
+    T, d = x.shape
+    q = torch.empty((T, d // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((T, d // 16), dtype=torch.uint8, device=dev)
+    ts = torch.empty((2,), dtype=torch.float32, device=dev)
+    for _ in range(warmup):
+        Lb.fp8_quant_nvfp4(x, q=q, scales=s, tensor_scale=ts)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        Lb.fp8_quant_nvfp4(x, q=q, scales=s, tensor_scale=ts)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nbytes = T * d * (2 + 2 + 0.5 + 1 / 16)      # x read by both passes, codes and scales written
+    return {"workload": f"x [{T}, {d}] bf16 -> NVFP4 (16-element E4M3-scaled blocks, fp32 tensor scale)",
+            "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "launches": 2, "note": "x (117 MB) fits L2, so the second pass may read it from L2"}
+
+
 def run_payload(dev, seed, steps, warmup, peaks):
     """The routed-experts payload at one byte per id: a [64, 8, 131072] int32
     payload (64 layers x top-8 x 128K tokens, 268 MB, replayed-id
@@ -745,7 +772,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dispatch-combine", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the replay-workload line")
-    ap.add_argument("--no-mx", action="store_true", help="skip the power-of-two-scale (block-scaled MMA) line")
+    ap.add_argument("--no-mx", action="store_true",
+                    help="skip the power-of-two-scale (block-scaled MMA) line and the NVFP4 quantiser timing")
     ap.add_argument("--no-backward", action="store_true", help="skip the expert-path backward line")
     ap.add_argument("--router-kernels", action="store_true",
                     help="time only the router kernels (route_topk, route_replay) and print their line")
@@ -874,6 +902,14 @@ def main():
     if cfg.name == "large" and not args.no_dispatch_combine:
         out["payload"] = run_payload(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
                                      args.seed + rank, max(3, args.steps // 2), 3, peaks)
+    if cfg.name == "large" and not args.no_mx:
+        import torch
+        torch.cuda.empty_cache()
+        try:
+            out["nvfp4_quant"] = run_nvfp4_quant(cfg, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
+                                                 args.seed + rank, max(3, args.steps // 2), 3, peaks)
+        except Exception as exc:   # an extra measurement: report, do not lose the line
+            out["nvfp4_quant"] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, args.seed, args.cpu_tokens, "cuda")
     if rank == 0:
