@@ -1543,8 +1543,9 @@ MOE_API moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_sT, const u
                                   const int32_t *pad, int E, int M, int N, int64_t ld, float *out,
                                   int32_t *dev_status, void *stream)
 {
+    // the output rows e * M + m are 32-bit TMA coordinates
     if (E < 1 || E > MAX_E || M <= 0 || N <= 0 || M % BM != 0 || N % 128 != 0 || ld <= 0 || ld % 128 != 0 ||
-        ld >= (1LL << 31) || (int64_t)M >= (1LL << 31) || (int64_t)N >= (1LL << 31))
+        ld >= (1LL << 31) || (int64_t)E * M >= (1LL << 31) || (int64_t)N >= (1LL << 31))
         return MOE_ERR_SHAPE;
     if (!a_q || !a_sT || !b_q || !b_sT || !pad || !out) return MOE_ERR_NULL;
     if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(out) || !aligned16(a_sT) || !aligned16(b_sT))

@@ -379,10 +379,10 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  *                          forward's per-block promotion), a [M, ld], b [N,
  *                          ld], both scale arrays kb-major [ld/128, *] (as
  *                          moe_wgrad_quant writes them with scales_kb_major);
- *                          M, N multiples of 128; experts without rows get
- *                          zeros; pad entries outside [0, ld] or not
- *                          multiples of 128 run no tile and set
- *                          MOE_DEV_ROWS.
+ *                          M, N multiples of 128, E * M < 2^31; experts
+ *                          without rows get zeros; pad entries outside
+ *                          [0, ld] or not multiples of 128 run no tile and
+ *                          set MOE_DEV_ROWS.
  * The router's backward is not provided (d_gates are returned for it).
  * Errors: NULL, SHAPE, ALIGN, CUDA (WORKSPACE for the _train call).
  * ---------------------------------------------------------------------- */

@@ -103,6 +103,7 @@ def test_host_side_errors(lib):
     assert L.moe_wgrad_gemm(x, x, x, x, x, 4, 256, 200, 256, x, null, null) == 2        # N % 128
     assert L.moe_wgrad_gemm(x, x, x, x, x, 4, 256, 256, 200, x, null, null) == 2        # ld % 128
     assert L.moe_wgrad_gemm(x, x, x, x, x, 2000, 256, 256, 256, x, null, null) == 2     # E > max
+    assert L.moe_wgrad_gemm(x, x, x, x, x, 1024, 1 << 21, 256, 256, x, null, null) == 2  # E * M >= 2^31
     assert L.moe_wgrad_gemm(x, null, x, x, x, 4, 256, 256, 256, x, null, null) == 1
     assert L.moe_wgrad_gemm(x, y, x, x, x, 4, 256, 256, 256, x, null, null) == 3        # a_sT for the bulk copy
     # NVFP4 quantiser
