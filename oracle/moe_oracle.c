@@ -327,30 +327,85 @@ void or_quant_nvfp4(const uint16_t *src, int64_t rows, int64_t cols, int64_t ld_
         }
 }
 
+/* Sum over k (ascending) of e2m1(a_k) * e4m3(sa) * e2m1(b_k) * e4m3(sb) for
+ * one row of each NVFP4 operand (packed codes, 16-element block scales).
+ * Each product has at most 12 significant bits and lies in [2^-20, 2^23],
+ * so the sum is exact for K <= 1024 (and rounded in ascending k beyond). */
+static double nvfp4_dot(const uint8_t *aq, const uint8_t *as, const uint8_t *bq, const uint8_t *bs, int64_t K)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; k++) {
+        const uint8_t ab = aq[k / 2], bb = bq[k / 2];
+        const double av = or_e2m1_decode((k & 1) ? (ab >> 4) : (ab & 15)) * or_e4m3_decode(as[k / 16]);
+        const double bv = or_e2m1_decode((k & 1) ? (bb >> 4) : (bb & 15)) * or_e4m3_decode(bs[k / 16]);
+        acc += av * bv;
+    }
+    return acc;
+}
+
 /* out[m, n] = sum over k of dec(a[m, k]) * dec(b[n, k]) for NVFP4 operands
- * a [M, K] and b [N, K] as or_quant_nvfp4 writes them (K a multiple of 16),
- * computed as (sum over k, ascending, of e2m1(a) * e4m3(sa) * e2m1(b) *
- * e4m3(sb)) / (a_enc * b_enc) in double.  Each product has at most 12
- * significant bits and lies in [2^-20, 2^23], so the sum is exact for
- * K <= 1024 (and rounded in ascending k beyond); a_enc * b_enc is exact;
- * one division rounds.  The tensor-core result (fp32, order unspecified)
- * is compared with this. */
+ * a [M, K] and b [N, K] as or_quant_nvfp4 writes them (K a multiple of 16):
+ * nvfp4_dot / (a_enc * b_enc) in double (a_enc * b_enc is exact; one
+ * division rounds).  The tensor-core result (fp32, order unspecified) is
+ * compared with this. */
 void or_gemm_nvfp4(const uint8_t *aq, const uint8_t *as, float a_enc, const uint8_t *bq, const uint8_t *bs,
                    float b_enc, int64_t M, int64_t N, int64_t K, double *out)
 {
     const double enc = (double)a_enc * (double)b_enc;
 #pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < M; m++)
-        for (int64_t n = 0; n < N; n++) {
-            double acc = 0.0;
-            for (int64_t k = 0; k < K; k++) {
-                const uint8_t ab = aq[m * (K / 2) + k / 2], bb = bq[n * (K / 2) + k / 2];
-                const double av = or_e2m1_decode((k & 1) ? (ab >> 4) : (ab & 15)) * or_e4m3_decode(as[m * (K / 16) + k / 16]);
-                const double bv = or_e2m1_decode((k & 1) ? (bb >> 4) : (bb & 15)) * or_e4m3_decode(bs[n * (K / 16) + k / 16]);
-                acc += av * bv;
-            }
-            out[m * N + n] = acc / enc;
+        for (int64_t n = 0; n < N; n++)
+            out[m * N + n] = nvfp4_dot(aq + m * (K / 2), as + m * (K / 16), bq + n * (K / 2), bs + n * (K / 16), K) /
+                             enc;
+}
+
+/* SwiGLU expert FFN in NVFP4 on n sorted rows (row r belongs to expert
+ * row_expert[r]):
+ *   x rows: NVFP4 with one tensor scale x_enc (the token tensor's);
+ *   w13[e] [2F, d] and w2[e] [d, F]: NVFP4 with one tensor scale per expert
+ *     matrix (w13_enc[e], w2_enc[e]);
+ *   h = the exact GEMM1 value rounded once to binary32 (gate columns 0..F-1,
+ *     up F..2F-1);
+ *   act = silu(g) * u in double rounded to binary32 (the recipe FFN's
+ *     formula), then to bf16 -- the act tensor is materialised, because its
+ *     NVFP4 tensor scale needs the amax over all n rows first;
+ *   act [n, F] -> NVFP4 (or_quant_nvfp4: one tensor scale act_enc);
+ *   out = bf16(binary32(exact GEMM2 value)).
+ * h [n, 2F] f32 and act_bf16 [n, F] are outputs; act_q [n, F/2], act_s
+ * [n, F/16], *act_enc; out [n, d] bf16.  d, F multiples of 16. */
+void or_expert_ffn_nvfp4(const uint8_t *xq, const uint8_t *xs, float x_enc, int64_t n, const int32_t *row_expert,
+                         int d, int F, const uint8_t *w13_q, const uint8_t *w13_s, const float *w13_enc,
+                         const uint8_t *w2_q, const uint8_t *w2_s, const float *w2_enc, float *h, uint16_t *act_bf16,
+                         uint8_t *act_q, uint8_t *act_s, float *act_enc, uint16_t *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; r++) {
+        const int64_t e = row_expert[r];
+        const double enc = (double)x_enc * (double)w13_enc[e];
+        for (int64_t j = 0; j < 2 * F; j++) {
+            const int64_t wrow = e * 2 * F + j;
+            h[r * 2 * F + j] = (float)(nvfp4_dot(xq + r * (d / 2), xs + r * (d / 16), w13_q + wrow * (d / 2),
+                                                 w13_s + wrow * (d / 16), d) /
+                                       enc);
         }
+        for (int64_t c = 0; c < F; c++) {
+            const double g = h[r * 2 * F + c], u = h[r * 2 * F + F + c];
+            act_bf16[r * F + c] = or_f32_to_bf16((float)((g / (1.0 + exp(-g))) * u));
+        }
+    }
+    or_quant_nvfp4(act_bf16, n, F, F, act_q, act_s, act_enc);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; r++) {
+        const int64_t e = row_expert[r];
+        const double enc = (double)(*act_enc) * (double)w2_enc[e];
+        for (int64_t c = 0; c < d; c++) {
+            const int64_t wrow = e * d + c;
+            const double v = nvfp4_dot(act_q + r * (F / 2), act_s + r * (F / 16), w2_q + wrow * (F / 2),
+                                       w2_s + wrow * (F / 16), F) /
+                             enc;
+            out[r * d + c] = or_f32_to_bf16((float)v);
+        }
+    }
 }
 
 /* ------------------------------------------------------------------ */

@@ -59,6 +59,7 @@ def _load():
                 "or_e2m1_encode": (ctypes.c_uint8, [F]),
                 "or_quant_nvfp4": (None, [P, I64, I64, I64, P, P, P]),
                 "or_gemm_nvfp4": (None, [P, P, F, P, P, F, I64, I64, I64, P]),
+                "or_expert_ffn_nvfp4": (None, [P, P, F, I64, P, I, I, P, P, P, P, P, P, P, P, P, P, P, P]),
                 "or_quant_1x128": (None, [P, I64, I64, I64, P, P]),
                 "or_quant_128x128": (None, [P, I64, I64, I64, P, P]),
                 "or_router_logits": (None, [P, P, I64, I, I, P]),
@@ -208,6 +209,41 @@ def gemm_nvfp4(aq: np.ndarray, as_: np.ndarray, a_enc: float, bq: np.ndarray, bs
     out = np.empty((M, N), np.float64)
     _load().or_gemm_nvfp4(_p(aq), _p(as_), a_enc, _p(bq), _p(bs), b_enc, M, N, K, _p(out))
     return out
+
+
+def expert_ffn_nvfp4(xq: np.ndarray, xs: np.ndarray, x_enc: float, row_expert: np.ndarray,
+                     w13_q: np.ndarray, w13_s: np.ndarray, w13_enc: np.ndarray,
+                     w2_q: np.ndarray, w2_s: np.ndarray, w2_enc: np.ndarray):
+    """SwiGLU FFN in NVFP4 on sorted rows: x rows (packed [n, d/2], scales [n, d/16], tensor scale x_enc),
+    w13 [E, 2F, d/2] / [E, 2F, d/16] / [E], w2 [E, d, F/2] / [E, d, F/16] / [E].
+    Returns (h [n, 2F] f32, act bf16 bits [n, F], act_q [n, F/2], act_s [n, F/16], act_enc, out bf16 bits [n, d])."""
+    xq = _c(xq, np.uint8)
+    xs = _c(xs, np.uint8)
+    re = _c(row_expert, np.int32)
+    w13_q = _c(w13_q, np.uint8)
+    w13_s = _c(w13_s, np.uint8)
+    w13_enc = _c(w13_enc, np.float32)
+    w2_q = _c(w2_q, np.uint8)
+    w2_s = _c(w2_s, np.uint8)
+    w2_enc = _c(w2_enc, np.float32)
+    n, d = xq.shape[0], xq.shape[1] * 2
+    Ew, twoF = w13_q.shape[0], w13_q.shape[1]
+    F = twoF // 2
+    assert w13_q.shape == (Ew, twoF, d // 2) and w13_s.shape == (Ew, twoF, d // 16) and w13_enc.shape == (Ew,)
+    assert w2_q.shape == (Ew, d, F // 2) and w2_s.shape == (Ew, d, F // 16) and w2_enc.shape == (Ew,)
+    assert xs.shape == (n, d // 16) and re.shape == (n,) and F % 16 == 0
+    if n:
+        assert re.min() >= 0 and re.max() < Ew
+    h = np.empty((n, twoF), np.float32)
+    act = np.empty((n, F), np.uint16)
+    act_q = np.empty((n, F // 2), np.uint8)
+    act_s = np.empty((n, F // 16), np.uint8)
+    act_enc = ctypes.c_float(0.0)
+    out = np.empty((n, d), np.uint16)
+    _load().or_expert_ffn_nvfp4(_p(xq), _p(xs), x_enc, n, _p(re), d, F, _p(w13_q), _p(w13_s), _p(w13_enc),
+                                _p(w2_q), _p(w2_s), _p(w2_enc), _p(h), _p(act), _p(act_q), _p(act_s),
+                                ctypes.byref(act_enc), _p(out))
+    return h, act, act_q, act_s, act_enc.value, out
 
 
 def router_logits(x_bf16: np.ndarray, wr_bf16: np.ndarray) -> np.ndarray:

@@ -150,3 +150,54 @@ def test_gemm_nvfp4_against_float64(oracle):
     # the typical entry)
     exact = a.double().numpy() @ b.double().numpy().T
     assert np.abs(out - exact).max() / np.abs(exact).max() < 0.25
+
+
+def _deq(q, s, enc):
+    return _decode_codes(_unpack(q)) * np.repeat(e4m3_to_f64(s), 16, axis=1) / enc
+
+
+def test_expert_ffn_nvfp4_stages_against_float64(oracle):
+    """Two experts (rows interleaved): GEMM1 against a float64 product of
+    operands decoded here (within binary32 rounding), act against torch's
+    float64 silu (within bf16 rounding), the act re-quantisation against the
+    quantiser applied to that act, GEMM2 against float64 (within bf16
+    rounding), and the whole FFN against the unquantised float64 SwiGLU
+    layer (4-bit operands: a loose bound)."""
+    from tests.helpers import bf16_to_f64
+    g = torch.Generator().manual_seed(21)
+    E, d, F, n = 2, 128, 96, 40
+    x = torch.randn(n, d, generator=g).to(torch.bfloat16)
+    w13 = (torch.randn(E, 2 * F, d, generator=g) * 0.05).to(torch.bfloat16)
+    w2 = (torch.randn(E, d, F, generator=g) * 0.05).to(torch.bfloat16)
+    re = (np.arange(n) % E).astype(np.int32)
+    xq, xs, xe = oracle.quant_nvfp4(bf16_bits(x))
+    qs = [oracle.quant_nvfp4(bf16_bits(w13[e])) for e in range(E)]
+    q2 = [oracle.quant_nvfp4(bf16_bits(w2[e])) for e in range(E)]
+    w13q, w13s = np.stack([a[0] for a in qs]), np.stack([a[1] for a in qs])
+    w13e = np.array([a[2] for a in qs], np.float32)
+    w2q, w2s = np.stack([a[0] for a in q2]), np.stack([a[1] for a in q2])
+    w2e = np.array([a[2] for a in q2], np.float32)
+    h, act, aq, as_, ae, out = oracle.expert_ffn_nvfp4(xq, xs, xe, re, w13q, w13s, w13e, w2q, w2s, w2e)
+    xd = _deq(xq, xs, xe)
+    h_ref = np.stack([xd[r] @ _deq(w13q[re[r]], w13s[re[r]], w13e[re[r]]).T for r in range(n)])
+    assert np.all(np.abs(h - h_ref) <= np.abs(h_ref) * 2.0 ** -23 + 1e-30)
+    gt, up = torch.from_numpy(h[:, :F]).double(), torch.from_numpy(h[:, F:]).double()
+    act_ref = (torch.nn.functional.silu(gt) * up).numpy()
+    assert np.all(np.abs(bf16_to_f64(act) - act_ref) <= np.abs(act_ref) * 2.0 ** -8 + 1e-30)
+    rq, rs, renc = oracle.quant_nvfp4(act)
+    np.testing.assert_array_equal(aq, rq)
+    np.testing.assert_array_equal(as_, rs)
+    assert ae == renc
+    ad = _deq(aq, as_, ae)
+    out_ref = np.stack([ad[r] @ _deq(w2q[re[r]], w2s[re[r]], w2e[re[r]]).T for r in range(n)])
+    assert np.all(np.abs(bf16_to_f64(out) - out_ref) <= np.abs(out_ref) * 2.0 ** -8 * (1 + 2.0 ** -20) + 1e-30)
+    # end to end against the unquantised layer
+    xf = x.double()
+    exact = []
+    for r in range(n):
+        hh = xf[r] @ w13[re[r]].double().T
+        a = torch.nn.functional.silu(hh[:F]) * hh[F:]
+        exact.append((a @ w2[re[r]].double().T).numpy())
+    exact = np.stack(exact)
+    err = np.abs(bf16_to_f64(out) - exact).max(1) / np.abs(exact).max(1)
+    assert err.max() < 0.5, err.max()
