@@ -330,13 +330,17 @@ __device__ void build_schedule(SmemT &s, const ParamsT &p, int n_tiles)
     for (int base = 0; base <= p.E; base += 32) {
         const int e = base + lane;
         int32_t lo = 0, hi = 0;
+        // offsets outside [0, max_rows] are clipped into it (and flagged), so
+        // no tile ever addresses a row outside the buffers
         if (e <= p.E) {
             lo = __ldg(p.offsets + e);
+            if (lo < 0) { lo = 0; clipped = true; }
             if ((int64_t)lo > p.max_rows) { lo = (int32_t)p.max_rows; clipped = true; }
             s.row_lo[e] = lo;
         }
         if (e < p.E) {
             hi = __ldg(p.offsets + e + 1);
+            if (hi < 0) hi = 0;
             if ((int64_t)hi > p.max_rows) hi = (int32_t)p.max_rows;
         }
         const int32_t tiles = (e < p.E && hi > lo) ? ((hi - lo + BM - 1) / BM) * n_tiles : 0;
@@ -354,19 +358,147 @@ __device__ void build_schedule(SmemT &s, const ParamsT &p, int n_tiles)
 
 // ------------------------------------------------------------------ kernel
 
+// The forward kernel runs twelve warps in three warpgroups:
+//   warps 0-7   promotion and tile epilogue (warpgroups 0 and 1, 224
+//               registers each after setmaxnreg): warp w reads TMEM lane
+//               quadrant w % 4 (32 rows) and column half w / 4 (128 of the
+//               256 accumulator columns: GEMM1 64 gate + 64 up columns of the
+//               same 64 act columns, GEMM2 one 128-column weight block), so
+//               each thread keeps 128 promoted accumulators in registers;
+//   warp 8      TMA producer (4-stage ring, as before);
+//   warp 9      MMA issuer and TMEM owner;
+//   warp 10     scale warp: per K block it copies the rows' scales sa[r, kb]
+//               and the two weight-block scales (GEMM1: gate and up blocks;
+//               GEMM2: the tile's two 128-column blocks) into a shared-memory
+//               ring of FT_SLOTS slots with register-free cp.async copies, so
+//               up to FT_SLOTS K blocks of scales are in flight and their L2
+//               latency never reaches the promotion warps;
+//   warp 11     idle (completes warpgroup 2 for setmaxnreg).
+// Per K block a promotion thread reads its 128 columns as two rounds of two
+// 32-column TMEM loads (one wait per round) and releases the TMEM buffer as
+// soon as the second round has landed in registers, before its FMAs, so the
+// MMA of K block kb + 2 waits only for the reads of K block kb.
+constexpr int FT_THREADS = 384;
+constexpr int FT_EPI_WARPS = 8;
+constexpr int FT_PRODUCER = 8;
+constexpr int FT_MMA = 9;
+constexpr int FT_SCALE = 10;
+constexpr int FT_SLOTS = 16;           // scale ring (K blocks whose scales may be in flight)
+constexpr int FT_LAUNCH_REGS = 168;    // registers per thread at launch (12 warps, one CTA per SM)
+constexpr int FT_EPI_REGS = 224;       // promotion warpgroups after setmaxnreg.inc
+constexpr int FT_AUX_REGS = 56;        // warpgroup 2 after setmaxnreg.dec
+static_assert(FT_EPI_WARPS * 32 * FT_EPI_REGS + (FT_THREADS - FT_EPI_WARPS * 32) * FT_AUX_REGS <=
+                  FT_THREADS * FT_LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+
+struct SmemF {
+    uint8_t a[STAGES][A_BYTES];
+    uint8_t b[STAGES][B_BYTES];
+    float sa[FT_SLOTS][BM];             // K block j's row scales in slot j % FT_SLOTS
+    float sb[FT_SLOTS][4];              //   and its two weight-block scales
+    float red[2][2][BM];                // GEMM1: per-half partial amax (by tile parity)
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t sfull[FT_SLOTS];
+    uint64_t sempty[FT_SLOTS];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int32_t tile_prefix[MAX_E + 1];     // tiles before expert e
+    int32_t row_lo[MAX_E + 1];          // clipped expert row ranges
+};
+constexpr size_t SMEM_F_BYTES = sizeof(SmemF) + 1024;  // + alignment slack
+static_assert(SMEM_F_BYTES <= 227 * 1024, "forward GEMM shared memory");
+
+// 4-byte asynchronous global -> shared copy (no register holds the value)
+__device__ __forceinline__ void cp_async4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// one arrival on `bar` once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival)
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
+// 32 TMEM lanes x 32 columns into r[0..31], completion left to a tied wait
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+                   "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+                   "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+
+// ties 32 more registers after a preceding tcgen05.wait::ld (no instruction):
+// volatile statements keep their order, so no use of r moves above the wait
+__device__ __forceinline__ void tmem_tie32(uint32_t *r)
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// acc[i] = fma(c, v[i], acc[i]) for 64 values, two per packed instruction
+// (each lane of the pair rounded as the scalar fmaf)
+__device__ __forceinline__ void promote64(float *acc, const uint32_t *v, float c)
+{
+    const float2 c2 = make_float2(c, c);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+        const float2 r = __ffma2_rn(c2, make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                    make_float2(acc[i], acc[i + 1]));
+        acc[i] = r.x;
+        acc[i + 1] = r.y;
+    }
+}
+
+// barrier over the two promotion warps of TMEM lane quarter q (warps q and
+// q + 4; named barrier 1 + q) that also ORs a predicate across them
+__device__ __forceinline__ bool pair_bar_or(int q, bool pred)
+{
+    uint32_t out;
+    asm volatile("{\n\t.reg .pred p, r;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "barrier.cta.red.or.pred r, %2, 64, p;\n\tselp.u32 %0, 1, 0, r;\n\t}"
+                 : "=r"(out)
+                 : "r"((uint32_t)pred), "r"(1 + q)
+                 : "memory");
+    return out != 0;
+}
+
 // GATHER (the gathered form): GEMM1 loads its A rows straight from the
 // token-major activation codes (row = sorted_to_slot[r] / top_k, four rows
 // per tile::gather4, one per producer lane) and takes their scales from the
 // token-major scale array; GEMM2 writes each output row to its slot
 // (row sorted_to_slot[r] of a [T*top_k, d] array) instead of its sorted
-// position.
+// position.  A slot outside [0, max_rows) marks its row as not routed: it
+// gathers token 0, stores nothing and sets MOE_DEV_ROWS.
 template <int MODE, bool GATHER>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(FT_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                         const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
-    Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemF &s = *reinterpret_cast<SmemF *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // K extent and N tiling of this GEMM
@@ -381,7 +513,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&s.tfull[i], 1);
-            mbar_init(&s.tempty[i], EPI_WARPS);
+            mbar_init(&s.tempty[i], FT_EPI_WARPS);
+        }
+        for (int i = 0; i < FT_SLOTS; i++) {
+            mbar_init(&s.sfull[i], 32);
+            mbar_init(&s.sempty[i], FT_EPI_WARPS);
         }
         mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
@@ -389,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 0) build_schedule(s, p, n_tiles);
-    if (warp == MMA_WARP) tmem_alloc(&s.tmem_base, TMEM_COLS);
+    if (warp == FT_MMA) tmem_alloc(&s.tmem_base, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -397,7 +533,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int total = s.tile_prefix[p.E];
     volatile int *abort_flag = &s.abort_flag;
 
-    if (warp == PRODUCER_WARP) {
+    if (warp >= FT_EPI_WARPS) {
+    setmaxnreg_dec<FT_AUX_REGS>();
+    if (warp == FT_PRODUCER) {
         // ---------------- TMA producer ----------------
         // lane 0 alone, or the whole warp when it gathers A rows
         constexpr bool GA = GATHER && MODE == 1;
@@ -412,7 +550,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
                         const int r = 4 * lane + i;
-                        if (r < tl.rows) tok[i] = __ldg(p.sorted_to_slot + tl.row0 + r) / p.top_k;
+                        if (r < tl.rows) {
+                            const int32_t slot = __ldg(p.sorted_to_slot + tl.row0 + r);
+                            if (slot >= 0 && (int64_t)slot < p.max_rows) tok[i] = slot / p.top_k;
+                        }
                     }
                 }
                 for (int kb = 0; kb < nkb; kb++, j++) {
@@ -452,7 +593,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 while (!mbar_try_wait(&s.full[i], (last / STAGES) & 1) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
             }
         }
-    } else if (warp == MMA_WARP) {
+    } else if (warp == FT_MMA) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_f8(BM, BN);
@@ -482,143 +623,187 @@ __global__ void __launch_bounds__(THREADS, 1)
             while (!mbar_try_wait(&s.mma_done, 0) && globaltimer_ns() - t0 < TIMEOUT_NS) {}
         }
         __syncwarp();
+    } else if (warp == FT_SCALE) {
+        // ---------------- scale warp ----------------
+        // walks the same (tile, K block) sequence as the MMA; lane i copies
+        // the scales of rows i, i+32, i+64, i+96, lanes 0 and 1 the two
+        // weight-block scales
+        const int nkb_a = K / 128;     // A scale row length
+        uint32_t j = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const Tile tl = decode_tile(s, p.E, n_tiles, t);
+            const float *pa[4];        // owned rows' scale rows (null: no row)
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int r = lane + 32 * i;
+                pa[i] = nullptr;
+                if (r < tl.rows) {
+                    int64_t row = (int64_t)tl.row0 + r;
+                    if (GATHER && MODE == 1) {
+                        const int32_t slot = __ldg(p.sorted_to_slot + row);
+                        row = (slot >= 0 && (int64_t)slot < p.max_rows) ? slot / p.top_k : -1;
+                    }
+                    if (row >= 0) pa[i] = p.a_scales + row * nkb_a;
+                }
+            }
+            const float *pb = nullptr;  // this lane's weight-block scale row (lanes 0, 1)
+            if (lane < 2) {
+                if (MODE == 1) {
+                    pb = p.b_scales + ((int64_t)tl.e * (2 * p.F / 128) + (lane ? p.F / 128 : 0) + tl.n_blk) * nkb;
+                } else {
+                    const int nbk = tl.n_blk * 2 + lane;
+                    if (nbk < p.d / 128) pb = p.b_scales + ((int64_t)tl.e * (p.d / 128) + nbk) * nkb;
+                }
+            }
+            for (int kb = 0; kb < nkb; kb++, j++) {
+                const int slot = j % FT_SLOTS;
+                if (!wait_or_abort(&s.sempty[slot], ((j / FT_SLOTS) & 1) ^ 1, abort_flag, p.dev_status)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    if (pa[i]) cp_async4(&s.sa[slot][lane + 32 * i], pa[i] + kb);
+                if (lane < 2) {
+                    if (pb) cp_async4(&s.sb[slot][lane], pb + kb);
+                    else s.sb[slot][lane] = 0.0f;
+                }
+                cp_async_arrive_noinc(&s.sfull[slot]);
+            }
+        }
+        // no copy may still be in flight when the CTA exits
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
     } else {
-        // ---------------- epilogue (warps 0..15) ----------------
+        setmaxnreg_inc<FT_EPI_REGS>();
+        // ---------------- promotion + tile epilogue (warps 0..7) ----------------
         const int q = warp & 3;        // TMEM lane quadrant = rows 32q .. 32q+31
-        const int cg = warp >> 2;      // column group 0..3
+        const int cg = warp >> 2;      // column half 0..1
         const int r_in = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        const int nkb_a = K / 128;     // A scale row length
+        // accumulator columns of this thread: GEMM1 gate 64cg.. and up
+        // 128+64cg..; GEMM2 the 128-column run 128cg..
+        const int col0 = MODE == 1 ? 64 * cg : 128 * cg;
+        const int col1 = MODE == 1 ? 128 + 64 * cg : 128 * cg + 64;
         uint32_t j = 0;
         bool aborted = false;
         bool stop = false;     // GEMM1: abort decided at the row quarter's amax exchange
         int red_par = 0;       // GEMM1: exchange buffer of this tile
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile tl = decode_tile(s, p.E, n_tiles, t);
-            const bool row_ok = r_in < tl.rows;
+            bool row_ok = r_in < tl.rows;
             const int64_t row = (int64_t)tl.row0 + r_in;
-            // gathered form: GEMM1 scales by token, GEMM2 stores by slot
-            int64_t srow = row, orow = row;
-            if (GATHER && row_ok) {
+            // gathered form: GEMM2 stores by slot
+            int64_t orow = row;
+            if (GATHER && MODE == 2 && row_ok) {
                 const int32_t slot = __ldg(p.sorted_to_slot + row);
-                if (MODE == 1) srow = slot / p.top_k;
-                else orow = slot;
+                if (slot >= 0 && (int64_t)slot < p.max_rows) {
+                    orow = slot;
+                } else {
+                    row_ok = false;
+                    dev_flag(p.dev_status, MOE_DEV_ROWS);
+                }
             }
-            // accumulator columns of this thread: two 32-wide halves (GEMM1:
-            // gate 32cg.., up 128+32cg..) or one 64-wide run (GEMM2: 64cg..)
-            const int col0 = MODE == 1 ? 32 * cg : 64 * cg;
-            const int col1 = MODE == 1 ? 128 + 32 * cg : 64 * cg + 32;
-            // weight-scale rows (128-column blocks) of the two halves
-            const int64_t nb0 = MODE == 1 ? (int64_t)tl.e * (2 * p.F / 128) + tl.n_blk
-                                          : (int64_t)tl.e * (p.d / 128) + tl.n_blk * 2 + (cg >> 1);
-            const int64_t nb1 = MODE == 1 ? nb0 + p.F / 128 : nb0;
-            const bool nb_ok = MODE == 1 || (tl.n_blk * 2 + (cg >> 1)) < p.d / 128;
-            float acc0[32], acc1[32];
+            if (GATHER && MODE == 1 && row_ok) {
+                const int32_t slot = __ldg(p.sorted_to_slot + row);
+                if (slot < 0 || (int64_t)slot >= p.max_rows) {
+                    row_ok = false;
+                    dev_flag(p.dev_status, MOE_DEV_ROWS);
+                }
+            }
+            float acc[128];
 #pragma unroll
-            for (int i = 0; i < 32; i++) acc0[i] = acc1[i] = 0.0f;
-            float sa_next = row_ok ? __ldg(p.a_scales + srow * nkb_a) : 0.0f;
+            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
             for (int kb = 0; kb < nkb; kb++, j++) {
                 const int buf = j & 1;
-                const float sa = sa_next;
-                if (kb + 1 < nkb) sa_next = row_ok ? __ldg(p.a_scales + srow * nkb_a + kb + 1) : 0.0f;
-                const float sb0 = nb_ok ? __ldg(p.b_scales + nb0 * nkb + kb) : 0.0f;
-                const float sb1 = nb_ok ? __ldg(p.b_scales + nb1 * nkb + kb) : 0.0f;
-                const float c0 = sa * sb0, c1 = sa * sb1;
+                const int slot = j % FT_SLOTS;
+                float c0 = 0.0f, c1 = 0.0f;
+                if (!aborted && !wait_or_abort(&s.sfull[slot], (j / FT_SLOTS) & 1, abort_flag, p.dev_status))
+                    aborted = true;
+                if (!aborted) {
+                    const float sa = s.sa[slot][r_in];
+                    c0 = sa * s.sb[slot][MODE == 1 ? 0 : cg];
+                    c1 = MODE == 1 ? sa * s.sb[slot][1] : c0;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.sempty[slot]);
+                }
                 if (!aborted && !wait_or_abort(&s.tfull[buf], (j >> 1) & 1, abort_flag, p.dev_status))
                     aborted = true;
                 if (!aborted) {
                     tc_fence_after();
                     const uint32_t base = tmem + lane_addr + buf * BN;
-                    // acc += c * v, two columns per packed instruction (each
-                    // lane of the pair rounded as the scalar fmaf)
-                    const float2 c02 = make_float2(c0, c0), c12 = make_float2(c1, c1);
-                    float v[16];
-#pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        tmem_ld16(base + col0 + 16 * h, v);
-#pragma unroll
-                        for (int i = 0; i < 16; i += 2) {
-                            const float2 r = __ffma2_rn(c02, make_float2(v[i], v[i + 1]),
-                                                        make_float2(acc0[16 * h + i], acc0[16 * h + i + 1]));
-                            acc0[16 * h + i] = r.x;
-                            acc0[16 * h + i + 1] = r.y;
-                        }
-                    }
-#pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        tmem_ld16(base + col1 + 16 * h, v);
-#pragma unroll
-                        for (int i = 0; i < 16; i += 2) {
-                            const float2 r = __ffma2_rn(c12, make_float2(v[i], v[i + 1]),
-                                                        make_float2(acc1[16 * h + i], acc1[16 * h + i + 1]));
-                            acc1[16 * h + i] = r.x;
-                            acc1[16 * h + i + 1] = r.y;
-                        }
-                    }
+                    uint32_t v[64];
+                    tmem_ld32_nowait(base + col0, v);
+                    tmem_ld32_nowait(base + col0 + 32, v + 32);
+                    tmem_wait_ld32(v);
+                    tmem_tie32(v + 32);
+                    promote64(acc, v, c0);
+                    tmem_ld32_nowait(base + col1, v);
+                    tmem_ld32_nowait(base + col1 + 32, v + 32);
+                    tmem_wait_ld32(v);
+                    tmem_tie32(v + 32);
+                    // the partial is in registers: hand the buffer back first
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&s.tempty[buf]);
+                    promote64(acc + 64, v, c1);
                 }
             }
             if (MODE == 1) {
                 if (p.h_out != nullptr && row_ok && !aborted) {
                     // the pre-activations, kept for the backward: gate then up columns
-                    float4 *hg = reinterpret_cast<float4 *>(p.h_out + row * 2 * p.F + tl.n_blk * 128 + 32 * cg);
-                    float4 *hu = reinterpret_cast<float4 *>(p.h_out + row * 2 * p.F + p.F + tl.n_blk * 128 + 32 * cg);
+                    float4 *hg = reinterpret_cast<float4 *>(p.h_out + row * 2 * p.F + tl.n_blk * 128 + 64 * cg);
+                    float4 *hu = reinterpret_cast<float4 *>(p.h_out + row * 2 * p.F + p.F + tl.n_blk * 128 + 64 * cg);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        hg[i] = make_float4(acc0[4 * i], acc0[4 * i + 1], acc0[4 * i + 2], acc0[4 * i + 3]);
-                        hu[i] = make_float4(acc1[4 * i], acc1[4 * i + 1], acc1[4 * i + 2], acc1[4 * i + 3]);
+                    for (int i = 0; i < 16; i++) {
+                        hg[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                        hu[i] = make_float4(acc[64 + 4 * i], acc[64 + 4 * i + 1], acc[64 + 4 * i + 2], acc[64 + 4 * i + 3]);
                     }
                 }
-                // act = silu(gate) * up for 32 of the tile's 128 act columns
+                // act = silu(gate) * up for 64 of the tile's 128 act columns
                 float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    const float g = acc0[i];
-                    acc0[i] = __fdiv_rn(g, 1.0f + expf(-g)) * acc1[i];
-                    amax = fmaxf(amax, fabsf(acc0[i]));
+                for (int i = 0; i < 64; i++) {
+                    const float g = acc[i];
+                    acc[i] = __fdiv_rn(g, 1.0f + expf(-g)) * acc[64 + i];
+                    amax = fmaxf(amax, fabsf(acc[i]));
                 }
-                // the row's amax over the four column groups: the warps of
-                // row quarter q meet at their own barrier, which also ORs
-                // their abort state so that they leave together; the
-                // exchange buffer alternates by tile, so the next tile's
-                // writes never meet this tile's reads
+                // the row's amax over both halves: the two warps of row
+                // quarter q meet at their own barrier, which also ORs their
+                // abort state so that they leave together; the exchange
+                // buffer alternates by tile, so the next tile's writes never
+                // meet this tile's reads
                 s.red[red_par][cg][r_in] = amax;
-                stop = quarter_bar_or(q, aborted || *abort_flag);
-                amax = fmaxf(fmaxf(s.red[red_par][0][r_in], s.red[red_par][1][r_in]),
-                             fmaxf(s.red[red_par][2][r_in], s.red[red_par][3][r_in]));
+                stop = pair_bar_or(q, aborted || *abort_flag);
+                amax = fmaxf(s.red[red_par][0][r_in], s.red[red_par][1][r_in]);
                 red_par ^= 1;
                 const float sc = block_scale(amax);
                 if (row_ok && !aborted) {
-                    uint32_t w[8];
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.act_q + row * p.F + tl.n_blk * 128 + 64 * cg);
 #pragma unroll
-                    for (int i = 0; i < 8; i++)
-                        w[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i], sc), __fdiv_rn(acc0[4 * i + 1], sc)) |
-                               ((uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sc),
-                                                      __fdiv_rn(acc0[4 * i + 3], sc))
-                                << 16);
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.act_q + row * p.F + tl.n_blk * 128 + 32 * cg);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int u = 0; u < 4; u++) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const float *a = acc + 16 * u + 4 * i;
+                            w[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(a[0], sc), __fdiv_rn(a[1], sc)) |
+                                   ((uint32_t)pack_e4m3x2(__fdiv_rn(a[2], sc), __fdiv_rn(a[3], sc)) << 16);
+                        }
+                        dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
                     if (cg == 0) p.act_s[row * (p.F / 128) + tl.n_blk] = sc;
                 }
             } else {
-                const int c_glob = tl.n_blk * BN + 64 * cg;
+                const int c_glob = tl.n_blk * BN + 128 * cg;
                 if (row_ok && !aborted && c_glob < p.d) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * p.d + c_glob);
 #pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        dst[i] = make_uint4(pack_bf16x2(acc0[8 * i], acc0[8 * i + 1]),
-                                            pack_bf16x2(acc0[8 * i + 2], acc0[8 * i + 3]),
-                                            pack_bf16x2(acc0[8 * i + 4], acc0[8 * i + 5]),
-                                            pack_bf16x2(acc0[8 * i + 6], acc0[8 * i + 7]));
-#pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        dst[4 + i] = make_uint4(pack_bf16x2(acc1[8 * i], acc1[8 * i + 1]),
-                                                pack_bf16x2(acc1[8 * i + 2], acc1[8 * i + 3]),
-                                                pack_bf16x2(acc1[8 * i + 4], acc1[8 * i + 5]),
-                                                pack_bf16x2(acc1[8 * i + 6], acc1[8 * i + 7]));
+                    for (int i = 0; i < 16; i++)
+                        dst[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]),
+                                            pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
+                                            pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
+                                            pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
                 }
             }
             // GEMM1 leaves by its row quarter's decision; GEMM2's warps share
@@ -630,7 +815,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == FT_MMA) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// Registers per thread the forward kernel was compiled to launch with.  The
+// setmaxnreg split inside it assumes exactly FT_LAUNCH_REGS: with fewer, the
+// promotion warps' setmaxnreg.inc could not be satisfied and would wait, so
+// the host refuses to launch unless the count matches.
+template <int MODE, bool GATHER>
+static bool forward_kernel_regs_ok()
+{
+    static const bool ok = [] {
+        cudaFuncAttributes a;
+        if (cudaFuncGetAttributes(&a, grouped_gemm_kernel<MODE, GATHER>) != cudaSuccess) return false;
+        return a.numRegs == FT_LAUNCH_REGS;
+    }();
+    return ok;
 }
 
 // ------------------------------------------------------------------ host
@@ -1380,10 +1580,11 @@ static moe_status ffn_launch(const uint8_t *xq, int64_t x_rows, const float *xs,
     prm.d = d;
     prm.F = F;
     prm.top_k = top_k;
+    if (!forward_kernel_regs_ok<1, GATHER>() || !forward_kernel_regs_ok<2, GATHER>()) return MOE_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(grouped_gemm_kernel<1, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess ||
+                             (int)SMEM_F_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(grouped_gemm_kernel<2, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
+                             (int)SMEM_F_BYTES) != cudaSuccess)
         return MOE_ERR_CUDA;
     const int grid = sm_count();
     cudaStream_t st = as_stream(stream);
@@ -1391,11 +1592,11 @@ static moe_status ffn_launch(const uint8_t *xq, int64_t x_rows, const float *xs,
     p1.a_scales = xs;
     p1.b_scales = w13_s;
     p1.h_out = h_out;
-    grouped_gemm_kernel<1, GATHER><<<grid, THREADS, SMEM_BYTES, st>>>(ma1, mb1, p1);
+    grouped_gemm_kernel<1, GATHER><<<grid, FT_THREADS, SMEM_F_BYTES, st>>>(ma1, mb1, p1);
     Params p2 = prm;
     p2.a_scales = act_s;
     p2.b_scales = w2_s;
-    grouped_gemm_kernel<2, GATHER><<<grid, THREADS, SMEM_BYTES, st>>>(ma2, mb2, p2);
+    grouped_gemm_kernel<2, GATHER><<<grid, FT_THREADS, SMEM_F_BYTES, st>>>(ma2, mb2, p2);
     return launch_status();
 }
 
@@ -1455,10 +1656,11 @@ MOE_API moe_status moe_grouped_gemm_fp8(const uint8_t *a_q, const float *a_s, co
     prm.d = N;
     prm.F = K;
     prm.top_k = 1;
+    if (!forward_kernel_regs_ok<2, false>()) return MOE_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(grouped_gemm_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
+                             (int)SMEM_F_BYTES) != cudaSuccess)
         return MOE_ERR_CUDA;
-    grouped_gemm_kernel<2, false><<<sm_count(), THREADS, SMEM_BYTES, as_stream(stream)>>>(ma, mb, prm);
+    grouped_gemm_kernel<2, false><<<sm_count(), FT_THREADS, SMEM_F_BYTES, as_stream(stream)>>>(ma, mb, prm);
     return launch_status();
 }
 
