@@ -383,7 +383,7 @@ constexpr int FT_EPI_WARPS = 8;
 constexpr int FT_PRODUCER = 8;
 constexpr int FT_MMA = 9;
 constexpr int FT_SCALE = 10;
-constexpr int FT_SLOTS = 16;           // scale ring (K blocks whose scales may be in flight)
+constexpr int FT_SLOTS = 8;            // scale ring (K blocks whose scales may be in flight)
 constexpr int FT_LAUNCH_REGS = 168;    // registers per thread at launch (12 warps, one CTA per SM)
 constexpr int FT_EPI_REGS = 224;       // promotion warpgroups after setmaxnreg.inc
 constexpr int FT_AUX_REGS = 56;        // warpgroup 2 after setmaxnreg.dec
@@ -397,6 +397,7 @@ struct SmemF {
     float sa[FT_SLOTS][BM];             // K block j's row scales in slot j % FT_SLOTS
     float sb[FT_SLOTS][4];              //   and its two weight-block scales
     float red[2][2][BM];                // GEMM1: per-half partial amax (by tile parity)
+    uint4 ostage[FT_EPI_WARPS][32 * 4]; // GEMM2: a warp's 32 rows x 32 bf16 columns on their way out
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tfull[2];
@@ -762,11 +763,14 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
                     }
                 }
                 // act = silu(gate) * up for 64 of the tile's 128 act columns
+                // (fast exponential and reciprocal: act is re-quantised to
+                // E4M3 next, 3 mantissa bits, so their few-ulp errors move a
+                // code only at a rounding tie)
                 float amax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 64; i++) {
                     const float g = acc[i];
-                    acc[i] = __fdiv_rn(g, 1.0f + expf(-g)) * acc[64 + i];
+                    acc[i] = __fdividef(g, 1.0f + __expf(-g)) * acc[64 + i];
                     amax = fmaxf(amax, fabsf(acc[i]));
                 }
                 // the row's amax over both halves: the two warps of row
@@ -779,6 +783,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
                 amax = fmaxf(s.red[red_par][0][r_in], s.red[red_par][1][r_in]);
                 red_par ^= 1;
                 const float sc = block_scale(amax);
+                const float rs = __frcp_rn(sc);   // one correctly rounded reciprocal per row
                 if (row_ok && !aborted) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.act_q + row * p.F + tl.n_blk * 128 + 64 * cg);
 #pragma unroll
@@ -787,23 +792,50 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 4; i++) {
                             const float *a = acc + 16 * u + 4 * i;
-                            w[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(a[0], sc), __fdiv_rn(a[1], sc)) |
-                                   ((uint32_t)pack_e4m3x2(__fdiv_rn(a[2], sc), __fdiv_rn(a[3], sc)) << 16);
+                            w[i] = (uint32_t)pack_e4m3x2(a[0] * rs, a[1] * rs) |
+                                   ((uint32_t)pack_e4m3x2(a[2] * rs, a[3] * rs) << 16);
                         }
                         dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                     if (cg == 0) p.act_s[row * (p.F / 128) + tl.n_blk] = sc;
                 }
             } else {
+                // bf16 rows leave through a per-warp staging buffer, 32
+                // columns at a time: each lane writes its row's 64 bytes, then
+                // the warp stores 8 rows x 64 contiguous bytes per instruction
+                // (16-byte pieces swizzled by row so that neither side of the
+                // staging has bank conflicts)
                 const int c_glob = tl.n_blk * BN + 128 * cg;
-                if (row_ok && !aborted && c_glob < p.d) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * p.d + c_glob);
+                if (!aborted && c_glob < p.d) {
+                    uint4 *stg = s.ostage[warp];
+                    const int sr = lane >> 2, sp = lane & 3;   // row within a group of 8, 16-byte piece
+                    int64_t drow[4];
+                    bool dok[4];
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        dst[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]),
-                                            pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
-                                            pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
-                                            pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+                    for (int m = 0; m < 4; m++) {
+                        const int rr = sr + 8 * m;
+                        drow[m] = __shfl_sync(0xFFFFFFFFu, orow, rr);
+                        dok[m] = __shfl_sync(0xFFFFFFFFu, (int)row_ok, rr) != 0;
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 4; ch++) {
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const float *a = acc + 32 * ch + 8 * i;
+                            stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
+                                make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                                           pack_bf16x2(a[6], a[7]));
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int m = 0; m < 4; m++) {
+                            const int rr = sr + 8 * m;
+                            const uint4 v = stg[rr * 4 + (sp ^ ((rr >> 1) & 3))];
+                            if (dok[m])
+                                *reinterpret_cast<uint4 *>(p.out + drow[m] * p.d + c_glob + 32 * ch + 8 * sp) = v;
+                        }
+                    }
                 }
             }
             // GEMM1 leaves by its row quarter's decision; GEMM2's warps share
