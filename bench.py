@@ -41,6 +41,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
+L2_FLUSH_BYTES = 512 * 1024 * 1024      # written between timed steps (not timed) so no step starts warm
+FP32_ALU_TFLOPS_DERIVED = 152 * 128 * 2 * 2.07e9 / 1e12   # 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz
 # DRAM bytes (read + write) per routed row of the grouped FFN at d=7168, F=2048,
 # ~256 rows per expert: ncu capture of grouped_gemm_kernel<1> and <2> on the
 # large_e64 profiling shape (A = 16384 rows): 2.649e9 + 0.051e9 + 0.975e9 +
@@ -56,6 +58,64 @@ def _peaks():
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def fp8_peak_tflops(dev, n: int = 8192, reps: int = 10):
+    """Dense FP8 (e4m3 x e4m3 -> bf16) GEMM throughput of cuBLASLt through
+    torch._scaled_mm at n^3, best of `reps` with CUDA events: the measured
+    FP8 peak beside the nominal 2 x bf16 one.  None if unsupported."""
+    import torch
+    try:
+        g = torch.Generator(device=dev).manual_seed(7)
+        a = torch.randn((n, n), generator=g, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), generator=g, device=dev).to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1)
+            best = t if best is None else min(best, t)
+        del a, b
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:                                   # a measurement beside the line, not a step of it
+        return None
+
+
+def cpu_model() -> str:
+    """The host CPU's name (x86 model name, or Arm implementer/part)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    for line in info.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    impl = part = None
+    for line in info.splitlines():
+        if line.startswith("CPU implementer"):
+            impl = line.split(":", 1)[1].strip()
+        elif line.startswith("CPU part"):
+            part = line.split(":", 1)[1].strip()
+    names = {("0x41", "0xd4f"): "Arm Neoverse V2 (NVIDIA Grace)", ("0x41", "0xd40"): "Arm Neoverse V1",
+             ("0x41", "0xd0c"): "Arm Neoverse N1"}
+    if impl and part:
+        return names.get((impl, part), f"Arm implementer {impl} part {part}")
+    return "unknown"
+
+
+def padded_fraction(counts, bm: int = 128) -> float:
+    """Rows the grouped GEMM computes (each expert's rows rounded up to whole
+    bm-row tiles) over the rows routed."""
+    c = [int(v) for v in counts]
+    A = max(sum(c), 1)
+    return sum(bm * ((v + bm - 1) // bm) for v in c) / A
 
 
 class Clocks:
@@ -113,14 +173,16 @@ class Clocks:
 
 # ------------------------------------------------------------------ workload
 
-def build_workload(cfg, dev, seed, gathered=False, ue8m0=False):
+def build_weights(cfg, dev, seed, layer=0, ue8m0=False):
+    """One layer's router weights and 128x128-quantised expert weights (bf16
+    drawn 16 experts at a time, quantised, freed)."""
     import torch
     from block_scaled_fp8_router_gb300 import synthetic as S
-    from block_scaled_fp8_router_gb300.layer import MoELayerFP8, MoEWeightsFP8, quantize_weights
+    from block_scaled_fp8_router_gb300.layer import MoEWeightsFP8, quantize_weights
 
     E, d, F = cfg.E, cfg.d, cfg.F
     sdt = torch.uint8 if ue8m0 else torch.float32     # power-of-two exponents or fp32 scales
-    w = MoEWeightsFP8(S.make_router_w(cfg, dev, seed),
+    w = MoEWeightsFP8(S.make_router_w(cfg, dev, seed, layer),
                       torch.empty((E, 2 * F, d), dtype=torch.uint8, device=dev),
                       torch.empty((E, 2 * F // 128, d // 128), dtype=sdt, device=dev),
                       torch.empty((E, d, F), dtype=torch.uint8, device=dev),
@@ -128,10 +190,18 @@ def build_workload(cfg, dev, seed, gathered=False, ue8m0=False):
     chunk = 16
     for e0 in range(0, E, chunk):
         n = min(chunk, E - e0)
-        w13 = torch.stack([S.make_w13_expert(cfg, e, dev, seed) for e in range(e0, e0 + n)])
-        w2 = torch.stack([S.make_w2_expert(cfg, e, dev, seed) for e in range(e0, e0 + n)])
+        w13 = torch.stack([S.make_w13_expert(cfg, e, dev, seed, layer) for e in range(e0, e0 + n)])
+        w2 = torch.stack([S.make_w2_expert(cfg, e, dev, seed, layer) for e in range(e0, e0 + n)])
         quantize_weights(w13, w2, out=w, e0=e0)
         del w13, w2
+    return w
+
+
+def build_workload(cfg, dev, seed, gathered=False, ue8m0=False):
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    from block_scaled_fp8_router_gb300.layer import MoELayerFP8
+
+    w = build_weights(cfg, dev, seed, 0, ue8m0)
     layer = MoELayerFP8(w, cfg.T, cfg.k, cfg.score_fn, cfg.renorm, cfg.route_scale, gathered=gathered)
     x = S.make_x(cfg, dev, seed)
     replay = S.make_replay_payload(cfg.with_(layers=1), dev, seed)[0] if cfg.mode == "replay" else None
@@ -213,27 +283,35 @@ def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None, ue8m0=F
             dist.barrier()
         torch.cuda.synchronize()
 
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
+        flush.zero_()
         step(False)
     barrier()
-    # ---- device-resident timed region: K steps between two events ----
+    # ---- device-resident timed region: K steps, each bracketed by its own
+    # events, with an L2 flush (a 512 MB write) before each step outside them ----
     with Clocks(dev.index) as clk:
         t0, t1 = ev(), ev()
         t0.record()
-        per = [step(True) for _ in range(steps)]
+        per = []
+        for _ in range(steps):
+            flush.zero_()
+            per.append(step(True))
         t1.record()
         barrier()
     clocks = clk.summary()
-    total_ms = t0.elapsed_time(t1)
+    total_ms = sum(e[0].elapsed_time(e[5]) for e in per)
+    bracket_ms = t0.elapsed_time(t1)
     for e in per:
         for i, n in enumerate(("route", "quant", "dispatch", "ffn", "combine")):
             marks[n].append(e[i].elapsed_time(e[i + 1]))
     status = Lb.check_status(layer.dev_status)
+    padded = padded_fraction(layer.counts.cpu())
 
     if not with_e2e:
         avg = {n: sum(v) / len(v) for n, v in marks.items()}
         total_ms = reduce_max([total_ms], world)[0]
-        return dict(cfg=cfg, total_ms=total_ms, avg=avg, clocks=clocks, status=status, steps=steps)
+        return dict(cfg=cfg, total_ms=total_ms, avg=avg, clocks=clocks, status=status, steps=steps, padded=padded)
 
     # ---- end to end through the public layer API: pinned host x in, y out,
     # copies overlapped with compute by HostStreamer (two copy streams) ----
@@ -274,7 +352,7 @@ def run_gpu(args, rank, world, workload=None, with_e2e=True, steps=None, ue8m0=F
     total_ms, e2e_ms = reduce_max([total_ms, e2e_ms], world)
     avg = {n: sum(v) / len(v) for n, v in marks.items()}
     return dict(cfg=cfg, total_ms=total_ms, e2e_ms=e2e_ms, avg=avg, clocks=clocks, status=status, h2d=h2d,
-                d2h=T * d * 2, x=x, layer=layer)
+                d2h=T * d * 2, x=x, layer=layer, padded=padded, bracket_ms=bracket_ms)
 
 
 def reduce_max(vals, world):
@@ -316,6 +394,10 @@ def rooflines(cfg, avg, peaks, gathered=False, ue8m0=False):
            "traffic_note": "dram read+write bytes of both GEMM kernels from one ncu capture of the profiling shape "
                            "(large_e64: same per-expert shape, 1/4 of the experts), scaled by routed rows"}
     ffn["frac"] = ffn["achieved"] / ffn["peak"]
+    if peaks.get("fp8_tflops_measured"):
+        ffn["peak_fp8_measured"] = peaks["fp8_tflops_measured"]
+        ffn["frac_of_fp8_measured"] = ffn["achieved"] / peaks["fp8_tflops_measured"]
+        ffn["fp8_measured_note"] = "cuBLASLt e4m3 GEMM 8192^3 via torch._scaled_mm, best of 10, this run"
     hbm = peaks["hbm_gbs"]
     row = d + (1 if ue8m0 else 4) * d / 128     # one FP8 row with its 1x128 scales (fp32 or exponent bytes)
     bytes_quant = T * d * 2 + T * row
@@ -329,12 +411,90 @@ def rooflines(cfg, avg, peaks, gathered=False, ue8m0=False):
         "dispatch": {"ms": avg["dispatch"], "GB/s": bytes_disp / (avg["dispatch"] * 1e-3) / 1e9},
         "combine": {"ms": avg["combine"], "GB/s": bytes_comb / (avg["combine"] * 1e-3) / 1e9},
         ("route_topk" if cfg.mode == "route" else "route_replay"):
-            {"ms": avg["route"], "fp32 TFLOP/s": route_flops / (avg["route"] * 1e-3) / 1e12},
+            {"ms": avg["route"], "fp32 TFLOP/s": route_flops / (avg["route"] * 1e-3) / 1e12,
+             "frac_of_fp32_alu_derived": route_flops / (avg["route"] * 1e-3) / 1e12 / FP32_ALU_TFLOPS_DERIVED,
+             "fp32_alu_peak_derived": FP32_ALU_TFLOPS_DERIVED,
+             "peak_note": "derived, not measured: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz"},
         "ffn": {"ms": avg["ffn"]},
     }
     for key in ("quant_1x128", "dispatch", "combine"):
         extra[key]["frac_hbm"] = extra[key]["GB/s"] / hbm
     return ffn, extra
+
+
+def run_multilayer(dev, seed, steps, warmup, peaks):
+    """The stacked replay workload as written: 8 layers of the large shape
+    (d=7168, 256 experts, top-8, F=2048), T=16384 tokens, one routed-experts
+    payload [8, 8, 16384] (30% of slots to 8 hot experts, 8 experts that
+    receive nothing).  All 8 layers' FP8 weights stay resident (8 x 11.3 GB);
+    one sweep runs every layer in turn: replay of its payload slab (gates
+    from its router) -> 1x128 quantisation -> dispatch -> grouped FFN ->
+    combine.  A 512 MB L2 flush precedes each timed sweep."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    from block_scaled_fp8_router_gb300.layer import MoELayerFP8
+    cfg = S.CONFIGS["multilayer_replay"]
+    Ln, T, k, d, F, E = cfg.layers, cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
+    A = T * k
+    payload = S.make_replay_payload(cfg, dev, seed)                 # [L, k, T]
+    weights = [build_weights(cfg, dev, seed, l) for l in range(Ln)]
+    xs = [S.make_x(cfg, dev, seed, l) for l in range(Ln)]
+    layer = MoELayerFP8(weights[0], T, k, cfg.score_fn, cfg.renorm, cfg.route_scale)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    padded = []
+
+    def sweep(ffn_ev=None):
+        for l in range(Ln):
+            layer.w = weights[l]
+            layer.route(xs[l], payload[l])
+            xq, xsc = Lb.fp8_block_quant(xs[l], 1, q=layer.xq[:T], scales=layer.xs[:T])
+            Lb.moe_dispatch(layer.ids[:T], E, rows=xq, row_scales=xsc, expert_counts=layer.counts,
+                            expert_offsets=layer.offsets, sorted_to_slot=layer.s2s[:A], slot_to_sorted=layer.sl2[:A],
+                            rows_sorted=layer.xq_sorted[:A], scales_sorted=layer.xs_sorted[:A], workspace=layer.dsp_ws,
+                            dev_status=layer.dev_status)
+            if ffn_ev: ffn_ev[l][0].record()
+            Lb.moe_grouped_ffn_fp8(layer.xq_sorted[:A], layer.xs_sorted[:A], layer.offsets, layer.w.w13_q,
+                                   layer.w.w13_s, layer.w.w2_q, layer.w.w2_s, out_sorted=layer.out_sorted[:A],
+                                   workspace=layer.ffn_ws, dev_status=layer.dev_status)
+            if ffn_ev: ffn_ev[l][1].record()
+            Lb.moe_combine(layer.out_sorted[:A], layer.sl2[:A], layer.gates[:T], y=layer.y[:T])
+            if ffn_ev is not None and len(padded) < Ln:
+                padded.append(layer.counts.clone())
+
+    for _ in range(warmup):
+        flush.zero_()
+        sweep()
+    torch.cuda.synchronize()
+    per, ffn = [], []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = ev(), ev()
+        fe = [[ev(), ev()] for _ in range(Ln)]
+        a.record()
+        sweep(fe)
+        b.record()
+        per.append((a, b))
+        ffn.append(fe)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in per) / steps
+    ffn_ms = sum(sum(e[0].elapsed_time(e[1]) for e in fe) for fe in ffn) / steps
+    flops = 6.0 * A * d * F * Ln
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    out = {"workload": f"multilayer_replay: {Ln} layers x T={T} d={d} E={E} top_k={k} F={F}, payload "
+                       f"[{Ln}, {k}, {T}] (8 hot / 8 empty experts per layer), all layers' FP8 weights resident "
+                       f"({Ln * (3 * E * d * F) / 1e9:.1f} GB)",
+           "tokens_x_layers/s": T * Ln / (ms * 1e-3), "ms_per_sweep": ms, "ms_per_layer": ms / Ln,
+           "ffn_ms_per_layer": ffn_ms / Ln, "ffn_TFLOP/s": flops / (ffn_ms * 1e-3) / 1e12,
+           "ffn_frac": flops / (ffn_ms * 1e-3) / 1e12 / fp8_peak, "peak": fp8_peak,
+           "gemm_padded_rows_per_layer": [padded_fraction(c.cpu()) for c in padded],
+           "steps": steps, "status": Lb.check_status(layer.dev_status)}
+    if peaks.get("fp8_tflops_measured"):
+        out["ffn_frac_of_fp8_measured"] = flops / (ffn_ms * 1e-3) / 1e12 / peaks["fp8_tflops_measured"]
+    del weights, xs, layer, payload
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_dispatch_combine(dev, seed, steps, warmup, peaks):
@@ -724,23 +884,28 @@ class OracleSample:
         from oracle import oracle as O
         return O.topk(logits, self.cfg.k) if self.replay is None else O.replay(self.replay, self.cfg.E)[0]
 
-    def run(self):
-        """One timed pass of the whole layer over the sample; returns seconds."""
+    def run(self, n: int | None = None, with_y: bool = False):
+        """One timed pass of the whole layer over the first n tokens of the
+        sample (all of it by default); returns seconds (and y's bf16 bits)."""
         import numpy as np
         from oracle import oracle as O
         cfg = self.cfg
+        n = self.n if n is None else n
+        xb = np.ascontiguousarray(self.xb[:n])
+        replay = None if self.replay is None else np.ascontiguousarray(self.replay[:, :n])
         t0 = time.perf_counter()
-        l = O.router_logits(self.xb, self.wrb)
-        ids = self._ids(l)
+        l = O.router_logits(xb, self.wrb)
+        ids = O.topk(l, cfg.k) if replay is None else O.replay(replay, cfg.E)[0]
         g = O.gates(l, ids, cfg.score_fn, cfg.renorm, cfg.route_scale)
-        xq, xs = O.quant_1x128(self.xb)
+        xq, xs = O.quant_1x128(xb)
         counts, offsets, s2s, sl2, _ = O.dispatch(ids, cfg.E)
-        A = self.n * cfg.k
+        A = n * cfg.k
         row_e = self.remap[np.repeat(np.arange(cfg.E, dtype=np.int32), counts)]
         _, _, _, out = O.expert_ffn(O.gather_rows(xq, s2s, A, cfg.k), O.gather_rows(xs, s2s, A, cfg.k),
                                     row_e, *self.w)
-        O.combine(out, sl2, g)
-        return time.perf_counter() - t0
+        y = O.combine(out, sl2, g)
+        secs = time.perf_counter() - t0
+        return (secs, y) if with_y else secs
 
     def describe(self, secs):
         cfg = self.cfg
@@ -749,12 +914,43 @@ class OracleSample:
                 f"{self.n * cfg.k} expert rows, combine); expert weight quantisation untimed; {secs:.2f} s")
 
 
-def cpu_baseline(cfg, seed, n_tokens, gen_dev):
+def error_report(y_gpu_bits, y_ref_bits):
+    """The output comparison of the layer contract on a token sample: per row
+    max |y - ref| / max(max |ref|, 1e-6) (the bar, 2e-2), and element-wise
+    |y - ref| / max(|ref|, 1e-2 * rowmax)."""
+    import numpy as np
+    import torch
+    to64 = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).double().numpy()
+    y, ref = to64(y_gpu_bits), to64(y_ref_bits)
+    rowmax = np.abs(ref).max(axis=1, keepdims=True)
+    row = np.abs(y - ref).max(axis=1) / np.maximum(rowmax[:, 0], 1e-6)
+    elem = np.abs(y - ref) / np.maximum(np.abs(ref), 1e-2 * rowmax)
+    return {"tokens": int(y.shape[0]), "row_rel_err_max": float(row.max()), "elem_rel_err_max": float(elem.max()),
+            "elem_rel_err_mean": float(elem.mean()), "bar_row_rel_err": 2e-2}
+
+
+def cpu_baseline(cfg, seed, n_tokens, gen_dev, y_gpu_bits=None):
+    """The CPU oracle on the host cores: all cores over n_tokens, one thread
+    over n_tokens / 16, and (given the GPU layer's y for the same tokens) the
+    output error of the GPU against it."""
+    import os as _os
     from oracle import oracle as O
     smp = OracleSample(cfg, n_tokens, seed, gen_dev)
-    secs = smp.run()
-    return {"value": n_tokens / secs, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
-            "sample": smp.describe(secs)}
+    secs, y = smp.run(with_y=True)
+    cores = O.num_threads()
+    out = {"value": n_tokens / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": smp.describe(secs), "cpu_model": cpu_model(), "host_cpus": _os.cpu_count()}
+    n1 = max(8, n_tokens // 16)
+    O.set_num_threads(1)
+    try:
+        s1 = smp.run(n1)
+    finally:
+        O.set_num_threads(cores)
+    out["single_thread"] = {"value": n1 / s1, "unit": "tokens/s", "cores": 1,
+                            "sample": f"the first {n1} tokens of the same sample, one thread; {s1:.2f} s"}
+    if y_gpu_bits is not None:
+        out["gpu_vs_oracle"] = error_report(y_gpu_bits[:n_tokens], y)
+    return out
 
 
 # ------------------------------------------------------------------ main
@@ -775,6 +971,8 @@ def main():
     ap.add_argument("--no-mx", action="store_true",
                     help="skip the power-of-two-scale (block-scaled MMA) line and the NVFP4 quantiser timing")
     ap.add_argument("--no-backward", action="store_true", help="skip the expert-path backward line")
+    ap.add_argument("--no-multilayer", action="store_true",
+                    help="skip the 8-layer replay sweep (all layers' FP8 weights resident)")
     ap.add_argument("--router-kernels", action="store_true",
                     help="time only the router kernels (route_topk, route_replay) and print their line")
     ap.add_argument("--hbm-kernels", action="store_true",
@@ -794,7 +992,8 @@ def main():
     config = {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} top_k={cfg.k} F={cfg.F} "
                           f"{'sigmoid' if cfg.score_fn else 'softmax'} {cfg.mode}",
               "tokens_per_gpu": cfg.T, "parallelism": f"token-sharded x{world}" if world > 1 else "single GPU",
-              "l2": "inputs larger than L2 (FP8 expert weights streamed from HBM every step)",
+              "l2": "flushed: a 512 MB device write before every timed step, outside the step's events "
+                    "(the FP8 expert weights, 11.3 GB, are streamed from HBM every step as well)",
               "form": args.form, "scales": args.scales}
     metric = "MoE-layer tokens/s (7168d/256e/top-8 FP8)" if cfg.name == "large" else f"MoE-layer tokens/s ({cfg.name})"
 
@@ -830,7 +1029,8 @@ def main():
                           "vs_baseline": None, "dtype": "f64 block sums, f32 fma chains (CPU oracle)",
                           "data": "synthetic", "config": config,
                           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(),
-                                           "kind": "oracle", "sample": smp.describe(total / args.steps)},
+                                           "kind": "oracle", "sample": smp.describe(total / args.steps),
+                                           "cpu_model": cpu_model()},
                           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}))
         return
@@ -842,9 +1042,13 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     peaks = _peaks()
+    peaks["fp8_tflops_measured"] = fp8_peak_tflops(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
     main_mx = args.scales == "ue8m0"
     r = run_gpu(args, rank, world, ue8m0=main_mx)
     cfg = r["cfg"]
+    y_first = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        y_first = r["layer"].y[:args.cpu_tokens].contiguous().cpu().view(torch.int16).numpy().view("uint16")
     value = job_throughput(cfg.T, args.steps, world, r["total_ms"])
     e2e = job_throughput(cfg.T, args.steps, world, r["e2e_ms"])
     gathered = args.form == "gathered" and not main_mx
@@ -860,7 +1064,11 @@ def main():
            "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                    "d2h_bytes_per_step": r["d2h"]},
            "roofline": ffn, "extra": extra, "gpu_launches": launches * args.steps, "clocks": r["clocks"],
-           "dev_status": r["status"], "peaks_source": peaks["source"]}
+           "dev_status": r["status"], "peaks_source": peaks["source"],
+           "gemm_padded_rows": {"tile_rows": 128, "fraction": r["padded"],
+                                "note": "rows the grouped GEMMs compute (each expert rounded up to 128-row "
+                                        "tiles) over the routed rows"},
+           "timing": {"ms_sum_of_steps": r["total_ms"], "ms_bracket_with_flushes": r["bracket_ms"]}}
     if cfg.name == "large" and not args.no_replay:
         import torch
         del r
@@ -873,9 +1081,15 @@ def main():
                         f"F={rcfg.F}, replayed payload with 8 hot and 8 empty experts, sigmoid gates",
             "tokens/s": job_throughput(rcfg.T, rr["steps"], world, rr["total_ms"]),
             "ms_per_step": rr["total_ms"] / rr["steps"], "ffn_TFLOP/s": rffn["achieved"],
-            "ffn_frac": rffn["frac"], "steps": rextra, "dev_status": rr["status"]}
+            "ffn_frac": rffn["frac"], "ffn_frac_of_fp8_measured": rffn.get("frac_of_fp8_measured"),
+            "gemm_padded_rows": rr["padded"], "steps": rextra, "dev_status": rr["status"]}
         del rr
         torch.cuda.empty_cache()
+    if cfg.name == "large" and not args.no_multilayer and not main_mx:
+        import torch
+        torch.cuda.empty_cache()
+        out["multilayer_sweep"] = run_multilayer(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
+                                                 rank_seed(args.seed, rank), max(3, args.steps // 4), 3, peaks)
     if cfg.name in ("large", "large_e16") and not args.no_backward and not main_mx:
         import torch
         torch.cuda.empty_cache()
@@ -911,7 +1125,7 @@ def main():
         except Exception as exc:   # an extra measurement: report, do not lose the line
             out["nvfp4_quant"] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cfg, args.seed, args.cpu_tokens, "cuda")
+        out["cpu_baseline"] = cpu_baseline(cfg, args.seed, args.cpu_tokens, "cuda", y_first)
     if rank == 0:
         print(json.dumps(out))
     if world > 1:

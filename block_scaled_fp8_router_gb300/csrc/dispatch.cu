@@ -219,7 +219,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint8_t *__restrict__
 // in flight before the first fma (16 x 16 B per lane keeps enough bytes in
 // flight to saturate HBM).  k > 8 runs the slots in groups of 8, in order.
 // SLOTS: the expert outputs are stored in slot order (row t*k + j), and
-// slot_to_sorted only says which slots were routed (>= 0).
+// slot_to_sorted only says which slots were routed (>= 0).  Map entries
+// outside [0, T*k) are skipped, so a corrupt map never reads outside the
+// expert outputs.
 template <bool SLOTS>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ out_sorted,
                                                       const int32_t *__restrict__ slot_to_sorted,
@@ -232,6 +234,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t t = gw; t < T; t += nw) {
         int32_t my_src = lane < k ? __ldg(slot_to_sorted + t * k + lane) : -1;
+        // out_sorted holds at most T*k rows: an entry past them (a map not
+        // written by moe_dispatch) is read as an unrouted slot
+        if ((int64_t)my_src >= (int64_t)T * k) my_src = -1;
         if (SLOTS && my_src >= 0) my_src = (int32_t)(t * k + lane);
         const float my_g = lane < k ? (gates ? __ldg(gates + t * k + lane) : 1.0f) : 0.0f;  // no gates: unit
         for (int v0 = 0; v0 < nvec; v0 += 64) {

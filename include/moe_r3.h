@@ -21,7 +21,9 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued on it; no call synchronises the host or
  *     copies device data to the host, and no call allocates or frees memory.
- *     Scratch memory is caller-provided workspace whose size is queried.
+ *     Scratch memory is caller-provided workspace whose size is queried,
+ *     except for moe_dispatch_noalloc, whose scratch is a static device array
+ *     inside the library (see that call).
  *   - Errors the host can see (NULL pointers, unsupported shapes, misaligned
  *     pointers, short workspace) are returned before anything is launched and
  *     nothing is written.  A failed launch returns MOE_ERR_CUDA.
@@ -29,7 +31,10 @@
  *     caller-zeroed int32 word `dev_status` (nullable: then not reported).
  *     Kernels never write out of bounds because of them.  Every device wait
  *     is bounded; on expiry the kernel sets MOE_DEV_TIMEOUT and returns.
- *   - Calls are thread-safe (no global mutable state) and stream-ordered.
+ *   - Calls are stream-ordered and thread-safe: no call keeps global mutable
+ *     state, except moe_dispatch_noalloc, whose calls share one static
+ *     scratch array, so the caller must order noalloc calls that could
+ *     overlap on the GPU (other streams or threads).
  */
 #ifndef MOE_R3_H
 #define MOE_R3_H
@@ -269,7 +274,8 @@ moe_status moe_dispatch_noalloc(const int32_t *topk_ids, int T, int k, int E, co
  * xq_sorted [max_rows, d] e4m3, xs_sorted [max_rows, d/128] fp32;
  * w13_q [E, 2F, d], w13_s [E, 2F/128, d/128]; w2_q [E, d, F],
  * w2_s [E, d/128, F/128]; out_sorted [max_rows, d] bf16.  max_rows bounds
- * expert_offsets[E] (rows beyond it set MOE_DEV_ROWS and are skipped).
+ * expert_offsets[E]: offsets outside [0, max_rows] are clipped into it and
+ * set MOE_DEV_ROWS, so rows outside the buffers are never read or written.
  * workspace: moe_grouped_ffn_workspace_size(max_rows, d, F) bytes (holds
  * act_q and its scales), 256-byte aligned.
  * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
@@ -296,7 +302,9 @@ moe_status moe_grouped_ffn_fp8(const uint8_t *xq_sorted, const float *xs_sorted,
  *   and moe_combine_slots reads each token's k rows contiguously.
  * xq [T, d] e4m3, xs [T, d/128] fp32, sorted_to_slot and expert_offsets from
  * moe_dispatch (maps only); out_slots [T*k, d] bf16 (rows of unrouted slots
- * are not written); workspace: moe_grouped_ffn_workspace_size(T*k, d, F).
+ * are not written; a sorted_to_slot entry outside [0, T*k) marks its row as
+ * not routed: nothing is stored for it and MOE_DEV_ROWS is set);
+ * workspace: moe_grouped_ffn_workspace_size(T*k, d, F).
  * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
  * ---------------------------------------------------------------------- */
 moe_status moe_grouped_ffn_fp8_gathered(const uint8_t *xq, const float *xs, int T, int k,
@@ -419,6 +427,8 @@ moe_status moe_wgrad_gemm(const uint8_t *a_q, const float *a_sT, const uint8_t *
  *   y[t,c] = bf16( sum_{j=0}^{k-1} gates[t,j] * out_sorted[slot_to_sorted[t*k+j], c] ),
  *   one binary32 fused multiply-add chain over j in slot order from +0,
  *   rounded to nearest even; slots with slot_to_sorted = -1 are skipped.
+ *   slot_to_sorted should come from moe_dispatch unchanged; an entry outside
+ *   [0, T*k) is skipped like -1, so no read leaves out_sorted's T*k rows.
  * out_sorted [*, d] bf16, y [T, d] bf16; d a multiple of 8; out_sorted and y
  * 16-byte aligned.  Errors: NULL, SHAPE, ALIGN.
  * ---------------------------------------------------------------------- */

@@ -29,3 +29,12 @@ def row_rel_err(y: np.ndarray, ref: np.ndarray) -> np.ndarray:
     num = np.abs(y - ref).max(axis=1)
     den = np.maximum(np.abs(ref).max(axis=1), 1e-6)
     return num / den
+
+
+def elem_rel_err(y: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """Element-wise |y - ref| / max(|ref|, 1e-2 * rowmax |ref|) (reported
+    beside the per-row bar)."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rowmax = np.abs(ref).max(axis=1, keepdims=True)
+    return np.abs(y - ref) / np.maximum(np.abs(ref), np.maximum(1e-2 * rowmax, 1e-30))

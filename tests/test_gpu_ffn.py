@@ -75,7 +75,7 @@ def _oracle_ffn(oracle, r, rows):
     ([0, 0, 200, 0], 256, 384),
     ([260, 3, 0, 64], 384, 256),          # d % 256 == 128: GEMM2 N tail
 ])
-def test_grouped_ffn_against_oracle(L, oracle, counts, d, F):
+def test_grouped_ffn_against_oracle(L, oracle, parity_report, counts, d, F):
     r = _run_ffn(L, counts, d, F, seed=len(counts) + d)
     assert r["st"] == 0
     A = r["A"]
@@ -87,10 +87,10 @@ def test_grouped_ffn_against_oracle(L, oracle, counts, d, F):
     g_acts = ws[off: off + A * (F // 128) * 4].view(np.float32).reshape(A, F // 128)
     g_act = e4m3_to_f64(g_actq) * np.repeat(g_acts.astype(np.float64), 128, axis=1)
     ref_act = e4m3_to_f64(act_q) * np.repeat(act_s.astype(np.float64), 128, axis=1)
-    assert row_rel_err(g_act, ref_act).max() <= TOL
+    assert parity_report(f"act {counts[:3]}.. d={d} F={F}", g_act, ref_act).max() <= TOL
     flips = (g_actq != act_q).mean()
     assert flips < 1e-2, flips
-    err = row_rel_err(bf16_to_f64(bf16_bits(r["out"][:A])), bf16_to_f64(out))
+    err = parity_report(f"out {counts[:3]}.. d={d} F={F}", bf16_to_f64(bf16_bits(r["out"][:A])), bf16_to_f64(out))
     assert err.max() <= TOL, err.max()
     print(f"counts={counts} d={d} F={F}: max row rel err {err.max():.2e}, act code flips {flips:.1e}")
 
@@ -112,7 +112,7 @@ def test_grouped_ffn_all_empty(L):
 
 
 @pytest.mark.parametrize("name", ["tiny", "replay"])
-def test_layer_against_oracle(L, oracle, name):
+def test_layer_against_oracle(L, oracle, parity_report, name):
     """The composed layer (route or replay -> quant -> dispatch -> FFN ->
     combine) on the tiny and router-replay workloads, every token checked."""
     from block_scaled_fp8_router_gb300.layer import MoELayerFP8, MoEWeightsFP8, quantize_weights
@@ -147,6 +147,33 @@ def test_layer_against_oracle(L, oracle, name):
     _, _, _, out = oracle.expert_ffn(oracle.gather_rows(xq, s2s, A, cfg.k), oracle.gather_rows(xs, s2s, A, cfg.k),
                                      row_e, *w)
     y_ref = oracle.combine(out, sl2, g)
-    err = row_rel_err(bf16_to_f64(bf16_bits(y)), bf16_to_f64(y_ref))
+    err = parity_report(f"{name} layer y, all tokens", bf16_to_f64(bf16_bits(y)), bf16_to_f64(y_ref))
     assert err.max() <= TOL, err.max()
-    print(f"{name}: layer max row rel err {err.max():.2e}")
+
+
+def test_grouped_ffn_negative_offset_is_clipped(L, oracle):
+    """An expert offset below 0 is clipped to row 0 and flagged
+    (MOE_DEV_ROWS = 0x4): guard rows on both sides of the output and guard
+    bytes before the workspace stay untouched, and the rows inside are the
+    clipped experts' outputs."""
+    d, F, E, mr, guard = 256, 256, 2, 200, 64
+    cfg = S.CONFIGS["tiny"].with_(d=d, F=F, E=E, w_std=0.02)
+    w13, w2, (w13_q, w13_s, w2_q, w2_s) = _weights(L, cfg, range(E), 3)
+    g = torch.Generator(device=DEV).manual_seed(4)
+    x = torch.randn((mr, d), generator=g, device=DEV).to(torch.bfloat16)
+    xq, xs = L.fp8_block_quant(x, 1)
+    offsets = torch.tensor([-50, 100, 200], dtype=torch.int32, device=DEV)
+    buf = torch.full((mr + 2 * guard, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = buf[guard:guard + mr]
+    need = L.moe_grouped_ffn_workspace_size(mr, d, F)
+    ws_buf = torch.full((need + 2 * 4096,), 0xAB, dtype=torch.uint8, device=DEV)
+    ws = ws_buf[4096:4096 + need]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_grouped_ffn_fp8(xq, xs, offsets, w13_q, w13_s, w2_q, w2_s, out_sorted=out, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert L.check_status(st) & 0x4
+    assert torch.isnan(buf[:guard].float()).all() and torch.isnan(buf[guard + mr:].float()).all()
+    assert (ws_buf[:4096] == 0xAB).all() and (ws_buf[4096 + need:] == 0xAB).all()
+    _, _, _, ref = _oracle_ffn(oracle, dict(x=x, w13=w13, w2=w2, counts=[100, 100]), np.arange(mr))
+    err = row_rel_err(bf16_to_f64(bf16_bits(out)), bf16_to_f64(ref))
+    assert err.max() <= TOL, err.max()

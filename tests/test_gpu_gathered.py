@@ -128,3 +128,37 @@ def test_gathered_full_size_equals_sorted(L):
     b.forward(x)
     torch.cuda.synchronize()
     _check_same(L, a, b, cfg.T, cfg.k)
+
+
+def test_gathered_out_of_range_slot_is_skipped(L):
+    """A sorted_to_slot entry outside [0, T*k) marks its row as not routed:
+    MOE_DEV_ROWS (0x4) is set, nothing is stored for it (guard rows on both
+    sides of out_slots stay untouched) and every other slot's output equals
+    the sorted form's."""
+    cfg = S.CONFIGS["tiny"]
+    a, _, _, _ = _layers(cfg)
+    x = S.make_x(cfg, DEV)
+    a.forward(x)
+    torch.cuda.synchronize()
+    T, k, d = cfg.T, cfg.k, cfg.d
+    A = T * k
+    s2s = a.s2s[:A].clone()
+    bad_rows = [3, 10]
+    lost = [int(s2s[r]) for r in bad_rows]
+    s2s[3] = A + 7
+    s2s[10] = -5
+    guard = 32
+    buf = torch.full((A + 2 * guard, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = buf[guard:guard + A]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    w = a.w
+    L.moe_grouped_ffn_fp8_gathered(a.xq[:T], a.xs[:T], k, s2s, a.offsets, w.w13_q, w.w13_s, w.w2_q, w.w2_s,
+                                   out_slots=out, dev_status=st)
+    torch.cuda.synchronize()
+    assert L.check_status(st) & 0x4
+    assert torch.isnan(buf[:guard].float()).all() and torch.isnan(buf[guard + A:].float()).all()
+    sl2 = a.sl2[:A]
+    keep = sl2 >= 0
+    keep[lost] = False
+    assert torch.isnan(out[lost].float()).all()
+    assert torch.equal(out[keep].view(torch.int16), a.out_sorted[:A][sl2[keep].long()].view(torch.int16))

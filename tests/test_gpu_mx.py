@@ -179,7 +179,7 @@ def _oracle_mx_tokens(oracle, cfg, layer, tokens, ids, gates_ref, x, seed=0):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", None), ("replay", 600)])
-def test_mx_layer_against_oracle(L, oracle, name, T):
+def test_mx_layer_against_oracle(L, oracle, parity_report, name, T):
     cfg = S.CONFIGS[name]
     if T:
         cfg = cfg.with_(T=T)
@@ -199,12 +199,12 @@ def test_mx_layer_against_oracle(L, oracle, name, T):
     g = oracle.gates(lg, ids, cfg.score_fn, cfg.renorm, cfg.route_scale)
     tokens = np.arange(cfg.T)
     y_ref = _oracle_mx_tokens(oracle, cfg, layer, tokens, ids, g, x)
-    err = row_rel_err(bf16_to_f64(bf16_bits(y)), bf16_to_f64(y_ref))
+    err = parity_report("power-of-two layer y", bf16_to_f64(bf16_bits(y)), bf16_to_f64(y_ref))
     assert err.max() <= TOL, err.max()
     print(f"mx layer {name}: max row rel err {err.max():.2e}")
 
 
-def test_mx_layer_full_size_sampled(L, oracle):
+def test_mx_layer_full_size_sampled(L, oracle, parity_report):
     """The 8192-token large layer with power-of-two scales: ids, codes and
     exponents of x in full, and the output of 64 sampled tokens."""
     cfg = S.CONFIGS["large"]
@@ -224,6 +224,7 @@ def test_mx_layer_full_size_sampled(L, oracle):
     np.testing.assert_array_equal(layer.ids[torch.as_tensor(tokens, device=DEV)].cpu().numpy(), ids)
     g = oracle.gates(lg, ids, cfg.score_fn, cfg.renorm, cfg.route_scale)
     y_ref = _oracle_mx_tokens(oracle, cfg, layer, tokens, ids, g, x)
-    err = row_rel_err(bf16_to_f64(bf16_bits(y[torch.as_tensor(tokens, device=DEV)])), bf16_to_f64(y_ref))
+    err = parity_report("power-of-two large y, sampled", bf16_to_f64(bf16_bits(y[torch.as_tensor(tokens, device=DEV)])),
+                        bf16_to_f64(y_ref))
     assert err.max() <= TOL, err.max()
     print(f"mx large: {len(tokens)} sampled tokens, max row rel err {err.max():.2e}")
