@@ -70,7 +70,7 @@ __device__ __forceinline__ float warp_gate(int lane, int k, float my_l, int scor
     return g * route_scale;
 }
 
-// ---- cluster helpers (route_topk runs one cluster per 32 tokens, one CTA
+// ---- cluster helpers (route_topk runs one cluster per 64 tokens, one CTA
 // per 128 experts) ----
 __device__ __forceinline__ uint32_t cl_rank()
 {
