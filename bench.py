@@ -652,6 +652,78 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
     return out
 
 
+def run_nvfp4_layer(cfg, dev, seed, steps, warmup, peaks):
+    """The layer with NVFP4 activations and expert weights (E2M1 codes, E4M3
+    scales per 16 elements, fp32 tensor scales; the FP4 variant) on the large
+    workload: route -> NVFP4 x -> dispatch -> moe_grouped_ffn_nvfp4 (two
+    kind::mxf4nvf4 block-scaled GEMMs with act requantised between them) ->
+    combine.  Weights quantised once before timing; an L2 flush before each
+    step."""
+    import torch
+    from block_scaled_fp8_router_gb300 import moe_r3 as Lb
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    from block_scaled_fp8_router_gb300.layer import (MoELayerNVFP4, MoEWeightsNVFP4, finish_nvfp4_weights,
+                                                     quantize_weights_nvfp4)
+    T, k, d, F, E = cfg.T, cfg.k, cfg.d, cfg.F, cfg.E
+    A = T * k
+    e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+    W = MoEWeightsNVFP4(S.make_router_w(cfg, dev, seed), e((E, 2 * F, d // 2), torch.uint8),
+                        e((E, 2 * F, d // 16), torch.uint8), e((E,), torch.float32), None,
+                        e((E, d, F // 2), torch.uint8), e((E, d, F // 16), torch.uint8), e((E,), torch.float32), None)
+    for e0 in range(0, E, 16):
+        n = min(16, E - e0)
+        w13 = torch.stack([S.make_w13_expert(cfg, i, dev, seed) for i in range(e0, e0 + n)])
+        w2 = torch.stack([S.make_w2_expert(cfg, i, dev, seed) for i in range(e0, e0 + n)])
+        quantize_weights_nvfp4(W.w_router, w13, w2, out=W, e0=e0)
+        del w13, w2
+    finish_nvfp4_weights(W)
+    layer = MoELayerNVFP4(W, T, k, cfg.score_fn, cfg.renorm, cfg.route_scale)
+    x = S.make_x(cfg, dev, seed)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def ffn():
+        Lb.moe_grouped_ffn_nvfp4(layer.xq_sorted[:A], layer.xs_sorted[:A], layer.x_ts, layer.offsets, W.w13_q,
+                                 W.w13_sf, W.w13_enc, W.w2_q, W.w2_sf, W.w2_enc, out_sorted=layer.out_sorted[:A],
+                                 workspace=layer.ffn_ws, dev_status=layer.dev_status)
+
+    for _ in range(warmup):
+        flush.zero_()
+        layer.forward(x)
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record()
+        layer.forward(x)
+        b.record()
+        per.append((a, b))
+    fper = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record()
+        ffn()
+        b.record()
+        fper.append((a, b))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in per) / steps
+    ffn_ms = sum(a.elapsed_time(b) for a, b in fper) / steps
+    flops = 6.0 * A * d * F
+    fp4_peak = 6.0 * peaks["bf16_tflops"]
+    out = {"workload": f"{cfg.name}: T={T} d={d} E={E} top_k={k} F={F}, NVFP4 activations and weights "
+                       f"({E * 3 * d * F / 2 / 1e9:.2f} GB of E2M1 weight codes)",
+           "tokens/s": T / (ms * 1e-3), "ms_per_step": ms, "ffn_ms": ffn_ms,
+           "ffn_TFLOP/s": flops / (ffn_ms * 1e-3) / 1e12,
+           "ffn_frac_of_fp4_peak": flops / (ffn_ms * 1e-3) / 1e12 / fp4_peak, "fp4_peak": fp4_peak,
+           "peak_note": "FP4 dense = 6 x measured bf16 burst (the nominal FP4:BF16 ratio, 13.5 / 2.25 PFLOP/s)",
+           "status": Lb.check_status(layer.dev_status)}
+    del layer, W, x
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_nvfp4_quant(cfg, dev, seed, steps, warmup, peaks):
     """The NVFP4 quantiser (fp8_quant_nvfp4: tensor amax pass, then E4M3 block
     scales and packed E2M1 codes) on the layer's activations [T, d] bf16."""
@@ -1119,6 +1191,8 @@ def main():
     if cfg.name == "large" and not args.no_mx:
         import torch
         torch.cuda.empty_cache()
+        out["nvfp4_layer"] = run_nvfp4_layer(cfg, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
+                                             rank_seed(args.seed, rank), max(3, args.steps // 2), 3, peaks)
         try:
             out["nvfp4_quant"] = run_nvfp4_quant(cfg, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
                                                  args.seed + rank, max(3, args.steps // 2), 3, peaks)

@@ -16,6 +16,7 @@
 #include <cuda_fp4.h>
 
 #include "common.cuh"
+#include "nvfp4_internal.cuh"
 
 namespace moe {
 
@@ -78,6 +79,19 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const uint16_t *__rest
     }
 }
 
+moe_status nvfp4_quant_blocks(const uint16_t *src, int64_t rows, int64_t cols, float *tensor_scale, uint8_t *q,
+                              uint8_t *scales, cudaStream_t st)
+{
+    const int64_t cap = (int64_t)sm_count() * 8;
+    // launched even for rows == 0: it writes the tensor scale (1 for an
+    // empty or all-zero tensor)
+    int64_t g2 = (rows * (cols / 16) + 255) / 256;
+    if (g2 < 1) g2 = 1;
+    if (g2 > cap) g2 = cap;
+    nvfp4_quant_kernel<<<(unsigned)g2, 256, 0, st>>>(src, rows, cols, tensor_scale, q, scales);
+    return launch_status();
+}
+
 } // namespace moe
 
 using namespace moe;
@@ -97,11 +111,5 @@ MOE_API moe_status fp8_quant_nvfp4(const uint16_t *src, int64_t rows, int64_t co
         if (g1 > cap) g1 = cap;
         nvfp4_amax_kernel<<<(unsigned)g1, 256, 0, st>>>(src, n8, tensor_scale + 1);
     }
-    // launched even for rows == 0: it writes the tensor scale (1 for an
-    // empty or all-zero tensor)
-    int64_t g2 = (rows * (cols / 16) + 255) / 256;
-    if (g2 < 1) g2 = 1;
-    if (g2 > cap) g2 = cap;
-    nvfp4_quant_kernel<<<(unsigned)g2, 256, 0, st>>>(src, rows, cols, tensor_scale, q, scales);
-    return launch_status();
+    return nvfp4_quant_blocks(src, rows, cols, tensor_scale, q, scales, st);
 }

@@ -254,6 +254,128 @@ class MoELayerFP8:
         return w["dW13"], w["dW2"]
 
 
+@dataclass
+class MoEWeightsNVFP4:
+    """NVFP4 expert weights (E2M1 codes two per byte, E4M3 scales per 16
+    elements, one fp32 tensor scale per expert matrix) with the scale images
+    the NVFP4 GEMM copies to tensor memory."""
+    w_router: torch.Tensor   # [E, d] bf16
+    w13_q: torch.Tensor      # [E, 2F, d/2]
+    w13_s: torch.Tensor      # [E, 2F, d/16] E4M3 block scales
+    w13_enc: torch.Tensor    # [E] fp32 tensor scales
+    w13_sf: torch.Tensor     # tiled scale images of w13_s
+    w2_q: torch.Tensor       # [E, d, F/2]
+    w2_s: torch.Tensor       # [E, d, F/16]
+    w2_enc: torch.Tensor     # [E]
+    w2_sf: torch.Tensor
+
+    @property
+    def E(self) -> int:
+        return self.w13_q.shape[0]
+
+    @property
+    def d(self) -> int:
+        return self.w13_q.shape[2] * 2
+
+    @property
+    def F(self) -> int:
+        return self.w13_q.shape[1] // 2
+
+
+def quantize_weights_nvfp4(w_router: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, out=None, e0: int = 0):
+    """NVFP4 quantisation of bf16 expert weights w13 [n, 2F, d], w2 [n, d, F],
+    one tensor scale per expert matrix (once per weight update).  With `out`
+    (an MoEWeightsNVFP4), experts e0 .. e0+n-1 are written in place and the
+    scale images are rebuilt by finish_nvfp4_weights."""
+    n, twoF, d = w13.shape
+    F = twoF // 2
+    dev = w13.device
+    if out is None:
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+        out = MoEWeightsNVFP4(w_router, e((n, twoF, d // 2), torch.uint8), e((n, twoF, d // 16), torch.uint8),
+                              e((n,), torch.float32), None, e((n, d, F // 2), torch.uint8),
+                              e((n, d, F // 16), torch.uint8), e((n,), torch.float32), None)
+        e0 = 0
+    ts = torch.empty((2,), dtype=torch.float32, device=dev)
+    for i in range(n):
+        L.fp8_quant_nvfp4(w13[i], q=out.w13_q[e0 + i], scales=out.w13_s[e0 + i], tensor_scale=ts)
+        out.w13_enc[e0 + i] = ts[0]
+        L.fp8_quant_nvfp4(w2[i], q=out.w2_q[e0 + i], scales=out.w2_s[e0 + i], tensor_scale=ts)
+        out.w2_enc[e0 + i] = ts[0]
+    if out.w13_sf is None or e0 + n == out.E:
+        finish_nvfp4_weights(out)
+    return out
+
+
+def finish_nvfp4_weights(w: MoEWeightsNVFP4) -> MoEWeightsNVFP4:
+    """(Re)build the tiled scale images of all experts."""
+    E, d, F = w.E, w.d, w.F
+    w.w13_sf = L.moe_nvfp4_tile_scales(w.w13_s.view(E * 2 * F, d // 16), d, out=w.w13_sf)
+    w.w2_sf = L.moe_nvfp4_tile_scales(w.w2_s.view(E * d, F // 16), F, out=w.w2_sf)
+    return w
+
+
+class MoELayerNVFP4:
+    """Forward of one MoE layer with NVFP4 activations and expert weights:
+    route or replay -> NVFP4 quantisation of x (one tensor scale) -> dispatch
+    of the codes and scales -> moe_grouped_ffn_nvfp4 -> combine.  Buffers are
+    allocated once for T_max tokens."""
+
+    def __init__(self, weights: MoEWeightsNVFP4, T_max: int, k: int, score_fn: int, renorm: int = 1,
+                 route_scale: float = 1.0):
+        self.w = weights
+        self.k, self.score_fn, self.renorm, self.route_scale = k, score_fn, renorm, route_scale
+        dev = weights.w13_q.device
+        E, d, F = weights.E, weights.d, weights.F
+        if d % 64 != 0:
+            raise ValueError("d must be a multiple of 64 (the scales travel as fp32 words)")
+        A = T_max * k
+        self.T_max = T_max
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+        self.ids = e((T_max, k), torch.int32)
+        self.gates = e((T_max, k), torch.float32)
+        self.xq = e((T_max, d // 2), torch.uint8)
+        self.xs = e((T_max, d // 16), torch.uint8)
+        self.x_ts = e((2,), torch.float32)
+        self.counts = e((E,), torch.int32)
+        self.offsets = e((E + 1,), torch.int32)
+        self.s2s = e((A,), torch.int32)
+        self.sl2 = e((A,), torch.int32)
+        self.xq_sorted = e((A, d // 2), torch.uint8)
+        self.xs_sorted = e((A, d // 16), torch.uint8)
+        self.out_sorted = e((A, d), torch.bfloat16)
+        self.y = e((T_max, d), torch.bfloat16)
+        self.dsp_ws = e((L.moe_dispatch_workspace_size(T_max, k, E),), torch.uint8)
+        self.ffn_ws = e((L.moe_grouped_ffn_nvfp4_workspace_size(A, d, F),), torch.uint8)
+        self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def forward(self, x: torch.Tensor, replay_kT: torch.Tensor | None = None, y: torch.Tensor | None = None):
+        T = x.shape[0]
+        if T > self.T_max:
+            raise ValueError(f"T={T} exceeds T_max={self.T_max}")
+        A = T * self.k
+        d = self.w.d
+        ids, gates = self.ids[:T], self.gates[:T]
+        if replay_kT is None:
+            L.moe_route_topk(x, self.w.w_router, self.k, self.score_fn, self.renorm, self.route_scale,
+                             topk_ids=ids, topk_gates=gates)
+        else:
+            L.moe_route_replay(replay_kT, self.w.E, x, self.w.w_router, self.score_fn, self.renorm,
+                               self.route_scale, topk_ids=ids, topk_gates=gates, dev_status=self.dev_status)
+        L.fp8_quant_nvfp4(x, q=self.xq[:T], scales=self.xs[:T], tensor_scale=self.x_ts)
+        # the E4M3 scale bytes ride with the codes as d/64 fp32 words per row
+        L.moe_dispatch(ids, self.w.E, rows=self.xq[:T], row_scales=self.xs[:T].view(torch.float32),
+                       expert_counts=self.counts, expert_offsets=self.offsets, sorted_to_slot=self.s2s[:A],
+                       slot_to_sorted=self.sl2[:A], rows_sorted=self.xq_sorted[:A],
+                       scales_sorted=self.xs_sorted[:A].view(torch.float32), workspace=self.dsp_ws,
+                       dev_status=self.dev_status)
+        L.moe_grouped_ffn_nvfp4(self.xq_sorted[:A], self.xs_sorted[:A], self.x_ts, self.offsets, self.w.w13_q,
+                                self.w.w13_sf, self.w.w13_enc, self.w.w2_q, self.w.w2_sf, self.w.w2_enc,
+                                out_sorted=self.out_sorted[:A], workspace=self.ffn_ws, dev_status=self.dev_status)
+        y = self.y[:T] if y is None else y
+        return L.moe_combine(self.out_sorted[:A], self.sl2[:A], gates, y=y)
+
+
 class HostStreamer:
     """Forward of a sequence of host batches with the copies overlapped.
 

@@ -54,6 +54,10 @@ _SIGS = {
     "moe_wgrad_quant": (I, [I, P, P, P, P, I, P, P, I, P, P, I, I64, I64, I, P, P, P]),
     "moe_wgrad_gemm": (I, [P, P, P, P, P, I, I, I, I64, P, P, P]),
     "fp8_quant_nvfp4": (I, [P, I64, I64, P, P, P, P]),
+    "moe_nvfp4_tiled_scales_size": (SZ, [I64, I64]),
+    "moe_nvfp4_tile_scales": (I, [P, I64, I64, P, P]),
+    "moe_grouped_ffn_nvfp4_workspace_size": (SZ, [I64, I, I]),
+    "moe_grouped_ffn_nvfp4": (I, [P, P, P, P, I64, I, I, I, P, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_grouped_ffn_mx": (I, [P, P, P, I, I, P, I64, I, I, I, P, P, P, P, P, P, SZ, P, P]),
     "moe_debug_bounded_wait": (I, [I64, P, P]),
     "moe_device_sm_count": (I, []),
@@ -424,6 +428,58 @@ def moe_grouped_ffn_mx(xq_sorted, x_exp, sorted_to_slot, top_k, expert_offsets, 
         _ptr(xq_sorted), _ptr(x_exp), _ptr(sorted_to_slot), T, top_k, _ptr(expert_offsets), max_rows, E, d, F,
         _ptr(w13_q), _ptr(w13_exp), _ptr(w2_q), _ptr(w2_exp), _ptr(out_sorted), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+    return out_sorted
+
+
+def moe_nvfp4_tiled_scales_size(rows: int, K: int) -> int:
+    return int(_lib.moe_nvfp4_tiled_scales_size(rows, K))
+
+
+def moe_nvfp4_tile_scales(s, K, out=None, stream=None):
+    """E4M3 block scales [rows, K/16] of an NVFP4 weight matrix -> the scale
+    images the NVFP4 GEMM copies to tensor memory (uint8, flat)."""
+    rows = s.shape[0]
+    _want(s, torch.uint8, (rows, K // 16), "s")
+    n = moe_nvfp4_tiled_scales_size(rows, K)
+    out = _empty((n,), torch.uint8, s) if out is None else out
+    _want(out, torch.uint8, (n,), "out")
+    _check("moe_nvfp4_tile_scales", _lib.moe_nvfp4_tile_scales(_ptr(s), rows, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def moe_grouped_ffn_nvfp4_workspace_size(max_rows: int, d: int, F: int) -> int:
+    return int(_lib.moe_grouped_ffn_nvfp4_workspace_size(max_rows, d, F))
+
+
+def moe_grouped_ffn_nvfp4(xq_sorted, xs_sorted, x_enc, expert_offsets, w13_q, w13_sf_tiled, w13_enc, w2_q,
+                          w2_sf_tiled, w2_enc, out_sorted=None, workspace=None, dev_status=None, stream=None):
+    """Grouped SwiGLU FFN in NVFP4 -> out_sorted [max_rows, d] bf16.  xq_sorted
+    [max_rows, d/2] E2M1 codes, xs_sorted [max_rows, d/16] E4M3 scales, x_enc
+    (one device float: the token tensor's s_enc); w13_q [E, 2F, d/2], w2_q
+    [E, d, F/2] with their tiled scale images and per-expert s_enc [E]."""
+    max_rows, dh = xq_sorted.shape
+    d = 2 * dh
+    E, twoF, _ = w13_q.shape
+    F = twoF // 2
+    _want(xq_sorted, torch.uint8, (max_rows, d // 2), "xq_sorted")
+    _want(xs_sorted, torch.uint8, (max_rows, d // 16), "xs_sorted")
+    if x_enc.dtype != torch.float32 or x_enc.numel() < 1 or not x_enc.is_cuda:
+        raise ValueError("x_enc: float32 CUDA tensor (its first element is the tensor scale)")
+    _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _want(w13_q, torch.uint8, (E, 2 * F, d // 2), "w13_q")
+    _want(w13_sf_tiled, torch.uint8, (moe_nvfp4_tiled_scales_size(E * 2 * F, d),), "w13_sf_tiled")
+    _want(w13_enc, torch.float32, (E,), "w13_enc")
+    _want(w2_q, torch.uint8, (E, d, F // 2), "w2_q")
+    _want(w2_sf_tiled, torch.uint8, (moe_nvfp4_tiled_scales_size(E * d, F),), "w2_sf_tiled")
+    _want(w2_enc, torch.float32, (E,), "w2_enc")
+    out_sorted = _empty((max_rows, d), torch.bfloat16, xq_sorted) if out_sorted is None else out_sorted
+    _want(out_sorted, torch.bfloat16, (max_rows, d), "out_sorted")
+    if workspace is None:
+        workspace = _empty((moe_grouped_ffn_nvfp4_workspace_size(max_rows, d, F),), torch.uint8, xq_sorted)
+    _check("moe_grouped_ffn_nvfp4", _lib.moe_grouped_ffn_nvfp4(
+        _ptr(xq_sorted), _ptr(xs_sorted), _ptr(x_enc), _ptr(expert_offsets), max_rows, E, d, F, _ptr(w13_q),
+        _ptr(w13_sf_tiled), _ptr(w13_enc), _ptr(w2_q), _ptr(w2_sf_tiled), _ptr(w2_enc), _ptr(out_sorted),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
     return out_sorted
 
 

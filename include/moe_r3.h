@@ -186,6 +186,55 @@ moe_status fp8_quant_nvfp4(const uint16_t *src, int64_t rows, int64_t cols, uint
                            float *tensor_scale, void *stream);
 
 /* ------------------------------------------------------------------------
+ * moe_nvfp4_tile_scales -- the E4M3 block scales of an NVFP4 weight matrix
+ * (fp8_quant_nvfp4 layout, s [rows, K/16]) rearranged once per weight
+ * update into the images the NVFP4 GEMM copies to tensor memory: per
+ * 128-row group g and 256-element K block kb, 2048 contiguous bytes
+ * [MMA 0..3][r 0..31][q 0..3] of 32-bit words, word (g, kb, m, r, q) =
+ * scale bytes 16kb + 4m .. 16kb + 4m + 3 of row 128g + 32q + r (0 past K/16).
+ * rows % 128 == 0, K % 128 == 0; s 4-byte aligned, s_tiled 16-byte aligned,
+ * moe_nvfp4_tiled_scales_size(rows, K) bytes.
+ * Errors: NULL, SHAPE, ALIGN.
+ * ---------------------------------------------------------------------- */
+size_t moe_nvfp4_tiled_scales_size(int64_t rows, int64_t K);
+moe_status moe_nvfp4_tile_scales(const uint8_t *s, int64_t rows, int64_t K, uint8_t *s_tiled, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_ffn_nvfp4 -- the grouped SwiGLU expert FFN in NVFP4 (the FP4
+ * variant listed as future work for training and inference in "RL at 1T
+ * Scale", closing section) on the block-scaled tensor-core MMA
+ * (tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X).
+ *
+ * Operands as fp8_quant_nvfp4 writes them: E2M1 codes two per byte, E4M3
+ * scales per 16 elements along K, one fp32 tensor scale s_enc (decoded
+ * value = e2m1 * scale / s_enc).  For sorted row r of expert e:
+ *   h[r, n]  = sum_k xdec[r, k] * w13dec[e][n, k] (the tensor core applies
+ *              the block scales, accumulates in fp32; the epilogue divides
+ *              by x_enc * w13_enc[e]);
+ *   act[r,c] = bf16( silu(h[r, c]) * h[r, F + c] )  (c < F), materialised
+ *              in the workspace with its amax over the routed rows, then
+ *              quantised to NVFP4 with one tensor scale (fp8_quant_nvfp4);
+ *   out[r,:] = bf16( act_dec[r] W2dec[e]^T ), likewise.
+ * xq_sorted [max_rows, d/2], xs_sorted [max_rows, d/16] (moe_dispatch of the
+ * token-major codes and scales), x_enc: the token tensor's s_enc (device);
+ * w13_q [E, 2F, d/2], w13_sf_tiled = moe_nvfp4_tile_scales of w13's scales
+ * [E*2F, d/16], w13_enc [E] (device, one per expert matrix); w2_q
+ * [E, d, F/2], w2_sf_tiled of [E*d, F/16], w2_enc [E]; out_sorted
+ * [max_rows, d] bf16.  d, F multiples of 128; max_rows bounds
+ * expert_offsets[E] as in moe_grouped_ffn_fp8 (clipped, MOE_DEV_ROWS).
+ * workspace: moe_grouped_ffn_nvfp4_workspace_size bytes, 256-byte aligned
+ * (act in bf16 and NVFP4, and the act tensor's scale).
+ * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
+ * ---------------------------------------------------------------------- */
+size_t moe_grouped_ffn_nvfp4_workspace_size(int64_t max_rows, int d, int F);
+moe_status moe_grouped_ffn_nvfp4(const uint8_t *xq_sorted, const uint8_t *xs_sorted, const float *x_enc,
+                                 const int32_t *expert_offsets, int64_t max_rows, int E, int d, int F,
+                                 const uint8_t *w13_q, const uint8_t *w13_sf_tiled, const float *w13_enc,
+                                 const uint8_t *w2_q, const uint8_t *w2_sf_tiled, const float *w2_enc,
+                                 uint16_t *out_sorted, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * fp8_block_quant_ue8m0 -- fp8_block_quant with power-of-two block scales
  * (the UE8M0 scale format of MXFP8 and of the hardware block-scaled MMA; a
  * variant of the "FP8 training" recipe, whose scales are arbitrary fp32).
