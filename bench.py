@@ -1188,7 +1188,7 @@ def main():
     if cfg.name == "large" and not args.no_dispatch_combine:
         out["payload"] = run_payload(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
                                      args.seed + rank, max(3, args.steps // 2), 3, peaks)
-    if cfg.name == "large" and not args.no_mx:
+    if cfg.name in ("large", "large_e64") and not args.no_mx:
         import torch
         torch.cuda.empty_cache()
         out["nvfp4_layer"] = run_nvfp4_layer(cfg, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),

@@ -31,8 +31,12 @@
 // images are laid out once per weight update by moe_nvfp4_tile_scales (per
 // 128-row group and K block: 4 MMAs x 512 bytes, contiguous), so the
 // producer moves them with two bulk copies; the activation rows start
-// anywhere, so the producer lanes gather their scale bytes and write the
-// images themselves.
+// anywhere, so the producer lanes gather their scale words straight into
+// the images with 4-byte cp.async copies (zero-filled past the tile), kept
+// F4_SF_AHEAD K blocks in flight: a stage is complete when its TMA bytes
+// have landed and, on a second arrival, its gathered words (waited for with
+// cp.async.wait_group and fenced to the async proxy, which tcgen05.cp
+// reads through).
 #include "tcgen05.cuh"
 #include "nvfp4_internal.cuh"
 
@@ -43,6 +47,8 @@ constexpr int F4_SFA_STAGE = 2048;      // A: 4 MMAs x 512 bytes
 constexpr int F4_SFB_STAGE = 4096;      // B: 2 row groups x 4 MMAs x 512 bytes
 constexpr int F4_SF_COL0 = 256;         // TMEM column of stage 0's scale words
 constexpr int F4_SF_COLS = 48;          // per stage: A 4 x 4 columns, B 4 x 8
+constexpr int F4_SF_AHEAD = 3;          // K blocks of A scale words in flight (< STAGES)
+static_assert(F4_SF_AHEAD < STAGES, "a stage's scale words must land before the stage is reused");
 static_assert(F4_SF_COL0 + STAGES * F4_SF_COLS <= TMEM_COLS, "NVFP4 scale words in TMEM");
 
 struct SmemF4 {
@@ -96,17 +102,15 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
                  : "memory");
 }
 
-// 16 scale bytes of one row for one K block (256 elements), as four words
-// (word ks = the bytes of MMA ks, 16-element block b of it in byte b);
-// bytes past the row's K/16 read as 0
-__device__ __forceinline__ uint4 row_scale_words(const uint8_t *row_sf, int kb, int nsf)
+// 4 bytes global -> shared, asynchronously; src_bytes 0 writes zeros
+__device__ __forceinline__ void cp_async4_zfill(void *dst, const void *src, uint32_t src_bytes)
 {
-    const int c0 = 16 * kb;
-    uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
-    if (c0 < nsf) lo = __ldg(reinterpret_cast<const uint2 *>(row_sf + c0));
-    if (c0 + 8 < nsf) hi = __ldg(reinterpret_cast<const uint2 *>(row_sf + c0 + 8));
-    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; i++) {
-            mbar_init(&s.full[i], 1);
+            mbar_init(&s.full[i], 2);    // TMA bytes (with lane 0's arrival) + the A scale words' arrival
             mbar_init(&s.empty[i], 1);
         }
         mbar_init(&s.tfull, 1);
@@ -144,10 +148,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == PRODUCER_WARP) {
         // ---------------- TMA producer + scale-word images (whole warp) ----------------
+        // K block j: wait for its stage, gather its A scale words (cp.async,
+        // one commit group per K block), issue its TMA and bulk copies; then
+        // complete the stage of K block j - F4_SF_AHEAD, whose words have
+        // landed (wait_group), fenced to the async proxy.
         uint32_t j = 0;
         uint32_t issued = 0;
         bool ok = true;
-        const int64_t groups_b = MODE == 1 ? (int64_t)p.E * (2 * p.F / 128) : (int64_t)p.E * (p.d / 128);
+        auto complete_words = [&](uint32_t jj) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.full[jj % STAGES]);
+        };
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             const Tile tl = decode_tile(s, p.E, n_tiles, t);
             // scale rows of the tile's A rows lane + 32q (null past the tile)
@@ -163,16 +175,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                                          : (int64_t)tl.e * (p.d / 128) + tl.n_blk * 2;
             const int64_t g1 = MODE == 1 ? g0 + p.F / 128 : g0 + 1;
             const bool g1_ok = MODE == 1 || (tl.n_blk * 2 + 1) < p.d / 128;
-            (void)groups_b;
-            uint4 wa[4], na[4];
-#pragma unroll
-            for (int q = 0; q < 4; q++) wa[q] = arow[q] ? row_scale_words(arow[q], 0, nsf) : make_uint4(0u, 0u, 0u, 0u);
             for (int kb = 0; kb < nkb; kb++, j++) {
                 const int st = j % STAGES;
-                // next K block's words, fetched while this one waits for its stage
-#pragma unroll
-                for (int q = 0; q < 4; q++)
-                    na[q] = (arow[q] && kb + 1 < nkb) ? row_scale_words(arow[q], kb + 1, nsf) : make_uint4(0u, 0u, 0u, 0u);
                 bool w = true;
                 if (lane == 0) w = wait_or_abort(&s.empty[st], ((j / STAGES) & 1) ^ 1, abort_flag, p.dev_status);
                 w = __shfl_sync(0xFFFFFFFFu, w, 0);
@@ -180,14 +184,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                // image of MMA ks: row `lane` holds the words of rows lane, +32, +64, +96
-                uint4 *img = reinterpret_cast<uint4 *>(s.sfa[st]);
-                img[0 * 32 + lane] = make_uint4(wa[0].x, wa[1].x, wa[2].x, wa[3].x);
-                img[1 * 32 + lane] = make_uint4(wa[0].y, wa[1].y, wa[2].y, wa[3].y);
-                img[2 * 32 + lane] = make_uint4(wa[0].z, wa[1].z, wa[2].z, wa[3].z);
-                img[3 * 32 + lane] = make_uint4(wa[0].w, wa[1].w, wa[2].w, wa[3].w);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
+                // image of MMA ks: row `lane` holds the words of rows lane, +32,
+                // +64, +96 (the bytes 16kb + 4ks .. +3 of each row; zeros past
+                // the tile or past the row)
+                uint8_t *img = s.sfa[st];
+#pragma unroll
+                for (int ks = 0; ks < 4; ks++) {
+                    const int c = 16 * kb + 4 * ks;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const bool have = arow[q] != nullptr && c < nsf;
+                        cp_async4_zfill(img + 512 * ks + 16 * lane + 4 * q, have ? arow[q] + c : p.a_sf, have ? 4u : 0u);
+                    }
+                }
+                cp_async_commit();
                 if (lane == 0) {
                     const uint32_t sfb_bytes = g1_ok ? 2u * 2048u : 2048u;
                     mbar_arrive_expect_tx(&s.full[st], A_BYTES + B_BYTES + sfb_bytes);
@@ -203,10 +213,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (g1_ok) bulk_load_1d(s.sfb[st] + 2048, p.b_sf_tiled + (g1 * nkb + kb) * 2048, 2048, &s.full[st]);
                     issued |= 1u << st;
                 }
-#pragma unroll
-                for (int q = 0; q < 4; q++) wa[q] = na[q];
+                if (j >= (uint32_t)F4_SF_AHEAD) {
+                    cp_async_wait_group<F4_SF_AHEAD>();
+                    complete_words(j - F4_SF_AHEAD);
+                }
             }
         }
+        // the last K blocks' words (the loop may also have stopped early)
+        cp_async_wait_group<0>();
+        for (uint32_t jj = j > (uint32_t)F4_SF_AHEAD ? j - F4_SF_AHEAD : 0; jj < j; jj++) complete_words(jj);
         if (lane == 0) {
             for (int i = 0; i < STAGES; i++) {
                 if (!(issued & (1u << i)) || j == 0) continue;
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // GEMM1: gate columns 32cg.. and up 128+32cg..; GEMM2: 64cg..
             const int col0 = MODE == 1 ? 32 * cg : 64 * cg;
             const int col1 = MODE == 1 ? 128 + 32 * cg : 64 * cg + 32;
-            const float enc = a_enc * __ldg(p.b_enc + tl.e);
+            const float inv = __frcp_rn(a_enc * __ldg(p.b_enc + tl.e));
             float acc0[32], acc1[32];
             if (!aborted && !wait_or_abort(&s.tfull, tcount & 1, abort_flag, p.dev_status)) aborted = true;
             if (!aborted) {
@@ -285,8 +300,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_wait_ld32(r1);   // order every use of the values after it
 #pragma unroll
                 for (int i = 0; i < 32; i++) {
-                    acc0[i] = __fdiv_rn(__uint_as_float(r0[i]), enc);
-                    acc1[i] = __fdiv_rn(__uint_as_float(r1[i]), enc);
+                    acc0[i] = __uint_as_float(r0[i]) * inv;
+                    acc1[i] = __uint_as_float(r1[i]) * inv;
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -298,8 +313,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
                         const float g0 = acc0[2 * i], g1 = acc0[2 * i + 1];
-                        w[i] = pack_bf16x2(__fdiv_rn(g0, 1.0f + expf(-g0)) * acc1[2 * i],
-                                           __fdiv_rn(g1, 1.0f + expf(-g1)) * acc1[2 * i + 1]);
+                        w[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * acc1[2 * i],
+                                           __fdividef(g1, 1.0f + __expf(-g1)) * acc1[2 * i + 1]);
                         amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFFu)),
                                                  fabsf(bf16_bits_to_f32(w[i] >> 16))));
                     }
