@@ -45,9 +45,9 @@ L2_FLUSH_BYTES = 512 * 1024 * 1024      # written between timed steps (not timed
 FP32_ALU_TFLOPS_DERIVED = 152 * 128 * 2 * 2.07e9 / 1e12   # 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz
 # DRAM bytes (read + write) per routed row of the grouped FFN at d=7168, F=2048,
 # ~256 rows per expert: ncu capture of grouped_gemm_kernel<1> and <2> on the
-# large_e64 profiling shape (A = 16384 rows): 2.649e9 + 0.051e9 + 0.975e9 +
-# 0.217e9 bytes.  Valid for the kernel that capture measured.
-FFN_DRAM_BYTES_PER_ROW = (2.6488e9 + 0.0510e9 + 0.9750e9 + 0.2169e9) / 16384
+# large_e64 profiling shape (A = 16384 rows): 2.0422e9 + 0.0353e9 + 0.9750e9 +
+# 0.2185e9 bytes.  Valid for the kernel that capture measured.
+FFN_DRAM_BYTES_PER_ROW = (2.0422e9 + 0.0353e9 + 0.9750e9 + 0.2185e9) / 16384
 KERNELS_PER_STEP = {"route": 1, "replay": 1, "quant": 1, "dispatch": 4, "ffn": 2, "combine": 1}
 
 
