@@ -576,7 +576,7 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
     def step(e=None):
         if e: e[0].record()
         Lb.moe_combine_backward(dy, layer.gates[:T], layer.out_sorted[:A], layer.sl2[:A], d_out_q=b["d_out_q"][:A],
-                                d_out_s=b["d_out_s"][:A], d_gates=b["d_gates"][:T])
+                                d_out_s=b["d_out_s"][:A], d_gates=b["d_gates"][:T], dev_status=layer.dev_status)
         if e: e[1].record()
         Lb.moe_grouped_gemm_fp8(b["d_out_q"][:A], b["d_out_s"][:A], layer.offsets, w2t_q, w2t_s, out=b["d_act"][:A],
                                 dev_status=layer.dev_status)
@@ -643,6 +643,19 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
         out["steps"][n]["frac_hbm"] = out["steps"][n]["GB/s"] / hbm
     # the weight-gradient GEMMs are bound by their fp32 stores: output bytes
     # per launch over the launch time, against the measured copy bandwidth
+    # the 128 x 1 operand quantisations: source rows read once per routed row
+    # (dy and x gathered per slot), codes and scales over the padded rows P
+    cnt = (layer.offsets[1:E + 1] - layer.offsets[:E]).cpu().to(torch.int64)
+    P = int((((cnt + 127) // 128) * 128).sum())
+    codes = lambda C: C * P * (1 + 4 / 128)
+    b_q = {"quant_d_out": A * d * 2 + A * 8 + codes(d), "quant_act": A * 2 * F * 4 + codes(F),
+           "quant_dh": A * F * 2 + A * 2 * F * 4 + codes(2 * F), "quant_x": A * d * 2 + A * 4 + codes(d)}
+    for n, nb in b_q.items():
+        st = out["weight_grads"]["steps"][n]
+        st["bytes"] = nb
+        st["GB/s"] = nb / (st["ms"] * 1e-3) / 1e9
+        st["frac_hbm"] = st["GB/s"] / hbm
+    out["weight_grads"]["padded_rows"] = P
     for n, nb in (("gemm_dW2", 4.0 * E * d * F), ("gemm_dW13", 4.0 * E * 2 * F * d)):
         st = out["weight_grads"]["steps"][n]
         st["store GB/s"] = nb / (st["ms"] * 1e-3) / 1e9

@@ -16,14 +16,32 @@
 // that copy once per weight update (block quantisation commutes with
 // transposition, so it is the quantisation of the transposed weights).
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 
-// One warp per token: the token's dy row is read once (16 bytes per lane per
-// step) and multiplied by each slot's gate; every 128-column block of the
-// product is one half-warp (amax by four shuffles) and is written with its
-// scale to the slot's sorted row.  The gate gradient is the warp-reduced dot
-// of dy with the slot's expert output row.
+// SwiGLU backward of one element from the gate pre-activation g, the up
+// value u and the incoming gradient a = d_act: d_gate = a * u * sg *
+// (1 + g * (1 - sg)) and d_up = a * g * sg with sg = sigmoid(g) (fast
+// exponential and reciprocal, as the GEMM1 epilogue forms silu; below
+// g = -87 the reciprocal of a sum past 2^126 is 0, the limit).  The dgrad operand (swiglu_backward_kernel)
+// and the weight-gradient operand (quant_128x1_kernel) both take it from here.
+__device__ __forceinline__ float dswiglu_gate(float a, float g, float u, float sg)
+{
+    return a * u * sg * (1.0f + g * (1.0f - sg));
+}
+__device__ __forceinline__ float dswiglu_up(float a, float g, float sg) { return a * (g * sg); }
+__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+
+// One warp per (token, slot): the slot's gate times the token's dy row,
+// 32 lanes x 8 columns per step (two 128-column blocks; the second half-warp
+// idles on the last step when d / 128 is odd), CB_U steps loaded before the
+// first is encoded.  Every 128-column block is one half-warp (amax by four
+// shuffles), written with its scale to the slot's sorted row.  The gate
+// gradient is the warp-reduced dot of dy with the slot's expert output row
+// (each lane accumulates its columns in order).
+constexpr int CB_U = 4;
+
 __global__ void __launch_bounds__(256) combine_backward_kernel(const uint16_t *__restrict__ dy,
                                                                const float *__restrict__ gates,
                                                                const uint16_t *__restrict__ out_sorted,
@@ -37,27 +55,39 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const uint16_t *_
     const unsigned half_mask = 0xFFFFu << (lane & 16);
     const int nvec = d >> 3;
     const int nb = d >> 7;
+    const int64_t n = (int64_t)T * k;
     const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t t = gw; t < T; t += nw) {
-        for (int j = 0; j < k; j++) {
-            const int32_t r = __ldg(slot_to_sorted + t * k + j);
-            if (r < 0 || r >= A) {
-                if (lane == 0) d_gates[t * k + j] = 0.0f;
-                continue;
+    for (int64_t p = gw; p < n; p += nw) {
+        const int32_t r = __ldg(slot_to_sorted + p);
+        if (r < 0 || r >= A) {
+            if (lane == 0) d_gates[p] = 0.0f;
+            continue;
+        }
+        const int64_t t = p / k;
+        const float g = __ldg(gates + p);
+        const uint4 *dyr = reinterpret_cast<const uint4 *>(dy + t * d);
+        const uint4 *outr = reinterpret_cast<const uint4 *>(out_sorted + (int64_t)r * d);
+        float dot = 0.0f;
+        for (int v0 = 0; v0 < nvec; v0 += 32 * CB_U) {
+            uint4 a[CB_U], b[CB_U];
+#pragma unroll
+            for (int u = 0; u < CB_U; u++) {
+                const int v = v0 + 32 * u + lane;
+                a[u] = make_uint4(0u, 0u, 0u, 0u);
+                b[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (v < nvec) {
+                    a[u] = __ldg(dyr + v);
+                    b[u] = __ldcs(outr + v);
+                }
             }
-            const float g = __ldg(gates + t * k + j);
-            float dot = 0.0f;
-            // 32 lanes x 8 columns = two 128-column blocks per step (the
-            // second half-warp idles on the last step when d / 128 is odd)
-            for (int v0 = 0; v0 < nvec; v0 += 32) {
-                const int v = v0 + lane;
-                const bool on = v < nvec;
+#pragma unroll
+            for (int u = 0; u < CB_U; u++) {
+                if (v0 + 32 * u >= nvec) break;                 // uniform over the warp
+                const int v = v0 + 32 * u + lane;
                 float f[8], o[8];
-                unpack_bf16x8(on ? __ldg(reinterpret_cast<const uint4 *>(dy + t * d) + v) : make_uint4(0, 0, 0, 0), f);
-                unpack_bf16x8(on ? __ldcs(reinterpret_cast<const uint4 *>(out_sorted + (int64_t)r * d) + v)
-                                 : make_uint4(0, 0, 0, 0),
-                              o);
+                unpack_bf16x8(a[u], f);
+                unpack_bf16x8(b[u], o);
                 float amax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 8; i++) {
@@ -68,26 +98,209 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const uint16_t *_
 #pragma unroll
                 for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, off, 16));
                 const float s = block_scale(amax);
-                uint2 q;
-                q.x = (uint32_t)pack_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
-                      ((uint32_t)pack_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
-                q.y = (uint32_t)pack_e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
-                      ((uint32_t)pack_e4m3x2(__fdiv_rn(f[6], s), __fdiv_rn(f[7], s)) << 16);
-                if (on) {
+                const uint2 q = e4m3x8_scaled<2>(f, s);
+                if (v < nvec) {
                     __stcs(reinterpret_cast<uint2 *>(d_out_q + (int64_t)r * d + (int64_t)v * 8), q);
                     if (sub == 0) d_out_s[(int64_t)r * nb + (v >> 4)] = s;
                 }
             }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
+        if (lane == 0) d_gates[p] = dot;
+    }
+}
+
+// The same combine backward with the rows staged in shared memory by bulk
+// asynchronous copies (d <= CBT_MAX_D).  A producer lane copies each token's
+// dy row (two buffers) and the expert output row of each routed slot (a
+// CBT_STAGES ring) with 1-D bulk copies, so that whole rows stay in flight
+// to HBM; 16 consumer warps (32 half-warps, each holding its 128-column
+// blocks of the token's dy) form g * dy, its 1x128 codes and scales, and
+// each warp's part of the dot with the output row.  A warp releases a stage with its part of the dot; the
+// producer, before it refills the stage, sums the parts in warp order (a
+// fixed order) into the slot's gate gradient.  Persistent: CTA c takes tokens c, c + grid, ...
+// Every wait is bounded: one that runs out sets MOE_DEV_TIMEOUT and the
+// abort flag, the consumers leave, and the producer waits (bounded) for its
+// copies still in flight before the CTA exits.
+constexpr int CBT_WARPS = 16;
+constexpr int CBT_THREADS = (CBT_WARPS + 1) * 32;
+constexpr int CBT_STAGES = 4;
+constexpr int CBT_MAX_D = 8192;
+constexpr int CBT_MAXB = CBT_MAX_D / 128 / (2 * CBT_WARPS);     // blocks per half-warp
+constexpr int CBT_HDR = 512;
+
+struct CbtHdr {
+    uint64_t dy_full[2], dy_empty[2], out_full[CBT_STAGES], out_empty[CBT_STAGES];
+    float partial[CBT_STAGES][CBT_WARPS];
+    int abort_flag;
+};
+static_assert(sizeof(CbtHdr) <= CBT_HDR, "combine backward header");
+
+// a bounded wait whose outcome is the same for the whole warp
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *dev_status)
+{
+    return __all_sync(0xFFFFFFFFu, ffn::wait_or_abort(bar, parity, abort_flag, dev_status));
+}
+
+__global__ void __launch_bounds__(CBT_THREADS, 2)
+    combine_backward_tma_kernel(const uint16_t *__restrict__ dy, const float *__restrict__ gates,
+                                const uint16_t *__restrict__ out_sorted, const int32_t *__restrict__ slot_to_sorted,
+                                int T, int k, int d, int64_t A, uint8_t *__restrict__ d_out_q,
+                                float *__restrict__ d_out_s, float *__restrict__ d_gates, int32_t *dev_status)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    CbtHdr &hd = *reinterpret_cast<CbtHdr *>(smem);
+    uint16_t *dyb = reinterpret_cast<uint16_t *>(smem + CBT_HDR);        // [2][d]
+    uint16_t *outb = dyb + 2 * (int64_t)d;                                // [CBT_STAGES][d]
+    volatile int *abort_flag = &hd.abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t row_bytes = (uint32_t)d * 2u;
+    if (tid == 0) {
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&hd.dy_full[i], 1);
+            mbar_init(&hd.dy_empty[i], CBT_WARPS);
+        }
+        for (int i = 0; i < CBT_STAGES; i++) {
+            mbar_init(&hd.out_full[i], 1);
+            mbar_init(&hd.out_empty[i], CBT_WARPS);
+        }
+        hd.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == CBT_WARPS) {
+        if (lane != 0) return;
+        // producer; pend[st] is the slot whose gate gradient stage st holds
+        int64_t pend[CBT_STAGES];
+        int64_t it = 0, sc = 0;
+        bool ok = true;
+        // the gate gradient of use u of a stage, once its eight parts are in
+        auto finish = [&](int64_t u) -> bool {
+            const int st = (int)(u % CBT_STAGES);
+            if (!ffn::wait_or_abort(&hd.out_empty[st], (uint32_t)((u / CBT_STAGES) & 1), abort_flag, dev_status))
+                return false;
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < CBT_WARPS; w++) sum += hd.partial[st][w];
+            d_gates[pend[st]] = sum;
+            return true;
+        };
+        for (int64_t t = blockIdx.x; t < T && ok; t += gridDim.x, it++) {
+            const int db = (int)(it & 1);
+            if (it >= 2 && !ffn::wait_or_abort(&hd.dy_empty[db], (uint32_t)(((it >> 1) - 1) & 1), abort_flag,
+                                               dev_status)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&hd.dy_full[db], row_bytes);
+            ffn::bulk_load_1d(dyb + (int64_t)db * d, dy + t * d, row_bytes, &hd.dy_full[db]);
+            for (int j = 0; j < k; j++) {
+                const int64_t p = t * k + j;
+                const int32_t r = __ldg(slot_to_sorted + p);
+                if (r < 0 || r >= A) {
+                    d_gates[p] = 0.0f;
+                    continue;
+                }
+                const int st = (int)(sc % CBT_STAGES);
+                if (sc >= CBT_STAGES && !finish(sc - CBT_STAGES)) {
+                    ok = false;
+                    break;
+                }
+                pend[st] = p;
+                mbar_arrive_expect_tx(&hd.out_full[st], row_bytes);
+                ffn::bulk_load_1d(outb + (int64_t)st * d, out_sorted + (int64_t)r * d, row_bytes, &hd.out_full[st]);
+                sc++;
+            }
+        }
+        // the last uses of the stages
+        for (int64_t u = sc - CBT_STAGES < 0 ? 0 : sc - CBT_STAGES; u < sc && ok; u++) ok = finish(u);
+        // drain: every copy issued has landed before the CTA may exit
+        for (int64_t u = it - 2 < 0 ? 0 : it - 2; u < it; u++)
+            if (!mbar_wait_bounded(&hd.dy_full[u & 1], (uint32_t)((u >> 1) & 1), ffn::TIMEOUT_NS))
+                dev_flag(dev_status, MOE_DEV_TIMEOUT);
+        for (int64_t u = sc - CBT_STAGES < 0 ? 0 : sc - CBT_STAGES; u < sc; u++)
+            if (!mbar_wait_bounded(&hd.out_full[u % CBT_STAGES], (uint32_t)((u / CBT_STAGES) & 1),
+                                   ffn::TIMEOUT_NS))
+                dev_flag(dev_status, MOE_DEV_TIMEOUT);
+        return;
+    }
+    // consumers: half-warp h of a token holds its blocks h, h + 32, ... of dy
+    // in registers for all the token's slots (the split rotated from token to
+    // token), with each block's amax of |dy|: since rounding is monotonic,
+    // the amax of a block of RN(g * dy) is exactly RN(|g| * amax |dy|), so a
+    // slot's block scales need no reduction
+    const int sub = lane & 15, hwid = tid >> 4;
+    const unsigned half_mask = 0xFFFFu << (lane & 16);
+    const int nb = d >> 7;
+    int64_t it = 0, sc = 0;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x, it++) {
+        const int db = (int)(it & 1);
+        if (!warp_wait(&hd.dy_full[db], (uint32_t)((it >> 1) & 1), abort_flag, dev_status)) return;
+        const uint16_t *dyr = dyb + (int64_t)db * d;
+        const int h = (hwid + (int)(it & 1) * CBT_WARPS) & (2 * CBT_WARPS - 1);
+        float dv[CBT_MAXB][8], am[CBT_MAXB];
+#pragma unroll
+        for (int u = 0; u < CBT_MAXB; u++) {
+            const int blk = h + 2 * CBT_WARPS * u;
+            unpack_bf16x8(blk < nb ? *reinterpret_cast<const uint4 *>(dyr + blk * 128 + sub * 8)
+                                   : make_uint4(0u, 0u, 0u, 0u),
+                          dv[u]);
+            am[u] = fmaxf(fmaxf(fmaxf(fabsf(dv[u][0]), fabsf(dv[u][1])), fmaxf(fabsf(dv[u][2]), fabsf(dv[u][3]))),
+                          fmaxf(fmaxf(fabsf(dv[u][4]), fabsf(dv[u][5])), fmaxf(fabsf(dv[u][6]), fabsf(dv[u][7]))));
+        }
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) {
+#pragma unroll
+            for (int u = 0; u < CBT_MAXB; u++) am[u] = fmaxf(am[u], __shfl_xor_sync(half_mask, am[u], off, 16));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd.dy_empty[db]);            // dy now lives in registers
+        for (int j = 0; j < k; j++) {
+            const int64_t p = t * k + j;
+            const int32_t r = __ldg(slot_to_sorted + p);
+            if (r < 0 || r >= A) continue;
+            const int st = (int)(sc % CBT_STAGES);
+            if (!warp_wait(&hd.out_full[st], (uint32_t)((sc / CBT_STAGES) & 1), abort_flag, dev_status)) return;
+            sc++;
+            const float g = __ldg(gates + p), ag = fabsf(g);
+            const uint16_t *outr = outb + (int64_t)st * d;
+            float dot = 0.0f;
+#pragma unroll
+            for (int u = 0; u < CBT_MAXB; u++) {
+                const int blk = h + 2 * CBT_WARPS * u;
+                if (blk < nb) {
+                    float o[8], f[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(outr + blk * 128 + sub * 8), o);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        dot = fmaf(dv[u][i], o[i], dot);
+                        f[i] = g * dv[u][i];
+                    }
+                    const float s = block_scale(__fmul_rn(ag, am[u]));
+                    __stcs(reinterpret_cast<uint2 *>(d_out_q + (int64_t)r * d + blk * 128 + sub * 8),
+                           e4m3x8_scaled<2>(f, s));
+                    if (sub == 0) d_out_s[(int64_t)r * nb + blk] = s;
+                }
+            }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
-            if (lane == 0) d_gates[t * k + j] = dot;
+            if (lane == 0) {
+                hd.partial[st][warp] = dot;
+                mbar_arrive(&hd.out_empty[st]);
+            }
         }
     }
 }
 
 // One half-warp per (row, 128-column block of F): 8 columns per lane of
 // d_act (bf16), gate and up (fp32); the two dh blocks (gate part at column
-// 128b, up part at F + 128b) are quantised separately.
+// 128b, up part at F + 128b) are quantised separately.  SB blocks per pass
+// with all their loads issued first (80 bytes per block per lane); the
+// (row, block) pairs advance by the quotient and remainder of the stride.
+constexpr int SB = 2;
+
 __global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint16_t *__restrict__ d_act,
                                                               const float *__restrict__ h, int64_t rows, int F,
                                                               uint8_t *__restrict__ dh_q, float *__restrict__ dh_s)
@@ -96,48 +309,72 @@ __global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint16_t *__
     const int sub = lane & 15;
     const unsigned half_mask = 0xFFFFu << (lane & 16);
     const int nbf = F >> 7;
-    const int64_t nblocks = rows * nbf;
-    int64_t b = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 4;
-    const int64_t step = ((int64_t)gridDim.x * blockDim.x) >> 4;
-    for (; b < nblocks; b += step) {
-        const int64_t r = b / nbf, cb = b - r * nbf;
-        const int64_t c0 = cb * 128 + sub * 8;
-        float da[8], gt[8], up[8];
-        unpack_bf16x8(__ldcs(reinterpret_cast<const uint4 *>(d_act + r * F + c0)), da);
-        const float4 *hg = reinterpret_cast<const float4 *>(h + r * 2 * F + c0);
-        const float4 *hu = reinterpret_cast<const float4 *>(h + r * 2 * F + F + c0);
-        const float4 g0 = __ldcs(hg), g1 = __ldcs(hg + 1), u0 = __ldcs(hu), u1 = __ldcs(hu + 1);
-        gt[0] = g0.x; gt[1] = g0.y; gt[2] = g0.z; gt[3] = g0.w; gt[4] = g1.x; gt[5] = g1.y; gt[6] = g1.z; gt[7] = g1.w;
-        up[0] = u0.x; up[1] = u0.y; up[2] = u0.z; up[3] = u0.w; up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
-        float dg[8], du[8], ag = 0.0f, au = 0.0f;
+    const int64_t hw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 4;
+    const int64_t nhw = ((int64_t)gridDim.x * blockDim.x) >> 4;
+    const int64_t dr = nhw / nbf;
+    const int dc = (int)(nhw - dr * nbf);
+    int64_t r = hw / nbf;
+    int cb = (int)(hw - r * nbf);
+    while (r < rows) {
+        int64_t rr[SB];
+        int cc[SB];
+        uint4 ra[SB];
+        float4 rg[SB][2], ru[SB][2];
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const float sg = __fdiv_rn(1.0f, 1.0f + expf(-gt[i]));
-            dg[i] = da[i] * up[i] * sg * (1.0f + gt[i] * (1.0f - sg));
-            du[i] = da[i] * (gt[i] * sg);
-            ag = fmaxf(ag, fabsf(dg[i]));
-            au = fmaxf(au, fabsf(du[i]));
+        for (int u = 0; u < SB; u++) {
+            rr[u] = r;
+            cc[u] = cb;
+            ra[u] = make_uint4(0u, 0u, 0u, 0u);
+            rg[u][0] = rg[u][1] = ru[u][0] = ru[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < rows) {
+                const int64_t c0 = (int64_t)cb * 128 + sub * 8;
+                ra[u] = __ldcs(reinterpret_cast<const uint4 *>(d_act + r * F + c0));
+                const float4 *hg = reinterpret_cast<const float4 *>(h + r * 2 * F + c0);
+                const float4 *hu = reinterpret_cast<const float4 *>(h + r * 2 * F + F + c0);
+                rg[u][0] = __ldcs(hg);
+                rg[u][1] = __ldcs(hg + 1);
+                ru[u][0] = __ldcs(hu);
+                ru[u][1] = __ldcs(hu + 1);
+            }
+            cb += dc;
+            r += dr;
+            if (cb >= nbf) {
+                cb -= nbf;
+                r++;
+            }
         }
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) {
-            ag = fmaxf(ag, __shfl_xor_sync(half_mask, ag, off, 16));
-            au = fmaxf(au, __shfl_xor_sync(half_mask, au, off, 16));
-        }
-        const float sg_ = block_scale(ag), su = block_scale(au);
-        uint2 qg, qu;
-        qg.x = (uint32_t)pack_e4m3x2(__fdiv_rn(dg[0], sg_), __fdiv_rn(dg[1], sg_)) |
-               ((uint32_t)pack_e4m3x2(__fdiv_rn(dg[2], sg_), __fdiv_rn(dg[3], sg_)) << 16);
-        qg.y = (uint32_t)pack_e4m3x2(__fdiv_rn(dg[4], sg_), __fdiv_rn(dg[5], sg_)) |
-               ((uint32_t)pack_e4m3x2(__fdiv_rn(dg[6], sg_), __fdiv_rn(dg[7], sg_)) << 16);
-        qu.x = (uint32_t)pack_e4m3x2(__fdiv_rn(du[0], su), __fdiv_rn(du[1], su)) |
-               ((uint32_t)pack_e4m3x2(__fdiv_rn(du[2], su), __fdiv_rn(du[3], su)) << 16);
-        qu.y = (uint32_t)pack_e4m3x2(__fdiv_rn(du[4], su), __fdiv_rn(du[5], su)) |
-               ((uint32_t)pack_e4m3x2(__fdiv_rn(du[6], su), __fdiv_rn(du[7], su)) << 16);
-        *reinterpret_cast<uint2 *>(dh_q + r * 2 * F + c0) = qg;
-        *reinterpret_cast<uint2 *>(dh_q + r * 2 * F + F + c0) = qu;
-        if (sub == 0) {
-            dh_s[r * 2 * nbf + cb] = sg_;
-            dh_s[r * 2 * nbf + nbf + cb] = su;
+        for (int u = 0; u < SB; u++) {
+            if (rr[u] >= rows) break;                            // uniform over the half-warp
+            const int64_t c0 = (int64_t)cc[u] * 128 + sub * 8;
+            float da[8];
+            unpack_bf16x8(ra[u], da);
+            const float gt[8] = {rg[u][0].x, rg[u][0].y, rg[u][0].z, rg[u][0].w,
+                                 rg[u][1].x, rg[u][1].y, rg[u][1].z, rg[u][1].w};
+            const float up[8] = {ru[u][0].x, ru[u][0].y, ru[u][0].z, ru[u][0].w,
+                                 ru[u][1].x, ru[u][1].y, ru[u][1].z, ru[u][1].w};
+            float dg[8], du[8], ag = 0.0f, au = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const float sg = sigmoid_fast(gt[i]);
+                dg[i] = dswiglu_gate(da[i], gt[i], up[i], sg);
+                du[i] = dswiglu_up(da[i], gt[i], sg);
+                ag = fmaxf(ag, fabsf(dg[i]));
+                au = fmaxf(au, fabsf(du[i]));
+            }
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) {
+                ag = fmaxf(ag, __shfl_xor_sync(half_mask, ag, off, 16));
+                au = fmaxf(au, __shfl_xor_sync(half_mask, au, off, 16));
+            }
+            const float sg_ = block_scale(ag), su = block_scale(au);
+            const uint2 qg = e4m3x8_scaled<2>(dg, sg_), qu = e4m3x8_scaled<2>(du, su);
+            *reinterpret_cast<uint2 *>(dh_q + rr[u] * 2 * F + c0) = qg;
+            *reinterpret_cast<uint2 *>(dh_q + rr[u] * 2 * F + F + c0) = qu;
+            if (sub == 0) {
+                dh_s[rr[u] * 2 * nbf + cc[u]] = sg_;
+                dh_s[rr[u] * 2 * nbf + nbf + cc[u]] = su;
+            }
         }
     }
 }
@@ -216,66 +453,89 @@ struct WgSrc {
     int k, F;
 };
 
-// 32 consecutive channels c0 .. c0+31 of sorted row r (16-byte loads)
+// Rows 4 rg .. 4 rg + 3 of one 128-row block, channels c0 .. c0 + 7, as fp32
+// values (zero past the expert's last row): every global load of the four
+// rows is issued before the first value is formed.
 template <int SRC>
-__device__ __forceinline__ void wg_row32(const WgSrc &w, int64_t r, int64_t c0, int64_t C, float *v)
+__device__ __forceinline__ void wg_rows4x8(const WgSrc &w, int64_t r0, int64_t rend, int64_t c0, int64_t C,
+                                           float (&v)[4][8])
 {
-    if (SRC == SRC_GDY || SRC == SRC_X) {
-        const int32_t slot = __ldg(w.sorted_to_slot + r);
-        const float g = SRC == SRC_GDY ? __ldg(w.gates + slot) : 1.0f;
-        const uint4 *src = reinterpret_cast<const uint4 *>((SRC == SRC_GDY ? w.dy : w.x) + (int64_t)(slot / w.k) * C + c0);
+    if constexpr (SRC == SRC_GDY || SRC == SRC_X) {
+        int32_t slot[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) slot[i] = r0 + i < rend ? __ldg(w.sorted_to_slot + r0 + i) : -1;
+        float g[4];
+        uint4 raw[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            unpack_bf16x8(__ldg(src + i), v + 8 * i);
-            if (SRC == SRC_GDY) {
-#pragma unroll
-                for (int j = 0; j < 8; j++) v[8 * i + j] = g * v[8 * i + j];
+            g[i] = 1.0f;
+            raw[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (slot[i] >= 0) {
+                if (SRC == SRC_GDY) g[i] = __ldg(w.gates + slot[i]);
+                raw[i] = __ldg(reinterpret_cast<const uint4 *>((SRC == SRC_GDY ? w.dy : w.x) +
+                                                               (int64_t)(slot[i] / w.k) * C + c0));
             }
         }
-    } else if (SRC == SRC_ACT) {
-        const float4 *hg = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + c0);
-        const float4 *hu = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + w.F + c0);
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const float4 g4 = __ldg(hg + i), u4 = __ldg(hu + i);
-            v[4 * i + 0] = __fdiv_rn(g4.x, 1.0f + expf(-g4.x)) * u4.x;
-            v[4 * i + 1] = __fdiv_rn(g4.y, 1.0f + expf(-g4.y)) * u4.y;
-            v[4 * i + 2] = __fdiv_rn(g4.z, 1.0f + expf(-g4.z)) * u4.z;
-            v[4 * i + 3] = __fdiv_rn(g4.w, 1.0f + expf(-g4.w)) * u4.w;
+        for (int i = 0; i < 4; i++) {
+            unpack_bf16x8(raw[i], v[i]);
+            if (SRC == SRC_GDY) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) v[i][j] = g[i] * v[i][j];
+            }
         }
     } else {
-        const bool up_half = c0 >= w.F;
+        // SRC_ACT: channels of F; SRC_DH: channels of 2F, the gate half below
+        // F and the up half above (8-channel groups never straddle F)
+        const bool up_half = SRC == SRC_DH && c0 >= w.F;
         const int64_t f0 = up_half ? c0 - w.F : c0;
-        float da[32];
-        const uint4 *a4 = reinterpret_cast<const uint4 *>(w.d_act + r * w.F + f0);
+        float4 hg[4][2], hu[4][2];
+        uint4 ra[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) unpack_bf16x8(__ldg(a4 + i), da + 8 * i);
-        const float4 *hg = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + f0);
-        const float4 *hu = reinterpret_cast<const float4 *>(w.h + r * 2 * w.F + w.F + f0);
+        for (int i = 0; i < 4; i++) {
+            hg[i][0] = hg[i][1] = hu[i][0] = hu[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            ra[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (r0 + i < rend) {
+                const float4 *pg = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * w.F + f0);
+                const float4 *pu = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * w.F + w.F + f0);
+                hg[i][0] = __ldg(pg);
+                hg[i][1] = __ldg(pg + 1);
+                hu[i][0] = __ldg(pu);
+                hu[i][1] = __ldg(pu + 1);
+                if (SRC == SRC_DH) ra[i] = __ldg(reinterpret_cast<const uint4 *>(w.d_act + (r0 + i) * w.F + f0));
+            }
+        }
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const float4 g4 = __ldg(hg + i), u4 = __ldg(hu + i);
-            const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, uu[4] = {u4.x, u4.y, u4.z, u4.w};
+        for (int i = 0; i < 4; i++) {
+            const float gg[8] = {hg[i][0].x, hg[i][0].y, hg[i][0].z, hg[i][0].w,
+                                 hg[i][1].x, hg[i][1].y, hg[i][1].z, hg[i][1].w};
+            const float uu[8] = {hu[i][0].x, hu[i][0].y, hu[i][0].z, hu[i][0].w,
+                                 hu[i][1].x, hu[i][1].y, hu[i][1].z, hu[i][1].w};
+            if (SRC == SRC_ACT) {
+                // the activation as the GEMM1 epilogue forms it
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const float g = gg[j], sg = __fdiv_rn(1.0f, 1.0f + expf(-g));
-                const float a = da[4 * i + j];
-                v[4 * i + j] = up_half ? a * (g * sg) : a * uu[j] * sg * (1.0f + g * (1.0f - sg));
+                for (int j = 0; j < 8; j++) v[i][j] = __fdividef(gg[j], 1.0f + __expf(-gg[j])) * uu[j];
+            } else {
+                float da[8];
+                unpack_bf16x8(ra[i], da);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float sg = sigmoid_fast(gg[j]);
+                    v[i][j] = up_half ? dswiglu_up(da[j], gg[j], sg) : dswiglu_gate(da[j], gg[j], uu[j], sg);
+                }
             }
         }
     }
 }
 
-// the transpose tile: row stride 65 words, and each 32-row group shifted by 8
-// more words, so that the column reads (8 channels x 4 row groups per warp)
-// and the row writes (32 rows per warp) hit 32 distinct banks
-__device__ __forceinline__ int q1_idx(int r, int c) { return r * 65 + c + (r >> 5) * 8; }
-constexpr int Q1_TILE = 127 * 65 + 64 + 3 * 8;
-
-// One CTA per (64 channels, padded 128-row block): the block's values are
-// staged in shared memory, each channel's amax over the expert's rows is a
-// 4-thread reduction, and each thread writes 32 codes of one channel (the
-// 128 codes of a channel are one contiguous 128-byte run of q).
+// One CTA per (64 channels, padded 128-row block).  Thread (rg, cg) =
+// (tid / 8, tid % 8) holds rows 4 rg .. 4 rg + 3 and channels 8 cg .. 8 cg + 7
+// (each 16-byte load of a warp covers four 128-byte row segments).  Channel
+// amax: over the thread's four rows, the warp's four row groups (two
+// shuffles) and the eight warps (shared memory).  The four codes of a
+// channel form one 32-bit word, stored to a [channel][32 words] shared tile
+// at word (rg + 4 cg) mod 32 (conflict-free); each channel's 128 codes then
+// leave as eight 16-byte stores (one contiguous 128-byte run of q).
 // Scales channel-major sc[c * ld/128 + kb] or block-major sc[kb * C + c] (the
 // layout the weight-gradient GEMM takes for both operands: a tile's 128
 // scales of one K block are one contiguous 512-byte run).
@@ -285,7 +545,9 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t
                                                           int64_t ld, bool kb_major, uint8_t *__restrict__ q,
                                                           float *__restrict__ sc)
 {
-    __shared__ float tile[Q1_TILE];
+    __shared__ __align__(16) uint32_t tq[64 * 32];
+    __shared__ float red[8][64];
+    __shared__ __align__(16) float ssc[64];
     __shared__ int64_t s_r0, s_rend;
     const int64_t P = __ldg(pad + E);
     const int64_t kb = blockIdx.y;
@@ -303,44 +565,187 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t
         }
     }
     __syncthreads();
-    const int64_t r0 = s_r0, rend = s_rend;
-    const int64_t c0 = (int64_t)blockIdx.x * 64;
-    const int tid = threadIdx.x;
-    {
-        const int rr = tid & 127, ch = (tid >> 7) * 32;
-        const int64_t r = r0 + rr;
-        float v[32];
-        if (r < rend) {
-            wg_row32<SRC>(w, r, c0 + ch, C, v);
-        } else {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid & 7, rg = tid >> 3;
+    const int64_t cbase = (int64_t)blockIdx.x * 64;
+    float v[4][8];
+    wg_rows4x8<SRC>(w, s_r0 + 4 * rg, s_rend, cbase + 8 * cg, C, v);
+    float am[8];
 #pragma unroll
-            for (int i = 0; i < 32; i++) v[i] = 0.0f;
-        }
+    for (int j = 0; j < 8; j++) {
+        am[j] = fmaxf(fmaxf(fabsf(v[0][j]), fabsf(v[1][j])), fmaxf(fabsf(v[2][j]), fabsf(v[3][j])));
+        am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], 8));
+        am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], 16));
+    }
+    if (lane < 8) {
 #pragma unroll
-        for (int i = 0; i < 32; i++) tile[q1_idx(rr, ch + i)] = v[i];
+        for (int j = 0; j < 8; j++) red[warp][8 * cg + j] = am[j];
     }
     __syncthreads();
-    const int cc = tid >> 2, part = tid & 3;
-    float amax = 0.0f;
-#pragma unroll 8
-    for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(tile[q1_idx(part * 32 + i, cc)]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    const float s = block_scale(amax);
-    const int64_t c = c0 + cc;
-    if (c < C) {
-        uint32_t wds[8];
+    if (tid < 64) {
+        float a = red[0][tid];
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const float *t4 = &tile[q1_idx(part * 32 + 4 * i, cc)];   // rows +1..+3 are +65 words each
-            wds[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(t4[0], s), __fdiv_rn(t4[65], s)) |
-                     ((uint32_t)pack_e4m3x2(__fdiv_rn(t4[130], s), __fdiv_rn(t4[195], s)) << 16);
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(q + c * ld + kb * 128 + part * 32);
-        dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-        dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
-        if (part == 0) sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
+        for (int i = 1; i < 8; i++) a = fmaxf(a, red[i][tid]);
+        const float s = block_scale(a);
+        ssc[tid] = s;
+        const int64_t c = cbase + tid;
+        sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
     }
+    __syncthreads();
+    const float4 s0 = *reinterpret_cast<const float4 *>(&ssc[8 * cg]);
+    const float4 s1 = *reinterpret_cast<const float4 *>(&ssc[8 * cg + 4]);
+    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        // x is bf16 (one correction step suffices); the others are fp32 values
+        tq[(8 * cg + j) * 32 + ((rg + 4 * cg) & 31)] =
+            e4m3x4_scaled<SRC == SRC_X ? 1 : 2>(v[0][j], v[1][j], v[2][j], v[3][j], s[j]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const int u = tid + 256 * it, ch = u >> 3, chunk = u & 7;
+        const uint4 val = *reinterpret_cast<const uint4 *>(&tq[ch * 32 + ((4 * chunk + 4 * (ch >> 3)) & 31)]);
+        *reinterpret_cast<uint4 *>(q + (cbase + ch) * ld + kb * 128 + 16 * chunk) = val;
+    }
+}
+
+// The same quantiser for the bf16 operands (SRC_GDY: g * dy of each routed
+// row's token, SRC_X: x of that token), persistent over channel tiles so
+// that loads stay in flight across them: a CTA of 256 threads takes one
+// padded 128-row block and Q1_TPC consecutive 64-channel tiles.  Thread
+// (rg, cg) = (tid / 8, tid % 8) owns rows 4 rg .. 4 rg + 3 and, in every
+// tile, channels 8 cg .. 8 cg + 7: it looks its rows' tokens (and gates) up
+// once, then copies its four 16-byte pieces of each tile into a
+// Q1_STAGES-deep shared-memory ring with cp.async, Q1_STAGES - 1 tiles
+// ahead (each thread reads back only its own pieces, so the ring needs no
+// barrier).  Per tile: channel amax over the thread's rows, its warp (two
+// shuffles) and the eight warps (shared memory), then the four codes of a
+// channel as one word at word (rg + 4 cg) mod 32 of the channel's row of
+// the code tile (conflict-free), and each channel's 128 codes leave as
+// eight 16-byte stores.
+constexpr int Q1_STAGES = 4;
+constexpr int Q1_TPC = 28;
+constexpr int Q1_STAGE_BYTES = 128 * 64 * 2;
+constexpr int Q1_SMEM = Q1_STAGES * Q1_STAGE_BYTES;
+
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int SRC>
+__global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const int32_t *__restrict__ offsets,
+                                                               const int32_t *__restrict__ pad, int E, int64_t C,
+                                                               int64_t ld, bool kb_major, uint8_t *__restrict__ q,
+                                                               float *__restrict__ sc)
+{
+    extern __shared__ __align__(128) uint8_t q1_ring[];
+    __shared__ __align__(16) uint32_t tq[64 * 32];
+    __shared__ float red[8][64];
+    __shared__ __align__(16) float ssc[64];
+    __shared__ int64_t s_r0, s_rend;
+    const int64_t P = __ldg(pad + E);
+    const int64_t kb = blockIdx.y;
+    const int ntiles = (int)(C / 64);
+    const int t0 = blockIdx.x * Q1_TPC;
+    const int t1 = t0 + Q1_TPC < ntiles ? t0 + Q1_TPC : ntiles;
+    if (kb * 128 >= P || kb * 128 >= ld || t0 >= ntiles) return;
+    if (threadIdx.x == 0) s_r0 = s_rend = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t p0 = __ldg(pad + e), p1 = __ldg(pad + e + 1);
+        if (p0 <= kb * 128 && kb * 128 < p1) {
+            s_r0 = __ldg(offsets + e) + (kb * 128 - p0);
+            s_rend = __ldg(offsets + e + 1);
+        }
+    }
+    __syncthreads();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid & 7, rg = tid >> 3;
+    const int64_t r0 = s_r0 + 4 * rg, rend = s_rend;
+    const uint16_t *src = SRC == SRC_GDY ? w.dy : w.x;
+    int64_t off[4];            // element offset of the row's token, or -1
+    float g[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int32_t slot = r0 + i < rend ? __ldg(w.sorted_to_slot + r0 + i) : -1;
+        off[i] = slot >= 0 ? (int64_t)(slot / w.k) * C + 8 * cg : -1;
+        g[i] = SRC == SRC_GDY && slot >= 0 ? __ldg(w.gates + slot) : 1.0f;
+    }
+    uint4 *ring = reinterpret_cast<uint4 *>(q1_ring);      // [stage][row][cg]
+    auto issue = [&](int t) {
+        uint4 *dst = ring + (t % Q1_STAGES) * (128 * 8) + (4 * rg) * 8 + cg;
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            cp_async16_zfill(dst + 8 * i, off[i] >= 0 ? src + off[i] + (int64_t)t * 64 : src, off[i] >= 0);
+    };
+#pragma unroll
+    for (int u = 0; u < Q1_STAGES - 1; u++) {
+        if (t0 + u < t1) issue(t0 + u);
+        cp_async_commit();
+    }
+    for (int t = t0; t < t1; t++) {
+        if (t + Q1_STAGES - 1 < t1) issue(t + Q1_STAGES - 1);
+        cp_async_commit();
+        cp_async_wait<Q1_STAGES - 1>();                   // this thread's pieces of tile t
+        float v[4][8];
+        const uint4 *mine = ring + (t % Q1_STAGES) * (128 * 8) + (4 * rg) * 8 + cg;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            unpack_bf16x8(mine[8 * i], v[i]);
+            if (SRC == SRC_GDY) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) v[i][j] = g[i] * v[i][j];
+            }
+        }
+        float am[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            am[j] = fmaxf(fmaxf(fabsf(v[0][j]), fabsf(v[1][j])), fmaxf(fabsf(v[2][j]), fabsf(v[3][j])));
+#pragma unroll
+        for (int j = 0; j < 8; j++) am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], 8));
+#pragma unroll
+        for (int j = 0; j < 8; j++) am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], 16));
+        if (lane < 8) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) red[warp][8 * cg + j] = am[j];
+        }
+        __syncthreads();
+        const int64_t cbase = (int64_t)t * 64;
+        if (tid < 64) {
+            float a = red[0][tid];
+#pragma unroll
+            for (int i = 1; i < 8; i++) a = fmaxf(a, red[i][tid]);
+            const float s = block_scale(a);
+            ssc[tid] = s;
+            const int64_t c = cbase + tid;
+            sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
+        }
+        __syncthreads();
+        const float4 s0 = *reinterpret_cast<const float4 *>(&ssc[8 * cg]);
+        const float4 s1 = *reinterpret_cast<const float4 *>(&ssc[8 * cg + 4]);
+        const float s8[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            // x is bf16 (one correction step suffices); g * dy is an fp32 product
+            constexpr int ST = SRC == SRC_X ? 1 : 2;
+            tq[(8 * cg + j) * 32 + ((rg + 4 * cg) & 31)] = e4m3x4_scaled<ST>(v[0][j], v[1][j], v[2][j], v[3][j], s8[j]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            const int u = tid + 256 * it, ch = u >> 3, chunk = u & 7;
+            const uint4 val = *reinterpret_cast<const uint4 *>(&tq[ch * 32 + ((4 * chunk + 4 * (ch >> 3)) & 31)]);
+            *reinterpret_cast<uint4 *>(q + (cbase + ch) * ld + kb * 128 + 16 * chunk) = val;
+        }
+    }
+    cp_async_wait<0>();
 }
 
 } // namespace moe
@@ -349,17 +754,33 @@ using namespace moe;
 
 MOE_API moe_status moe_combine_backward(const uint16_t *dy, const float *gates, const uint16_t *out_sorted,
                                         const int32_t *slot_to_sorted, int T, int k, int d, int64_t A,
-                                        uint8_t *d_out_q, float *d_out_s, float *d_gates, void *stream)
+                                        uint8_t *d_out_q, float *d_out_s, float *d_gates, int32_t *dev_status,
+                                        void *stream)
 {
     if (T < 0 || k < 1 || k > 32 || d <= 0 || d % 128 != 0 || A < 0) return MOE_ERR_SHAPE;
     if (T == 0) return MOE_OK;
     if (!dy || !gates || !out_sorted || !slot_to_sorted || !d_out_q || !d_out_s || !d_gates) return MOE_ERR_NULL;
     if (!aligned16(dy) || !aligned16(out_sorted) || !aligned16(d_out_q)) return MOE_ERR_ALIGN;
-    int64_t grid = ((int64_t)T + 7) / 8;
+    cudaStream_t st = as_stream(stream);
+    if (d <= CBT_MAX_D) {
+        const size_t smem = CBT_HDR + (size_t)(2 + CBT_STAGES) * d * 2;
+        if (cudaFuncSetAttribute(combine_backward_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        // two CTAs per SM (both fit in the SM's shared memory for every
+        // d <= CBT_MAX_D), persistent over tokens
+        const int per_sm = smem * 2 <= 227 * 1024 ? 2 : 1;
+        int64_t grid = (int64_t)sm_count() * per_sm;
+        if (grid > T) grid = T;
+        combine_backward_tma_kernel<<<(unsigned)grid, CBT_THREADS, smem, st>>>(
+            dy, gates, out_sorted, slot_to_sorted, T, k, d, A, d_out_q, d_out_s, d_gates, dev_status);
+        return launch_status();
+    }
+    int64_t grid = ((int64_t)T * k + 7) / 8;                  // one warp per (token, slot)
     const int64_t cap = (int64_t)sm_count() * 8;
     if (grid > cap) grid = cap;
-    combine_backward_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(dy, gates, out_sorted, slot_to_sorted, T,
-                                                                          k, d, A, d_out_q, d_out_s, d_gates);
+    combine_backward_kernel<<<(unsigned)grid, 256, 0, st>>>(dy, gates, out_sorted, slot_to_sorted, T, k, d, A,
+                                                           d_out_q, d_out_s, d_gates);
     return launch_status();
 }
 
@@ -422,14 +843,33 @@ MOE_API moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gat
         return MOE_ERR_ALIGN;
     if (max_pad == 0) return MOE_OK;
     // one CTA per (64 channels, 128-row block) of the largest possible padded
-    // extent; blocks past pad[E] (known on the device only) return at once
+    // extent (the bf16 operands: per (Q1_TPC 64-channel tiles, 128-row
+    // block)); blocks past pad[E] (known on the device only) return at once
     const dim3 grid((unsigned)((C + 63) / 64), (unsigned)(max_pad / 128));
+    const dim3 grid_bf16((unsigned)((C / 64 + Q1_TPC - 1) / Q1_TPC), (unsigned)(max_pad / 128));
     cudaStream_t st = as_stream(stream);
+    const bool kbm = scales_kb_major != 0;
     switch (src) {
-    case SRC_GDY: quant_128x1_kernel<SRC_GDY><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
-    case SRC_ACT: quant_128x1_kernel<SRC_ACT><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
-    case SRC_DH: quant_128x1_kernel<SRC_DH><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
-    case SRC_X: quant_128x1_kernel<SRC_X><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, scales_kb_major != 0, q, scales); break;
+    case SRC_GDY:
+        if (cudaFuncSetAttribute(quant_128x1_bf16_kernel<SRC_GDY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Q1_SMEM) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        quant_128x1_bf16_kernel<SRC_GDY><<<grid_bf16, 256, Q1_SMEM, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm,
+                                                                         q, scales);
+        break;
+    case SRC_ACT:
+        quant_128x1_kernel<SRC_ACT><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm, q, scales);
+        break;
+    case SRC_DH:
+        quant_128x1_kernel<SRC_DH><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm, q, scales);
+        break;
+    case SRC_X:
+        if (cudaFuncSetAttribute(quant_128x1_bf16_kernel<SRC_X>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Q1_SMEM) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        quant_128x1_bf16_kernel<SRC_X><<<grid_bf16, 256, Q1_SMEM, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm, q,
+                                                                       scales);
+        break;
     default: return MOE_ERR_SHAPE;
     }
     return launch_status();

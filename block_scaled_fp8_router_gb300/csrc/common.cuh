@@ -56,11 +56,86 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi)
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// block scale of the DeepSeek-V3 recipe: amax / 448 (IEEE division), 1 when 0
+// block scale of the DeepSeek-V3 recipe: amax / 448 (IEEE division), 1 when
+// 0.  For 2^-100 <= amax <= 2^127 the quotient comes from the constant
+// RN(1/448) and one fused correction step q + RN(amax - 448 q) / 448 (the
+// step Markstein's theorem describes), which equals the IEEE quotient for
+// every such binary32 amax (checked exhaustively against IEEE division; see
+// the division test); other values take __fdiv_rn.
 __device__ __forceinline__ float block_scale(float amax)
 {
-    float s = __fdiv_rn(amax, 448.0f);
-    return s == 0.0f ? 1.0f : s;
+    if (!(amax >= 0x1p-100f && amax <= 0x1p127f)) {
+        const float s = __fdiv_rn(amax, 448.0f);
+        return s == 0.0f ? 1.0f : s;
+    }
+    constexpr float y = 1.0f / 448.0f;
+    const float q = __fmul_rn(amax, y);          // never contracted into an FMA
+    return fmaf(fmaf(q, -448.0f, amax), y, q);
+}
+
+// Division by a block scale with the scale's reciprocal shared by the block,
+// giving the correctly rounded v / s (the value of __fdiv_rn(v, s)) on the
+// fast path.  y = RN(1/s), q0 = RN(v*y), and each step replaces q by
+// q - RN(q*s - v) * y with fused multiply-adds, i.e. q + RN(v - q*s) * y.
+// Markstein's theorem (J.-M. Muller et al., Handbook of Floating-Point
+// Arithmetic, on division with an FMA): when q is a faithful rounding of v/s
+// the residual is exact and one step returns RN(v/s).  q0 can be 1.5 ulp off,
+// but one step from it lands within 2^-22 ulp of v/s before rounding, so it
+// is faithful: STEPS = 2 is correct for every input.  STEPS = 1 returns
+// RN(v/s) for every bf16 v and every scale of the 1 x 128 rule on the fast
+// path (checked exhaustively against IEEE division; see the division test).
+// The fast path needs 2^-90 <= s <= 2^126 (residuals above the underflow
+// threshold for |v / s| >= 2^-12, and a normal reciprocal); other scales,
+// inf and NaN take __fdiv_rn.  A quotient below 2^-12 can differ from
+// RN(v/s) in its last bits, which does not change its E4M3 code (zero of the
+// same sign).  The residual is taken negated, q*s - v, so that a zero
+// dividend keeps its sign: -0 gives q0 = -0, residual +0, and
+// -0 + (-(+0) * y) = -0.
+__device__ __forceinline__ bool fast_scale(float s) { return s >= 0x1p-90f && s <= 0x1p126f; }
+
+template <int STEPS>
+__device__ __forceinline__ float div_fast(float v, float s, float y)
+{
+    float q = __fmul_rn(v, y);                   // never contracted into an FMA
+#pragma unroll
+    for (int i = 0; i < STEPS; i++) q = fmaf(-fmaf(q, s, -v), y, q);
+    return q;
+}
+
+// eight values divided by one scale -> eight E4M3 codes (round to nearest
+// even, saturated), value 0 in the low byte; one branch per block
+template <int STEPS>
+__device__ __forceinline__ uint2 e4m3x8_scaled(const float (&v)[8], float s)
+{
+    float q[8];
+    if (fast_scale(s)) {
+        const float y = __frcp_rn(s);
+#pragma unroll
+        for (int i = 0; i < 8; i++) q[i] = div_fast<STEPS>(v[i], s, y);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; i++) q[i] = __fdiv_rn(v[i], s);
+    }
+    uint2 out;
+    out.x = (uint32_t)pack_e4m3x2(q[0], q[1]) | ((uint32_t)pack_e4m3x2(q[2], q[3]) << 16);
+    out.y = (uint32_t)pack_e4m3x2(q[4], q[5]) | ((uint32_t)pack_e4m3x2(q[6], q[7]) << 16);
+    return out;
+}
+
+// four values (v0..v3) -> four codes, value 0 in the low byte
+template <int STEPS>
+__device__ __forceinline__ uint32_t e4m3x4_scaled(float v0, float v1, float v2, float v3, float s)
+{
+    float q[4] = {v0, v1, v2, v3};
+    if (fast_scale(s)) {
+        const float y = __frcp_rn(s);
+#pragma unroll
+        for (int i = 0; i < 4; i++) q[i] = div_fast<STEPS>(q[i], s, y);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) q[i] = __fdiv_rn(q[i], s);
+    }
+    return (uint32_t)pack_e4m3x2(q[0], q[1]) | ((uint32_t)pack_e4m3x2(q[2], q[3]) << 16);
 }
 
 __device__ __forceinline__ void dev_flag(int32_t *status, int32_t bits)

@@ -488,7 +488,15 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
                 amax = fmaxf(s.red[red_par][0][r_in], s.red[red_par][1][r_in]);
                 red_par ^= 1;
                 const float sc = block_scale(amax);
-                const float rs = __frcp_rn(sc);   // one correctly rounded reciprocal per row
+                // one reciprocal per row, the correctly rounded act / sc per element
+                if (fast_scale(sc)) {
+                    const float y = __frcp_rn(sc);
+#pragma unroll
+                    for (int i = 0; i < 64; i++) acc[i] = div_fast<2>(acc[i], sc, y);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; i++) acc[i] = __fdiv_rn(acc[i], sc);
+                }
                 if (row_ok && !aborted) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.act_q + row * p.F + tl.n_blk * 128 + 64 * cg);
 #pragma unroll
@@ -497,8 +505,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 4; i++) {
                             const float *a = acc + 16 * u + 4 * i;
-                            w[i] = (uint32_t)pack_e4m3x2(a[0] * rs, a[1] * rs) |
-                                   ((uint32_t)pack_e4m3x2(a[2] * rs, a[3] * rs) << 16);
+                            w[i] = (uint32_t)pack_e4m3x2(a[0], a[1]) | ((uint32_t)pack_e4m3x2(a[2], a[3]) << 16);
                         }
                         dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
@@ -1159,13 +1166,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t e8 = ue8m0_exp_of(amax);
                 const float sc = e8 == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e8 << 23);
                 if (row_ok && !aborted) {
+                    // sc is a power of two from 2^-127 to 2^127: its reciprocal
+                    // is exact, so v * (1/sc) is the correctly rounded v / sc
+                    const float rsc = __frcp_rn(sc);
                     uint32_t w[8];
 #pragma unroll
                     for (int i = 0; i < 8; i++)
-                        w[i] = (uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i], sc), __fdiv_rn(acc0[4 * i + 1], sc)) |
-                               ((uint32_t)pack_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sc),
-                                                      __fdiv_rn(acc0[4 * i + 3], sc))
-                                << 16);
+                        w[i] = (uint32_t)pack_e4m3x2(acc0[4 * i] * rsc, acc0[4 * i + 1] * rsc) |
+                               ((uint32_t)pack_e4m3x2(acc0[4 * i + 2] * rsc, acc0[4 * i + 3] * rsc) << 16);
                     uint4 *dst = reinterpret_cast<uint4 *>(p.act_q + row * p.F + tl.n_blk * 128 + 32 * cg);
                     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);

@@ -56,37 +56,58 @@ __device__ __forceinline__ void store_scale(void *scales, int64_t i, float s, ui
     else reinterpret_cast<float *>(scales)[i] = s;
 }
 
+// One half-warp per 1x128 block, QB blocks per pass with all their loads
+// issued before the first is encoded (QB x 16 bytes in flight per lane).
+// A half-warp's blocks are hw, hw + nhw, ...; their (row, column block)
+// advance by the fixed quotient and remainder of nhw / nbc.
+constexpr int QB = 4;
+
 template <bool MX>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t *__restrict__ src, int64_t rows,
                                                           int64_t cols, int64_t ld, uint8_t *__restrict__ q,
                                                           void *__restrict__ scales)
 {
-    const int64_t nbc = cols >> 7;
-    const int64_t nblocks = rows * nbc;
+    const int nbc = (int)(cols >> 7);
     const int lane = threadIdx.x & 31;
     const int sub = lane & 15;
     const unsigned half_mask = 0xFFFFu << (lane & 16);
-    int64_t b = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 4;
-    const int64_t step = ((int64_t)gridDim.x * blockDim.x) >> 4;
-    for (; b < nblocks; b += step) {
-        const int64_t r = b / nbc, cb = b - r * nbc;
-        const uint4 raw = __ldcs(reinterpret_cast<const uint4 *>(src + r * ld + cb * 128 + sub * 8));
-        float v[8];
-        unpack_bf16x8(raw, v);
-        float amax = 0.0f;
+    const int64_t hw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 4;
+    const int64_t nhw = ((int64_t)gridDim.x * blockDim.x) >> 4;
+    const int64_t dr = nhw / nbc;
+    const int dc = (int)(nhw - dr * nbc);
+    int64_t r = hw / nbc;
+    int cb = (int)(hw - r * nbc);
+    while (r < rows) {
+        int64_t rr[QB];
+        int cc[QB];
+        uint4 raw[QB];
 #pragma unroll
-        for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+        for (int u = 0; u < QB; u++) {
+            rr[u] = r;
+            cc[u] = cb;
+            raw[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows) raw[u] = __ldcs(reinterpret_cast<const uint4 *>(src + r * ld + cb * 128 + sub * 8));
+            cb += dc;
+            r += dr;
+            if (cb >= nbc) {
+                cb -= nbc;
+                r++;
+            }
+        }
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o, 16));
-        uint32_t e8;
-        const float s = rule_scale<MX>(amax, e8);
-        uint2 out;
-        out.x = (uint32_t)pack_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
-                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
-        out.y = (uint32_t)pack_e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) |
-                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
-        *reinterpret_cast<uint2 *>(q + r * cols + cb * 128 + sub * 8) = out;
-        if (sub == 0) store_scale<MX>(scales, b, s, e8);
+        for (int u = 0; u < QB; u++) {
+            if (rr[u] >= rows) break;      // uniform over the half-warp
+            float v[8];
+            unpack_bf16x8(raw[u], v);
+            float amax = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                               fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o, 16));
+            uint32_t e8;
+            const float s = rule_scale<MX>(amax, e8);
+            *reinterpret_cast<uint2 *>(q + rr[u] * cols + cc[u] * 128 + sub * 8) = e4m3x8_scaled<1>(v, s);
+            if (sub == 0) store_scale<MX>(scales, rr[u] * nbc + cc[u], s, e8);
+        }
     }
 }
 
@@ -127,11 +148,7 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t *__re
     for (int i = 0; i < 8; i++) {
         float v[8];
         unpack_bf16x8(raw[i], v);
-        uint2 out;
-        out.x = (uint32_t)pack_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
-                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
-        out.y = (uint32_t)pack_e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) |
-                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
+        const uint2 out = e4m3x8_scaled<1>(v, s);
         const int64_t r = br * 128 + tr + 16 * i;
         *reinterpret_cast<uint2 *>(q + r * cols + bc * 128 + tc * 8) = out;
     }

@@ -200,7 +200,7 @@ class MoELayerFP8:
         b = self._bw
         w2t_q, w2t_s, w13t_q, w13t_s = self.w.transposed()
         L.moe_combine_backward(dy, self.gates[:T], self.out_sorted[:A], self.sl2[:A], d_out_q=b["d_out_q"][:A],
-                               d_out_s=b["d_out_s"][:A], d_gates=b["d_gates"][:T])
+                               d_out_s=b["d_out_s"][:A], d_gates=b["d_gates"][:T], dev_status=self.dev_status)
         L.moe_grouped_gemm_fp8(b["d_out_q"][:A], b["d_out_s"][:A], self.offsets, w2t_q, w2t_s, out=b["d_act"][:A],
                                dev_status=self.dev_status)
         L.moe_swiglu_backward(b["d_act"][:A], self.h[:A], dh_q=b["dh_q"][:A], dh_s=b["dh_s"][:A])

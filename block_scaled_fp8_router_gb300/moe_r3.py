@@ -47,7 +47,7 @@ _SIGS = {
     "moe_grouped_ffn_fp8_train": (I, [P, P, P, I64, I, I, I, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_grouped_gemm_fp8": (I, [P, P, P, I64, I, I, I, P, P, P, P, P]),
     "fp8_weight_transpose": (I, [P, P, I64, I64, I64, P, P, P]),
-    "moe_combine_backward": (I, [P, P, P, P, I, I, I, I64, P, P, P, P]),
+    "moe_combine_backward": (I, [P, P, P, P, I, I, I, I64, P, P, P, P, P]),
     "moe_swiglu_backward": (I, [P, P, I64, I, P, P, P]),
     "moe_dispatch_backward": (I, [P, P, I, I, I, P, P]),
     "moe_wgrad_pad_offsets": (I, [P, I, P, P]),
@@ -536,7 +536,7 @@ def fp8_weight_transpose(q, s, qt=None, st=None, stream=None):
 
 
 def moe_combine_backward(dy, gates, out_sorted, slot_to_sorted, d_out_q=None, d_out_s=None, d_gates=None,
-                         stream=None):
+                         dev_status=None, stream=None):
     """-> (d_out_q [A, d] e4m3, d_out_s [A, d/128], d_gates [T, k])."""
     T, k = gates.shape
     A, d = out_sorted.shape
@@ -552,7 +552,7 @@ def moe_combine_backward(dy, gates, out_sorted, slot_to_sorted, d_out_q=None, d_
     _want(d_gates, torch.float32, (T, k), "d_gates")
     _check("moe_combine_backward", _lib.moe_combine_backward(
         _ptr(dy), _ptr(gates), _ptr(out_sorted), _ptr(slot_to_sorted), T, k, d, A, _ptr(d_out_q), _ptr(d_out_s),
-        _ptr(d_gates), _stream(stream)))
+        _ptr(d_gates), _ptr(dev_status), _stream(stream)))
     return d_out_q, d_out_s, d_gates
 
 

@@ -317,7 +317,8 @@ moe_status moe_dispatch_noalloc(const int32_t *topk_ids, int T, int k, int E, co
  *              P_kb = the 128-deep block product of E4M3 codes accumulated
  *              in fp32, promoted into an fp32 accumulator block by block;
  *   act[r,c] = silu(h[r,c]) * h[r,F+c]   (c < F; w13 rows 0..F-1 gate,
- *              F..2F-1 up), requantised 1x128 along F as fp8_block_quant;
+ *              F..2F-1 up; silu from the fast exponential and reciprocal),
+ *              requantised 1x128 along F as fp8_block_quant;
  *   out_sorted[r,:] = bf16 (round to nearest even) of act_q[r,:] W2[e]^T by
  *              the same block promotion.
  * xq_sorted [max_rows, d] e4m3, xs_sorted [max_rows, d/128] fp32;
@@ -396,12 +397,18 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  *                          quantised 1x128 along d as fp8_block_quant, to the
  *                          slot's sorted row r = slot_to_sorted[t*k+j];
  *                          d_gates[t,j] = <dy[t], out_sorted[r]> (fp32
- *                          accumulation), 0 for an unrouted slot.
+ *                          accumulation in a fixed order), 0 for an
+ *                          unrouted slot.  For d <= 8192 the rows are
+ *                          staged by bulk copies and every wait is bounded:
+ *                          one that runs out ORs MOE_DEV_TIMEOUT into
+ *                          dev_status (nullable) and the call's outputs are
+ *                          then incomplete.
  *   moe_grouped_gemm_fp8   with W2 transposed: d_act = d_out W2 (bf16).
  *   moe_swiglu_backward    from the saved pre-activations h = [g | u]:
  *                          d_g = d_act * u * s(g) * (1 + g (1 - s(g))),
- *                          d_u = d_act * g * s(g) (s the logistic sigmoid),
- *                          quantised 1x128 along 2F.
+ *                          d_u = d_act * g * s(g) (s the logistic sigmoid,
+ *                          from the fast exponential and reciprocal as the
+ *                          forward's silu), quantised 1x128 along 2F.
  *   moe_grouped_gemm_fp8   with W13 transposed: dx_sorted = dh W13 (bf16).
  *   moe_dispatch_backward  dx[t] = bf16(sum_j dx_sorted[r(t,j)]), a binary32
  *                          sum in slot order.
@@ -427,7 +434,9 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  *                          bound of pad[E] (multiple of 128, e.g.
  *                          (ceil(A/128) + E) * 128).  src selects the operand
  *                          0: g * dy (d_out, C = d), 1: silu(g) * u from h
- *                          (act, C = F), 2: dh from d_act and h (C = 2F),
+ *                          (act, C = F, silu as the forward's GEMM1 epilogue
+ *                          forms it), 2: dh from d_act and h (C = 2F, as
+ *                          moe_swiglu_backward forms it),
  *                          3: x (C = d); rows map to tokens by
  *                          sorted_to_slot / k.  C a multiple of 128; q and
  *                          the source buffers 16-byte aligned.
@@ -455,7 +464,7 @@ moe_status fp8_weight_transpose(const uint8_t *q, const float *s, int64_t E, int
                                 float *st, void *stream);
 moe_status moe_combine_backward(const uint16_t *dy, const float *gates, const uint16_t *out_sorted,
                                 const int32_t *slot_to_sorted, int T, int k, int d, int64_t A, uint8_t *d_out_q,
-                                float *d_out_s, float *d_gates, void *stream);
+                                float *d_out_s, float *d_gates, int32_t *dev_status, void *stream);
 moe_status moe_swiglu_backward(const uint16_t *d_act, const float *h, int64_t rows, int F, uint8_t *dh_q,
                                float *dh_s, void *stream);
 moe_status moe_dispatch_backward(const uint16_t *dx_sorted, const int32_t *slot_to_sorted, int T, int k, int d,

@@ -74,10 +74,10 @@ def test_host_side_errors(lib):
     assert L.moe_debug_bounded_wait(1000, null, null) == 1
     # backward of the expert path
     y = ctypes.c_void_p(0x1008)                                        # 8-byte aligned only
-    assert L.moe_combine_backward(x, x, x, x, 10, 2, 100, 20, x, x, x, null) == 2      # d % 128
-    assert L.moe_combine_backward(null, null, null, null, 0, 2, 128, 0, null, null, null, null) == 0   # empty
-    assert L.moe_combine_backward(x, x, x, null, 10, 2, 128, 20, x, x, x, null) == 1   # NULL
-    assert L.moe_combine_backward(y, x, x, x, 10, 2, 128, 20, x, x, x, null) == 3      # misaligned dy
+    assert L.moe_combine_backward(x, x, x, x, 10, 2, 100, 20, x, x, x, null, null) == 2      # d % 128
+    assert L.moe_combine_backward(null, null, null, null, 0, 2, 128, 0, null, null, null, null, null) == 0   # empty
+    assert L.moe_combine_backward(x, x, x, null, 10, 2, 128, 20, x, x, x, null, null) == 1   # NULL
+    assert L.moe_combine_backward(y, x, x, x, 10, 2, 128, 20, x, x, x, null, null) == 3      # misaligned dy
     assert L.moe_swiglu_backward(x, x, 10, 100, x, x, null) == 2                        # F % 128
     assert L.moe_swiglu_backward(null, null, 0, 128, null, null, null) == 0             # empty
     assert L.moe_swiglu_backward(x, x, 10, 128, y, x, null) == 3                        # misaligned dh_q

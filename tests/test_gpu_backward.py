@@ -38,8 +38,11 @@ def _deq_rows(q, s):
     return e4m3_to_f64(q) * np.repeat(s.astype(np.float64), 128, axis=1)
 
 
-@pytest.mark.parametrize("T,k,d", [(37, 3, 256), (300, 8, 384), (5, 1, 128)])
+@pytest.mark.parametrize("T,k,d", [(37, 3, 256), (300, 8, 384), (5, 1, 128), (700, 8, 7168), (9, 2, 16512)])
 def test_combine_backward_against_oracle(L, oracle, T, k, d):
+    """Rows staged by bulk copies (d <= 8192; T above the persistent grid at
+    d = 7168, so CTAs take several tokens and wrap the stage ring) and the
+    register path past that (d = 16512)."""
     g = torch.Generator(device=DEV).manual_seed(T + d)
     A = T * k
     sl2 = torch.randperm(A, generator=g, device=DEV).to(torch.int32)
@@ -47,7 +50,9 @@ def test_combine_backward_against_oracle(L, oracle, T, k, d):
     out = torch.randn((A, d), generator=g, device=DEV).to(torch.bfloat16)
     dy = torch.randn((T, d), generator=g, device=DEV).to(torch.bfloat16)
     gates = torch.rand((T, k), generator=g, device=DEV)
-    dq, ds, dg = L.moe_combine_backward(dy, gates, out, sl2)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dq, ds, dg = L.moe_combine_backward(dy, gates, out, sl2, dev_status=st)
+    assert int(st.item()) == 0
     rf, rq, rs, rg = oracle.combine_backward(bf16_bits(dy), gates.cpu().numpy(), bf16_bits(out), sl2.cpu().numpy())
     s = sl2.cpu().numpy()
     routed = s[s >= 0]

@@ -56,6 +56,33 @@ def test_quant_1x128_strided_source(L, oracle):
     np.testing.assert_array_equal(s.cpu().numpy(), rs)
 
 
+def test_quant_1x128_division_sweep(L, oracle):
+    """Every 61st positive bf16 value as a block amax, each block filled with
+    every bf16 magnitude <= amax (alternating signs), 127 per block: the codes
+    come from the scale's reciprocal and one correction step on the device,
+    from IEEE division in the oracle -- bit-exact."""
+    pos = (np.arange(1, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    blocks = []
+    for i in range(0, len(pos), 61):
+        v = pos[: i + 1].copy()
+        v[1::2] *= -1
+        for j in range(0, len(v), 127):
+            blk = np.zeros(128, np.float32)
+            blk[0] = pos[i]
+            blk[1:1 + len(v[j:j + 127])] = v[j:j + 127]
+            blocks.append(blk)
+    cols = 7168
+    per_row = cols // 128
+    nrows = (len(blocks) + per_row - 1) // per_row
+    flat = np.zeros((nrows * per_row, 128), np.float32)
+    flat[: len(blocks)] = np.stack(blocks)
+    x = torch.from_numpy(flat.reshape(nrows, cols)).to(torch.bfloat16).to(DEV)
+    q, s = L.fp8_block_quant(x, 1)
+    rq, rs = oracle.quant_1x128(bf16_bits(x))
+    np.testing.assert_array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+
+
 @pytest.mark.parametrize("rows,cols", [(128, 128), (384, 256), (1408 * 2, 2048)])
 def test_quant_128x128_bit_exact(L, oracle, rows, cols):
     w = _edge_rows(rows, cols, rows + cols)
