@@ -25,7 +25,7 @@ namespace moe {
 // (1 + g * (1 - sg)) and d_up = a * g * sg with sg = sigmoid(g) (fast
 // exponential and reciprocal, as the GEMM1 epilogue forms silu; below
 // g = -87 the reciprocal of a sum past 2^126 is 0, the limit).  The dgrad operand (swiglu_backward_kernel)
-// and the weight-gradient operand (quant_128x1_kernel) both take it from here.
+// and the weight-gradient operand (quant_128x1_dh_kernel) both take it from here.
 __device__ __forceinline__ float dswiglu_gate(float a, float g, float u, float sg)
 {
     return a * u * sg * (1.0f + g * (1.0f - sg));
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(CBT_THREADS, 2)
     if (warp == CBT_WARPS) {
         if (lane != 0) return;
         // producer; pend[st] is the slot whose gate gradient stage st holds
-        int64_t pend[CBT_STAGES];
+        int64_t pend[CBT_STAGES] = {};
         int64_t it = 0, sc = 0;
         bool ok = true;
         // the gate gradient of use u of a stage, once its eight parts are in
@@ -453,97 +453,44 @@ struct WgSrc {
     int k, F;
 };
 
-// Rows 4 rg .. 4 rg + 3 of one 128-row block, channels c0 .. c0 + 7, as fp32
-// values (zero past the expert's last row): every global load of the four
-// rows is issued before the first value is formed.
-template <int SRC>
-__device__ __forceinline__ void wg_rows4x8(const WgSrc &w, int64_t r0, int64_t rend, int64_t c0, int64_t C,
-                                           float (&v)[4][8])
+// The sorted rows [r0, rend) of padded 128-row block kb: the expert with
+// pad[e] <= 128 kb < pad[e+1] (E <= 1024; the CTA's threads check the
+// experts with independent loads; with offsets from moe_wgrad_pad_offsets
+// exactly one matches, otherwise the block is empty).  Called by every
+// thread of the CTA (two barriers).
+__device__ __forceinline__ void padded_block_rows(const int32_t *__restrict__ pad,
+                                                  const int32_t *__restrict__ offsets, int E, int64_t kb,
+                                                  int64_t &s_r0, int64_t &s_rend)
 {
-    if constexpr (SRC == SRC_GDY || SRC == SRC_X) {
-        int32_t slot[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) slot[i] = r0 + i < rend ? __ldg(w.sorted_to_slot + r0 + i) : -1;
-        float g[4];
-        uint4 raw[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            g[i] = 1.0f;
-            raw[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (slot[i] >= 0) {
-                if (SRC == SRC_GDY) g[i] = __ldg(w.gates + slot[i]);
-                raw[i] = __ldg(reinterpret_cast<const uint4 *>((SRC == SRC_GDY ? w.dy : w.x) +
-                                                               (int64_t)(slot[i] / w.k) * C + c0));
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            unpack_bf16x8(raw[i], v[i]);
-            if (SRC == SRC_GDY) {
-#pragma unroll
-                for (int j = 0; j < 8; j++) v[i][j] = g[i] * v[i][j];
-            }
-        }
-    } else {
-        // SRC_ACT: channels of F; SRC_DH: channels of 2F, the gate half below
-        // F and the up half above (8-channel groups never straddle F)
-        const bool up_half = SRC == SRC_DH && c0 >= w.F;
-        const int64_t f0 = up_half ? c0 - w.F : c0;
-        float4 hg[4][2], hu[4][2];
-        uint4 ra[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            hg[i][0] = hg[i][1] = hu[i][0] = hu[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            ra[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (r0 + i < rend) {
-                const float4 *pg = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * w.F + f0);
-                const float4 *pu = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * w.F + w.F + f0);
-                hg[i][0] = __ldg(pg);
-                hg[i][1] = __ldg(pg + 1);
-                hu[i][0] = __ldg(pu);
-                hu[i][1] = __ldg(pu + 1);
-                if (SRC == SRC_DH) ra[i] = __ldg(reinterpret_cast<const uint4 *>(w.d_act + (r0 + i) * w.F + f0));
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const float gg[8] = {hg[i][0].x, hg[i][0].y, hg[i][0].z, hg[i][0].w,
-                                 hg[i][1].x, hg[i][1].y, hg[i][1].z, hg[i][1].w};
-            const float uu[8] = {hu[i][0].x, hu[i][0].y, hu[i][0].z, hu[i][0].w,
-                                 hu[i][1].x, hu[i][1].y, hu[i][1].z, hu[i][1].w};
-            if (SRC == SRC_ACT) {
-                // the activation as the GEMM1 epilogue forms it
-#pragma unroll
-                for (int j = 0; j < 8; j++) v[i][j] = __fdividef(gg[j], 1.0f + __expf(-gg[j])) * uu[j];
-            } else {
-                float da[8];
-                unpack_bf16x8(ra[i], da);
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const float sg = sigmoid_fast(gg[j]);
-                    v[i][j] = up_half ? dswiglu_up(da[j], gg[j], sg) : dswiglu_gate(da[j], gg[j], uu[j], sg);
-                }
-            }
+    if (threadIdx.x == 0) s_r0 = s_rend = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t p0 = __ldg(pad + e), p1 = __ldg(pad + e + 1);
+        if (p0 <= kb * 128 && kb * 128 < p1) {
+            s_r0 = __ldg(offsets + e) + (kb * 128 - p0);
+            s_rend = __ldg(offsets + e + 1);
         }
     }
+    __syncthreads();
 }
 
-// One CTA per (64 channels, padded 128-row block).  Thread (rg, cg) =
+// The act operand (C = F): act = silu(gate) * up as the GEMM1 epilogue forms
+// it, one CTA per (64 channels, padded 128-row block).  Thread (rg, cg) =
 // (tid / 8, tid % 8) holds rows 4 rg .. 4 rg + 3 and channels 8 cg .. 8 cg + 7
-// (each 16-byte load of a warp covers four 128-byte row segments).  Channel
-// amax: over the thread's four rows, the warp's four row groups (two
+// (every load of the four rows issued before the first value is formed).
+// Channel amax: over the thread's four rows, the warp's four row groups (two
 // shuffles) and the eight warps (shared memory).  The four codes of a
 // channel form one 32-bit word, stored to a [channel][32 words] shared tile
 // at word (rg + 4 cg) mod 32 (conflict-free); each channel's 128 codes then
 // leave as eight 16-byte stores (one contiguous 128-byte run of q).
-// Scales channel-major sc[c * ld/128 + kb] or block-major sc[kb * C + c] (the
-// layout the weight-gradient GEMM takes for both operands: a tile's 128
-// scales of one K block are one contiguous 512-byte run).
-template <int SRC>
-__global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t *__restrict__ offsets,
-                                                          const int32_t *__restrict__ pad, int E, int64_t C,
-                                                          int64_t ld, bool kb_major, uint8_t *__restrict__ q,
-                                                          float *__restrict__ sc)
+// Scales, in every 128 x 1 kernel here: channel-major sc[c * ld/128 + kb] or
+// block-major sc[kb * C + c] (the layout the weight-gradient GEMM takes for
+// both operands: a tile's 128 scales of one K block are one contiguous
+// 512-byte run).
+__global__ void __launch_bounds__(256) quant_128x1_act_kernel(WgSrc w, const int32_t *__restrict__ offsets,
+                                                              const int32_t *__restrict__ pad, int E, int64_t C,
+                                                              int64_t ld, bool kb_major, uint8_t *__restrict__ q,
+                                                              float *__restrict__ sc)
 {
     __shared__ __align__(16) uint32_t tq[64 * 32];
     __shared__ float red[8][64];
@@ -552,24 +499,35 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t
     const int64_t P = __ldg(pad + E);
     const int64_t kb = blockIdx.y;
     if (kb * 128 >= P || kb * 128 >= ld) return;
-    // the expert with pad[e] <= 128 kb < pad[e+1] (E <= 1024: each thread
-    // checks up to four experts with independent loads; with offsets from
-    // moe_wgrad_pad_offsets exactly one matches, otherwise the block is empty)
-    if (threadIdx.x == 0) s_r0 = s_rend = 0;
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int32_t p0 = __ldg(pad + e), p1 = __ldg(pad + e + 1);
-        if (p0 <= kb * 128 && kb * 128 < p1) {
-            s_r0 = __ldg(offsets + e) + (kb * 128 - p0);     // first sorted row of the block
-            s_rend = __ldg(offsets + e + 1);
-        }
-    }
-    __syncthreads();
+    padded_block_rows(pad, offsets, E, kb, s_r0, s_rend);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid & 7, rg = tid >> 3;
-    const int64_t cbase = (int64_t)blockIdx.x * 64;
+    const int64_t cbase = (int64_t)blockIdx.x * 64, c0 = cbase + 8 * cg;
+    const int64_t r0 = s_r0 + 4 * rg, rend = s_rend;
+    const int F = w.F;
+    float4 hg[4][2], hu[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        hg[i][0] = hg[i][1] = hu[i][0] = hu[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r0 + i < rend) {
+            const float4 *pg = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * F + c0);
+            const float4 *pu = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * F + F + c0);
+            hg[i][0] = __ldg(pg);
+            hg[i][1] = __ldg(pg + 1);
+            hu[i][0] = __ldg(pu);
+            hu[i][1] = __ldg(pu + 1);
+        }
+    }
     float v[4][8];
-    wg_rows4x8<SRC>(w, s_r0 + 4 * rg, s_rend, cbase + 8 * cg, C, v);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float gg[8] = {hg[i][0].x, hg[i][0].y, hg[i][0].z, hg[i][0].w,
+                             hg[i][1].x, hg[i][1].y, hg[i][1].z, hg[i][1].w};
+        const float uu[8] = {hu[i][0].x, hu[i][0].y, hu[i][0].z, hu[i][0].w,
+                             hu[i][1].x, hu[i][1].y, hu[i][1].z, hu[i][1].w};
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[i][j] = __fdividef(gg[j], 1.0f + __expf(-gg[j])) * uu[j];
+    }
     float am[8];
 #pragma unroll
     for (int j = 0; j < 8; j++) {
@@ -592,21 +550,128 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(WgSrc w, const int32_t
         sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
     }
     __syncthreads();
-    const float4 s0 = *reinterpret_cast<const float4 *>(&ssc[8 * cg]);
-    const float4 s1 = *reinterpret_cast<const float4 *>(&ssc[8 * cg + 4]);
-    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        // x is bf16 (one correction step suffices); the others are fp32 values
+    for (int j = 0; j < 8; j++)
         tq[(8 * cg + j) * 32 + ((rg + 4 * cg) & 31)] =
-            e4m3x4_scaled<SRC == SRC_X ? 1 : 2>(v[0][j], v[1][j], v[2][j], v[3][j], s[j]);
-    }
+            e4m3x4_scaled<2>(v[0][j], v[1][j], v[2][j], v[3][j], ssc[8 * cg + j]);
     __syncthreads();
 #pragma unroll
     for (int it = 0; it < 2; it++) {
         const int u = tid + 256 * it, ch = u >> 3, chunk = u & 7;
         const uint4 val = *reinterpret_cast<const uint4 *>(&tq[ch * 32 + ((4 * chunk + 4 * (ch >> 3)) & 31)]);
         *reinterpret_cast<uint4 *>(q + (cbase + ch) * ld + kb * 128 + 16 * chunk) = val;
+    }
+}
+
+// The dh operand (C = 2F): one CTA per (32 columns f0 .. f0 + 31 of F,
+// padded 128-row block), holding channels f (the gate part) and F + f (the
+// up part) of those columns.  Thread (rg, cg) = (tid / 4, tid % 4) owns
+// rows 2 rg, 2 rg + 1 and columns f0 + 8 cg .. + 7: it reads d_act, the gate
+// and the up pre-activations there once and forms both d_gate and d_up with
+// one sigmoid per element.  Channel amax: the thread's two rows, its warp
+// (three shuffles) and the eight warps (shared memory).  The two codes of a
+// channel's row pair are one halfword of the channel's row of the code
+// tile, at halfword (rg + 8 cg) mod 64 (conflict-free; 16-byte runs stay
+// whole), and each channel's 128 codes leave as eight 16-byte stores.
+__global__ void __launch_bounds__(256) quant_128x1_dh_kernel(WgSrc w, const int32_t *__restrict__ offsets,
+                                                             const int32_t *__restrict__ pad, int E, int64_t C,
+                                                             int64_t ld, bool kb_major, uint8_t *__restrict__ q,
+                                                             float *__restrict__ sc)
+{
+    __shared__ __align__(16) uint16_t tq[64 * 64];
+    __shared__ float red[8][64];
+    __shared__ float ssc[64];
+    __shared__ int64_t s_r0, s_rend;
+    const int64_t P = __ldg(pad + E);
+    const int64_t kb = blockIdx.y;
+    if (kb * 128 >= P || kb * 128 >= ld) return;
+    padded_block_rows(pad, offsets, E, kb, s_r0, s_rend);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid & 3, rg = tid >> 2;
+    const int F = w.F;
+    const int64_t f0 = (int64_t)blockIdx.x * 32, fc = f0 + 8 * cg;
+    const int64_t r0 = s_r0 + 2 * rg, rend = s_rend;
+    uint4 ra[2];
+    float4 hg[2][2], hu[2][2];
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        ra[i] = make_uint4(0u, 0u, 0u, 0u);
+        hg[i][0] = hg[i][1] = hu[i][0] = hu[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r0 + i < rend) {
+            const float4 *pg = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * F + fc);
+            const float4 *pu = reinterpret_cast<const float4 *>(w.h + (r0 + i) * 2 * F + F + fc);
+            hg[i][0] = __ldg(pg);
+            hg[i][1] = __ldg(pg + 1);
+            hu[i][0] = __ldg(pu);
+            hu[i][1] = __ldg(pu + 1);
+            ra[i] = __ldg(reinterpret_cast<const uint4 *>(w.d_act + (r0 + i) * F + fc));
+        }
+    }
+    float vg[2][8], vu[2][8];
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        float da[8];
+        unpack_bf16x8(ra[i], da);
+        const float gg[8] = {hg[i][0].x, hg[i][0].y, hg[i][0].z, hg[i][0].w,
+                             hg[i][1].x, hg[i][1].y, hg[i][1].z, hg[i][1].w};
+        const float uu[8] = {hu[i][0].x, hu[i][0].y, hu[i][0].z, hu[i][0].w,
+                             hu[i][1].x, hu[i][1].y, hu[i][1].z, hu[i][1].w};
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const float sg = sigmoid_fast(gg[j]);
+            vg[i][j] = dswiglu_gate(da[j], gg[j], uu[j], sg);
+            vu[i][j] = dswiglu_up(da[j], gg[j], sg);
+        }
+    }
+    float ag[8], au[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        ag[j] = fmaxf(fabsf(vg[0][j]), fabsf(vg[1][j]));
+        au[j] = fmaxf(fabsf(vu[0][j]), fabsf(vu[1][j]));
+    }
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            ag[j] = fmaxf(ag[j], __shfl_xor_sync(0xFFFFFFFFu, ag[j], off));
+            au[j] = fmaxf(au[j], __shfl_xor_sync(0xFFFFFFFFu, au[j], off));
+        }
+    }
+    if (lane < 4) {
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            red[warp][8 * cg + j] = ag[j];
+            red[warp][32 + 8 * cg + j] = au[j];
+        }
+    }
+    __syncthreads();
+    auto gch = [&](int ch) -> int64_t { return ch < 32 ? f0 + ch : F + f0 + ch - 32; };
+    if (tid < 64) {
+        float a = red[0][tid];
+#pragma unroll
+        for (int i = 1; i < 8; i++) a = fmaxf(a, red[i][tid]);
+        const float s = block_scale(a);
+        ssc[tid] = s;
+        const int64_t c = gch(tid);
+        sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
+    }
+    __syncthreads();
+    const int hp = (rg + 8 * cg) & 63;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const int chg = 8 * cg + j, chu = 32 + 8 * cg + j;
+        const uint32_t cgw = e4m3x4_scaled<2>(vg[0][j], vg[1][j], 0.0f, 0.0f, ssc[chg]);
+        const uint32_t cuw = e4m3x4_scaled<2>(vu[0][j], vu[1][j], 0.0f, 0.0f, ssc[chu]);
+        tq[chg * 64 + hp] = (uint16_t)cgw;
+        tq[chu * 64 + hp] = (uint16_t)cuw;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const int u = tid + 256 * it, ch = u >> 3, chunk = u & 7;
+        const int pchunk = (chunk + ((ch & 31) >> 3)) & 7;
+        const uint4 val = *reinterpret_cast<const uint4 *>(&tq[ch * 64 + 8 * pchunk]);
+        *reinterpret_cast<uint4 *>(q + gch(ch) * ld + kb * 128 + 16 * chunk) = val;
     }
 }
 
@@ -629,16 +694,6 @@ constexpr int Q1_TPC = 28;
 constexpr int Q1_STAGE_BYTES = 128 * 64 * 2;
 constexpr int Q1_SMEM = Q1_STAGES * Q1_STAGE_BYTES;
 
-__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 template <int SRC>
 __global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const int32_t *__restrict__ offsets,
                                                                const int32_t *__restrict__ pad, int E, int64_t C,
@@ -656,16 +711,7 @@ __global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const in
     const int t0 = blockIdx.x * Q1_TPC;
     const int t1 = t0 + Q1_TPC < ntiles ? t0 + Q1_TPC : ntiles;
     if (kb * 128 >= P || kb * 128 >= ld || t0 >= ntiles) return;
-    if (threadIdx.x == 0) s_r0 = s_rend = 0;
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int32_t p0 = __ldg(pad + e), p1 = __ldg(pad + e + 1);
-        if (p0 <= kb * 128 && kb * 128 < p1) {
-            s_r0 = __ldg(offsets + e) + (kb * 128 - p0);
-            s_rend = __ldg(offsets + e + 1);
-        }
-    }
-    __syncthreads();
+    padded_block_rows(pad, offsets, E, kb, s_r0, s_rend);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid & 7, rg = tid >> 3;
     const int64_t r0 = s_r0 + 4 * rg, rend = s_rend;
@@ -845,7 +891,7 @@ MOE_API moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gat
     // one CTA per (64 channels, 128-row block) of the largest possible padded
     // extent (the bf16 operands: per (Q1_TPC 64-channel tiles, 128-row
     // block)); blocks past pad[E] (known on the device only) return at once
-    const dim3 grid((unsigned)((C + 63) / 64), (unsigned)(max_pad / 128));
+    const dim3 grid((unsigned)(src == SRC_DH ? F / 32 : (C + 63) / 64), (unsigned)(max_pad / 128));
     const dim3 grid_bf16((unsigned)((C / 64 + Q1_TPC - 1) / Q1_TPC), (unsigned)(max_pad / 128));
     cudaStream_t st = as_stream(stream);
     const bool kbm = scales_kb_major != 0;
@@ -858,10 +904,10 @@ MOE_API moe_status moe_wgrad_quant(int src, const uint16_t *dy, const float *gat
                                                                          q, scales);
         break;
     case SRC_ACT:
-        quant_128x1_kernel<SRC_ACT><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm, q, scales);
+        quant_128x1_act_kernel<<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm, q, scales);
         break;
     case SRC_DH:
-        quant_128x1_kernel<SRC_DH><<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm, q, scales);
+        quant_128x1_dh_kernel<<<grid, 256, 0, st>>>(w, expert_offsets, pad, E, C, max_pad, kbm, q, scales);
         break;
     case SRC_X:
         if (cudaFuncSetAttribute(quant_128x1_bf16_kernel<SRC_X>, cudaFuncAttributeMaxDynamicSharedMemorySize,

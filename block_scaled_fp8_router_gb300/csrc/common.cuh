@@ -150,6 +150,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ---- cp.async (16 bytes, global -> shared; zero fill when !valid) ----
+__device__ __forceinline__ uint32_t smem_u32(const void *p);
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---- mbarrier helpers (shared::cta) ----
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

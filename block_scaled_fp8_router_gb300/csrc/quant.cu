@@ -56,59 +56,63 @@ __device__ __forceinline__ void store_scale(void *scales, int64_t i, float s, ui
     else reinterpret_cast<float *>(scales)[i] = s;
 }
 
-// One half-warp per 1x128 block, QB blocks per pass with all their loads
-// issued before the first is encoded (QB x 16 bytes in flight per lane).
-// A half-warp's blocks are hw, hw + nhw, ...; their (row, column block)
-// advance by the fixed quotient and remainder of nhw / nbc.
-constexpr int QB = 4;
+// One half-warp per 1x128 block, each lane's 16 bytes of the next QD - 1
+// blocks in flight: every lane copies its piece of a block into its own
+// slot of a QD-deep shared-memory ring with cp.async (no registers held,
+// and no barrier: a lane reads back only its own slots).  A half-warp's
+// blocks are hw, hw + nhw, ...; their (row, column block) advance by the
+// fixed quotient and remainder of nhw / nbc.
+constexpr int QD = 8;
 
 template <bool MX>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t *__restrict__ src, int64_t rows,
                                                           int64_t cols, int64_t ld, uint8_t *__restrict__ q,
                                                           void *__restrict__ scales)
 {
+    __shared__ __align__(16) uint4 ring[QD][256];
     const int nbc = (int)(cols >> 7);
-    const int lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int sub = lane & 15;
     const unsigned half_mask = 0xFFFFu << (lane & 16);
-    const int64_t hw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 4;
+    const int64_t hw = (blockIdx.x * (int64_t)blockDim.x + tid) >> 4;
     const int64_t nhw = ((int64_t)gridDim.x * blockDim.x) >> 4;
     const int64_t dr = nhw / nbc;
     const int dc = (int)(nhw - dr * nbc);
-    int64_t r = hw / nbc;
-    int cb = (int)(hw - r * nbc);
-    while (r < rows) {
-        int64_t rr[QB];
-        int cc[QB];
-        uint4 raw[QB];
-#pragma unroll
-        for (int u = 0; u < QB; u++) {
-            rr[u] = r;
-            cc[u] = cb;
-            raw[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (r < rows) raw[u] = __ldcs(reinterpret_cast<const uint4 *>(src + r * ld + cb * 128 + sub * 8));
-            cb += dc;
-            r += dr;
-            if (cb >= nbc) {
-                cb -= nbc;
-                r++;
-            }
+    auto advance = [&](int64_t &r, int &cb) {
+        cb += dc;
+        r += dr;
+        if (cb >= nbc) {
+            cb -= nbc;
+            r++;
         }
+    };
+    int64_t ir = hw / nbc;                       // the next block to copy
+    int icb = (int)(hw - ir * nbc);
+    int64_t pr = ir;                             // the next block to encode
+    int pcb = icb;
+    auto issue = [&](int slot) {
+        if (ir < rows) cp_async16_zfill(&ring[slot][tid], src + ir * ld + icb * 128 + sub * 8, true);
+        cp_async_commit();
+        advance(ir, icb);
+    };
 #pragma unroll
-        for (int u = 0; u < QB; u++) {
-            if (rr[u] >= rows) break;      // uniform over the half-warp
-            float v[8];
-            unpack_bf16x8(raw[u], v);
-            float amax = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
-                               fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+    for (int i = 0; i < QD - 1; i++) issue(i);
+    for (int i = 0; pr < rows; i++) {
+        issue((i + QD - 1) % QD);
+        cp_async_wait<QD - 1>();                 // this lane's piece of block i
+        float v[8];
+        unpack_bf16x8(ring[i % QD][tid], v);
+        float amax = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                           fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o, 16));
-            uint32_t e8;
-            const float s = rule_scale<MX>(amax, e8);
-            *reinterpret_cast<uint2 *>(q + rr[u] * cols + cc[u] * 128 + sub * 8) = e4m3x8_scaled<1>(v, s);
-            if (sub == 0) store_scale<MX>(scales, rr[u] * nbc + cc[u], s, e8);
-        }
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o, 16));
+        uint32_t e8;
+        const float s = rule_scale<MX>(amax, e8);
+        *reinterpret_cast<uint2 *>(q + pr * cols + pcb * 128 + sub * 8) = e4m3x8_scaled<1>(v, s);
+        if (sub == 0) store_scale<MX>(scales, pr * nbc + pcb, s, e8);
+        advance(pr, pcb);
     }
+    cp_async_wait<0>();
 }
 
 template <bool MX>
@@ -174,8 +178,10 @@ static moe_status quant_launch(const uint16_t *src, int64_t rows, int64_t cols, 
     cudaStream_t st = as_stream(stream);
     if (block_rows == 1) {
         const int64_t nblocks = rows * (cols / 128);
+        // one resident wave (six CTAs per SM: 6 x 32 KB of rings, 40
+        // registers), each half-warp streaming many blocks through its ring
         int64_t grid = (nblocks + 15) / 16;
-        const int64_t cap = (int64_t)sm_count() * 16;
+        const int64_t cap = (int64_t)sm_count() * 6;
         if (grid > cap) grid = cap;
         quant_1x128_kernel<MX><<<(unsigned)grid, 256, 0, st>>>(src, rows, cols, ld_src, q, scales);
     } else {
