@@ -880,9 +880,60 @@ def run_hbm_kernels(dev, seed, steps, warmup, peaks):
     res["payload_pack_u8"] = {"ms": t, "bytes": 5 * n, "GB/s": gbs(5 * n, t)}
     t = timed(lambda: Lb.moe_payload_unpack_u8(packed, out=back))
     res["payload_unpack_u8"] = {"ms": t, "bytes": 5 * n, "GB/s": gbs(5 * n, t)}
+    del x, q, sc, rows, rsc, out, y, pl, packed, back, ws
+    torch.cuda.empty_cache()
+    # the backward's HBM-bound steps on the large layer's shape (T=8192,
+    # 256 rows per expert, so the 128 x 1 legs have no padding): combine
+    # backward, SwiGLU backward and the four 128 x 1 operand quantisations
+    Tb, F = 8192, 2048
+    Ab = Tb * k
+    g = torch.Generator(device=dev).manual_seed(seed + 7)
+    dy = torch.randn((Tb, d), generator=g, device=dev).to(torch.bfloat16)
+    outb = torch.randn((Ab, d), generator=g, device=dev).to(torch.bfloat16)
+    gb = torch.rand((Tb, k), generator=g, device=dev)
+    slb = torch.randperm(Ab, generator=g, device=dev).to(torch.int32)             # slot -> sorted row
+    s2b = torch.empty_like(slb)
+    s2b[slb.long()] = torch.arange(Ab, device=dev, dtype=torch.int32)
+    offb = torch.arange(E + 1, device=dev, dtype=torch.int32) * (Ab // E)
+    padb = Lb.moe_wgrad_pad_offsets(offb)
+    ld = (Ab // 128 + E) * 128
+    h = torch.randn((Ab, 2 * F), generator=g, device=dev)
+    d_act = torch.randn((Ab, F), generator=g, device=dev).to(torch.bfloat16)
+    qb = torch.empty((max(d, 2 * F), ld), dtype=torch.uint8, device=dev)
+    sbf = torch.empty((ld // 128) * max(d, 2 * F), dtype=torch.float32, device=dev)
+    sb = lambda C: sbf[:(ld // 128) * C].view(ld // 128, C)
+    dq = torch.empty((Ab, d), dtype=torch.uint8, device=dev)
+    ds = torch.empty((Ab, d // 128), dtype=torch.float32, device=dev)
+    dg = torch.empty((Tb, k), dtype=torch.float32, device=dev)
+    hq = torch.empty((Ab, 2 * F), dtype=torch.uint8, device=dev)
+    hs = torch.empty((Ab, 2 * F // 128), dtype=torch.float32, device=dev)
+    codes = lambda C: C * Ab * (1 + 4 / 128)
+    bw = {
+        "combine_backward": (lambda: Lb.moe_combine_backward(dy, gb, outb, slb, d_out_q=dq, d_out_s=ds, d_gates=dg,
+                                                             dev_status=st),
+                             Tb * d * 2 + Ab * d * 2 + Ab * row + Ab * 8),
+        "swiglu_backward": (lambda: Lb.moe_swiglu_backward(d_act, h, dh_q=hq, dh_s=hs),
+                            Ab * F * 2 + Ab * 2 * F * 4 + codes(2 * F)),
+        "wgrad_quant_d_out": (lambda: Lb.moe_wgrad_quant(0, offb, padb, d, ld, True, dy=dy, gates=gb.view(-1),
+                                                         sorted_to_slot=s2b, k=k, q=qb[:d], scales=sb(d)),
+                              Ab * d * 2 + Ab * 8 + codes(d)),
+        "wgrad_quant_act": (lambda: Lb.moe_wgrad_quant(1, offb, padb, F, ld, True, h=h, F=F, q=qb[:F],
+                                                       scales=sb(F)),
+                            Ab * 2 * F * 4 + codes(F)),
+        "wgrad_quant_dh": (lambda: Lb.moe_wgrad_quant(2, offb, padb, 2 * F, ld, True, h=h, d_act=d_act, F=F,
+                                                      q=qb[:2 * F], scales=sb(2 * F)),
+                           Ab * F * 2 + Ab * 2 * F * 4 + codes(2 * F)),
+        "wgrad_quant_x": (lambda: Lb.moe_wgrad_quant(3, offb, padb, d, ld, True, x=dy, sorted_to_slot=s2b, k=k,
+                                                     q=qb[:d], scales=sb(d)),
+                          Ab * d * 2 + Ab * 4 + codes(d)),
+    }
+    for name, (fn, nb) in bw.items():
+        t = timed(fn)
+        res[name] = {"ms": t, "bytes": nb, "GB/s": gbs(nb, t)}
     for v in res.values():
         v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
-    return {"workload": f"HBM kernels: T={T} d={d} E={E} top_k={k} (replayed uniform ids); payload [64, 8, 131072]",
+    return {"workload": f"HBM kernels: T={T} d={d} E={E} top_k={k} (replayed uniform ids); payload [64, 8, 131072]; "
+                        f"backward steps at T={Tb} F={F} (256 rows per expert)",
             "peak_GB/s": peaks["hbm_gbs"], "kernels": res, "status": Lb.check_status(st)}
 
 

@@ -318,7 +318,8 @@ moe_status moe_dispatch_noalloc(const int32_t *topk_ids, int T, int k, int E, co
  *              in fp32, promoted into an fp32 accumulator block by block;
  *   act[r,c] = silu(h[r,c]) * h[r,F+c]   (c < F; w13 rows 0..F-1 gate,
  *              F..2F-1 up; silu from the fast exponential and reciprocal),
- *              requantised 1x128 along F as fp8_block_quant;
+ *              requantised 1x128 along F with fp8_block_quant's scale rule,
+ *              codes E4M3(act * RN(1/s));
  *   out_sorted[r,:] = bf16 (round to nearest even) of act_q[r,:] W2[e]^T by
  *              the same block promotion.
  * xq_sorted [max_rows, d] e4m3, xs_sorted [max_rows, d/128] fp32;
