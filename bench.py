@@ -1086,7 +1086,40 @@ def cpu_baseline(cfg, seed, n_tokens, gen_dev, y_gpu_bits=None):
                             "sample": f"the first {n1} tokens of the same sample, one thread; {s1:.2f} s"}
     if y_gpu_bits is not None:
         out["gpu_vs_oracle"] = error_report(y_gpu_bits[:n_tokens], y)
+    out["configs"] = cpu_config_legs(seed, gen_dev)
     return out
+
+
+def cpu_config_legs(seed, gen_dev):
+    """The oracle on the other workloads (all host cores, bounded samples):
+    the tiny and replay layers through the whole layer, and the long-context
+    dispatch + combine of bf16 rows with identity experts."""
+    import numpy as np
+    import torch
+    from block_scaled_fp8_router_gb300 import synthetic as S
+    from oracle import oracle as O
+    legs = {}
+    for name, n in (("tiny", 256), ("replay", 512)):
+        c = S.CONFIGS[name]
+        secs = OracleSample(c, n, seed, gen_dev).run()
+        legs[name] = {"value": n / secs, "unit": "tokens/s", "sample": f"{n} of {c.T} tokens, whole layer, "
+                                                                       f"{secs:.2f} s"}
+    c = S.CONFIGS["long_dispatch"]
+    n = 8192
+    bits = lambda t: t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    xb = bits(S.make_x(c, gen_dev, seed, T=n))
+    ids = np.ascontiguousarray(S.make_replay_payload(c.with_(layers=1), gen_dev, seed)[0][:, :n].t().cpu().numpy())
+    g = np.ascontiguousarray(S.make_dirichlet_gates(c, gen_dev, seed)[:n].cpu().numpy())
+    t0 = time.perf_counter()
+    _, _, s2s, sl2, _ = O.dispatch(ids, c.E)
+    rows = O.gather_rows(xb, s2s, n * c.k, c.k)
+    O.combine(rows, sl2, g)
+    secs = time.perf_counter() - t0
+    nbytes = 2 * n * c.d * (2 + 2 * c.k)
+    legs["long_dispatch"] = {"value": n / secs, "unit": "tokens/s", "GB/s": nbytes / secs / 1e9,
+                             "sample": f"{n} of {c.T} tokens, dispatch + row gather + combine of bf16 rows "
+                                       f"(identity experts), {secs:.2f} s"}
+    return legs
 
 
 # ------------------------------------------------------------------ main
