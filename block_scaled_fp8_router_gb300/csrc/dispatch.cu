@@ -5,8 +5,9 @@
 // all-to-all, only the permutation).
 //
 // Dispatch is a stable counting sort of the slots s = t*k + j by expert:
-//   hist_kernel     one warp per run of DSP_RUN consecutive slots: per-run
-//                   expert histogram in shared memory -> ws[e][run]
+//   hist_kernel     one warp per run of consecutive slots (128, or 1024 when
+//                   the per-run counts of 128-slot runs would pass 1 MiB):
+//                   per-run expert histogram in shared memory -> ws[e][run]
 //   scan_kernel     one CTA per expert: exclusive prefix of ws[e][*] over
 //                   runs (in place) and the expert total
 //   scatter_kernel  one warp per run: exclusive scan of the totals (shared),
@@ -25,7 +26,8 @@
 
 namespace moe {
 
-constexpr int DSP_RUN = 1024;  // slots per warp run
+constexpr int DSP_RUN_SHORT = 128;    // slots per warp run: short runs spread the map
+constexpr int DSP_RUN_LONG = 1024;    // kernels over many warps; long runs bound ws
 constexpr int DSP_WARPS = 8;
 
 __device__ __forceinline__ unsigned lanemask_lt()
@@ -36,7 +38,7 @@ __device__ __forceinline__ unsigned lanemask_lt()
 }
 
 __global__ void __launch_bounds__(256) hist_kernel(const int32_t *__restrict__ ids, int64_t A, int E,
-                                                   int nruns, int32_t *__restrict__ ws,
+                                                   int nruns, int run_len, int32_t *__restrict__ ws,
                                                    int32_t *__restrict__ dev_status)
 {
     extern __shared__ int32_t hist[];  // [DSP_WARPS][E]
@@ -47,8 +49,8 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t *__restrict__ i
     const int run = blockIdx.x * DSP_WARPS + warp;
     bool bad = false;
     if (run < nruns) {
-        const int64_t s0 = (int64_t)run * DSP_RUN;
-        const int64_t s1 = min(s0 + DSP_RUN, A);
+        const int64_t s0 = (int64_t)run * run_len;
+        const int64_t s1 = min(s0 + run_len, A);
         for (int64_t s = s0 + lane; s < s1; s += 32) {
             const int32_t e = __ldg(ids + s);
             if (e >= 0 && e < E)
@@ -125,7 +127,7 @@ __device__ void block_offsets(const int32_t *__restrict__ counts, int E, int32_t
 }
 
 __global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict__ ids, int64_t A, int E,
-                                                      int nruns, const int32_t *__restrict__ ws,
+                                                      int nruns, int run_len, const int32_t *__restrict__ ws,
                                                       const int32_t *__restrict__ counts,
                                                       int32_t *__restrict__ expert_counts,
                                                       int32_t *__restrict__ expert_offsets,
@@ -149,8 +151,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t *__restrict_
     int32_t *p = pos + warp * E;
     for (int e = lane; e < E; e += 32) p[e] = off[e] + ws[(int64_t)e * nruns + run];
     __syncwarp();
-    const int64_t s0 = (int64_t)run * DSP_RUN;
-    const int64_t s1 = min(s0 + DSP_RUN, A);
+    const int64_t s0 = (int64_t)run * run_len;
+    const int64_t s1 = min(s0 + run_len, A);
     const unsigned lt = lanemask_lt();
     for (int64_t sb = s0; sb < s1; sb += 32) {
         const int64_t s = sb + lane;
@@ -290,7 +292,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     }
 }
 
-static inline int dsp_nruns(int64_t A) { return (int)((A + DSP_RUN - 1) / DSP_RUN); }
+static inline int dsp_run_len(int64_t A, int E)
+{
+    const int64_t short_runs = (A + DSP_RUN_SHORT - 1) / DSP_RUN_SHORT;
+    return (int64_t)E * short_runs * 4 <= (1 << 20) ? DSP_RUN_SHORT : DSP_RUN_LONG;
+}
+static inline int dsp_nruns(int64_t A, int E)
+{
+    const int rl = dsp_run_len(A, E);
+    return (int)((A + rl - 1) / rl);
+}
 
 } // namespace moe
 
@@ -300,7 +311,7 @@ MOE_API size_t moe_dispatch_workspace_size(int T, int k, int E)
 {
     if (T < 0 || k < 1 || E < 1) return 0;
     const int64_t A = (int64_t)T * k;
-    const size_t runs = (size_t)dsp_nruns(A);
+    const size_t runs = (size_t)dsp_nruns(A, E);
     const size_t a = sizeof(int32_t) * (size_t)E * (runs > 0 ? runs : 1);  // ws[E][runs]
     const size_t b = sizeof(int32_t) * (size_t)E;                         // totals
     return ((a + 255) & ~(size_t)255) + ((b + 255) & ~(size_t)255);
@@ -329,7 +340,8 @@ MOE_API moe_status moe_dispatch(const int32_t *topk_ids, int T, int k, int E, co
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MOE_ERR_ALIGN;
     cudaStream_t st = as_stream(stream);
-    const int nruns = dsp_nruns(A);
+    const int nruns = dsp_nruns(A, E);
+    const int run_len = dsp_run_len(A, E);
     int32_t *ws = reinterpret_cast<int32_t *>(workspace);
     int32_t *totals =
         reinterpret_cast<int32_t *>(reinterpret_cast<char *>(workspace) +
@@ -338,13 +350,14 @@ MOE_API moe_status moe_dispatch(const int32_t *topk_ids, int T, int k, int E, co
         if (cudaMemsetAsync(totals, 0, sizeof(int32_t) * E, st) != cudaSuccess) return MOE_ERR_CUDA;
     } else {
         const int grid = (nruns + DSP_WARPS - 1) / DSP_WARPS;
-        hist_kernel<<<grid, 256, sizeof(int32_t) * DSP_WARPS * E, st>>>(topk_ids, A, E, nruns, ws, dev_status);
+        hist_kernel<<<grid, 256, sizeof(int32_t) * DSP_WARPS * E, st>>>(topk_ids, A, E, nruns, run_len, ws,
+                                                                        dev_status);
         scan_kernel<<<E, 256, 0, st>>>(ws, nruns, totals);
     }
     const size_t ssm = sizeof(int32_t) * ((size_t)E + 1 + 8 + (size_t)DSP_WARPS * E);
     const int sgrid = A == 0 ? 1 : (nruns + DSP_WARPS - 1) / DSP_WARPS;
-    scatter_kernel<<<sgrid, 256, ssm, st>>>(topk_ids, A, E, nruns, ws, totals, expert_counts, expert_offsets,
-                                            sorted_to_slot, slot_to_sorted);
+    scatter_kernel<<<sgrid, 256, ssm, st>>>(topk_ids, A, E, nruns, run_len, ws, totals, expert_counts,
+                                            expert_offsets, sorted_to_slot, slot_to_sorted);
     if (with_rows && T > 0) {
         int64_t grid = ((int64_t)T + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 8;
