@@ -263,6 +263,18 @@ def test_dispatch_bf16_rows_skewed_with_empty_experts(L, oracle):
     assert st == 0
 
 
+@pytest.mark.parametrize("T", [16384, 16385])
+def test_dispatch_run_length_boundary(L, oracle, T):
+    """E = 256, top-8: 131072 slots are the most the 128-slot warp runs take
+    (their per-run counts fill 1 MiB); one more token switches to 1024-slot
+    runs.  Maps and rows bit-exact on both sides."""
+    cfg = S.CONFIGS["long_dispatch"].with_(T=T, d=128, layers=1)
+    ids = S.make_replay_payload(cfg, DEV)[0].t().contiguous()
+    x = S.make_x(cfg, DEV)
+    st, dropped = _check_dispatch(L, oracle, ids, cfg.E, x, None)
+    assert st == 0 and dropped == 0
+
+
 def test_dispatch_bad_ids_dropped(L, oracle):
     ids = torch.tensor([[2, 9], [-1, 1], [0, 2], [3, 3]], dtype=torch.int32, device=DEV)
     x = torch.randn(4, 128, device=DEV).to(torch.bfloat16)
