@@ -10,12 +10,12 @@
 // cores, whose accumulation order is not specified).
 //
 // route_topk_kernel: one cluster of ceil(E/128) CTAs per 64 tokens; each
-// 256-thread CTA computes 64 tokens x 128 experts with 8 x 4 fp32
-// accumulators per thread (three 16-byte shared loads per 32 FMAs, the next
-// hidden index's operands loaded while the current FMAs run), bf16 tiles of
-// x and W_r (32 deep) widened to fp32 in double-buffered shared memory with
-// conflict-free stores while the next tile loads into registers (one
-// barrier per tile).  Logits stay on chip: each CTA selects its own top-k,
+// 256-thread CTA computes 64 tokens x 128 experts, one 8-token group per
+// warp, 8 x 4 fp32 accumulators per thread (three 16-byte shared loads per
+// 32 FMAs, the next hidden index's operands loaded while the current FMAs
+// run), bf16 tiles of x and W_r (32 deep) read in whole 32-byte sectors and
+// widened to fp32 in double-buffered shared memory with conflict-free
+// stores while the next tile loads into registers (one barrier per tile).  Logits stay on chip: each CTA selects its own top-k,
 // CTA 0 merges the candidates it receives through distributed shared memory.
 #include "common.cuh"
 
@@ -154,16 +154,23 @@ constexpr int RC_BT = 64;           // tokens per cluster
 constexpr int RC_EC = 128;          // experts per CTA
 constexpr int RC_BK = 32;           // hidden indices per shared-memory tile
 constexpr int RC_LGS = RC_EC + 4;   // logits row stride (floats)
+// tile rows (one per hidden index) gain 8 floats of padding per 8 rows, so
+// that the transposing stores of a warp (8 rows x 4 eight-index parts) hit
+// 32 distinct banks
+__host__ __device__ constexpr int rc_xrow(int i) { return i * RC_BT + (i >> 3) * 8; }
+__host__ __device__ constexpr int rc_wrow(int i) { return i * RC_EC + (i >> 3) * 8; }
+constexpr int RC_XB = RC_BK * RC_BT + 32;  // floats per x tile buffer
+constexpr int RC_WB = RC_BK * RC_EC + 32;  // floats per W_r tile buffer
 // shared floats before the candidate arrays: the double-buffered tiles, or
 // the logits that replace them after the last tile, whichever is larger
-constexpr int RC_TILE_FLOATS = (2 * RC_BK * (RC_BT + RC_EC) > RC_BT * RC_LGS) ? 2 * RC_BK * (RC_BT + RC_EC)
-                                                                              : RC_BT * RC_LGS;
+constexpr int RC_TILE_FLOATS = (2 * (RC_XB + RC_WB) > RC_BT * RC_LGS) ? 2 * (RC_XB + RC_WB) : RC_BT * RC_LGS;
 
 // One cluster of ceil(E/128) CTAs per 64 tokens.  CTA r computes the logits
-// of experts 128r .. 128r+127 for the 64 tokens (256 threads, 8 tokens x 4
-// experts of fp32 fma-chain accumulators each: three 16-byte shared-memory
-// loads feed 32 fmas; eight warps per CTA so that one CTA per SM already
-// hides the shared-memory latency), keeps them in shared memory,
+// of experts 128r .. 128r+127 for the 64 tokens (256 threads; warp w owns
+// tokens 8w .. 8w+7, lane l experts 4l .. 4l+3: 8 x 4 fp32 fma-chain
+// accumulators per thread, three 16-byte shared-memory loads feed 32 fmas,
+// the two x loads a broadcast; eight warps per CTA so that one CTA per SM
+// already hides the shared-memory latency), keeps them in shared memory,
 // selects its own top-k per token and sends those (value, index) candidates
 // to CTA 0 of the cluster through distributed shared memory; CTA 0 merges
 // them into the top-k over all experts (every member of the global top-k is
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
     // filled while the other is read); the logits [RC_BT][RC_LGS] reuse the
     // same space after the last tile
     float *xs2 = reinterpret_cast<float *>(smem4);
-    float *ws2 = xs2 + 2 * RC_BK * RC_BT;
+    float *ws2 = xs2 + 2 * RC_XB;
     float *lg = xs2;
     float2 *cand = reinterpret_cast<float2 *>(xs2 + RC_TILE_FLOATS);  // CTA 0: [RC_BT][ncta*k]
     float2 *msum = cand + RC_BT * ncta * k;                           // CTA 0: [RC_BT][ncta]
@@ -191,15 +198,15 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = (int)cl_id() * RC_BT;
     const int e0 = rank * RC_EC;
-    const int tt = (lane >> 2) * 8;                 // my 8 tokens in the tile
-    const int ee = warp * 16 + (lane & 3) * 4;      // my 4 experts of this CTA's 128
+    const int tt = warp * 8;                        // my 8 tokens in the tile
+    const int ee = lane * 4;                        // my 4 experts of this CTA's 128
     const int nw = blockDim.x >> 5;
 
-    // tile loaders: one x chunk (token tid & 63, 8-wide part tid >> 6) and
-    // two W_r chunks (expert tid & 127, 16-wide part tid >> 7); consecutive
-    // lanes write consecutive shared-memory words
-    const int xt = tid & 63, xp = tid >> 6;          // token, 8-wide part 0..3
-    const int we = tid & 127, wp = tid >> 7;         // expert, 16-wide part 0..1
+    // tile loaders: four lanes read a row's 64 contiguous bytes (whole
+    // sectors); one x chunk (token tid >> 2, 8-wide part tid & 3) and two W_r
+    // chunks (experts tid >> 2 and 64 + (tid >> 2), part tid & 3)
+    const int xt = tid >> 2, xp = tid & 3;
+    const int we = tid >> 2, wp = tid & 3;
     float acc[8][4];
 #pragma unroll
     for (int a = 0; a < 8; a++)
@@ -210,26 +217,28 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
         const int t = t0 + xt;
         rx[0] = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * d + k0 + xp * 8))
                       : make_uint4(0, 0, 0, 0);
-        const int e = e0 + we;
 #pragma unroll
-        for (int r = 0; r < 2; r++)
-            rw[r] = e < E ? __ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + k0 + wp * 16 + r * 8))
+        for (int r = 0; r < 2; r++) {
+            const int e = e0 + we + 64 * r;
+            rw[r] = e < E ? __ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + k0 + wp * 8))
                           : make_uint4(0, 0, 0, 0);
+        }
     };
     load_tile(0);
     for (int k0 = 0, buf = 0; k0 < d; k0 += RC_BK, buf ^= 1) {
-        float *xs = xs2 + buf * RC_BK * RC_BT;
-        float *ws = ws2 + buf * RC_BK * RC_EC;
+        float *xs = xs2 + buf * RC_XB;
+        float *ws = ws2 + buf * RC_WB;
         {
+            // rows xp*8 + j: rc_xrow(xp*8 + j) = xp*(8*RC_BT + 8) + j*RC_BT
             float f[8];
             unpack_bf16x8(rx[0], f);
 #pragma unroll
-            for (int j = 0; j < 8; j++) xs[(xp * 8 + j) * RC_BT + xt] = f[j];
+            for (int j = 0; j < 8; j++) xs[xp * (8 * RC_BT + 8) + xt + j * RC_BT] = f[j];
 #pragma unroll
             for (int r = 0; r < 2; r++) {
                 unpack_bf16x8(rw[r], f);
 #pragma unroll
-                for (int j = 0; j < 8; j++) ws[(wp * 16 + r * 8 + j) * RC_EC + we] = f[j];
+                for (int j = 0; j < 8; j++) ws[wp * (8 * RC_EC + 8) + we + 64 * r + j * RC_EC] = f[j];
             }
         }
         // one barrier per tile: it publishes this tile and, since every
@@ -244,9 +253,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
         for (int i = 0; i < RC_BK; i++) {
             const float4 x0 = nx0, x1 = nx1, w0 = nw0;
             if (i + 1 < RC_BK) {
-                nx0 = *reinterpret_cast<const float4 *>(&xs[(i + 1) * RC_BT + tt]);
-                nx1 = *reinterpret_cast<const float4 *>(&xs[(i + 1) * RC_BT + tt + 4]);
-                nw0 = *reinterpret_cast<const float4 *>(&ws[(i + 1) * RC_EC + ee]);
+                nx0 = *reinterpret_cast<const float4 *>(&xs[rc_xrow(i + 1) + tt]);
+                nx1 = *reinterpret_cast<const float4 *>(&xs[rc_xrow(i + 1) + tt + 4]);
+                nw0 = *reinterpret_cast<const float4 *>(&ws[rc_wrow(i + 1) + ee]);
             }
             const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             const float wb[4] = {w0.x, w0.y, w0.z, w0.w};

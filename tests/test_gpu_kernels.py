@@ -165,6 +165,26 @@ def test_route_topk_k_equals_E_and_k32(L, oracle):
         np.testing.assert_allclose(gates.cpu().numpy(), oracle.gates(rl, rid, 1, 1, 1.0), rtol=1e-5)
 
 
+@pytest.mark.parametrize("T,E,d", [(8192, 256, 128), (4801, 250, 128), (9728, 256, 128), (16384, 256, 128),
+                                   (3000, 512, 128), (13, 256, 256)])
+def test_route_topk_token_blocks(L, oracle, T, E, d):
+    """Token counts of one and two waves of clusters on 152 SMs (8192, 9728,
+    16384), ragged token blocks (4801, 13: warps whose 8 tokens are partly
+    or wholly past the end), four-CTA clusters (E = 512) and a ragged last
+    expert CTA (E = 250): logits, ids and capture bit-exact."""
+    cfg = S.CONFIGS["large"].with_(E=E, d=d)
+    x, wr = _route_case(cfg, T, seed=T)
+    lg = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    cap = torch.full((8, T), -7, dtype=torch.int32, device=DEV)
+    ids, gates = L.moe_route_topk(x, wr, 8, 1, 1, 2.5, capture_kT=cap, logits_out=lg)
+    rl = oracle.router_logits(bf16_bits(x), bf16_bits(wr))
+    np.testing.assert_array_equal(lg.cpu().numpy().view(np.uint32), rl.view(np.uint32))
+    rid = oracle.topk(rl, 8)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_array_equal(cap.cpu().numpy(), rid.T)
+    np.testing.assert_allclose(gates.cpu().numpy(), oracle.gates(rl, rid, 1, 1, 2.5), rtol=1e-5, atol=0)
+
+
 def test_route_empty(L):
     cfg = S.CONFIGS["tiny"]
     x = torch.empty((0, cfg.d), dtype=torch.bfloat16, device=DEV)
