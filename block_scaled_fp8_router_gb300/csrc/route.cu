@@ -346,16 +346,41 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const uint16_t *__restr
     }
 }
 
-// Replay.  CTA = 256 threads = 256/TP tokens, TP = threads per token (2, 4
-// or 8, a power of two with TP * 4 >= k).  Copies the layer slab [k, T] to
+// V hidden values of a bf16 row, V = 8 (one 16-byte load) or 16 (one
+// 32-byte load: a whole sector per lane; the address 32-byte aligned)
+template <int V>
+struct Bf16Vec {
+    uint4 v[V / 8];
+};
+template <int V>
+__device__ __forceinline__ Bf16Vec<V> ldg_bf16(const uint16_t *p)
+{
+    Bf16Vec<V> r;
+    if constexpr (V == 8) {
+        r.v[0] = __ldg(reinterpret_cast<const uint4 *>(p));
+    } else {
+        asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(r.v[0].x), "=r"(r.v[0].y), "=r"(r.v[0].z), "=r"(r.v[0].w), "=r"(r.v[1].x), "=r"(r.v[1].y),
+              "=r"(r.v[1].z), "=r"(r.v[1].w)
+            : "l"(p));
+    }
+    return r;
+}
+
+// Replay.  CTA = 256 threads for up to 256/TP tokens, TP = threads per token
+// (2, 4 or 8, a power of two with TP * 4 >= k); CTA b of the grid takes
+// tokens floor(b*T/grid) .. floor((b+1)*T/grid) - 1, the grid a whole number
+// of waves of two CTAs per SM, so every SM gets the same number of tokens.
+// Copies the layer slab [k, T] to
 // [T, k] and checks the ids; if x is given, thread (token, part q) evaluates
 // the router logits of the token's slots q*SP .. q*SP+SP-1 (SP = ceil(k/TP)
 // <= 4) -- one fma chain per slot in ascending hidden index, as in
 // route_topk_kernel -- so every x value it loads feeds SP chains.  x and the
-// replayed W_r rows are read straight from L1/L2, 8 bf16 per load, one step
-// of 8 ahead.  Gates come from warp_gate, the routing kernel's code.
+// replayed W_r rows are read straight from L1/L2, V bf16 per load (V = 16
+// when both are 32-byte aligned: every load a whole sector), one step
+// ahead.  Gates come from warp_gate, the routing kernel's code.
 // IdT is the payload's id type: int32 or one byte (the compacted payload).
-template <int TP, typename IdT>
+template <int TP, int V, typename IdT>
 __global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restrict__ replay_kT,
                                                            const uint16_t *__restrict__ x,
                                                            const uint16_t *__restrict__ wr, int T, int d, int E,
@@ -369,8 +394,8 @@ __global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restr
     __shared__ float slg[TPC * 32];
     __shared__ int sbad[TPC];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * TPC;
-    const int nt = min(TPC, T - t0);
+    const int t0 = (int)((int64_t)blockIdx.x * T / gridDim.x);
+    const int nt = (int)((int64_t)(blockIdx.x + 1) * T / gridDim.x) - t0;  // <= TPC
 
     for (int idx = tid; idx < TPC * k; idx += blockDim.x) {
         const int j = idx / TPC, tl = idx % TPC;
@@ -409,27 +434,30 @@ __global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restr
     }
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (tok_ok) {
-        uint4 cx = __ldg(reinterpret_cast<const uint4 *>(xrow)), cw[4];
+        const Bf16Vec<V> zero = {};
+        Bf16Vec<V> cx = ldg_bf16<V>(xrow), cw[4];
 #pragma unroll
-        for (int u = 0; u < 4; u++) cw[u] = on[u] ? __ldg(reinterpret_cast<const uint4 *>(wrow[u])) : make_uint4(0, 0, 0, 0);
-        for (int i = 0; i < d; i += 8) {
-            uint4 nx = make_uint4(0, 0, 0, 0), nw[4];
-            const bool more = i + 8 < d;
-            if (more) nx = __ldg(reinterpret_cast<const uint4 *>(xrow + i + 8));
+        for (int u = 0; u < 4; u++) cw[u] = on[u] ? ldg_bf16<V>(wrow[u]) : zero;
+        for (int i = 0; i < d; i += V) {
+            Bf16Vec<V> nx = zero, nw[4];
+            const bool more = i + V < d;
+            if (more) nx = ldg_bf16<V>(xrow + i + V);
 #pragma unroll
-            for (int u = 0; u < 4; u++)
-                nw[u] = (more && on[u]) ? __ldg(reinterpret_cast<const uint4 *>(wrow[u] + i + 8)) : make_uint4(0, 0, 0, 0);
-            float xf[8];
-            unpack_bf16x8(cx, xf);
+            for (int u = 0; u < 4; u++) nw[u] = (more && on[u]) ? ldg_bf16<V>(wrow[u] + i + V) : zero;
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
-                if (!on[u]) continue;
-                float wf[8];
-                unpack_bf16x8(cw[u], wf);
-                float a = acc[u];
+            for (int h = 0; h < V / 8; h++) {
+                float xf[8];
+                unpack_bf16x8(cx.v[h], xf);
 #pragma unroll
-                for (int jj = 0; jj < 8; jj++) a = fmaf(xf[jj], wf[jj], a);
-                acc[u] = a;
+                for (int u = 0; u < 4; u++) {
+                    if (!on[u]) continue;
+                    float wf[8];
+                    unpack_bf16x8(cw[u].v[h], wf);
+                    float a = acc[u];
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) a = fmaf(xf[jj], wf[jj], a);
+                    acc[u] = a;
+                }
             }
             cx = nx;
 #pragma unroll
@@ -498,6 +526,35 @@ MOE_API moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, i
 
 namespace moe {
 
+// grid of the replay kernel: ceil(T / tpc) CTAs rounded up to a whole number
+// of waves of two CTAs per SM (the kernel's launch bound), at most T
+static unsigned replay_grid(int T, int tpc)
+{
+    const int64_t need = (T + tpc - 1) / tpc, wave = 2LL * sm_count();
+    const int64_t g = (need + wave - 1) / wave * wave;
+    return (unsigned)(g < T ? g : T);
+}
+
+template <int V, typename IdT>
+static void replay_launch_tp(const IdT *replay_kT, const uint16_t *x, const uint16_t *w_router, int T, int d, int E,
+                             int k, int score_fn, int renorm, float route_scale, int32_t *topk_ids,
+                             float *topk_gates, int32_t *dev_status, cudaStream_t st)
+{
+    if (k <= 8) {
+        route_replay_kernel<2, V, IdT><<<replay_grid(T, 128), 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
+                                                                             score_fn, renorm, route_scale,
+                                                                             topk_ids, topk_gates, dev_status);
+    } else if (k <= 16) {
+        route_replay_kernel<4, V, IdT><<<replay_grid(T, 64), 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
+                                                                            score_fn, renorm, route_scale,
+                                                                            topk_ids, topk_gates, dev_status);
+    } else {
+        route_replay_kernel<8, V, IdT><<<replay_grid(T, 32), 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
+                                                                            score_fn, renorm, route_scale,
+                                                                            topk_ids, topk_gates, dev_status);
+    }
+}
+
 template <typename IdT>
 static moe_status replay_launch(const IdT *replay_kT, const uint16_t *x, const uint16_t *w_router, int T, int d,
                                 int E, int k, int score_fn, int renorm, float route_scale, int32_t *topk_ids,
@@ -511,19 +568,15 @@ static moe_status replay_launch(const IdT *replay_kT, const uint16_t *x, const u
     if (x && (!w_router || !topk_gates)) return MOE_ERR_NULL;
     if (x && (!aligned16(x) || !aligned16(w_router))) return MOE_ERR_ALIGN;
     cudaStream_t st = as_stream(stream);
-    if (k <= 8) {
-        route_replay_kernel<2, IdT><<<(T + 127) / 128, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
-                                                                      score_fn, renorm, route_scale, topk_ids,
-                                                                      topk_gates, dev_status);
-    } else if (k <= 16) {
-        route_replay_kernel<4, IdT><<<(T + 63) / 64, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
-                                                                    score_fn, renorm, route_scale, topk_ids,
-                                                                    topk_gates, dev_status);
-    } else {
-        route_replay_kernel<8, IdT><<<(T + 31) / 32, 256, 0, st>>>(replay_kT, x, w_router, T, d, E, k,
-                                                                    score_fn, renorm, route_scale, topk_ids,
-                                                                    topk_gates, dev_status);
-    }
+    // 32-byte loads when the rows allow them (d is a multiple of 128)
+    const bool wide = x && (reinterpret_cast<uintptr_t>(x) & 31u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(w_router) & 31u) == 0;
+    if (wide)
+        replay_launch_tp<16>(replay_kT, x, w_router, T, d, E, k, score_fn, renorm, route_scale, topk_ids,
+                             topk_gates, dev_status, st);
+    else
+        replay_launch_tp<8>(replay_kT, x, w_router, T, d, E, k, score_fn, renorm, route_scale, topk_ids,
+                            topk_gates, dev_status, st);
     return launch_status();
 }
 

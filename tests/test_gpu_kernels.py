@@ -194,9 +194,23 @@ def test_route_empty(L):
 
 # ------------------------------------------------------------------ replay
 
-def test_replay_copies_and_round_trips(L, oracle):
-    cfg = S.CONFIGS["large"]
+def _offset_copy(t, offset):
+    """t's values in a tensor that starts `offset` elements into its buffer."""
+    if offset == 0:
+        return t
+    buf = torch.empty(t.numel() + offset, dtype=t.dtype, device=t.device)
+    buf[offset:] = t.flatten()
+    return buf[offset:].view(t.shape)
+
+
+@pytest.mark.parametrize("k,offset", [(8, 0), (8, 8), (16, 0), (32, 8)])
+def test_replay_copies_and_round_trips(L, oracle, k, offset):
+    """Capture then replay: ids and gates bit for bit.  offset 8 puts x and
+    W_r 16 bytes past a 32-byte boundary (the replay's 16-byte load path);
+    k = 16 and 32 take four and eight threads per token."""
+    cfg = S.CONFIGS["large"].with_(k=k)
     x, wr = _route_case(cfg, 300)
+    x, wr = _offset_copy(x, offset), _offset_copy(wr, offset)
     cap = torch.empty((cfg.k, 300), dtype=torch.int32, device=DEV)
     ids, gates = L.moe_route_topk(x, wr, cfg.k, cfg.score_fn, 1, 1.0, capture_kT=cap)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
