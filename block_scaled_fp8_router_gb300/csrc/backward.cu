@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(256) quant_128x1_act_kernel(WgSrc w, const int
 {
     __shared__ __align__(16) uint32_t tq[64 * 32];
     __shared__ float red[8][64];
-    __shared__ __align__(16) float ssc[64];
+    __shared__ __align__(16) float ssc[64], ysc[64];
     __shared__ int64_t s_r0, s_rend;
     const int64_t P = __ldg(pad + E);
     const int64_t kb = blockIdx.y;
@@ -546,6 +546,7 @@ __global__ void __launch_bounds__(256) quant_128x1_act_kernel(WgSrc w, const int
         for (int i = 1; i < 8; i++) a = fmaxf(a, red[i][tid]);
         const float s = block_scale(a);
         ssc[tid] = s;
+        ysc[tid] = scale_recip(s);
         const int64_t c = cbase + tid;
         sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
     }
@@ -553,7 +554,7 @@ __global__ void __launch_bounds__(256) quant_128x1_act_kernel(WgSrc w, const int
 #pragma unroll
     for (int j = 0; j < 8; j++)
         tq[(8 * cg + j) * 32 + ((rg + 4 * cg) & 31)] =
-            e4m3x4_scaled<2>(v[0][j], v[1][j], v[2][j], v[3][j], ssc[8 * cg + j]);
+            e4m3x4_div<2>(v[0][j], v[1][j], v[2][j], v[3][j], ssc[8 * cg + j], ysc[8 * cg + j]);
     __syncthreads();
 #pragma unroll
     for (int it = 0; it < 2; it++) {
@@ -580,7 +581,7 @@ __global__ void __launch_bounds__(256) quant_128x1_dh_kernel(WgSrc w, const int3
 {
     __shared__ __align__(16) uint16_t tq[64 * 64];
     __shared__ float red[8][64];
-    __shared__ float ssc[64];
+    __shared__ float ssc[64], ysc[64];
     __shared__ int64_t s_r0, s_rend;
     const int64_t P = __ldg(pad + E);
     const int64_t kb = blockIdx.y;
@@ -652,6 +653,7 @@ __global__ void __launch_bounds__(256) quant_128x1_dh_kernel(WgSrc w, const int3
         for (int i = 1; i < 8; i++) a = fmaxf(a, red[i][tid]);
         const float s = block_scale(a);
         ssc[tid] = s;
+        ysc[tid] = scale_recip(s);
         const int64_t c = gch(tid);
         sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
     }
@@ -660,10 +662,8 @@ __global__ void __launch_bounds__(256) quant_128x1_dh_kernel(WgSrc w, const int3
 #pragma unroll
     for (int j = 0; j < 8; j++) {
         const int chg = 8 * cg + j, chu = 32 + 8 * cg + j;
-        const uint32_t cgw = e4m3x4_scaled<2>(vg[0][j], vg[1][j], 0.0f, 0.0f, ssc[chg]);
-        const uint32_t cuw = e4m3x4_scaled<2>(vu[0][j], vu[1][j], 0.0f, 0.0f, ssc[chu]);
-        tq[chg * 64 + hp] = (uint16_t)cgw;
-        tq[chu * 64 + hp] = (uint16_t)cuw;
+        tq[chg * 64 + hp] = e4m3x2_div<2>(vg[0][j], vg[1][j], ssc[chg], ysc[chg]);
+        tq[chu * 64 + hp] = e4m3x2_div<2>(vu[0][j], vu[1][j], ssc[chu], ysc[chu]);
     }
     __syncthreads();
 #pragma unroll
@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const in
     extern __shared__ __align__(128) uint8_t q1_ring[];
     __shared__ __align__(16) uint32_t tq[64 * 32];
     __shared__ float red[8][64];
-    __shared__ __align__(16) float ssc[64];
+    __shared__ __align__(16) float ssc[64], ysc[64];
     __shared__ int64_t s_r0, s_rend;
     const int64_t P = __ldg(pad + E);
     const int64_t kb = blockIdx.y;
@@ -770,18 +770,22 @@ __global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const in
             for (int i = 1; i < 8; i++) a = fmaxf(a, red[i][tid]);
             const float s = block_scale(a);
             ssc[tid] = s;
+            ysc[tid] = scale_recip(s);
             const int64_t c = cbase + tid;
             sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
         }
         __syncthreads();
         const float4 s0 = *reinterpret_cast<const float4 *>(&ssc[8 * cg]);
         const float4 s1 = *reinterpret_cast<const float4 *>(&ssc[8 * cg + 4]);
+        const float4 y0 = *reinterpret_cast<const float4 *>(&ysc[8 * cg]);
+        const float4 y1 = *reinterpret_cast<const float4 *>(&ysc[8 * cg + 4]);
         const float s8[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const float y8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             // x is bf16 (one correction step suffices); g * dy is an fp32 product
             constexpr int ST = SRC == SRC_X ? 1 : 2;
-            tq[(8 * cg + j) * 32 + ((rg + 4 * cg) & 31)] = e4m3x4_scaled<ST>(v[0][j], v[1][j], v[2][j], v[3][j], s8[j]);
+            tq[(8 * cg + j) * 32 + ((rg + 4 * cg) & 31)] = e4m3x4_div<ST>(v[0][j], v[1][j], v[2][j], v[3][j], s8[j], y8[j]);
         }
         __syncthreads();
 #pragma unroll

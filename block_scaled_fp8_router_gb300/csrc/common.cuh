@@ -122,13 +122,19 @@ __device__ __forceinline__ uint2 e4m3x8_scaled(const float (&v)[8], float s)
     return out;
 }
 
-// four values (v0..v3) -> four codes, value 0 in the low byte
+// The reciprocal a block's divisions share: RN(1/s) on the fast path, else 0
+// (a fast-path reciprocal is never 0), which sends e4m3x4_div and
+// e4m3x2_div to IEEE division.  Computed once per block scale, by the
+// thread that forms the scale, when many threads encode with it.
+__device__ __forceinline__ float scale_recip(float s) { return fast_scale(s) ? __frcp_rn(s) : 0.0f; }
+
+// four values (v0..v3) divided by one scale s -> four codes (value 0 in the
+// low byte), the scale's reciprocal y = scale_recip(s) given
 template <int STEPS>
-__device__ __forceinline__ uint32_t e4m3x4_scaled(float v0, float v1, float v2, float v3, float s)
+__device__ __forceinline__ uint32_t e4m3x4_div(float v0, float v1, float v2, float v3, float s, float y)
 {
     float q[4] = {v0, v1, v2, v3};
-    if (fast_scale(s)) {
-        const float y = __frcp_rn(s);
+    if (y != 0.0f) {
 #pragma unroll
         for (int i = 0; i < 4; i++) q[i] = div_fast<STEPS>(q[i], s, y);
     } else {
@@ -136,6 +142,14 @@ __device__ __forceinline__ uint32_t e4m3x4_scaled(float v0, float v1, float v2, 
         for (int i = 0; i < 4; i++) q[i] = __fdiv_rn(q[i], s);
     }
     return (uint32_t)pack_e4m3x2(q[0], q[1]) | ((uint32_t)pack_e4m3x2(q[2], q[3]) << 16);
+}
+
+// two values (v0 in the low byte) with the reciprocal given
+template <int STEPS>
+__device__ __forceinline__ uint16_t e4m3x2_div(float v0, float v1, float s, float y)
+{
+    if (y != 0.0f) return pack_e4m3x2(div_fast<STEPS>(v0, s, y), div_fast<STEPS>(v1, s, y));
+    return pack_e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s));
 }
 
 __device__ __forceinline__ void dev_flag(int32_t *status, int32_t bits)

@@ -341,3 +341,40 @@ def test_wgrad_gemm_rejects_offsets_past_ld(L):
     torch.cuda.synchronize()
     assert int(st.item()) & L.MOE_DEV_ROWS
     assert torch.all(out == 7.0)
+
+
+def test_wgrad_quant_scales_off_the_fast_path(L, oracle):
+    """The 128 x 1 x and g * dy legs where block scales leave the range the
+    shared reciprocal serves (s < 2^-90: IEEE division), next to zero blocks
+    (scale 1), bf16's largest values and ordinary ones, through a hand-built
+    routing of 300 tokens over 3 experts: codes and scales bit-exact against
+    the oracle."""
+    T, k, E, d = 300, 2, 3, 256
+    slots = np.arange(T * k)
+    expert = (slots // k + slots % k) % E                     # two distinct experts per token
+    s2s = np.argsort(expert, kind="stable").astype(np.int32)  # sorted row -> slot
+    offsets = np.concatenate([[0], np.cumsum(np.bincount(expert, minlength=E))]).astype(np.int32)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    xf = torch.randn((T, d), generator=g)
+    xf[:, :64] *= 1e-30                                       # tiny blocks: s < 2^-90
+    xf[:, 128:192] = 0.0                                      # zero blocks
+    xf[::7, 192:] = 3.0e38                                    # bf16's largest values
+    x = xf.to(torch.bfloat16)
+    dy = torch.randn((T, d), generator=g).to(torch.bfloat16)
+    gates = torch.rand((T, k), generator=g) + 0.1
+    gates.view(-1)[torch.from_numpy(expert == 1)] = 1e-35     # expert 1's g * dy blocks tiny
+    dev_offsets = torch.from_numpy(offsets).to(DEV)
+    dev_s2s = torch.from_numpy(s2s).to(DEV)
+    pad = L.moe_wgrad_pad_offsets(dev_offsets)
+    ld = L.wgrad_ld(T * k, E)
+    x_rows = bf16_to_f64(bf16_bits(x)).astype(np.float32)[s2s // k]
+    dy_rows = bf16_to_f64(bf16_bits(dy)).astype(np.float32)[s2s // k]
+    gdy_rows = gates.numpy().reshape(-1)[s2s][:, None].astype(np.float32) * dy_rows   # RN(g * dy)
+    for src, kw, rows in ((L.WGRAD_SRC_X, dict(x=x.to(DEV)), x_rows),
+                          (L.WGRAD_SRC_GDY, dict(dy=dy.to(DEV), gates=gates.to(DEV)), gdy_rows)):
+        q, s = L.moe_wgrad_quant(src, dev_offsets, pad, d, ld, True, sorted_to_slot=dev_s2s, k=k, **kw)
+        oq, os_, opad = oracle.quant_128x1(rows, offsets)
+        P = int(opad[-1])
+        assert (os_ < 2.0 ** -90).any()                       # the IEEE path is exercised
+        np.testing.assert_array_equal(q.cpu().numpy()[:, :P], oq)
+        np.testing.assert_array_equal(s.cpu().numpy()[:P // 128].T.view(np.uint32), os_.view(np.uint32))

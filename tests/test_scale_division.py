@@ -159,3 +159,34 @@ def test_emulated_fma_step_matches_exact_rationals():
         ties = [c for c, dd in zip(cand, dist) if dd == best]
         want = ties[0] if len(ties) == 1 else [c for c in ties if (c.view(np.uint32) & 1) == 0][0]
         assert got[i] == want, (i, v[i], s[i])
+
+
+def _step_negated(v, s, y, q):
+    """The scalar device form: RN32(q + (-RN32(q*s - v)) * y)."""
+    d = q.astype(np.float64) * s.astype(np.float64) - v.astype(np.float64)   # exact
+    r = d.astype(F32)
+    return _rn32_of_sum(q.astype(np.float64), (-r).astype(np.float64) * y.astype(np.float64))
+
+
+@pytest.mark.parametrize("steps", [1, 2])
+def test_negated_residual_form_equals_copysign_form(steps):
+    """The device takes the residual negated, RN(q*s - v), so that a zero
+    dividend keeps its sign; the emulation above takes RN(v - q*s) and
+    restores the sign of v at the end.  Both give the same bits for every
+    value, zeros of both signs included, so the exhaustive checks above hold
+    for the device's form."""
+    rng = np.random.default_rng(steps)
+    n = 1_000_000
+    amax = (rng.uniform(1, 2, n) * 2.0 ** rng.integers(-80, 120, n)).astype(F32)
+    v = (amax.astype(np.float64) * rng.uniform(-1, 1, n)).astype(F32)
+    v[:1000] = F32(0.0)
+    v[1000:2000] = F32(-0.0)
+    v[2000:3000] = (amax[2000:3000] * F32(2.0 ** -30)).astype(F32)     # tiny quotients
+    s = (amax / F32(448.0)).astype(F32)
+    y = (F32(1.0) / s).astype(F32)
+    qn = (v * y).astype(F32)
+    for _ in range(steps):
+        qn = _step_negated(v, s, y, qn)
+    qc, _ = reciprocal_division(v, s, steps)
+    assert np.array_equal(qn.view(np.uint32), qc.view(np.uint32))
+    assert np.all(np.signbit(qn[:2000]) == np.signbit(v[:2000]))
