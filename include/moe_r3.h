@@ -87,8 +87,9 @@ const char *moe_status_str(moe_status s);
  *   capture_kT[j*T + t] = topk_ids[t,j] (nullable): one layer's [k, T] slab
  *                 of the routed-experts payload [num_layers, top_k, seq_len];
  *   logits_out[t,e] (nullable) = logits.
- * x [T,d] bf16; w_router [E,d] bf16; topk_ids [T,k] int32; topk_gates [T,k]
- * fp32.  T may be 0 (nothing launched).  Errors: NULL, SHAPE.
+ * x [T,d] bf16; w_router [E,d] bf16, both 16-byte aligned; topk_ids [T,k]
+ * int32; topk_gates [T,k] fp32.  T may be 0 (nothing launched).
+ * Errors: NULL, SHAPE, ALIGN.
  * ---------------------------------------------------------------------- */
 moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, int T, int d, int E, int k,
                           int score_fn, int renorm, float route_scale, int32_t *topk_ids,
@@ -107,7 +108,11 @@ moe_status moe_route_topk(const uint16_t *x, const uint16_t *w_router, int T, in
  *   (same logits, score function, renormalisation and scale as
  *   moe_route_topk, so replaying a capture reproduces its gates bit for
  *   bit).  If x == NULL, topk_gates may be NULL and is not written.
- * Errors: NULL, SHAPE.
+ * x and w_router 16-byte aligned when x != NULL (with both 32-byte aligned
+ * the logits read whole 32-byte sectors per load; same results either way).
+ * The full softmax over E (score_fn SOFTMAX, renorm 0) needs every logit
+ * and is not replayed from x: UNSUPPORTED.
+ * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED.
  * ---------------------------------------------------------------------- */
 moe_status moe_route_replay(const int32_t *replay_kT, const uint16_t *x, const uint16_t *w_router,
                             int T, int d, int E, int k, int score_fn, int renorm, float route_scale,

@@ -46,6 +46,12 @@ def test_host_side_errors(lib):
     assert L.moe_route_topk(null, null, 0, 128, 8, 2, 0, 1, 1.0, null, null, null, null, null) == 0    # empty
     x = ctypes.c_void_p(0x1000)
     assert L.moe_route_replay(x, x, x, 10, 128, 8, 2, 0, 0, 1.0, x, x, null, null) == 6   # softmax w/o renorm
+    m = ctypes.c_void_p(0x1008)                                                           # 8-byte aligned only
+    assert L.moe_route_topk(m, x, 10, 128, 8, 2, 0, 1, 1.0, x, x, null, null, null) == 3
+    assert L.moe_route_topk(x, m, 10, 128, 8, 2, 0, 1, 1.0, x, x, null, null, null) == 3
+    assert L.moe_route_replay(x, m, x, 10, 128, 8, 2, 1, 1, 1.0, x, x, null, null) == 3
+    assert L.moe_route_replay(x, x, m, 10, 128, 8, 2, 1, 1, 1.0, x, x, null, null) == 3
+    assert L.moe_route_replay(x, x, null, 10, 128, 8, 2, 1, 1, 1.0, x, x, null, null) == 1  # x without W_r
     assert L.fp8_block_quant(null, 4, 100, 100, 1, null, null, null) == 2
     assert L.fp8_block_quant(null, 4, 128, 128, 128, null, null, null) == 2                 # rows % 128
     assert L.fp8_block_quant(null, 0, 128, 128, 1, null, null, null) == 0
