@@ -698,32 +698,35 @@ __global__ void __launch_bounds__(256) quant_128x1_dh_kernel(WgSrc w, const int3
 // The same quantiser for the bf16 operands (SRC_GDY: g * dy of each routed
 // row's token, SRC_X: x of that token), persistent over channel tiles so
 // that loads stay in flight across them: a CTA of 256 threads takes one
-// padded 128-row block and Q1_TPC consecutive 64-channel tiles.  Thread
-// (rg, cg) = (tid / 8, tid % 8) owns rows 4 rg .. 4 rg + 3 and, in every
-// tile, channels 8 cg .. 8 cg + 7: it looks its rows' tokens (and gates) up
-// once, then copies its four 16-byte pieces of each tile into a
-// Q1_STAGES-deep shared-memory ring with cp.async, Q1_STAGES - 1 tiles
-// ahead (each thread reads back only its own pieces, so the ring needs no
-// barrier).  Per tile: channel amax over the thread's rows, its warp (two
-// shuffles) and the eight warps (shared memory), then the four codes of a
-// channel as one word at word (rg + 4 cg) mod 32 of the channel's row of
-// the code tile (conflict-free), and each channel's 128 codes leave as
-// eight 16-byte stores.
+// padded 128-row block and Q1_TPC consecutive 64-channel tiles.
+// Loads: thread (rg, cg) = (tid / 8, tid % 8) looks the tokens of rows
+// 4 rg .. 4 rg + 3 up once and copies their 16-byte pieces cg (channels
+// 8 cg .. 8 cg + 7) of each tile into a Q1_STAGES-deep shared-memory ring
+// with cp.async (eight lanes read a row's 128 contiguous bytes); piece cg
+// of row r lands at position cg ^ ((r / 4) % 8) of the row.
+// Work: warp w owns channels 8 w .. 8 w + 7 of the tile for all 128 rows,
+// lane l rows 4 l .. 4 l + 3 (the swizzle makes the warp's reads of one
+// piece column conflict-free), so a channel's amax is a warp reduction: a
+// reduce-scatter of nine shuffles leaves channel (l / 4) % 8's amax in
+// lane l, which forms that channel's scale and reciprocal, and sixteen
+// shuffles hand all eight to the warp.  The four codes of a channel's rows
+// in lane l form one word of the warp's own 8 x 32-word code tile, and
+// each channel's 128 codes leave as eight 16-byte stores.  One CTA barrier
+// per tile publishes the stage to every warp and frees the stage that is
+// refilled next.
 constexpr int Q1_STAGES = 4;
 constexpr int Q1_TPC = 28;
 constexpr int Q1_STAGE_BYTES = 128 * 64 * 2;
 constexpr int Q1_SMEM = Q1_STAGES * Q1_STAGE_BYTES;
 
 template <int SRC>
-__global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const int32_t *__restrict__ offsets,
+__global__ void __launch_bounds__(256, 3) quant_128x1_bf16_kernel(WgSrc w, const int32_t *__restrict__ offsets,
                                                                const int32_t *__restrict__ pad, int E, int64_t C,
                                                                int64_t ld, bool kb_major, uint8_t *__restrict__ q,
                                                                float *__restrict__ sc)
 {
     extern __shared__ __align__(128) uint8_t q1_ring[];
-    __shared__ __align__(16) uint32_t tq[64 * 32];
-    __shared__ float red[8][64];
-    __shared__ __align__(16) float ssc[64], ysc[64];
+    __shared__ __align__(16) uint32_t tq[8][8 * 32];       // per warp: [channel][32 words]
     __shared__ int64_t s_r0, s_rend;
     const int64_t P = __ldg(pad + E);
     const int64_t kb = blockIdx.y;
@@ -734,19 +737,25 @@ __global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const in
     padded_block_rows(pad, offsets, E, kb, s_r0, s_rend);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid & 7, rg = tid >> 3;
-    const int64_t r0 = s_r0 + 4 * rg, rend = s_rend;
+    const int64_t rend = s_rend;
     const uint16_t *src = SRC == SRC_GDY ? w.dy : w.x;
-    int64_t off[4];            // element offset of the row's token, or -1
-    float g[4];
+    int64_t off[4];            // loader rows 4 rg + i: element offset of the token's piece, or -1
+    float g[4];                // worker rows 4 lane + i: the gate (g * dy)
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        const int32_t slot = r0 + i < rend ? __ldg(w.sorted_to_slot + r0 + i) : -1;
+        const int64_t r = s_r0 + 4 * rg + i;
+        const int32_t slot = r < rend ? __ldg(w.sorted_to_slot + r) : -1;
         off[i] = slot >= 0 ? (int64_t)(slot / w.k) * C + 8 * cg : -1;
-        g[i] = SRC == SRC_GDY && slot >= 0 ? __ldg(w.gates + slot) : 1.0f;
+        g[i] = 1.0f;
+        if (SRC == SRC_GDY) {
+            const int64_t rw = s_r0 + 4 * lane + i;
+            const int32_t sw = rw < rend ? __ldg(w.sorted_to_slot + rw) : -1;
+            if (sw >= 0) g[i] = __ldg(w.gates + sw);
+        }
     }
-    uint4 *ring = reinterpret_cast<uint4 *>(q1_ring);      // [stage][row][cg]
+    uint4 *ring = reinterpret_cast<uint4 *>(q1_ring);      // [stage][row][position]
     auto issue = [&](int t) {
-        uint4 *dst = ring + (t % Q1_STAGES) * (128 * 8) + (4 * rg) * 8 + cg;
+        uint4 *dst = ring + (t % Q1_STAGES) * (128 * 8) + (4 * rg) * 8 + (cg ^ (rg & 7));
 #pragma unroll
         for (int i = 0; i < 4; i++)
             cp_async16_zfill(dst + 8 * i, off[i] >= 0 ? src + off[i] + (int64_t)t * 64 : src, off[i] >= 0);
@@ -756,15 +765,18 @@ __global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const in
         if (t0 + u < t1) issue(t0 + u);
         cp_async_commit();
     }
+    uint32_t *tqw = tq[warp];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
     for (int t = t0; t < t1; t++) {
+        cp_async_wait<Q1_STAGES - 2>();                   // this thread's pieces of tile t
+        __syncthreads();                                  // every piece of tile t; stage t - 1 read by all
         if (t + Q1_STAGES - 1 < t1) issue(t + Q1_STAGES - 1);
         cp_async_commit();
-        cp_async_wait<Q1_STAGES - 1>();                   // this thread's pieces of tile t
+        const uint4 *stg = ring + (t % Q1_STAGES) * (128 * 8);
         float v[4][8];
-        const uint4 *mine = ring + (t % Q1_STAGES) * (128 * 8) + (4 * rg) * 8 + cg;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            unpack_bf16x8(mine[8 * i], v[i]);
+            unpack_bf16x8(stg[(4 * lane + i) * 8 + (warp ^ (lane & 7))], v[i]);
             if (SRC == SRC_GDY) {
 #pragma unroll
                 for (int j = 0; j < 8; j++) v[i][j] = g[i] * v[i][j];
@@ -774,44 +786,38 @@ __global__ void __launch_bounds__(256) quant_128x1_bf16_kernel(WgSrc w, const in
 #pragma unroll
         for (int j = 0; j < 8; j++)
             am[j] = fmaxf(fmaxf(fabsf(v[0][j]), fabsf(v[1][j])), fmaxf(fabsf(v[2][j]), fabsf(v[3][j])));
+        // reduce-scatter: the xor-16, -8 and -4 steps each keep half of the
+        // channels (lane bit 4, 3, 2 chooses which), leaving channel
+        // 4 b4 + 2 b3 + b2 = (lane / 4) % 8; xor 2 and 1 finish its max
+        float a4[4], a2[2];
 #pragma unroll
-        for (int j = 0; j < 8; j++) am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], 8));
+        for (int i = 0; i < 4; i++)
+            a4[i] = fmaxf(b4 ? am[4 + i] : am[i], __shfl_xor_sync(0xFFFFFFFFu, b4 ? am[i] : am[4 + i], 16));
 #pragma unroll
-        for (int j = 0; j < 8; j++) am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], 16));
-        if (lane < 8) {
-#pragma unroll
-            for (int j = 0; j < 8; j++) red[warp][8 * cg + j] = am[j];
-        }
-        __syncthreads();
-        const int64_t cbase = (int64_t)t * 64;
-        if (tid < 64) {
-            float a = red[0][tid];
-#pragma unroll
-            for (int i = 1; i < 8; i++) a = fmaxf(a, red[i][tid]);
-            const float s = block_scale(a);
-            ssc[tid] = s;
-            ysc[tid] = scale_recip(s);
-            const int64_t c = cbase + tid;
+        for (int i = 0; i < 2; i++)
+            a2[i] = fmaxf(b3 ? a4[2 + i] : a4[i], __shfl_xor_sync(0xFFFFFFFFu, b3 ? a4[i] : a4[2 + i], 8));
+        float a1 = fmaxf(b2 ? a2[1] : a2[0], __shfl_xor_sync(0xFFFFFFFFu, b2 ? a2[0] : a2[1], 4));
+        a1 = fmaxf(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, 2));
+        a1 = fmaxf(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, 1));
+        const float s = block_scale(a1), y = scale_recip(s);
+        const int64_t cbase = (int64_t)t * 64 + 8 * warp;
+        if ((lane & 3) == 0) {
+            const int64_t c = cbase + (lane >> 2);
             sc[kb_major ? kb * C + c : c * (ld / 128) + kb] = s;
         }
-        __syncthreads();
-        const float4 s0 = *reinterpret_cast<const float4 *>(&ssc[8 * cg]);
-        const float4 s1 = *reinterpret_cast<const float4 *>(&ssc[8 * cg + 4]);
-        const float4 y0 = *reinterpret_cast<const float4 *>(&ysc[8 * cg]);
-        const float4 y1 = *reinterpret_cast<const float4 *>(&ysc[8 * cg + 4]);
-        const float s8[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        const float y8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+        __syncwarp();                                     // the previous tile's code reads are done
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             // x is bf16 (one correction step suffices); g * dy is an fp32 product
             constexpr int ST = SRC == SRC_X ? 1 : 2;
-            tq[(8 * cg + j) * 32 + ((rg + 4 * cg) & 31)] = e4m3x4_div<ST>(v[0][j], v[1][j], v[2][j], v[3][j], s8[j], y8[j]);
+            tqw[j * 32 + lane] = e4m3x4_div<ST>(v[0][j], v[1][j], v[2][j], v[3][j], __shfl_sync(0xFFFFFFFFu, s, 4 * j),
+                                                __shfl_sync(0xFFFFFFFFu, y, 4 * j));
         }
-        __syncthreads();
+        __syncwarp();
 #pragma unroll
-        for (int it = 0; it < 2; it++) {
-            const int u = tid + 256 * it, ch = u >> 3, chunk = u & 7;
-            const uint4 val = *reinterpret_cast<const uint4 *>(&tq[ch * 32 + ((4 * chunk + 4 * (ch >> 3)) & 31)]);
+        for (int r = 0; r < 2; r++) {
+            const int p = lane + 32 * r, ch = p >> 3, chunk = p & 7;
+            const uint4 val = *reinterpret_cast<const uint4 *>(&tqw[ch * 32 + 4 * chunk]);
             *reinterpret_cast<uint4 *>(q + (cbase + ch) * ld + kb * 128 + 16 * chunk) = val;
         }
     }
