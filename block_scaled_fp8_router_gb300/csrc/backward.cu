@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(256) quant_128x1_dh_kernel(WgSrc w, const int3
 // per tile publishes the stage to every warp and frees the stage that is
 // refilled next.
 constexpr int Q1_STAGES = 4;
-constexpr int Q1_TPC = 28;
+constexpr int Q1_TPC = 28;  // 14, 56 and 112 measured slower
 constexpr int Q1_STAGE_BYTES = 128 * 64 * 2;
 constexpr int Q1_SMEM = Q1_STAGES * Q1_STAGE_BYTES;
 
