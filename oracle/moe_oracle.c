@@ -510,6 +510,106 @@ void or_gates(const float *logits, const int32_t *ids, const uint8_t *valid, int
     }
 }
 
+/* Backward of the router for a fixed choice of experts ("RL at 1T Scale",
+ * "Router replay": the trainer replays the captured ids and still trains the
+ * router through the gates it recomputes from their logits).  Given
+ * d_gates[t,j] = dL/dg[t,j]:
+ *   l_j = x[t] . Wr[ids[t,j]], the binary32 fma chain of or_router_logits;
+ *   the gate function's derivative, in double (rs = route_scale):
+ *     softmax, renorm:    p_j = exp(l_j) / sum_{i<k} exp(l_i),
+ *                         dl_m = rs * p_m * (dg_m - sum_j dg_j p_j)
+ *     sigmoid, renorm:    s_j = 1 / (1 + exp(-l_j)), S = sum_{i<k} s_i,
+ *                         dl_m = rs * s_m (1 - s_m) * (dg_m - sum_j dg_j s_j / S) / S
+ *     sigmoid, no renorm: dl_m = rs * dg_m * s_m (1 - s_m)
+ *   (softmax without renorm depends on every expert's logit: not handled),
+ *   rounded once to binary32 as d_logits[t,j]; a token with valid[t] == 0
+ *   (valid nullable) gets zeros;
+ *   dx[t, c] = sum_j d_logits[t,j] * Wr[ids[t,j], c] and
+ *   dw[e, c] = sum over the (t, j) with ids[t,j] == e of d_logits[t,j] * x[t, c],
+ *   both summed in double and rounded once to binary32 (dx, dw nullable). */
+void or_router_backward(const uint16_t *x, const uint16_t *wr, const int32_t *ids, const uint8_t *valid,
+                        const float *d_gates, int64_t T, int d, int E, int k, int score_fn, int renorm,
+                        float route_scale, float *d_logits, float *dx, float *dw)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++) {
+        const int32_t *id = ids + t * k;
+        const float *dg = d_gates + t * k;
+        if (valid && !valid[t]) {
+            for (int j = 0; j < k; j++)
+                d_logits[t * k + j] = 0.0f;
+            continue;
+        }
+        double l[64], p[64], dl[64];
+        for (int j = 0; j < k; j++) {
+            float acc = 0.0f;
+            for (int i = 0; i < d; i++)
+                acc = fmaf(or_bf16_to_f32(x[t * d + i]), or_bf16_to_f32(wr[(int64_t)id[j] * d + i]), acc);
+            l[j] = acc;
+        }
+        const double rs = route_scale;
+        if (score_fn == 0) {
+            double m = -INFINITY, den = 0.0, dot = 0.0;
+            for (int j = 0; j < k; j++)
+                if (l[j] > m)
+                    m = l[j];
+            for (int j = 0; j < k; j++) {
+                p[j] = exp(l[j] - m);
+                den += p[j];
+            }
+            for (int j = 0; j < k; j++) {
+                p[j] /= den;
+                dot += (double)dg[j] * p[j];
+            }
+            for (int j = 0; j < k; j++)
+                dl[j] = rs * p[j] * ((double)dg[j] - dot);
+        } else {
+            double S = 0.0, dot = 0.0;
+            for (int j = 0; j < k; j++) {
+                p[j] = 1.0 / (1.0 + exp(-l[j]));
+                S += p[j];
+                dot += (double)dg[j] * p[j];
+            }
+            for (int j = 0; j < k; j++) {
+                const double ds = p[j] * (1.0 - p[j]);
+                dl[j] = renorm ? rs * ds * ((double)dg[j] - dot / S) / S : rs * (double)dg[j] * ds;
+            }
+        }
+        for (int j = 0; j < k; j++)
+            d_logits[t * k + j] = (float)dl[j];
+    }
+    if (dx) {
+#pragma omp parallel for schedule(static)
+        for (int64_t t = 0; t < T; t++)
+            for (int c = 0; c < d; c++) {
+                double acc = 0.0;
+                for (int j = 0; j < k; j++)
+                    if (!valid || valid[t])
+                        acc += (double)d_logits[t * k + j] * or_bf16_to_f32(wr[(int64_t)ids[t * k + j] * d + c]);
+                dx[t * d + c] = (float)acc;
+            }
+    }
+    if (dw) {
+#pragma omp parallel for schedule(dynamic)
+        for (int e = 0; e < E; e++) {
+            double *acc = calloc((size_t)d, sizeof(double));
+            for (int64_t t = 0; t < T; t++) {
+                if (valid && !valid[t])
+                    continue;
+                for (int j = 0; j < k; j++)
+                    if (ids[t * k + j] == e) {
+                        const double g = d_logits[t * k + j];
+                        for (int c = 0; c < d; c++)
+                            acc[c] += g * or_bf16_to_f32(x[t * d + c]);
+                    }
+            }
+            for (int c = 0; c < d; c++)
+                dw[(int64_t)e * d + c] = (float)acc[c];
+            free(acc);
+        }
+    }
+}
+
 /* Replay one layer slice of the routed-experts payload: payload_kT is
  * [top_k, seq_len] row-major (the layer's slab of [num_layers, top_k,
  * seq_len]); ids[t, j] = payload_kT[j, t], an exact copy in slot order.

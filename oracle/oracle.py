@@ -65,6 +65,7 @@ def _load():
                 "or_router_logits": (None, [P, P, I64, I, I, P]),
                 "or_topk": (None, [P, I64, I, I, P]),
                 "or_gates": (None, [P, P, P, I64, I, I, I, I, F, P]),
+                "or_router_backward": (None, [P, P, P, P, P, I64, I, I, I, I, I, F, P, P, P]),
                 "or_replay": (I64, [P, I64, I, I, P, P]),
                 "or_payload_pack_u8": (I64, [P, I64, I, P]),
                 "or_combine_backward": (None, [P, P, P, P, I64, I, I, I64, P, P, P, P]),
@@ -277,6 +278,28 @@ def gates(logits: np.ndarray, ids: np.ndarray, score_fn: int, renorm: int = 1,
     g = np.empty((T, k), np.float32)
     _load().or_gates(_p(l), _p(ids), _p(v), T, E, k, score_fn, renorm, route_scale, _p(g))
     return g
+
+
+def router_backward(x_bf16: np.ndarray, wr_bf16: np.ndarray, ids: np.ndarray, d_gates: np.ndarray,
+                    score_fn: int, renorm: int = 1, route_scale: float = 1.0,
+                    valid: np.ndarray | None = None, want_dx: bool = True, want_dw: bool = True):
+    """Router backward for fixed ids -> (d_logits [T, k], dx [T, d] or None, dw [E, d] or None), fp32."""
+    x = _c(x_bf16, np.uint16)
+    wr = _c(wr_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    dg = _c(d_gates, np.float32)
+    T, d = x.shape
+    E, d2 = wr.shape
+    k = ids.shape[1]
+    assert d == d2 and dg.shape == (T, k) and k <= 64
+    assert not (score_fn == 0 and not renorm)
+    v = None if valid is None else _c(valid, np.uint8)
+    dl = np.empty((T, k), np.float32)
+    dx = np.empty((T, d), np.float32) if want_dx else None
+    dw = np.empty((E, d), np.float32) if want_dw else None
+    _load().or_router_backward(_p(x), _p(wr), _p(ids), _p(v), _p(dg), T, d, E, k, score_fn, renorm,
+                               route_scale, _p(dl), _p(dx), _p(dw))
+    return dl, dx, dw
 
 
 def replay(payload_kT: np.ndarray, E: int):
