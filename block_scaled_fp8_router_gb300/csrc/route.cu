@@ -70,6 +70,40 @@ __device__ __forceinline__ float warp_gate(int lane, int k, float my_l, int scor
     return g * route_scale;
 }
 
+// Derivative of the gates with respect to the chosen logits: lane j < k
+// holds its slot's logit my_l and upstream gradient my_dg and returns
+// dL/dl_j (rs = route_scale):
+//   softmax, renorm:    p_j = exp(l_j) / sum_i exp(l_i), dl_j = rs p_j (dg_j - sum_i dg_i p_i)
+//   sigmoid, renorm:    s_j = 1 / (1 + exp(-l_j)), S = sum_i s_i,
+//                       dl_j = rs s_j (1 - s_j) (dg_j - sum_i dg_i s_i / S) / S
+//   sigmoid, no renorm: dl_j = rs dg_j s_j (1 - s_j)
+// (the full softmax over E is not handled here).  s (1 - s) is formed as
+// e s^2 with e = exp(-l), which keeps its relative accuracy for large l.
+__device__ __forceinline__ float warp_dgate(int lane, int k, float my_l, float my_dg, int score_fn, int renorm,
+                                            float route_scale)
+{
+    const bool mine = lane < k;
+    float dl;
+    if (score_fn == MOE_SCORE_SOFTMAX) {
+        const float m = warp_max(mine ? my_l : -INFINITY);
+        const float e = mine ? expf(my_l - m) : 0.0f;
+        const float p = __fdiv_rn(e, warp_sum(e));
+        const float dot = warp_sum(mine ? my_dg * p : 0.0f);
+        dl = route_scale * p * (my_dg - dot);
+    } else {
+        const float e = mine ? expf(-my_l) : 0.0f;
+        const float sg = mine ? __fdiv_rn(1.0f, 1.0f + e) : 0.0f;
+        const float ds = e * sg * sg;
+        if (renorm) {
+            const float S = warp_sum(sg), dot = warp_sum(mine ? my_dg * sg : 0.0f);
+            dl = route_scale * ds * __fdiv_rn(my_dg - __fdiv_rn(dot, S), S);
+        } else {
+            dl = route_scale * my_dg * ds;
+        }
+    }
+    return mine ? dl : 0.0f;
+}
+
 // ---- cluster helpers (route_topk runs one cluster per 64 tokens, one CTA
 // per 128 experts) ----
 __device__ __forceinline__ uint32_t cl_rank()
@@ -380,14 +414,19 @@ __device__ __forceinline__ Bf16Vec<V> ldg_bf16(const uint16_t *p)
 // when both are 32-byte aligned: every load a whole sector), one step
 // ahead.  Gates come from warp_gate, the routing kernel's code.
 // IdT is the payload's id type: int32 or one byte (the compacted payload).
-template <int TP, int V, typename IdT>
+// BWD: the router backward's first step -- the ids come as [T, k] (replay_kT
+// points at them; nothing is copied), the same logits are formed, and the
+// kernel writes d_logits (into `gates`) from the upstream d_gates through
+// warp_dgate instead of the gates.
+template <int TP, int V, typename IdT, bool BWD = false>
 __global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restrict__ replay_kT,
                                                            const uint16_t *__restrict__ x,
                                                            const uint16_t *__restrict__ wr, int T, int d, int E,
                                                            int k, int score_fn, int renorm, float route_scale,
                                                            int32_t *__restrict__ ids,
                                                            float *__restrict__ gates,
-                                                           int32_t *__restrict__ dev_status)
+                                                           int32_t *__restrict__ dev_status,
+                                                           const float *__restrict__ d_gates = nullptr)
 {
     constexpr int TPC = 256 / TP;  // tokens per CTA
     __shared__ int32_t sid[TPC * 32];
@@ -397,12 +436,16 @@ __global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restr
     const int t0 = (int)((int64_t)blockIdx.x * T / gridDim.x);
     const int nt = (int)((int64_t)(blockIdx.x + 1) * T / gridDim.x) - t0;  // <= TPC
 
-    for (int idx = tid; idx < TPC * k; idx += blockDim.x) {
-        const int j = idx / TPC, tl = idx % TPC;
-        if (tl < nt) {
-            const int32_t v = (int32_t)replay_kT[(int64_t)j * T + t0 + tl];
-            sid[tl * k + j] = v;
-            ids[(int64_t)(t0 + tl) * k + j] = v;
+    if (BWD) {
+        for (int idx = tid; idx < nt * k; idx += blockDim.x) sid[idx] = (int32_t)replay_kT[(int64_t)t0 * k + idx];
+    } else {
+        for (int idx = tid; idx < TPC * k; idx += blockDim.x) {
+            const int j = idx / TPC, tl = idx % TPC;
+            if (tl < nt) {
+                const int32_t v = (int32_t)replay_kT[(int64_t)j * T + t0 + tl];
+                sid[tl * k + j] = v;
+                ids[(int64_t)(t0 + tl) * k + j] = v;
+            }
         }
     }
     __syncthreads();
@@ -472,10 +515,89 @@ __global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restr
     __syncthreads();
     for (int t = warp; t < nt; t += 8) {
         const float my_l = lane < k ? slg[t * k + lane] : 0.0f;
-        float g = warp_gate(lane, k, my_l, score_fn, renorm, route_scale, 0.0f, 0.0f);
+        float g;
+        if (BWD) {
+            const float my_dg = lane < k ? d_gates[(int64_t)(t0 + t) * k + lane] : 0.0f;
+            g = warp_dgate(lane, k, my_l, my_dg, score_fn, renorm, route_scale);
+        } else {
+            g = warp_gate(lane, k, my_l, score_fn, renorm, route_scale, 0.0f, 0.0f);
+        }
         if (sbad[t]) g = 0.0f;
         if (lane < k) gates[(int64_t)(t0 + t) * k + lane] = g;
     }
+}
+
+// dx[t, c] = sum_j d_logits[t, j] * W_r[ids[t, j], c], the slots in order,
+// fp32.  One warp per token; lane l takes columns 8 (l + 32 i) .. + 7, the
+// k router rows (L2-resident) read 16 bytes at a time.  A slot whose id is
+// outside [0, E) is skipped (its d_logit is 0).
+__global__ void __launch_bounds__(256) router_dx_kernel(const int32_t *__restrict__ ids,
+                                                        const float *__restrict__ d_logits,
+                                                        const uint16_t *__restrict__ wr, int T, int d, int E, int k,
+                                                        float *__restrict__ dx)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const int32_t my_id = lane < k ? ids[t * k + lane] : -1;
+    const float my_dl = lane < k ? d_logits[t * k + lane] : 0.0f;
+    for (int c = 8 * lane; c < d; c += 256) {
+        float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        for (int j = 0; j < k; j++) {
+            const int32_t e = __shfl_sync(0xFFFFFFFFu, my_id, j);
+            const float g = __shfl_sync(0xFFFFFFFFu, my_dl, j);
+            if (e < 0 || e >= E) continue;
+            float w[8];
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(wr + (int64_t)e * d + c)), w);
+#pragma unroll
+            for (int i = 0; i < 8; i++) acc[i] = fmaf(g, w[i], acc[i]);
+        }
+        float4 *o = reinterpret_cast<float4 *>(dx + t * d + c);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
+// dw[e, c] = sum over expert e's dispatched rows r (sorted order) of
+// d_logits[slot(r)] * x[slot(r) / k, c], fp32, the rows in order.  One CTA
+// of 128 threads per (expert, 1024 columns); thread i takes columns
+// 8 i .. 8 i + 7 of its chunk, four rows' loads in flight.  A slot outside
+// [0, T k) is skipped; an expert without rows gets zeros.
+constexpr int RDW_COLS = 1024;
+__global__ void __launch_bounds__(128) router_dw_kernel(const int32_t *__restrict__ sorted_to_slot,
+                                                        const int32_t *__restrict__ offsets,
+                                                        const float *__restrict__ d_logits,
+                                                        const uint16_t *__restrict__ x, int T, int d, int k,
+                                                        float *__restrict__ dw)
+{
+    const int e = blockIdx.y;
+    const int c = blockIdx.x * RDW_COLS + 8 * threadIdx.x;
+    if (c >= d) return;
+    const int64_t r0 = offsets[e], r1 = offsets[e + 1], A = (int64_t)T * k;
+    float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    for (int64_t r = r0; r < r1; r += 4) {
+        float g[4];
+        uint4 xv[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int32_t slot = r + u < r1 ? __ldg(sorted_to_slot + r + u) : -1;
+            const bool ok = slot >= 0 && slot < A;
+            g[u] = ok ? __ldg(d_logits + slot) : 0.0f;
+            xv[u] = ok ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)(slot / k) * d + c))
+                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            if (r + u >= r1) break;
+            float xf[8];
+            unpack_bf16x8(xv[u], xf);
+#pragma unroll
+            for (int i = 0; i < 8; i++) acc[i] = fmaf(g[u], xf[i], acc[i]);
+        }
+    }
+    float4 *o = reinterpret_cast<float4 *>(dw + (int64_t)e * d + c);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 static moe_status check_route_args(int T, int d, int E, int k, int score_fn)
@@ -596,4 +718,58 @@ MOE_API moe_status moe_route_replay_u8(const uint8_t *replay_kT, const uint16_t 
 {
     return replay_launch(replay_kT, x, w_router, T, d, E, k, score_fn, renorm, route_scale, topk_ids, topk_gates,
                          dev_status, stream);
+}
+
+namespace moe {
+
+template <int V>
+static void router_dlogits_launch(const int32_t *ids, const uint16_t *x, const uint16_t *w_router, int T, int d,
+                                  int E, int k, int score_fn, int renorm, float route_scale, const float *d_gates,
+                                  float *d_logits, int32_t *dev_status, cudaStream_t st)
+{
+    if (k <= 8)
+        route_replay_kernel<2, V, int32_t, true><<<replay_grid(T, 128), 256, 0, st>>>(
+            ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, nullptr, d_logits, dev_status, d_gates);
+    else if (k <= 16)
+        route_replay_kernel<4, V, int32_t, true><<<replay_grid(T, 64), 256, 0, st>>>(
+            ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, nullptr, d_logits, dev_status, d_gates);
+    else
+        route_replay_kernel<8, V, int32_t, true><<<replay_grid(T, 32), 256, 0, st>>>(
+            ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, nullptr, d_logits, dev_status, d_gates);
+}
+
+} // namespace moe
+
+MOE_API moe_status moe_router_backward(const uint16_t *x, const uint16_t *w_router, const int32_t *topk_ids,
+                                       const float *d_gates, int T, int d, int E, int k, int score_fn, int renorm,
+                                       float route_scale, float *d_logits, float *dx,
+                                       const int32_t *sorted_to_slot, const int32_t *expert_offsets,
+                                       float *dw_router, int32_t *dev_status, void *stream)
+{
+    moe_status s = check_route_args(T, d, E, k, score_fn);
+    if (s != MOE_OK) return s;
+    if (score_fn == MOE_SCORE_SOFTMAX && !renorm) return MOE_ERR_UNSUPPORTED;
+    if (!x || !w_router || !topk_ids || !d_gates || !d_logits) return MOE_ERR_NULL;
+    if (dw_router && (!sorted_to_slot || !expert_offsets)) return MOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w_router) || (dx && !aligned16(dx)) || (dw_router && !aligned16(dw_router)))
+        return MOE_ERR_ALIGN;
+    cudaStream_t st = as_stream(stream);
+    if (T == 0) {   // no tokens: dw_router is all zeros
+        if (dw_router && cudaMemsetAsync(dw_router, 0, sizeof(float) * (size_t)E * d, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    const bool wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (reinterpret_cast<uintptr_t>(w_router) & 31u) == 0;
+    if (wide)
+        router_dlogits_launch<16>(topk_ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, d_gates, d_logits,
+                                  dev_status, st);
+    else
+        router_dlogits_launch<8>(topk_ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, d_gates, d_logits,
+                                 dev_status, st);
+    if (dx) router_dx_kernel<<<(unsigned)(((int64_t)T * 32 + 255) / 256), 256, 0, st>>>(topk_ids, d_logits, w_router, T,
+                                                                                      d, E, k, dx);
+    if (dw_router)
+        router_dw_kernel<<<dim3((unsigned)((d + RDW_COLS - 1) / RDW_COLS), (unsigned)E), 128, 0, st>>>(
+            sorted_to_slot, expert_offsets, d_logits, x, T, d, k, dw_router);
+    return launch_status();
 }

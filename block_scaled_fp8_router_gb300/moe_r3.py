@@ -31,6 +31,7 @@ _SIGS = {
     "moe_route_topk": (I, [P, P, I, I, I, I, I, I, F, P, P, P, P, P]),
     "moe_route_replay": (I, [P, P, P, I, I, I, I, I, I, F, P, P, P, P]),
     "moe_route_replay_u8": (I, [P, P, P, I, I, I, I, I, I, F, P, P, P, P]),
+    "moe_router_backward": (I, [P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P, P, P]),
     "moe_payload_pack_u8": (I, [P, I64, I, P, P, P]),
     "moe_payload_unpack_u8": (I, [P, I64, P, P]),
     "fp8_block_quant": (I, [P, I64, I64, I64, I, P, P, P]),
@@ -168,6 +169,44 @@ def moe_route_replay(replay_kT, E, x=None, w_router=None, score_fn=MOE_SCORE_SOF
         _ptr(replay_kT), _ptr(x), _ptr(w_router), T, d, E, k, score_fn, renorm, route_scale, _ptr(topk_ids),
         _ptr(topk_gates), _ptr(dev_status), _stream(stream)))
     return topk_ids, topk_gates
+
+
+def moe_router_backward(x, w_router, topk_ids, d_gates, score_fn=MOE_SCORE_SIGMOID, renorm=1, route_scale=1.0,
+                        dx=True, dw_router=False, sorted_to_slot=None, expert_offsets=None, d_logits=None,
+                        dev_status=None, stream=None):
+    """Router gradients for fixed ids -> (d_logits [T,k], dx [T,d] or None,
+    dw_router [E,d] or None), fp32.  dx / dw_router: True allocates, a tensor
+    is written, False / None skips; dw_router needs the dispatch maps."""
+    T, d = x.shape
+    E = w_router.shape[0]
+    k = topk_ids.shape[1]
+    _want(x, torch.bfloat16, (T, d), "x")
+    _want(w_router, torch.bfloat16, (E, d), "w_router")
+    _want(topk_ids, torch.int32, (T, k), "topk_ids")
+    _want(d_gates, torch.float32, (T, k), "d_gates")
+    d_logits = _empty((T, k), torch.float32, x) if d_logits is None else d_logits
+    _want(d_logits, torch.float32, (T, k), "d_logits")
+    if dx is True:
+        dx = _empty((T, d), torch.float32, x)
+    if dx is not None and dx is not False:
+        _want(dx, torch.float32, (T, d), "dx")
+    else:
+        dx = None
+    if dw_router is True:
+        dw_router = _empty((E, d), torch.float32, x)
+    if dw_router is not None and dw_router is not False:
+        _want(dw_router, torch.float32, (E, d), "dw_router")
+        _want(sorted_to_slot, torch.int32, (T * k,), "sorted_to_slot")
+        _want(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    else:
+        dw_router = None
+    if dev_status is not None:
+        _want(dev_status, torch.int32, (1,), "dev_status")
+    _check("moe_router_backward", _lib.moe_router_backward(
+        _ptr(x), _ptr(w_router), _ptr(topk_ids), _ptr(d_gates), T, d, E, k, score_fn, renorm, route_scale,
+        _ptr(d_logits), _ptr(dx), _ptr(sorted_to_slot), _ptr(expert_offsets), _ptr(dw_router), _ptr(dev_status),
+        _stream(stream)))
+    return d_logits, dx, dw_router
 
 
 def moe_route_replay_u8(replay_kT, E, **kw):

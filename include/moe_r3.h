@@ -133,6 +133,43 @@ moe_status moe_route_replay_u8(const uint8_t *replay_kT, const uint16_t *x, cons
                                int32_t *topk_ids, float *topk_gates, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * moe_router_backward -- gradients of the router for fixed expert ids
+ * ("Router replay": the trainer replays the captured ids and still trains
+ * the router through the gates it recomputes from their logits).
+ *
+ *   l[t,j] = the logit of expert topk_ids[t,j], the same binary32 fma chain
+ *            as moe_route_topk / moe_route_replay;
+ *   d_logits[t,j] = dL/dl[t,j] from d_gates[t,j] = dL/dg[t,j] through the
+ *            gate function (rs = route_scale):
+ *              softmax, renorm:    p_j = exp(l_j) / sum_i exp(l_i),
+ *                                  dl_j = rs p_j (dg_j - sum_i dg_i p_i)
+ *              sigmoid, renorm:    s_j = 1 / (1 + exp(-l_j)), S = sum_i s_i,
+ *                                  dl_j = rs s_j (1 - s_j) (dg_j - sum_i dg_i s_i / S) / S
+ *              sigmoid, no renorm: dl_j = rs dg_j s_j (1 - s_j)
+ *            in fp32; a token whose ids are not all in [0,E) and distinct
+ *            gets zeros and sets MOE_DEV_BAD_IDS;
+ *   dx[t,c] = sum_j d_logits[t,j] * w_router[topk_ids[t,j], c] (nullable;
+ *            fp32, the slots in order) -- the router's part of dL/dx;
+ *   dw_router[e,c] = sum over expert e's rows of the dispatch that produced
+ *            sorted_to_slot / expert_offsets for these ids, in that sorted
+ *            order, of d_logits[slot] * x[slot / k, c] (nullable; fp32; an
+ *            expert without rows gets zeros).
+ * x [T,d] bf16, w_router [E,d] bf16 (16-byte aligned; 32-byte alignment of
+ * both lets the logits read whole sectors), topk_ids [T,k] int32, d_gates,
+ * d_logits [T,k] fp32, dx [T,d] fp32, dw_router [E,d] fp32 (16-byte
+ * aligned); sorted_to_slot [T*k] and expert_offsets [E+1] are moe_dispatch's
+ * maps, needed only with dw_router.  T may be 0 (dw_router, if given, is
+ * zeroed).  The full softmax over E (score_fn SOFTMAX, renorm 0) depends on
+ * every expert's logit: UNSUPPORTED.
+ * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+moe_status moe_router_backward(const uint16_t *x, const uint16_t *w_router, const int32_t *topk_ids,
+                               const float *d_gates, int T, int d, int E, int k, int score_fn, int renorm,
+                               float route_scale, float *d_logits, float *dx, const int32_t *sorted_to_slot,
+                               const int32_t *expert_offsets, float *dw_router, int32_t *dev_status,
+                               void *stream);
+
+/* ------------------------------------------------------------------------
  * moe_payload_pack_u8 / moe_payload_unpack_u8 -- the routed-experts payload
  * at one byte per id ("Router replay": the [num_layers, top_k, seq_len]
  * payload is large enough to strain its transport; with E <= 256 every id

@@ -52,6 +52,13 @@ def test_host_side_errors(lib):
     assert L.moe_route_replay(x, m, x, 10, 128, 8, 2, 1, 1, 1.0, x, x, null, null) == 3
     assert L.moe_route_replay(x, x, m, 10, 128, 8, 2, 1, 1, 1.0, x, x, null, null) == 3
     assert L.moe_route_replay(x, x, null, 10, 128, 8, 2, 1, 1, 1.0, x, x, null, null) == 1  # x without W_r
+    # router backward: full softmax unsupported, nulls, dW_r without the maps, alignment, T = 0
+    assert L.moe_router_backward(x, x, x, x, 10, 128, 8, 2, 0, 0, 1.0, x, x, null, null, null, null, null) == 6
+    assert L.moe_router_backward(x, x, x, null, 10, 128, 8, 2, 1, 1, 1.0, x, x, null, null, null, null, null) == 1
+    assert L.moe_router_backward(x, x, x, x, 10, 128, 8, 2, 1, 1, 1.0, x, null, null, x, x, null, null) == 1
+    assert L.moe_router_backward(x, x, x, x, 10, 128, 8, 2, 1, 1, 1.0, x, m, null, null, null, null, null) == 3
+    assert L.moe_router_backward(x, x, x, x, 10, 100, 8, 2, 1, 1, 1.0, x, x, null, null, null, null, null) == 2
+    assert L.moe_router_backward(x, x, x, x, 0, 128, 8, 2, 1, 1, 1.0, x, x, null, null, null, null, null) == 0
     assert L.fp8_block_quant(null, 4, 100, 100, 1, null, null, null) == 2
     assert L.fp8_block_quant(null, 4, 128, 128, 128, null, null, null) == 2                 # rows % 128
     assert L.fp8_block_quant(null, 0, 128, 128, 1, null, null, null) == 0

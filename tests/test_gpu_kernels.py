@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from block_scaled_fp8_router_gb300 import synthetic as S
-from tests.helpers import bf16_bits
+from tests.helpers import bf16_bits, bf16_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -363,3 +363,78 @@ def test_host_errors_raise(L):
     x = torch.zeros((4, 100), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(L.MoEError):
         L.fp8_block_quant(x, 1)
+
+
+# ------------------------------------------------------------------ router backward
+
+def _dispatch_maps(L, ids, E):
+    T, k = ids.shape
+    s2s = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    L.moe_dispatch(ids, E, expert_offsets=offs, sorted_to_slot=s2s)
+    return s2s, offs
+
+
+@pytest.mark.parametrize("name,T,score_fn,renorm,rs", [("tiny", None, 0, 1, 1.0), ("replay", 1000, 0, 1, 2.0),
+                                                       ("large", 300, 1, 1, 1.0), ("large", 257, 1, 0, 2.5)])
+def test_router_backward_against_oracle(L, oracle, name, T, score_fn, renorm, rs):
+    """d_logits against the oracle (the logits are the same fp32 chain; the
+    gate derivative differs by fp32 vs double rounding); dx and dW_r against
+    a float64 sum of the kernel's own d_logits within the fp32 summation
+    bound n 2^-24 sum|terms|, and against the oracle's within 1e-4."""
+    cfg = S.CONFIGS[name]
+    x, wr = _route_case(cfg, T, seed=3)
+    T, E, k, d = x.shape[0], cfg.E, cfg.k, cfg.d
+    ids, _ = L.moe_route_topk(x, wr, k, score_fn, renorm, rs)
+    g = torch.Generator(device=DEV).manual_seed(T)
+    dg = torch.randn((T, k), generator=g, device=DEV)
+    s2s, offs = _dispatch_maps(L, ids, E)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dl, dx, dw = L.moe_router_backward(x, wr, ids, dg, score_fn, renorm, rs, dx=True, dw_router=True,
+                                       sorted_to_slot=s2s, expert_offsets=offs, dev_status=st)
+    assert L.check_status(st) == 0
+    rdl, rdx, rdw = oracle.router_backward(bf16_bits(x), bf16_bits(wr), ids.cpu().numpy(), dg.cpu().numpy(),
+                                           score_fn, renorm, rs)
+    dl_h = dl.cpu().numpy()
+    assert np.abs(dl_h - rdl).max() <= 1e-5 * np.abs(rdl).max()
+    xf = bf16_to_f64(bf16_bits(x))
+    wf = bf16_to_f64(bf16_bits(wr))
+    idn = ids.cpu().numpy()
+    # dx: k terms per element
+    terms = dl_h.astype(np.float64)[:, :, None] * wf[idn]                 # [T, k, d]
+    ex, ab = terms.sum(1), np.abs(terms).sum(1)
+    assert np.all(np.abs(dx.cpu().numpy() - ex) <= k * 2.0 ** -24 * ab + 1e-30)
+    # dW_r: the rows of each expert
+    onehot = np.zeros((E, T), np.float64)
+    np.add.at(onehot, (idn.reshape(-1), np.repeat(np.arange(T), k)), dl_h.reshape(-1).astype(np.float64))
+    absoh = np.zeros((E, T), np.float64)
+    np.add.at(absoh, (idn.reshape(-1), np.repeat(np.arange(T), k)), np.abs(dl_h.reshape(-1)).astype(np.float64))
+    ew, aw = onehot @ xf, absoh @ np.abs(xf)
+    n_e = np.bincount(idn.reshape(-1), minlength=E)[:, None]
+    assert np.all(np.abs(dw.cpu().numpy() - ew) <= n_e * 2.0 ** -24 * aw + 1e-30)
+    for got, ref in ((dx, rdx), (dw, rdw)):
+        assert np.abs(got.cpu().numpy() - ref).max() <= 1e-4 * np.abs(ref).max()
+
+
+def test_router_backward_bad_ids_and_unchosen_experts(L, oracle):
+    """A token with a repeated or out-of-range id gets zero d_logits (and
+    sets the flag); experts nobody chose get zero dW_r rows."""
+    cfg = S.CONFIGS["replay"].with_(E=70, d=256)
+    x, wr = _route_case(cfg, 200, seed=8)
+    T, k, E = 200, cfg.k, 70
+    ids = torch.stack([torch.randperm(60)[:k] for _ in range(T)]).to(torch.int32).to(DEV)   # 60..69 unused
+    ids[5, 1] = ids[5, 0]
+    dg = torch.randn((T, k), device=DEV)
+    s2s, offs = _dispatch_maps(L, ids, E)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dl, dx, dw = L.moe_router_backward(x, wr, ids, dg, 0, 1, 1.0, dw_router=True, sorted_to_slot=s2s,
+                                       expert_offsets=offs, dev_status=st)
+    assert L.check_status(st) & L.MOE_DEV_BAD_IDS
+    assert torch.all(dl[5] == 0) and torch.all(dx[5] == 0)
+    assert torch.all(dw[60:] == 0)
+    valid = np.ones(T, np.uint8)
+    valid[5] = 0
+    rdl, _, rdw = oracle.router_backward(bf16_bits(x), bf16_bits(wr), ids.cpu().numpy(), dg.cpu().numpy(), 0, 1, 1.0,
+                                         valid=valid)
+    assert np.abs(dl.cpu().numpy() - rdl).max() <= 1e-5 * np.abs(rdl).max()
+    assert np.abs(dw.cpu().numpy() - rdw).max() <= 1e-4 * np.abs(rdw).max()
