@@ -621,6 +621,31 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
         layer._weight_grads(dy, T, events=e)
     torch.cuda.synchronize()
     wg_split = {n: sum(e[i].elapsed_time(e[i + 1]) for e in wevs) / steps for i, n in enumerate(wg_names)}
+    # the router's backward (ids fixed): d_logits alone, + dx, + dW_r, each
+    # timed over `steps` calls; the splits are the differences
+    dgates = b["d_gates"][:T]
+    rb_dl = torch.empty((T, k), dtype=torch.float32, device=dev)
+    rb_dx = torch.empty((T, d), dtype=torch.float32, device=dev)
+    rb_dw = torch.empty((E, d), dtype=torch.float32, device=dev)
+
+    def rb_call(with_dx, with_dw):
+        Lb.moe_router_backward(x, layer.w.w_router, layer.ids[:T], dgates, layer.score_fn, layer.renorm,
+                               layer.route_scale, d_logits=rb_dl, dx=rb_dx if with_dx else None,
+                               dw_router=rb_dw if with_dw else None, sorted_to_slot=layer.s2s[:A],
+                               expert_offsets=layer.offsets, dev_status=layer.dev_status)
+
+    rb_ms = {}
+    for key, flags in (("dl", (False, False)), ("dl_dx", (True, False)), ("all", (True, True))):
+        for _ in range(warmup):
+            rb_call(*flags)
+        torch.cuda.synchronize()
+        a, bb = ev(), ev()
+        a.record()
+        for _ in range(steps):
+            rb_call(*flags)
+        bb.record()
+        torch.cuda.synchronize()
+        rb_ms[key] = a.elapsed_time(bb) / steps
     flops = 6.0 * A * d * F
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"]
@@ -638,6 +663,17 @@ def run_backward(cfg, dev, seed, steps, warmup, peaks):
                                     f"({4 * 3 * E * d * F / 1e9:.1f} GB)",
                             "steps": {n: {"ms": v} for n, v in wg_split.items()}},
            "status": Lb.check_status(layer.dev_status)}
+    dx_ms, dw_ms = rb_ms["dl_dx"] - rb_ms["dl"], rb_ms["all"] - rb_ms["dl_dx"]
+    out["router_bwd"] = {
+        "ms": rb_ms["all"],
+        "note": "gradients of the router for the fixed ids: d_logits (the chosen logits re-formed, gate "
+                "derivative), dx [T, d] and dW_r [E, d] in fp32; not part of ms_per_step",
+        "d_logits": {"ms": rb_ms["dl"], "router row bytes through L1": T * k * d * 2,
+                     "fp32 TFLOP/s": 2 * T * k * d / (rb_ms["dl"] * 1e-3) / 1e12},
+        "dx": {"ms": dx_ms, "bytes": T * d * 4 + T * k * 8, "GB/s": (T * d * 4 + T * k * 8) / (dx_ms * 1e-3) / 1e9,
+               "frac_hbm": (T * d * 4 + T * k * 8) / (dx_ms * 1e-3) / 1e9 / hbm},
+        "dW_r": {"ms": dw_ms, "x row bytes per routed row (L2)": A * d * 2, "bytes (HBM: x once, dW_r written)":
+                 T * d * 2 + E * d * 4}}
     for n, nb in (("combine_bwd", b_comb), ("swiglu_bwd", b_swi), ("dispatch_bwd", b_disp)):
         out["steps"][n]["GB/s"] = nb / (split[n] * 1e-3) / 1e9
         out["steps"][n]["frac_hbm"] = out["steps"][n]["GB/s"] / hbm

@@ -529,7 +529,8 @@ __global__ void __launch_bounds__(256, 2) route_replay_kernel(const IdT *__restr
 
 // dx[t, c] = sum_j d_logits[t, j] * W_r[ids[t, j], c], the slots in order,
 // fp32.  One warp per token; lane l takes columns 8 (l + 32 i) .. + 7, the
-// k router rows (L2-resident) read 16 bytes at a time.  A slot whose id is
+// k router rows (L2-resident) read 16 bytes at a time (two chunks per pass
+// measured slower).  A slot whose id is
 // outside [0, E) is skipped (its d_logit is 0).
 __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t *__restrict__ ids,
                                                         const float *__restrict__ d_logits,
@@ -561,7 +562,8 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t *__restric
 // dw[e, c] = sum over expert e's dispatched rows r (sorted order) of
 // d_logits[slot(r)] * x[slot(r) / k, c], fp32, the rows in order.  One CTA
 // of 128 threads per (expert, 1024 columns); thread i takes columns
-// 8 i .. 8 i + 7 of its chunk, four rows' loads in flight.  A slot outside
+// 8 i .. 8 i + 7 of its chunk, four rows' loads in flight (eight measured
+// no faster).  A slot outside
 // [0, T k) is skipped; an expert without rows gets zeros.
 constexpr int RDW_COLS = 1024;
 __global__ void __launch_bounds__(128) router_dw_kernel(const int32_t *__restrict__ sorted_to_slot,
@@ -727,10 +729,10 @@ static void router_dlogits_launch(const int32_t *ids, const uint16_t *x, const u
                                   int E, int k, int score_fn, int renorm, float route_scale, const float *d_gates,
                                   float *d_logits, int32_t *dev_status, cudaStream_t st)
 {
-    if (k <= 8)
-        route_replay_kernel<2, V, int32_t, true><<<replay_grid(T, 128), 256, 0, st>>>(
-            ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, nullptr, d_logits, dev_status, d_gates);
-    else if (k <= 16)
+    // four threads per token (two slot chains each for k <= 8): the
+    // backward runs on a layer's T tokens, too few for two per token to
+    // keep the SMs' loads in flight
+    if (k <= 16)
         route_replay_kernel<4, V, int32_t, true><<<replay_grid(T, 64), 256, 0, st>>>(
             ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, nullptr, d_logits, dev_status, d_gates);
     else

@@ -211,6 +211,27 @@ class MoELayerFP8:
             return dx, b["d_gates"][:T]
         return (dx, b["d_gates"][:T], *self._weight_grads(dy, T))
 
+    def router_backward(self, d_gates: torch.Tensor):
+        """Gradients of the router of the last forward(train=True), its ids
+        fixed: from d_gates [T, k] (as backward() returns them) ->
+        (dx_router [T, d] fp32, the router's part of dL/dx; dW_r [E, d] fp32).
+        The full softmax over E (softmax without renormalisation) is not
+        supported."""
+        T = getattr(self, "_T_train", None)
+        if T is None or self.mx or self.gathered:
+            raise ValueError("router_backward needs a forward(train=True) of the fp32-scale sorted form")
+        A = T * self.k
+        if getattr(self, "_rb", None) is None:
+            dev = d_gates.device
+            self._rb = dict(dl=torch.empty((self.T_max, self.k), dtype=torch.float32, device=dev),
+                            dx=torch.empty((self.T_max, self.w.d), dtype=torch.float32, device=dev),
+                            dw=torch.empty((self.w.E, self.w.d), dtype=torch.float32, device=dev))
+        r = self._rb
+        L.moe_router_backward(self._x_train, self.w.w_router, self.ids[:T], d_gates, self.score_fn, self.renorm,
+                              self.route_scale, dx=r["dx"][:T], dw_router=r["dw"], sorted_to_slot=self.s2s[:A],
+                              expert_offsets=self.offsets, d_logits=r["dl"][:T], dev_status=self.dev_status)
+        return r["dx"][:T], r["dw"]
+
     def _weight_grads(self, dy: torch.Tensor, T: int, events=None):
         """dW13, dW2 of the last train forward; `events` (seven CUDA events, for
         timing) are recorded around the six library calls."""

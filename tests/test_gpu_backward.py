@@ -378,3 +378,28 @@ def test_wgrad_quant_scales_off_the_fast_path(L, oracle):
         assert (os_ < 2.0 ** -90).any()                       # the IEEE path is exercised
         np.testing.assert_array_equal(q.cpu().numpy()[:, :P], oq)
         np.testing.assert_array_equal(s.cpu().numpy()[:P // 128].T.view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("replay", 500)])
+def test_layer_router_backward(L, oracle, name, T):
+    """layer.router_backward on the d_gates of layer.backward: the router's
+    dx and dW_r for the forward's ids (routed, or replayed from the payload)
+    against the oracle's (1e-4 of the largest entry: the gate derivative is
+    fp32 on the device)."""
+    cfg = S.CONFIGS[name]
+    if T:
+        cfg = cfg.with_(T=T)
+    layer = _layer(cfg)
+    x = S.make_x(cfg, DEV)
+    replay = S.make_replay_payload(cfg.with_(layers=1), DEV)[0] if cfg.mode == "replay" else None
+    layer.forward(x, replay_kT=replay, train=True)
+    g = torch.Generator(device=DEV).manual_seed(9)
+    dy = torch.randn((cfg.T, cfg.d), generator=g, device=DEV).to(torch.bfloat16)
+    _, d_gates = layer.backward(dy)
+    dxr, dw = layer.router_backward(d_gates)
+    torch.cuda.synchronize()
+    assert L.check_status(layer.dev_status) == 0
+    rdl, rdx, rdw = oracle.router_backward(bf16_bits(x), bf16_bits(layer.w.w_router), layer.ids[:cfg.T].cpu().numpy(),
+                                           d_gates.cpu().numpy(), cfg.score_fn, cfg.renorm, cfg.route_scale)
+    for got, ref in ((dxr, rdx), (dw, rdw)):
+        assert np.abs(got.cpu().numpy() - ref).max() <= 1e-4 * np.abs(ref).max()
