@@ -1004,6 +1004,20 @@ def run_router_kernels(dev, seed, steps, warmup):
     t = timed(lambda: Lb.moe_route_topk(x, wr, c.k, c.score_fn, c.renorm, c.route_scale, topk_ids=ids, topk_gates=g))
     res["route_topk"] = {"workload": f"T={c.T} d={c.d} E={c.E} top_k={c.k}", "ms": t,
                          "fp32 TFLOP/s": 2.0 * c.T * c.d * c.E / (t * 1e-3) / 1e12}
+    # the router's backward for these ids: d_logits, dx, dW_r (the dispatch
+    # maps for dW_r; a seeded upstream gradient)
+    s2s = torch.empty(c.T * c.k, dtype=torch.int32, device=dev)
+    offs = torch.empty(c.E + 1, dtype=torch.int32, device=dev)
+    Lb.moe_dispatch(ids, c.E, expert_offsets=offs, sorted_to_slot=s2s)
+    dgates = torch.empty((c.T, c.k), dtype=torch.float32, device=dev).normal_(
+        0.0, 1.0, generator=torch.Generator(device=dev).manual_seed(seed + 2))
+    dl = torch.empty_like(dgates)
+    dxr = torch.empty((c.T, c.d), dtype=torch.float32, device=dev)
+    dwr = torch.empty((c.E, c.d), dtype=torch.float32, device=dev)
+    t = timed(lambda: Lb.moe_router_backward(x, wr, ids, dgates, c.score_fn, c.renorm, c.route_scale, d_logits=dl,
+                                             dx=dxr, dw_router=dwr, sorted_to_slot=s2s, expert_offsets=offs))
+    res["router_backward"] = {"workload": f"T={c.T} d={c.d} E={c.E} top_k={c.k}", "ms": t,
+                              "dx bytes written": c.T * c.d * 4, "router row bytes through L1": c.T * c.k * c.d * 2}
     del x
     r = S.CONFIGS["multilayer_replay"]
     x = S.make_x(r, dev, seed)

@@ -562,41 +562,57 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t *__restric
 // dw[e, c] = sum over expert e's dispatched rows r (sorted order) of
 // d_logits[slot(r)] * x[slot(r) / k, c], fp32, the rows in order.  One CTA
 // of 128 threads per (expert, 1024 columns); thread i takes columns
-// 8 i .. 8 i + 7 of its chunk, four rows' loads in flight (eight measured
-// no faster).  A slot outside
-// [0, T k) is skipped; an expert without rows gets zeros.
+// 8 i .. 8 i + 7 of its chunk.  The rows' (token, d_logit) pairs are staged
+// in shared memory 128 at a time (one slot load and division per row for
+// the CTA), then every thread walks them with four rows' x loads in flight.
+// A slot outside [0, T k) adds nothing; an expert without rows gets zeros.
 constexpr int RDW_COLS = 1024;
+constexpr int RDW_BATCH = 128;
 __global__ void __launch_bounds__(128) router_dw_kernel(const int32_t *__restrict__ sorted_to_slot,
                                                         const int32_t *__restrict__ offsets,
                                                         const float *__restrict__ d_logits,
                                                         const uint16_t *__restrict__ x, int T, int d, int k,
                                                         float *__restrict__ dw)
 {
+    __shared__ int32_t s_tok[RDW_BATCH];
+    __shared__ float s_g[RDW_BATCH];
     const int e = blockIdx.y;
     const int c = blockIdx.x * RDW_COLS + 8 * threadIdx.x;
-    if (c >= d) return;
+    const bool col_ok = c < d;
     const int64_t r0 = offsets[e], r1 = offsets[e + 1], A = (int64_t)T * k;
     float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-    for (int64_t r = r0; r < r1; r += 4) {
-        float g[4];
-        uint4 xv[4];
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-            const int32_t slot = r + u < r1 ? __ldg(sorted_to_slot + r + u) : -1;
+    for (int64_t b0 = r0; b0 < r1; b0 += RDW_BATCH) {
+        const int nb = (int)(r1 - b0 < RDW_BATCH ? r1 - b0 : RDW_BATCH);
+        __syncthreads();                                   // the previous batch has been read
+        if ((int)threadIdx.x < nb) {
+            const int32_t slot = __ldg(sorted_to_slot + b0 + threadIdx.x);
             const bool ok = slot >= 0 && slot < A;
-            g[u] = ok ? __ldg(d_logits + slot) : 0.0f;
-            xv[u] = ok ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)(slot / k) * d + c))
-                       : make_uint4(0u, 0u, 0u, 0u);
+            s_tok[threadIdx.x] = ok ? slot / k : -1;
+            s_g[threadIdx.x] = ok ? __ldg(d_logits + slot) : 0.0f;
         }
+        __syncthreads();
+        if (!col_ok) continue;
+        for (int i = 0; i < nb; i += 4) {
+            float g[4];
+            uint4 xv[4];
 #pragma unroll
-        for (int u = 0; u < 4; u++) {
-            if (r + u >= r1) break;
-            float xf[8];
-            unpack_bf16x8(xv[u], xf);
+            for (int u = 0; u < 4; u++) {
+                const int tok = i + u < nb ? s_tok[i + u] : -1;
+                g[u] = i + u < nb ? s_g[i + u] : 0.0f;
+                xv[u] = tok >= 0 ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)tok * d + c))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-            for (int i = 0; i < 8; i++) acc[i] = fmaf(g[u], xf[i], acc[i]);
+            for (int u = 0; u < 4; u++) {
+                if (i + u >= nb) break;
+                float xf[8];
+                unpack_bf16x8(xv[u], xf);
+#pragma unroll
+                for (int j = 0; j < 8; j++) acc[j] = fmaf(g[u], xf[j], acc[j]);
+            }
         }
     }
+    if (!col_ok) return;
     float4 *o = reinterpret_cast<float4 *>(dw + (int64_t)e * d + c);
     o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
