@@ -405,9 +405,9 @@ __device__ __forceinline__ Bf16Vec<V> ldg_bf16(const uint16_t *p)
 // (2, 4 or 8, a power of two with TP * 4 >= k); CTA b of the grid takes
 // tokens floor(b*T/grid) .. floor((b+1)*T/grid) - 1, the grid a whole number
 // of waves of two CTAs per SM, so every SM gets the same number of tokens.
-// Copies the layer slab [k, T] to
-// [T, k] and checks the ids; if x is given, thread (token, part q) evaluates
-// the router logits of the token's slots q*SP .. q*SP+SP-1 (SP = ceil(k/TP)
+// Copies the layer slab [k, T] to [T, k] and checks the ids; if x is given,
+// thread (token, part q) evaluates the router logits of the token's slots
+// q*SP .. q*SP+SP-1 (SP = ceil(k/TP)
 // <= 4) -- one fma chain per slot in ascending hidden index, as in
 // route_topk_kernel -- so every x value it loads feeds SP chains.  x and the
 // replayed W_r rows are read straight from L1/L2, V bf16 per load (V = 16
