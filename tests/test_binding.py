@@ -48,3 +48,14 @@ def test_status_codes_raise_named_errors(L):
     L._check("moe_combine", 0)                                  # OK passes silently
     for s in range(7):
         assert L.moe_status_str(s)
+
+
+def test_router_backward_arguments_are_checked(L):
+    x = torch.zeros(8, 128, dtype=torch.bfloat16)               # host memory
+    wr = torch.zeros(16, 128, dtype=torch.bfloat16)
+    ids = torch.zeros(8, 2, dtype=torch.int32)
+    dg = torch.zeros(8, 2, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.moe_router_backward(x, wr, ids, dg)
+    with pytest.raises(TypeError, match="x: expected torch.bfloat16"):
+        L.moe_router_backward(x.float(), wr, ids, dg)
