@@ -1,5 +1,6 @@
 // route.cu -- MoE router: fused fp32 logits + warp top-k + gates + capture,
-// and replay of a captured routing payload.
+// replay of a captured routing payload, and the router's backward for fixed
+// ids (logit gradients through the gates, dx, dW_r).
 //
 // Router replay (R3) in "RL at 1T Scale: prime-rl Performance Deep Dive",
 // section "Router replay": the routing decision made at inference is
@@ -15,8 +16,9 @@
 // 32 FMAs, the next hidden index's operands loaded while the current FMAs
 // run), bf16 tiles of x and W_r (32 deep) read in whole 32-byte sectors and
 // widened to fp32 in double-buffered shared memory with conflict-free
-// stores while the next tile loads into registers (one barrier per tile).  Logits stay on chip: each CTA selects its own top-k,
-// CTA 0 merges the candidates it receives through distributed shared memory.
+// stores while the next tile loads into registers (one barrier per tile).
+// Logits stay on chip: each CTA selects its own top-k, CTA 0 merges the
+// candidates it receives through distributed shared memory.
 #include "common.cuh"
 
 namespace moe {
