@@ -110,6 +110,12 @@ def cpu_model() -> str:
     return "unknown"
 
 
+def fp8_weight_bytes(cfg) -> int:
+    """One layer's e4m3 expert weights (W13 [2F, d] and W2 [d, F] per expert),
+    without their 128x128 scales."""
+    return cfg.E * 3 * cfg.F * cfg.d
+
+
 def padded_fraction(counts, bm: int = 128) -> float:
     """Rows the grouped GEMM computes (each expert's rows rounded up to whole
     bm-row tiles) over the rows routed."""
@@ -1212,7 +1218,8 @@ def main():
                           f"{'sigmoid' if cfg.score_fn else 'softmax'} {cfg.mode}",
               "tokens_per_gpu": cfg.T, "parallelism": f"token-sharded x{world}" if world > 1 else "single GPU",
               "l2": "flushed: a 512 MB device write before every timed step, outside the step's events "
-                    "(the FP8 expert weights, 11.3 GB, are streamed from HBM every step as well)",
+                    f"(the FP8 expert weights, {fp8_weight_bytes(cfg) / 1e9:.3g} GB, are streamed from HBM "
+                    "every step as well)",
               "form": args.form, "scales": args.scales}
     metric = "MoE-layer tokens/s (7168d/256e/top-8 FP8)" if cfg.name == "large" else f"MoE-layer tokens/s ({cfg.name})"
 
