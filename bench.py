@@ -173,7 +173,7 @@ class Clocks:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
-                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None),
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 

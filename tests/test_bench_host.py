@@ -1,7 +1,8 @@
 """Host-side logic of bench.py, on the CPU: the JSON line of the reference
 arm (the CPU oracle timed on the host cores) at one rank and under torchrun
-with two ranks, and the roofline arithmetic against closed-form counts of
-the layer's work."""
+with two ranks, the roofline arithmetic against closed-form counts of the
+layer's work, the clock record parsed from nvidia-smi samples, and the
+output error report."""
 import json
 import os
 import socket
@@ -91,3 +92,38 @@ def test_padded_fraction_and_weight_bytes():
     assert bench.padded_fraction([0, 1, 128, 129]) == pytest.approx((0 + 128 + 128 + 256) / 258)
     assert bench.padded_fraction([]) == 0.0
     assert bench.fp8_weight_bytes(S.CONFIGS["large"]) == 256 * (2 * 2048 * 7168 + 7168 * 2048)
+
+
+def test_clock_summary_from_samples():
+    """The clock record beside the number: median SM clock under load, the
+    maximum, and every throttle reason seen active in any sample."""
+    import bench
+    c = bench.Clocks(0)
+    c.f.write("0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+              "0, 2055, 2070, 1380.0, 0x4, Not Active, Not Active, Not Active, Active\n"
+              "0, 2070, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active\n"
+              "garbage line\n")
+    s = c.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1380.0
+    c = bench.Clocks(0)
+    c.f.write("0, 1500, 2070, [N/A], 0x0, Active, Not Active, Active, Not Active\n")
+    s = c.summary()
+    assert s["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"] and s["power_w_max"] is None
+    assert bench.Clocks(0).summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+
+def test_error_report_closed_form():
+    """Row error is max |y - ref| over the row's largest |ref|; element error
+    divides by max(|ref|, 1e-2 rowmax)."""
+    import numpy as np
+    import torch
+    import bench
+    bits = lambda a: torch.tensor(a, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref = [[4.0, -2.0, 0.0, 1.0], [1.0, 1.0, 1.0, 1.0]]
+    y = [[4.0, -2.0, 0.03125, 1.0], [1.0, 1.0, 1.0, 1.0]]
+    r = bench.error_report(bits(y), bits(ref))
+    assert r["tokens"] == 2 and r["bar_row_rel_err"] == 2e-2
+    assert r["row_rel_err_max"] == pytest.approx(0.03125 / 4.0)
+    assert r["elem_rel_err_max"] == pytest.approx(0.03125 / 0.04)
+    assert r["elem_rel_err_mean"] == pytest.approx(0.03125 / 0.04 / 8)
