@@ -125,10 +125,14 @@ def padded_fraction(counts, bm: int = 128) -> float:
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling (every 100 ms) during the timed region.  The SM
+    clock reported is the median of the samples taken under load (GPU
+    utilisation at least 50%; all samples if none was); a throttle reason
+    counts if any sample shows it."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
+    PERIOD_MS = 100
 
     def __init__(self, index: int):
         self.index = index
@@ -138,7 +142,7 @@ class Clocks:
     def __enter__(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
@@ -165,7 +169,9 @@ class Clocks:
             os.unlink(self.f.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[1]) for r in rows]
+        util = lambda r: float(r[9]) if len(r) > 9 and r[9].replace(".", "").isdigit() else -1.0
+        loaded = [r for r in rows if util(r) >= 50.0]
+        sm = [float(r[1]) for r in (loaded or rows)]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -174,7 +180,7 @@ class Clocks:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
                 "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None),
-                "samples": len(rows), "reasons": sorted(reasons)}
+                "samples": len(rows), "samples_under_load": len(loaded), "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ workload
@@ -1183,7 +1189,7 @@ def cpu_config_legs(seed, gen_dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large")
     ap.add_argument("--seed", type=int, default=0)

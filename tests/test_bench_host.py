@@ -96,16 +96,27 @@ def test_padded_fraction_and_weight_bytes():
 
 def test_clock_summary_from_samples():
     """The clock record beside the number: median SM clock under load, the
-    maximum, and every throttle reason seen active in any sample."""
+    maximum, and every throttle reason seen active in any sample (the query's
+    fields in order: index, SM clock, its maximum, power, the active-reasons
+    mask, four reason flags, GPU utilisation)."""
     import bench
     c = bench.Clocks(0)
-    c.f.write("0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active\n"
-              "0, 2055, 2070, 1380.0, 0x4, Not Active, Not Active, Not Active, Active\n"
-              "0, 2070, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active\n"
+    c.f.write("0, 2070, 2070, 190.5, 0x0, Not Active, Not Active, Not Active, Not Active, 0\n"
+              "0, 2070, 2070, 210.0, 0x0, Not Active, Not Active, Not Active, Not Active, 3\n"
+              "0, 1950, 2070, 1380.0, 0x4, Not Active, Not Active, Not Active, Active, 100\n"
+              "0, 1965, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active, 98\n"
+              "0, 1980, 2070, 1210.0, 0x0, Not Active, Not Active, Not Active, Not Active, 100\n"
               "garbage line\n")
     s = c.summary()
-    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["sm_mhz"] == 1965.0 and s["sm_max_mhz"] == 2070.0   # the idle samples are left out
+    assert s["samples"] == 5 and s["samples_under_load"] == 3
     assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1380.0
+    c = bench.Clocks(0)                                           # no utilisation reading: all samples
+    c.f.write("0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+              "0, 2055, 2070, 1380.0, 0x4, Not Active, Not Active, Not Active, Active\n"
+              "0, 2070, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active, [N/A]\n")
+    s = c.summary()
+    assert s["sm_mhz"] == 2070.0 and s["samples"] == 3 and s["samples_under_load"] == 0
     c = bench.Clocks(0)
     c.f.write("0, 1500, 2070, [N/A], 0x0, Active, Not Active, Active, Not Active\n")
     s = c.summary()
