@@ -9,6 +9,8 @@ gates into the logits, the router weights and the tokens).
 - closed forms: with renormalisation a constant upstream gradient (and k = 1)
   gives zero; softmax logit gradients of a token sum to zero; an expert no
   token chose has a zero dW_r row; invalid tokens contribute nothing.
+- a hand-worked three-token case (tests/golden/worked_router_backward.txt):
+  exact values in all three gate modes.
 """
 import numpy as np
 import pytest
@@ -90,3 +92,27 @@ def test_unchosen_experts_and_invalid_tokens(oracle):
     dg2[[7, 30]] = 0
     _, _, dw2 = oracle.router_backward(bf16_bits(x), bf16_bits(wr), ids, dg2, 1, 1, 1.0, valid=valid)
     np.testing.assert_array_equal(dw, dw2)
+
+
+def test_worked_router_backward(oracle):
+    """The hand-worked three-token case in tests/golden/worked_router_backward.txt
+    (every chosen logit exactly zero, so every gradient is a short binary
+    fraction derived in the file's comments), in all three gate modes."""
+    import os
+    gd = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "worked_router_backward.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                key, *rest = line.split()
+                gd[key] = [float(v) for v in rest]
+    bf = lambda a, shape: bf16_bits(torch.tensor(a, dtype=torch.float32).reshape(shape).to(torch.bfloat16))
+    x, wr = bf(gd["x"], (3, 2)), bf(gd["w_r"], (4, 2))
+    ids = np.array(gd["ids"], np.int32).reshape(3, 2)
+    dg = np.array(gd["d_gates"], np.float32).reshape(3, 2)
+    np.testing.assert_array_equal(oracle.router_logits(x, wr)[:, :3], np.zeros((3, 3), np.float32))
+    for mode in "ABC":
+        score_fn, renorm, rs = gd[f"{mode}_mode"]
+        dl, dx, dw = oracle.router_backward(x, wr, ids, dg, int(score_fn), int(renorm), rs)
+        np.testing.assert_array_equal(dl.reshape(-1), np.array(gd[f"{mode}_d_logits"], np.float32), err_msg=mode)
+        np.testing.assert_array_equal(dx.reshape(-1), np.array(gd[f"{mode}_dx"], np.float32), err_msg=mode)
+        np.testing.assert_array_equal(dw.reshape(-1), np.array(gd[f"{mode}_dw"], np.float32), err_msg=mode)
