@@ -568,20 +568,25 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t *__restric
 // in shared memory 128 at a time (one slot load and division per row for
 // the CTA), then every thread walks them with four rows' x loads in flight.
 // A slot outside [0, T k) adds nothing; an expert without rows gets zeros.
+// Offsets outside [0, T k], or decreasing, are clamped into that range (no
+// read past the map) and set MOE_DEV_ROWS.
 constexpr int RDW_COLS = 1024;
 constexpr int RDW_BATCH = 128;
 __global__ void __launch_bounds__(128) router_dw_kernel(const int32_t *__restrict__ sorted_to_slot,
                                                         const int32_t *__restrict__ offsets,
                                                         const float *__restrict__ d_logits,
                                                         const uint16_t *__restrict__ x, int T, int d, int k,
-                                                        float *__restrict__ dw)
+                                                        float *__restrict__ dw, int32_t *dev_status)
 {
     __shared__ int32_t s_tok[RDW_BATCH];
     __shared__ float s_g[RDW_BATCH];
     const int e = blockIdx.y;
     const int c = blockIdx.x * RDW_COLS + 8 * threadIdx.x;
     const bool col_ok = c < d;
-    const int64_t r0 = offsets[e], r1 = offsets[e + 1], A = (int64_t)T * k;
+    const int64_t A = (int64_t)T * k, o0 = __ldg(offsets + e), o1 = __ldg(offsets + e + 1);
+    const int64_t r0 = o0 < 0 ? 0 : (o0 > A ? A : o0);
+    const int64_t r1 = o1 < r0 ? r0 : (o1 > A ? A : o1);
+    if ((r0 != o0 || r1 != o1) && blockIdx.x == 0 && threadIdx.x == 0) dev_flag(dev_status, MOE_DEV_ROWS);
     float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
     for (int64_t b0 = r0; b0 < r1; b0 += RDW_BATCH) {
         const int nb = (int)(r1 - b0 < RDW_BATCH ? r1 - b0 : RDW_BATCH);
@@ -790,6 +795,6 @@ MOE_API moe_status moe_router_backward(const uint16_t *x, const uint16_t *w_rout
                                                                                       d, E, k, dx);
     if (dw_router)
         router_dw_kernel<<<dim3((unsigned)((d + RDW_COLS - 1) / RDW_COLS), (unsigned)E), 128, 0, st>>>(
-            sorted_to_slot, expert_offsets, d_logits, x, T, d, k, dw_router);
+            sorted_to_slot, expert_offsets, d_logits, x, T, d, k, dw_router, dev_status);
     return launch_status();
 }

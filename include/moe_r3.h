@@ -153,7 +153,9 @@ moe_status moe_route_replay_u8(const uint8_t *replay_kT, const uint16_t *x, cons
  *   dw_router[e,c] = sum over expert e's rows of the dispatch that produced
  *            sorted_to_slot / expert_offsets for these ids, in that sorted
  *            order, of d_logits[slot] * x[slot / k, c] (nullable; fp32; an
- *            expert without rows gets zeros).
+ *            expert without rows gets zeros).  A slot outside [0, T*k) adds
+ *            nothing; offsets outside [0, T*k], or decreasing, are clamped
+ *            into that range and set MOE_DEV_ROWS.
  * x [T,d] bf16, w_router [E,d] bf16 (16-byte aligned; 32-byte alignment of
  * both lets the logits read whole sectors), topk_ids [T,k] int32, d_gates,
  * d_logits [T,k] fp32, dx [T,d] fp32, dw_router [E,d] fp32 (16-byte

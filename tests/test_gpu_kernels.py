@@ -438,3 +438,29 @@ def test_router_backward_bad_ids_and_unchosen_experts(L, oracle):
                                          valid=valid)
     assert np.abs(dl.cpu().numpy() - rdl).max() <= 1e-5 * np.abs(rdl).max()
     assert np.abs(dw.cpu().numpy() - rdw).max() <= 1e-4 * np.abs(rdw).max()
+
+
+def test_router_backward_clamps_bad_offsets(L):
+    """Expert offsets that are negative, decreasing or past T*k are clamped
+    into [0, T*k] (the kernel reads no row outside the map) and set
+    MOE_DEV_ROWS; experts whose two offsets are intact keep their exact
+    dW_r rows."""
+    cfg = S.CONFIGS["replay"].with_(E=70, d=256)
+    x, wr = _route_case(cfg, 200, seed=9)
+    T, k, E = 200, cfg.k, 70
+    ids = torch.stack([torch.randperm(E)[:k] for _ in range(T)]).to(torch.int32).to(DEV)
+    dg = torch.randn((T, k), device=DEV)
+    s2s, offs = _dispatch_maps(L, ids, E)
+    _, _, dw_ref = L.moe_router_backward(x, wr, ids, dg, 0, 1, 1.0, dx=False, dw_router=True, sorted_to_slot=s2s,
+                                         expert_offsets=offs)
+    bad = offs.clone()
+    bad[3] = -7                     # expert 2 ends before it starts, expert 3 starts before row 0
+    bad[E] = T * k + 1000            # the last expert runs past the map
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _, _, dw = L.moe_router_backward(x, wr, ids, dg, 0, 1, 1.0, dx=False, dw_router=True, sorted_to_slot=s2s,
+                                     expert_offsets=bad, dev_status=st)
+    torch.cuda.synchronize()
+    assert L.check_status(st) == L.MOE_DEV_ROWS
+    keep = [e for e in range(E) if e not in (2, 3, E - 1)]
+    assert torch.equal(dw[keep], dw_ref[keep])
+    assert torch.all(dw[2] == 0)    # an empty range after clamping
