@@ -485,6 +485,10 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  *                          3: x (C = d); rows map to tokens by
  *                          sorted_to_slot / k.  C a multiple of 128; q and
  *                          the source buffers 16-byte aligned.
+ *                          expert_offsets and pad are read as given (the
+ *                          outputs of moe_dispatch and moe_wgrad_pad_offsets
+ *                          for these rows): the source rows they name must
+ *                          exist; no store leaves q [C, ld] or its scales.
  *   moe_wgrad_gemm         out[e] [M, N] fp32 = sum over e's blocks kb of
  *                          (a_sT[kb, m] * b_sT[kb, n]) * P_kb(m, n) (the
  *                          forward's per-block promotion), a [M, ld], b [N,
@@ -494,7 +498,8 @@ moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x_exp, co
  *                          without rows get zeros; pad entries outside
  *                          [0, ld] or not multiples of 128 run no tile and
  *                          set MOE_DEV_ROWS.
- * The router's backward is not provided (d_gates are returned for it).
+ * The router's own gradients, from the d_gates that moe_combine_backward
+ * returns, are moe_router_backward's.
  * Errors: NULL, SHAPE, ALIGN, CUDA (WORKSPACE for the _train call).
  * ---------------------------------------------------------------------- */
 moe_status moe_grouped_ffn_fp8_train(const uint8_t *xq_sorted, const float *xs_sorted,
