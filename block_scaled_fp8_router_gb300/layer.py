@@ -183,7 +183,8 @@ class MoELayerFP8:
         """Backward of the expert path of the last forward(train=True) with its
         routing fixed (replayed): returns (dx [T, d] bf16 from the experts,
         d_gates [T, k] fp32), and with weight_grads also (dW13 [E, 2F, d],
-        dW2 [E, d, F]) fp32.  The router's backward is not computed."""
+        dW2 [E, d, F]) fp32.  The router's gradients from these d_gates are
+        router_backward's (not part of this call)."""
         T = getattr(self, "_T_train", None)
         if T is None or self.mx or self.gathered:
             raise ValueError("backward needs a forward(train=True) of the fp32-scale sorted form")
