@@ -774,16 +774,17 @@ MOE_API moe_status moe_router_backward(const uint16_t *x, const uint16_t *w_rout
     moe_status s = check_route_args(T, d, E, k, score_fn);
     if (s != MOE_OK) return s;
     if (score_fn == MOE_SCORE_SOFTMAX && !renorm) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = as_stream(stream);
+    if (T == 0) {   // no tokens (the [T, .] arrays may be NULL): dw_router is all zeros
+        if (!dw_router) return MOE_OK;
+        if (!aligned16(dw_router)) return MOE_ERR_ALIGN;
+        return cudaMemsetAsync(dw_router, 0, sizeof(float) * (size_t)E * d, st) == cudaSuccess ? MOE_OK
+                                                                                             : MOE_ERR_CUDA;
+    }
     if (!x || !w_router || !topk_ids || !d_gates || !d_logits) return MOE_ERR_NULL;
     if (dw_router && (!sorted_to_slot || !expert_offsets)) return MOE_ERR_NULL;
     if (!aligned16(x) || !aligned16(w_router) || (dx && !aligned16(dx)) || (dw_router && !aligned16(dw_router)))
         return MOE_ERR_ALIGN;
-    cudaStream_t st = as_stream(stream);
-    if (T == 0) {   // no tokens: dw_router is all zeros
-        if (dw_router && cudaMemsetAsync(dw_router, 0, sizeof(float) * (size_t)E * d, st) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        return MOE_OK;
-    }
     const bool wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (reinterpret_cast<uintptr_t>(w_router) & 31u) == 0;
     if (wide)
         router_dlogits_launch<16>(topk_ids, x, w_router, T, d, E, k, score_fn, renorm, route_scale, d_gates, d_logits,

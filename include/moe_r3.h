@@ -160,8 +160,9 @@ moe_status moe_route_replay_u8(const uint8_t *replay_kT, const uint16_t *x, cons
  * both lets the logits read whole sectors), topk_ids [T,k] int32, d_gates,
  * d_logits [T,k] fp32, dx [T,d] fp32, dw_router [E,d] fp32 (16-byte
  * aligned); sorted_to_slot [T*k] and expert_offsets [E+1] are moe_dispatch's
- * maps, needed only with dw_router.  T may be 0 (dw_router, if given, is
- * zeroed).  The full softmax over E (score_fn SOFTMAX, renorm 0) depends on
+ * maps, needed only with dw_router.  T may be 0: the [T, .] arrays and the
+ * maps may then be NULL and dw_router, if given, is zeroed.  The full
+ * softmax over E (score_fn SOFTMAX, renorm 0) depends on
  * every expert's logit: UNSUPPORTED.
  * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED.
  * ---------------------------------------------------------------------- */

@@ -59,6 +59,11 @@ def test_host_side_errors(lib):
     assert L.moe_router_backward(x, x, x, x, 10, 128, 8, 2, 1, 1, 1.0, x, m, null, null, null, null, null) == 3
     assert L.moe_router_backward(x, x, x, x, 10, 100, 8, 2, 1, 1, 1.0, x, x, null, null, null, null, null) == 2
     assert L.moe_router_backward(x, x, x, x, 0, 128, 8, 2, 1, 1, 1.0, x, x, null, null, null, null, null) == 0
+    # T = 0 with every [T, .] array NULL (what empty tensors pass) and no dW_r: nothing to do
+    assert L.moe_router_backward(null, null, null, null, 0, 128, 8, 2, 1, 1, 1.0, null, null, null, null, null,
+                                 null, null) == 0
+    assert L.moe_router_backward(null, null, null, null, 0, 128, 8, 2, 1, 1, 1.0, null, null, null, null, m,
+                                 null, null) == 3                                       # dW_r misaligned
     assert L.fp8_block_quant(null, 4, 100, 100, 1, null, null, null) == 2
     assert L.fp8_block_quant(null, 4, 128, 128, 128, null, null, null) == 2                 # rows % 128
     assert L.fp8_block_quant(null, 0, 128, 128, 1, null, null, null) == 0

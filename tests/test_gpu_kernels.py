@@ -464,3 +464,50 @@ def test_router_backward_clamps_bad_offsets(L):
     keep = [e for e in range(E) if e not in (2, 3, E - 1)]
     assert torch.equal(dw[keep], dw_ref[keep])
     assert torch.all(dw[2] == 0)    # an empty range after clamping
+
+
+def test_router_backward_edge_cases(L, oracle):
+    """T = 0 (empty tensors, dW_r zeroed); k = 1 under renormalisation (the
+    gate is route_scale whatever the logit, so no gradient); k = 24 (eight
+    threads per token in the logit pass) against the oracle; x and W_r 16
+    bytes past a 32-byte boundary (the 16-byte load path) bit-identical to
+    the aligned run."""
+    cfg = S.CONFIGS["replay"].with_(E=64, d=256)
+    E, d = 64, 256
+    _, wr = _route_case(cfg, 8, seed=1)
+    # T = 0
+    x0 = torch.empty((0, d), dtype=torch.bfloat16, device=DEV)
+    dw0 = torch.full((E, d), 7.0, device=DEV)
+    dl, dx, dw = L.moe_router_backward(x0, wr, torch.empty((0, 6), dtype=torch.int32, device=DEV),
+                                       torch.empty((0, 6), device=DEV), 1, 1, 1.0, dx=True, dw_router=dw0,
+                                       sorted_to_slot=torch.empty(0, dtype=torch.int32, device=DEV),
+                                       expert_offsets=torch.zeros(E + 1, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    assert dl.shape == (0, 6) and dx.shape == (0, d) and torch.all(dw == 0)
+    # k = 1
+    T = 130
+    x, _ = _route_case(cfg, T, seed=2)
+    ids1 = torch.randint(0, E, (T, 1), device=DEV, dtype=torch.int32)
+    dg1 = torch.randn((T, 1), device=DEV)
+    dl, dx, _ = L.moe_router_backward(x, wr, ids1, dg1, 0, 1, 1.0)
+    assert torch.all(dl == 0) and torch.all(dx == 0)
+    dl, _, _ = L.moe_router_backward(x, wr, ids1, dg1, 1, 1, 1.0)
+    assert dl.abs().max().item() <= 1e-6 * dg1.abs().max().item()
+    # k = 24, both alignments
+    k = 24
+    ids = torch.stack([torch.randperm(E)[:k] for _ in range(T)]).to(torch.int32).to(DEV)
+    dg = torch.randn((T, k), device=DEV)
+    s2s, offs = _dispatch_maps(L, ids, E)
+    outs = []
+    for off in (0, 8):
+        xo, wro = _offset_copy(x, off), _offset_copy(wr, off)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        outs.append(L.moe_router_backward(xo, wro, ids, dg, 1, 1, 1.5, dx=True, dw_router=True,
+                                          sorted_to_slot=s2s, expert_offsets=offs, dev_status=st))
+        assert L.check_status(st) == 0
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    rdl, rdx, rdw = oracle.router_backward(bf16_bits(x), bf16_bits(wr), ids.cpu().numpy(), dg.cpu().numpy(), 1, 1,
+                                           1.5)
+    for got, ref, tol in zip(outs[0], (rdl, rdx, rdw), (1e-5, 1e-4, 1e-4)):
+        assert np.abs(got.cpu().numpy() - ref).max() <= tol * np.abs(ref).max()
