@@ -562,10 +562,13 @@ moe_status moe_combine_slots(const uint16_t *out_slots, const int32_t *slot_to_s
  * pipelined kernel uses: one CTA waits on an mbarrier that nothing arrives
  * at, for at most timeout_ns, then sets MOE_DEV_TIMEOUT in *dev_status and
  * returns.  For fault-handling tests; no counterpart in the method.
+ * timeout_ns in [0, 10^10] (ten seconds at most).
+ * Errors: NULL (dev_status), SHAPE (timeout_ns out of range), CUDA.
  * ---------------------------------------------------------------------- */
 moe_status moe_debug_bounded_wait(int64_t timeout_ns, int32_t *dev_status, void *stream);
 
-/* Number of SMs and the device ordinal the library sees (for sizing). */
+/* Number of SMs of the current CUDA device (the figure the persistent
+ * kernels size their grids by); 1 if the device cannot be queried. */
 int moe_device_sm_count(void);
 
 #ifdef __cplusplus

@@ -90,6 +90,7 @@ def test_host_side_errors(lib):
     assert L.moe_route_replay_u8(null, null, null, 10, 100, 8, 2, 1, 1, 1.0, null, null, null, null) == 2
     assert L.moe_route_replay_u8(null, null, null, 10, 128, 8, 2, 1, 1, 1.0, null, null, null, null) == 1
     assert L.moe_debug_bounded_wait(1000, null, null) == 1
+    assert L.moe_debug_bounded_wait(-1, x, null) == 2 and L.moe_debug_bounded_wait(10 ** 10 + 1, x, null) == 2
     # backward of the expert path
     y = ctypes.c_void_p(0x1008)                                        # 8-byte aligned only
     assert L.moe_combine_backward(x, x, x, x, 10, 2, 100, 20, x, x, x, null, null) == 2      # d % 128
