@@ -1230,9 +1230,9 @@ static moe_status ffn_launch(const uint8_t *xq, int64_t x_rows, const float *xs,
         F % 128 != 0)
         return MOE_ERR_SHAPE;
     if ((int64_t)E * 2 * F >= (1LL << 31) || (int64_t)E * d >= (1LL << 31)) return MOE_ERR_SHAPE;
+    if (max_rows == 0) return MOE_OK;   // nothing to compute (the workspace may be empty too)
     const size_t need = moe_grouped_ffn_workspace_size(max_rows, d, F);
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-    if (max_rows == 0) return MOE_OK;
     if (!xq || !xs || !expert_offsets || !w13_q || !w13_s || !w2_q || !w2_s || !out) return MOE_ERR_NULL;
     if (GATHER && !sorted_to_slot) return MOE_ERR_NULL;
     if (!aligned16(xq) || !aligned16(w13_q) || !aligned16(w2_q) || !aligned16(out) ||
@@ -1299,7 +1299,7 @@ MOE_API moe_status moe_grouped_ffn_fp8_train(const uint8_t *xq_sorted, const flo
                                              const float *w2_s, uint16_t *out_sorted, float *h_out, void *workspace,
                                              size_t workspace_bytes, int32_t *dev_status, void *stream)
 {
-    if (!h_out) return MOE_ERR_NULL;
+    if (max_rows != 0 && !h_out) return MOE_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(h_out) & 15) return MOE_ERR_ALIGN;
     return ffn_launch<false>(xq_sorted, max_rows, xs_sorted, nullptr, 1, expert_offsets, max_rows, E, d, F, w13_q,
                              w13_s, w2_q, w2_s, out_sorted, workspace, workspace_bytes, dev_status, stream, h_out);
@@ -1374,9 +1374,9 @@ MOE_API moe_status moe_grouped_ffn_mx(const uint8_t *xq_sorted, const uint8_t *x
         F % 128 != 0 || T < 0 || k < 1 || k > 32)
         return MOE_ERR_SHAPE;
     if ((int64_t)E * 2 * F >= (1LL << 31) || (int64_t)E * d >= (1LL << 31)) return MOE_ERR_SHAPE;
+    if (max_rows == 0 || T == 0) return MOE_OK;   // nothing to compute (the workspace may be empty too)
     const size_t need = moe_grouped_ffn_mx_workspace_size(max_rows, d, F);
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-    if (max_rows == 0 || T == 0) return MOE_OK;
     if (!xq_sorted || !x_exp || !sorted_to_slot || !expert_offsets || !w13_q || !w13_exp || !w2_q || !w2_exp ||
         !out_sorted)
         return MOE_ERR_NULL;

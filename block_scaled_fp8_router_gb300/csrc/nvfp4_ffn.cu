@@ -429,9 +429,9 @@ MOE_API moe_status moe_grouped_ffn_nvfp4(const uint8_t *xq_sorted, const uint8_t
         F % 128 != 0)
         return MOE_ERR_SHAPE;
     if ((int64_t)E * 2 * F >= (1LL << 31) || (int64_t)E * d >= (1LL << 31)) return MOE_ERR_SHAPE;
+    if (max_rows == 0) return MOE_OK;   // nothing to compute (the workspace may be empty too)
     const size_t need = moe_grouped_ffn_nvfp4_workspace_size(max_rows, d, F);
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-    if (max_rows == 0) return MOE_OK;
     if (!xq_sorted || !xs_sorted || !x_enc || !expert_offsets || !w13_q || !w13_sf_tiled || !w13_enc || !w2_q ||
         !w2_sf_tiled || !w2_enc || !out_sorted)
         return MOE_ERR_NULL;

@@ -268,7 +268,8 @@ moe_status moe_nvfp4_tile_scales(const uint8_t *s, int64_t rows, int64_t K, uint
  * [max_rows, d] bf16.  d, F multiples of 128; max_rows bounds
  * expert_offsets[E] as in moe_grouped_ffn_fp8 (clipped, MOE_DEV_ROWS).
  * workspace: moe_grouped_ffn_nvfp4_workspace_size bytes, 256-byte aligned
- * (act in bf16 and NVFP4, and the act tensor's scale).
+ * (act in bf16 and NVFP4, and the act tensor's scale).  max_rows may be 0:
+ * nothing is launched, and the buffers and the workspace may then be NULL.
  * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
  * ---------------------------------------------------------------------- */
 size_t moe_grouped_ffn_nvfp4_workspace_size(int64_t max_rows, int d, int F);
@@ -373,7 +374,8 @@ moe_status moe_dispatch_noalloc(const int32_t *topk_ids, int T, int k, int E, co
  * expert_offsets[E]: offsets outside [0, max_rows] are clipped into it and
  * set MOE_DEV_ROWS, so rows outside the buffers are never read or written.
  * workspace: moe_grouped_ffn_workspace_size(max_rows, d, F) bytes (holds
- * act_q and its scales), 256-byte aligned.
+ * act_q and its scales), 256-byte aligned.  max_rows may be 0: nothing is
+ * launched, and the buffers and the workspace may then be NULL.
  * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
  * ---------------------------------------------------------------------- */
 size_t moe_grouped_ffn_workspace_size(int64_t max_rows, int d, int F);
@@ -425,7 +427,8 @@ moe_status moe_grouped_ffn_fp8_gathered(const uint8_t *xq, const float *xs, int 
  * token-major (row r's exponents are x_exp[sorted_to_slot[r] / k]);
  * w13_q [E, 2F, d], w13_exp [E, 2F/128, d/128]; w2_q [E, d, F],
  * w2_exp [E, d/128, F/128]; workspace moe_grouped_ffn_mx_workspace_size
- * bytes (act_q and its exponents), 256-byte aligned.
+ * bytes (act_q and its exponents), 256-byte aligned.  max_rows or T may be
+ * 0: nothing is launched, and the buffers and the workspace may then be NULL.
  * Errors: NULL, SHAPE, ALIGN, WORKSPACE, CUDA.
  * ---------------------------------------------------------------------- */
 size_t moe_grouped_ffn_mx_workspace_size(int64_t max_rows, int d, int F);

@@ -79,6 +79,13 @@ def test_host_side_errors(lib):
     fws = L.moe_grouped_ffn_workspace_size(1000, 256, 512)
     assert fws > 0
     assert L.moe_grouped_ffn_fp8(x, x, x, 1000, 8, 200, 512, x, x, x, x, x, x, fws, null, null) in (2, 6)
+    # no rows: nothing launched, every buffer and the workspace may be NULL (what empty tensors pass)
+    n7 = [null] * 7
+    assert L.moe_grouped_ffn_fp8(null, null, null, 0, 8, 256, 512, *n7[:5], null, 0, null, null) == 0
+    assert L.moe_grouped_ffn_fp8_train(null, null, null, 0, 8, 256, 512, *n7[:5], null, null, 0, null, null) == 0
+    assert L.moe_grouped_ffn_mx(null, null, null, 0, 8, null, 0, 8, 256, 512, *n7[:5], null, 0, null, null) == 0
+    assert L.moe_grouped_ffn_nvfp4(null, null, null, null, 0, 8, 256, 512, *n7[:7], null, 0, null, null) == 0
+    assert L.moe_grouped_ffn_fp8_train(x, x, x, 16, 8, 256, 512, x, x, x, x, x, null, x, fws, null, null) == 1
     assert L.moe_grouped_ffn_fp8(x, x, x, 1000, 8, 256, 512, x, x, x, x, x, x, fws - 1, null, null) in (4, 6)
     assert L.moe_payload_pack_u8(x, -1, 8, x, x, null) == 2          # n < 0
     assert L.moe_payload_pack_u8(x, 16, 0, x, x, null) == 2          # E < 1
