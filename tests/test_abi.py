@@ -1,7 +1,8 @@
 """The C-ABI library loads, exports every entry point include/moe_r3.h
-declares, and rejects bad arguments on the host before launching anything
-(these calls return before any CUDA API is touched, so they run without a
-GPU)."""
+declares, the binding passes every argument at the width the prototype
+declares, and the library rejects bad arguments on the host before
+launching anything (these calls return before any CUDA API is touched, so
+they run without a GPU)."""
 import ctypes
 import os
 import re
@@ -139,3 +140,36 @@ def test_host_side_errors(lib):
     assert L.fp8_quant_nvfp4(y, 4, 64, x, x, x, null) == 3                              # misaligned src
     for s in range(7):
         assert lib.moe_status_str(s)
+
+
+def _decl_signatures():
+    """name -> (return type, [parameter types]) from the header's prototypes."""
+    src = open(os.path.join(ROOT, "include", "moe_r3.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(r"^\s*((?:const\s+)?\w+\s*\**)\s*\b((?:moe|fp8)_\w+)\s*\(([^)]*)\)\s*;",
+                                        src, flags=re.M):
+        types = []
+        for prm in params.split(","):
+            prm = " ".join(prm.split())
+            if prm in ("", "void"):
+                continue
+            types.append(prm[:prm.rfind("*") + 1] if "*" in prm else prm.rsplit(" ", 1)[0])
+        out[name] = (" ".join(ret.split()), types)
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every prototype's return and parameter types against the argtypes the
+    binding sets (a pointer as a void pointer, int32 as int, int64_t and
+    size_t at their own widths), so no argument is passed at the wrong width."""
+    want = {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "float": ctypes.c_float,
+            "moe_status": ctypes.c_int}
+    sigs = _decl_signatures()
+    assert set(sigs) == set(lib.EXPORTED)
+    for name, (ret, params) in sigs.items():
+        fn = getattr(lib._lib, name)
+        assert fn.restype == (ctypes.c_char_p if ret.endswith("*") else want[ret]), name
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), len(params))
+        for i, (t, a) in enumerate(zip(params, fn.argtypes)):
+            assert a == (ctypes.c_void_p if t.endswith("*") else want[t]), (name, i, t, a)
