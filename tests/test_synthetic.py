@@ -49,3 +49,22 @@ def test_uniform_payload_and_gates():
     g = S.make_dirichlet_gates(cfg, "cpu")
     assert g.shape == (2000, 8) and torch.all(g > 0)
     assert torch.allclose(g.double().sum(1), torch.ones(2000, dtype=torch.float64), atol=1e-6)
+
+
+def test_value_distributions():
+    """x ~ N(0, 1), router rows ~ N(0, 0.02), expert weights ~ N(0, w_std)
+    (0.02 for the small workloads, 0.006 for the large shapes), all bf16,
+    with the layouts the layer takes."""
+    for name, w_std in (("tiny", 0.02), ("large", 0.006)):
+        cfg = S.CONFIGS[name]
+        x = S.make_x(cfg, "cpu", T=512)
+        wr = S.make_router_w(cfg, "cpu")
+        w13 = S.make_w13_expert(cfg, 1, "cpu")
+        w2 = S.make_w2_expert(cfg, 1, "cpu")
+        assert x.dtype == wr.dtype == w13.dtype == w2.dtype == torch.bfloat16
+        assert x.shape == (512, cfg.d) and wr.shape == (cfg.E, cfg.d)
+        assert w13.shape == (2 * cfg.F, cfg.d) and w2.shape == (cfg.d, cfg.F)
+        assert cfg.w_std == w_std
+        for t, sd in ((x, 1.0), (wr, 0.02), (w13, w_std), (w2, w_std)):
+            v = t.double()
+            assert abs(v.mean().item()) < 0.05 * sd and abs(v.std().item() / sd - 1) < 0.05, (name, sd)
