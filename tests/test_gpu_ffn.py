@@ -111,6 +111,13 @@ def test_grouped_ffn_all_empty(L):
     assert torch.isnan(r["out"].float()).all()      # nothing written
 
 
+def test_grouped_ffn_no_rows(L):
+    """max_rows = 0: the call launches nothing and accepts the empty
+    tensors' NULL pointers, an empty workspace included."""
+    r = _run_ffn(L, [0, 0, 0], 256, 256, max_rows=0)
+    assert r["st"] == 0 and r["out"].shape == (0, 256) and r["ws"].numel() == 0
+
+
 @pytest.mark.parametrize("name", ["tiny", "replay"])
 def test_layer_against_oracle(L, oracle, parity_report, name):
     """The composed layer (route or replay -> quant -> dispatch -> FFN ->
